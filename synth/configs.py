@@ -1,0 +1,93 @@
+"""Model shapes of the synthetic workloads (data only, no arithmetic).
+
+Each field mirrors one axis of the decoder forward pass described on the pages:
+the llama family (SmolLM2-135M shape), llama3 with RoPE scaling, and the
+Gemma3-style local/global tower with QK-norm, sandwich norms, a GELU-gated FFN,
+a scaled embedding and a final-logit softcap.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+
+
+@dataclass(frozen=True)
+class ModelConfig:
+    name: str
+    n_layers: int
+    hidden: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    intermediate: int
+    vocab: int
+    rms_eps: float = 1e-5
+    rope_theta_global: float = 10000.0
+    rope_theta_local: float = 10000.0
+    rope_scaling: str = "none"          # "none" | "llama3"
+    rope_factor: float = 1.0
+    rope_low_freq_factor: float = 1.0
+    rope_high_freq_factor: float = 4.0
+    rope_orig_max_pos: int = 8192
+    act: str = "silu"                   # "silu" | "gelu_tanh"
+    norm_layout: str = "pre"            # "pre" | "sandwich"
+    qk_norm: bool = False
+    sliding_window: int = 0             # 0 = no local layers
+    layer_kinds: tuple = field(default=())  # per layer: 0 = global, 1 = local (empty = all global)
+    embed_scale: str = "none"           # "none" | "sqrt_hidden_bf16"
+    final_softcap: float = 0.0          # 0 = off
+    tied: bool = True
+
+    def kinds(self) -> tuple:
+        return self.layer_kinds if self.layer_kinds else (0,) * self.n_layers
+
+    def with_(self, **kw) -> "ModelConfig":
+        return replace(self, **kw)
+
+
+def _gemma_kinds(n_layers: int, period: int = 6) -> tuple:
+    # five local layers then one global, repeating: layer l is global iff (l+1) % 6 == 0
+    return tuple(0 if (l + 1) % period == 0 else 1 for l in range(n_layers))
+
+
+SMOLLM2_135M = ModelConfig(
+    name="smollm2-135m", n_layers=30, hidden=576, n_q_heads=9, n_kv_heads=3, head_dim=64,
+    intermediate=1536, vocab=49152, rms_eps=1e-5, rope_theta_global=100000.0,
+    rope_theta_local=100000.0, tied=True)
+
+LLAMA3_8B = ModelConfig(
+    name="llama3-8b", n_layers=32, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+    intermediate=14336, vocab=128256, rms_eps=1e-5, rope_theta_global=500000.0,
+    rope_theta_local=500000.0, rope_scaling="llama3", rope_factor=8.0, rope_low_freq_factor=1.0,
+    rope_high_freq_factor=4.0, rope_orig_max_pos=8192, tied=False)
+
+GEMMA3_TOWER = ModelConfig(
+    name="gemma3-tower", n_layers=48, hidden=3840, n_q_heads=16, n_kv_heads=8, head_dim=256,
+    intermediate=15360, vocab=262144, rms_eps=1e-6, rope_theta_global=1000000.0,
+    rope_theta_local=10000.0, act="gelu_tanh", norm_layout="sandwich", qk_norm=True,
+    sliding_window=1024, layer_kinds=_gemma_kinds(48), embed_scale="sqrt_hidden_bf16",
+    final_softcap=30.0, tied=True)
+
+CONFIGS = {c.name: c for c in (SMOLLM2_135M, LLAMA3_8B, GEMMA3_TOWER)}
+
+
+def tiny_config(kind: str = "llama", **kw) -> ModelConfig:
+    """Small models for brute-force checks and fast parity cases."""
+    if kind == "llama":
+        base = ModelConfig(name="tiny-llama", n_layers=2, hidden=16, n_q_heads=4, n_kv_heads=2,
+                           head_dim=4, intermediate=24, vocab=32, rms_eps=1e-5,
+                           rope_theta_global=10000.0, rope_theta_local=10000.0)
+    elif kind == "llama3":
+        base = ModelConfig(name="tiny-llama3", n_layers=2, hidden=32, n_q_heads=4, n_kv_heads=2,
+                           head_dim=8, intermediate=40, vocab=48, rms_eps=1e-5,
+                           rope_theta_global=500000.0, rope_theta_local=500000.0, rope_scaling="llama3",
+                           rope_factor=8.0, rope_low_freq_factor=1.0, rope_high_freq_factor=4.0,
+                           rope_orig_max_pos=512, tied=False)
+    elif kind == "gemma":
+        base = ModelConfig(name="tiny-gemma", n_layers=3, hidden=16, n_q_heads=4, n_kv_heads=2,
+                           head_dim=8, intermediate=24, vocab=40, rms_eps=1e-6,
+                           rope_theta_global=1000000.0, rope_theta_local=10000.0, act="gelu_tanh",
+                           norm_layout="sandwich", qk_norm=True, sliding_window=4,
+                           layer_kinds=(1, 1, 0), embed_scale="sqrt_hidden_bf16", final_softcap=30.0)
+    else:
+        raise ValueError(kind)
+    return replace(base, **kw)
