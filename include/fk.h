@@ -1,0 +1,229 @@
+/*
+ * fk -- decoder-only transformer forward pass (bf16) on one NVIDIA GB300.
+ *
+ * C ABI. Plain pointers and sizes only; no C++ or framework types cross it.
+ *
+ * What it computes (the pages' own terms):
+ *   "N7 · model/forward-parity", Theorem 1: embedding lookup, the decoder
+ *   stack (RMSNorm, Q/K/V projections, RoPE, causal GQA attention, SwiGLU FFN,
+ *   residuals), final norm and the (tied) LM head, giving per-layer hidden
+ *   states and per-position logits and argmax; a cached session whose prefill
+ *   last-position logits equal the cacheless forward; greedy generation.
+ *   Theorem 2: family axes -- QK-norm, sliding-window local layers, sandwich
+ *   norm placement, llama3 RoPE scaling.
+ *   "pegainfer issue #878", Proposed Plan: scaled embedding, layer dispatch
+ *   by a parsed local/global layer map, final-logit softcap validated
+ *   positive, geometry derived from the config as the one source of buffer
+ *   sizes, token ids bounds-checked before upload.
+ *   "N9 · metalgemm", Theorem 1: the GEMM Y = X·Wᵀ of the projections.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers ("d_" prefix) point to GPU global memory that the
+ *     caller allocated and owns; the library never allocates device memory
+ *     and never frees caller memory. Sizes come from the *_bytes queries.
+ *     Device buffers must be 256-byte aligned.
+ *   - Host pointers ("h_" prefix, or as stated) are read during the call only.
+ *   - Work is queued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: outputs are valid once the stream has
+ *     synchronised.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and returns a status != FK_OK, with a
+ *     message in fk_last_error() (thread-local).
+ *   - Device-side faults that can only be seen on the device (a token id read
+ *     from device memory that is out of range, a pipeline wait that timed
+ *     out) never trap: they set the model's device error word, which
+ *     fk_sync_status() reports and clears.
+ *   - bf16 tensors are row-major arrays of IEEE bfloat16; fp32 tensors are
+ *     row-major float.
+ *   - A model may be shared by several sessions; a model or session must not
+ *     be used from two host threads at once.
+ */
+#ifndef FK_H
+#define FK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fk_status {
+  FK_OK = 0,
+  FK_ERR_INVALID_ARG = 1,     /* null pointer, bad size, misaligned buffer */
+  FK_ERR_INVALID_CONFIG = 2,  /* model geometry rejected */
+  FK_ERR_TOKEN_RANGE = 3,     /* a host token id outside [0, vocab) */
+  FK_ERR_CONTEXT_FULL = 4,    /* session would exceed its max_seq */
+  FK_ERR_NO_DEVICE = 5,       /* no CUDA device, or not a GB300-class sm_103 device */
+  FK_ERR_CUDA = 6,            /* a CUDA runtime or driver call failed */
+  FK_ERR_DEVICE_FLAG = 7,     /* the device error word was set (see fk_sync_status) */
+  FK_ERR_TIMEOUT = 8,         /* fk_sync_status deadline passed */
+  FK_ERR_WORKSPACE = 9        /* a caller buffer is smaller than its *_bytes query */
+} fk_status;
+
+/* Bits of the device error word. */
+#define FK_DEVERR_TOKEN_RANGE 0x1u   /* a device-resident token id was out of range (clamped) */
+#define FK_DEVERR_PIPE_TIMEOUT 0x2u  /* a kernel pipeline wait gave up */
+
+typedef enum { FK_ROPE_NONE = 0, FK_ROPE_LLAMA3 = 1 } fk_rope_scaling;
+typedef enum { FK_ACT_SILU = 0, FK_ACT_GELU_TANH = 1 } fk_act;
+typedef enum { FK_NORM_PRE = 0, FK_NORM_SANDWICH = 1 } fk_norm_layout;
+typedef enum { FK_EMBED_SCALE_NONE = 0, FK_EMBED_SCALE_SQRT_HIDDEN_BF16 = 1 } fk_embed_scale;
+
+/*
+ * Model geometry ("pegainfer #878": one typed config is the single source of
+ * every buffer size). Validation rules (FK_ERR_INVALID_CONFIG otherwise):
+ *   n_layers >= 1; hidden, n_q_heads, n_kv_heads, head_dim, intermediate,
+ *   vocab >= 1; n_q_heads % n_kv_heads == 0; head_dim even, a multiple of 8
+ *   and <= 256; hidden, intermediate and n_q_heads*head_dim multiples of 64;
+ *   rms_eps > 0; rope thetas > 1; llama3 scaling needs factor >= 1,
+ *   high_freq_factor > low_freq_factor > 0 and orig_max_pos > 0;
+ *   sliding_window >= 0 (0 = no local layers; local layer kinds then
+ *   rejected); final_softcap == 0 (off) or > 0 and finite.
+ */
+typedef struct fk_config {
+  int32_t n_layers;
+  int32_t hidden;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t intermediate;
+  int32_t vocab;
+  float rms_eps;
+  double rope_theta_global;     /* RoPE base of global layers */
+  double rope_theta_local;      /* RoPE base of local (sliding-window) layers */
+  int32_t rope_scaling;         /* fk_rope_scaling */
+  float rope_factor;            /* llama3: divisor of the low-frequency band */
+  float rope_low_freq_factor;   /* llama3: a */
+  float rope_high_freq_factor;  /* llama3: b */
+  int32_t rope_orig_max_pos;    /* llama3: original context C */
+  int32_t act;                  /* fk_act: FFN gate activation */
+  int32_t norm_layout;          /* fk_norm_layout */
+  int32_t qk_norm;              /* 1 = per-head RMSNorm on q and k before RoPE */
+  int32_t sliding_window;       /* W of local layers: query i sees key j iff 0 <= i-j < W */
+  const uint8_t* layer_kinds;   /* host, n_layers entries, 0 = global, 1 = local; NULL = all global */
+  int32_t embed_scale;          /* fk_embed_scale */
+  float final_softcap;          /* c of z -> c*tanh(z/c); 0 = off */
+  int32_t tied;                 /* 1 = LM head is the embedding matrix */
+} fk_config;
+
+/* Per-layer device weights, all bf16. Matrices are [out, in] row-major.
+ * q_norm/k_norm [head_dim] are read only when qk_norm; post_attn_norm and
+ * post_ffn_norm [hidden] only for FK_NORM_SANDWICH. Norm weights are the
+ * effective multipliers (a "1 + w" convention is folded in by the caller). */
+typedef struct fk_layer_weights {
+  const void* attn_norm;       /* [hidden] */
+  const void* wq;              /* [n_q_heads*head_dim, hidden] */
+  const void* wk;              /* [n_kv_heads*head_dim, hidden] */
+  const void* wv;              /* [n_kv_heads*head_dim, hidden] */
+  const void* wo;              /* [hidden, n_q_heads*head_dim] */
+  const void* q_norm;          /* [head_dim] */
+  const void* k_norm;          /* [head_dim] */
+  const void* post_attn_norm;  /* [hidden] */
+  const void* ffn_norm;        /* [hidden] */
+  const void* w_gate;          /* [intermediate, hidden] */
+  const void* w_up;            /* [intermediate, hidden] */
+  const void* w_down;          /* [hidden, intermediate] */
+  const void* post_ffn_norm;   /* [hidden] */
+} fk_layer_weights;
+
+typedef struct fk_weights {
+  const void* embed;                /* [vocab, hidden] bf16, device */
+  const void* lm_head;              /* [vocab, hidden] bf16, device; ignored (may be NULL) if tied */
+  const void* final_norm;           /* [hidden] bf16, device */
+  const fk_layer_weights* layers;   /* host array of n_layers entries */
+} fk_weights;
+
+typedef struct fk_model fk_model;
+typedef struct fk_session fk_session;
+
+/* ---------------------------------------------------------------------------
+ * Status and errors
+ * ------------------------------------------------------------------------- */
+const char* fk_status_string(fk_status s);
+/* Message of the last failing call on this host thread ("" if none). */
+const char* fk_last_error(void);
+/* Library version, e.g. "fk 0.1 sm_103a". */
+const char* fk_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Model
+ * ------------------------------------------------------------------------- */
+/* Device arena the model needs (RoPE cos/sin tables for positions
+ * [0, max_positions) of each layer kind, and the device error word).
+ * Returns 0 if cfg is invalid. */
+size_t fk_model_arena_bytes(const fk_config* cfg, int32_t max_positions);
+
+/* Validate cfg, bind the caller's device weights (borrowed: they must outlive
+ * the model), fill the arena (synchronously, on the current device) and
+ * return a host handle in *out. max_positions bounds every sequence the model
+ * will see (sessions' max_seq and forward's seq). */
+fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, int32_t max_positions,
+                          void* d_arena, size_t arena_bytes, fk_model** out);
+void fk_model_free(fk_model* m);
+
+/* ---------------------------------------------------------------------------
+ * Cacheless forward ("N7", Thm 1: Forward)
+ * ------------------------------------------------------------------------- */
+size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, int32_t seq);
+
+/* Forward over ids [batch, seq] (positions 0..seq-1 per sequence).
+ *   ids: host int32 when ids_on_device == 0 (checked in [0, vocab) before
+ *        anything is queued: FK_ERR_TOKEN_RANGE), else device int32 (checked
+ *        on the device: out-of-range ids are clamped and set
+ *        FK_DEVERR_TOKEN_RANGE).
+ *   d_hidden: NULL, or fp32 [n_layers+2][batch*seq][hidden]: slot 0 the
+ *        (scaled) embedding, slot l+1 the residual stream after layer l, slot
+ *        n_layers+1 the final-norm output.
+ *   d_logits: NULL, or fp32 [batch*seq][vocab] (after the softcap, if any).
+ *   d_argmax: NULL, or int32 [batch*seq]: lowest index of the row maximum.
+ * A host `ids` buffer is copied synchronously before the call returns. */
+fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
+                     void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------
+ * KV-cached session ("N7", Thm 1: NewSession().Prefill and greedy Generate)
+ * batch sequences of equal length; K/V cache bf16 [layer][batch][kv_head][max_seq][head_dim].
+ * Prefill is processed in chunks of at most max_chunk tokens per sequence.
+ * ------------------------------------------------------------------------- */
+size_t fk_session_bytes(const fk_model* m, int32_t batch, int32_t max_seq, int32_t max_chunk);
+fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_seq, int32_t max_chunk, void* d_mem,
+                            size_t bytes, fk_session** out);
+void fk_session_free(fk_session* s);
+
+/* Append ids [batch, seq] (host or device as in fk_forward) after the tokens
+ * already in the session. d_last_logits: NULL or fp32 [batch][vocab] of the
+ * last position; d_next: NULL or int32 [batch], the greedy next ids (also
+ * kept in the session for fk_decode_step). FK_ERR_CONTEXT_FULL if the
+ * session would exceed max_seq. */
+fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32_t ids_on_device, int32_t seq,
+                             float* d_last_logits, int32_t* d_next, void* stream);
+
+/* One greedy decode step: feed d_ids [batch] (device int32), or the session's
+ * last greedy ids when d_ids is NULL; write logits / next ids as in prefill. */
+fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next, void* stream);
+
+/* Forget all tokens (length 0); the cache memory is reused. */
+fk_status fk_session_reset(fk_session* s);
+int32_t fk_session_length(const fk_session* s);
+
+/* Wait up to timeout_ms for `stream` to drain, then read and clear the device
+ * error word: FK_OK, FK_ERR_DEVICE_FLAG (bits in *flags if non-NULL), or
+ * FK_ERR_TIMEOUT (the stream is still busy; nothing was read). */
+fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t* flags);
+
+/* ---------------------------------------------------------------------------
+ * Op-level entry points (per-kernel parity; same kernels as the forward)
+ * ------------------------------------------------------------------------- */
+/* Y[P,N] = X[P,K] · W[N,K]ᵀ, bf16 inputs, fp32 accumulation ("N9 · metalgemm",
+ * Thm 1). Y is bf16 (y_fp32 == 0) or fp32. K % 8 == 0, N % 8 == 0 (16-byte
+ * rows). No scratch memory. */
+fk_status fk_gemm_bf16(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
+                       int32_t y_fp32, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FK_H */

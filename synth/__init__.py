@@ -18,7 +18,7 @@ import threading
 
 import numpy as np
 
-from .configs import ModelConfig, CONFIGS, tiny_config  # noqa: F401
+from .configs import ModelConfig, CONFIGS, small_config, tiny_config  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "_gen.c")

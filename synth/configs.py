@@ -91,3 +91,26 @@ def tiny_config(kind: str = "llama", **kw) -> ModelConfig:
     else:
         raise ValueError(kind)
     return replace(base, **kw)
+
+
+def small_config(kind: str = "llama", **kw) -> ModelConfig:
+    """Small models whose shapes the CUDA kernels accept (head_dim 64/128/256,
+    widths multiples of 64), for fast device-vs-oracle parity cases."""
+    if kind == "llama":
+        base = ModelConfig(name="small-llama", n_layers=2, hidden=128, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                           intermediate=256, vocab=512, rms_eps=1e-5, rope_theta_global=10000.0,
+                           rope_theta_local=10000.0, tied=True)
+    elif kind == "llama3":
+        base = ModelConfig(name="small-llama3", n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=128,
+                           intermediate=384, vocab=1024, rms_eps=1e-5, rope_theta_global=500000.0,
+                           rope_theta_local=500000.0, rope_scaling="llama3", rope_factor=8.0,
+                           rope_low_freq_factor=1.0, rope_high_freq_factor=4.0, rope_orig_max_pos=64, tied=False)
+    elif kind == "gemma":
+        base = ModelConfig(name="small-gemma", n_layers=3, hidden=256, n_q_heads=2, n_kv_heads=1, head_dim=256,
+                           intermediate=512, vocab=1024, rms_eps=1e-6, rope_theta_global=1000000.0,
+                           rope_theta_local=10000.0, act="gelu_tanh", norm_layout="sandwich", qk_norm=True,
+                           sliding_window=16, layer_kinds=(1, 1, 0), embed_scale="sqrt_hidden_bf16",
+                           final_softcap=30.0, tied=True)
+    else:
+        raise ValueError(kind)
+    return replace(base, **kw)

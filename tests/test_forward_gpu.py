@@ -1,0 +1,93 @@
+"""Device forward vs the float64 oracle ("N7 · model/forward-parity", Thm 1:
+hidden-state cosine >= 0.9999 at every slot, last-position logit max|Δ| <=
+0.05, per-position argmax equal to the oracle's wherever the oracle's
+top-1/top-2 margin exceeds 1e-2; Thm 2 family axes through the small
+llama3 and Gemma-style models)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import cosine, weights_to_dev
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-2
+
+
+def check_forward(fk, cfg, B, S, norm_mode="ones", sigma=0.02, seed=7):
+    import torch
+    wb = synth.make_weights(cfg, seed=seed, sigma=sigma, norm_mode=norm_mode)
+    ids = synth.make_ids(cfg, B, S, seed=99)
+    dev = weights_to_dev(wb)
+    model = fk.Model(cfg, dev, max_positions=max(S, 16))
+    out = model.forward(ids)
+    torch.cuda.synchronize()
+    st, flags = model.sync_status()
+    assert st == 0, flags
+    ref = oracle.forward(cfg, wb, ids)
+    hid = out["hidden"].cpu().numpy().reshape(cfg.n_layers + 2, B, S, cfg.hidden)
+    worst = min(cosine(hid[l, b, s], ref["hidden"][l, b, s])
+                for l in range(cfg.n_layers + 2) for b in range(B) for s in range(S))
+    assert worst >= 0.9999, worst
+    z = out["logits"].cpu().numpy().reshape(B, S, cfg.vocab)
+    zr = ref["logits"]
+    last = np.max(np.abs(z[:, -1] - zr[:, -1]))
+    assert last <= 0.05, last
+    am = out["argmax"].cpu().numpy().reshape(B, S)
+    margin = oracle.top2_margin(zr)
+    decided = margin > MARGIN
+    np.testing.assert_array_equal(am[decided], oracle.argmax_first(zr)[decided])
+    # the argmax kernel itself: exact on the device's own logits
+    np.testing.assert_array_equal(am, np.argmax(z, axis=-1))
+    return {"worst_cos": worst, "last_maxabs": float(last), "decided": float(decided.mean()),
+            "logit_err": float(np.max(np.abs(z - zr)))}
+
+
+@pytest.mark.parametrize("kind", ["llama", "llama3", "gemma"])
+@pytest.mark.parametrize("B,S", [(1, 9), (2, 70), (1, 130)])
+def test_small_models(fk, kind, B, S):
+    cfg = synth.small_config(kind)
+    r = check_forward(fk, cfg, B, S, norm_mode="random", sigma=0.05)
+    print(kind, B, S, r)
+
+
+def test_smollm2_shape_9_tokens(fk):
+    """The SmolLM2-135M-shaped llama, one sequence of 9 ids, norm weights 1.0."""
+    r = check_forward(fk, synth.CONFIGS["smollm2-135m"], 1, 9)
+    print(r)
+
+
+def test_bitwise_replay(fk):
+    import torch
+    cfg = synth.small_config("gemma")
+    wb = synth.make_weights(cfg, norm_mode="random", sigma=0.05)
+    model = fk.Model(cfg, weights_to_dev(wb), max_positions=64)
+    ids = synth.make_ids(cfg, 2, 40)
+    a = model.forward(ids)
+    b = model.forward(ids)
+    torch.cuda.synchronize()
+    for k in ("hidden", "logits", "argmax"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_token_range_rejected_on_host(fk):
+    cfg = synth.small_config("llama")
+    model = fk.Model(cfg, weights_to_dev(synth.make_weights(cfg)), max_positions=16)
+    ids = synth.make_ids(cfg, 1, 5)
+    ids[0, 3] = cfg.vocab
+    with pytest.raises(fk.FkError) as ei:
+        model.forward(ids)
+    assert ei.value.status == 3
+
+
+def test_token_range_flagged_on_device(fk):
+    import torch
+    cfg = synth.small_config("llama")
+    model = fk.Model(cfg, weights_to_dev(synth.make_weights(cfg)), max_positions=16)
+    ids = torch.tensor([[1, 2, cfg.vocab + 5, 3]], dtype=torch.int32, device="cuda")
+    model.forward(ids)
+    st, flags = model.sync_status()
+    assert st == 7 and flags & fk.DEVERR_TOKEN_RANGE
+    st, flags = model.sync_status()
+    assert st == 0 and flags == 0

@@ -1,0 +1,81 @@
+"""tcgen05 GEMM vs the float64 oracle ("N9 · metalgemm", Thm 1: err/scale =
+max|Δ| / max|ref| < 1e-2 against a float64-accumulated triple loop).
+
+Inputs are the same bf16-rounded X ~ N(0,1) and W ~ N(0, 0.02^2) on both sides,
+so the measured error is the kernel's own (fp32 accumulation, output rounding).
+Tighter bounds than the page's 1e-2 are derived from the arithmetic: with fp32
+accumulation over K <= 16384 terms the relative error of a dot product stays
+below about K * 2^-24 ~ 1e-3 in the worst case and ~1e-6 in practice; a bf16
+output adds at most 2^-9 relative rounding.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import err_scale, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [(16, 64, 96), (64, 512, 256), (256, 1536, 1536)]
+RAGGED = [(1, 64, 8), (129, 72, 136), (200, 8, 200), (300, 1000, 520), (7, 4096, 1032)]
+
+
+def _inputs(P, K, N, s=0):
+    x = synth.normal_bf16(synth.SEED_GEMM_X, 10 + s, (P, K), 1.0)
+    w = synth.normal_bf16(synth.SEED_WEIGHTS, 20 + s, (N, K), 0.02)
+    return x, w
+
+
+@pytest.mark.parametrize("P,K,N", SMALL + RAGGED)
+@pytest.mark.parametrize("fp32", [True, False])
+def test_gemm_full(fk, P, K, N, fp32):
+    import torch
+    x, w = _inputs(P, K, N)
+    ref = oracle.gemm(oracle.bf16_to_f64(x), oracle.bf16_to_f64(w))
+    y = fk.gemm(to_dev_bf16(x), to_dev_bf16(w), out_fp32=fp32)
+    torch.cuda.synchronize()
+    got = y.float().cpu().numpy()
+    e = err_scale(got, ref)
+    assert e < 1e-2
+    assert e < (2e-5 if fp32 else 6e-3), e
+
+
+def test_gemm_exact_integers(fk):
+    import torch
+    P, K, N = 130, 128, 264
+    rng = np.random.default_rng(5)
+    xi = rng.integers(-4, 5, size=(P, K)).astype(np.float32)
+    wi = rng.integers(-4, 5, size=(N, K)).astype(np.float32)
+    x = torch.from_numpy(xi).bfloat16().cuda()
+    w = torch.from_numpy(wi).bfloat16().cuda()
+    y = fk.gemm(x, w, out_fp32=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y.cpu().numpy(), oracle.gemm(xi, wi))  # partial sums < 2^24: exact
+
+
+@pytest.mark.parametrize("P,K,N", [(4096, 4096, 14336), (4096, 4096, 128256)])
+def test_gemm_large_sampled(fk, P, K, N):
+    import torch
+    x, w = _inputs(P, K, N, s=1)
+    y = fk.gemm(to_dev_bf16(x), to_dev_bf16(w), out_fp32=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(P, 64, replace=False))
+    cols = np.sort(rng.choice(N, 256, replace=False))
+    xf = oracle.bf16_to_f64(x)
+    ref_rows = oracle.gemm(xf[rows], oracle.bf16_to_f64(w))
+    got_rows = y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert err_scale(got_rows, ref_rows) < 2e-5
+    ref_cols = oracle.gemm(xf, oracle.bf16_to_f64(w[cols]))
+    got_cols = y[:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    assert err_scale(got_cols, ref_cols) < 2e-5
+
+
+def test_gemm_rejects_bad_args(fk):
+    import torch
+    x = torch.zeros((4, 12), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 12), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fk.FkError) as ei:
+        fk.gemm(x, w)
+    assert ei.value.status == 1

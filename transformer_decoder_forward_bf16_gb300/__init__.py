@@ -1,0 +1,312 @@
+"""Python binding of libfk, the GB300 (sm_103a) decoder-only transformer forward.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels of ``libfk.so`` behind the C ABI declared in ``include/fk.h``. PyTorch
+is used here only to own device memory and to name streams. There is no CPU
+fallback: if the library or a sm_103 GPU is missing, calls raise.
+
+Low-level functions carry the C names (``fk_forward``, ``fk_session_prefill``
+...) and take raw pointers; :class:`Model` and :class:`Session` wrap them for
+torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from ctypes import POINTER, c_double, c_float, c_int32, c_size_t, c_uint32, c_void_p
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+FK_OK = 0
+STATUS = {0: "FK_OK", 1: "FK_ERR_INVALID_ARG", 2: "FK_ERR_INVALID_CONFIG", 3: "FK_ERR_TOKEN_RANGE",
+          4: "FK_ERR_CONTEXT_FULL", 5: "FK_ERR_NO_DEVICE", 6: "FK_ERR_CUDA", 7: "FK_ERR_DEVICE_FLAG",
+          8: "FK_ERR_TIMEOUT", 9: "FK_ERR_WORKSPACE"}
+DEVERR_TOKEN_RANGE = 0x1
+DEVERR_PIPE_TIMEOUT = 0x2
+
+
+class FkError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
+
+
+class FkConfig(ctypes.Structure):
+    _fields_ = [("n_layers", c_int32), ("hidden", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32),
+                ("head_dim", c_int32), ("intermediate", c_int32), ("vocab", c_int32), ("rms_eps", c_float),
+                ("rope_theta_global", c_double), ("rope_theta_local", c_double), ("rope_scaling", c_int32),
+                ("rope_factor", c_float), ("rope_low_freq_factor", c_float), ("rope_high_freq_factor", c_float),
+                ("rope_orig_max_pos", c_int32), ("act", c_int32), ("norm_layout", c_int32), ("qk_norm", c_int32),
+                ("sliding_window", c_int32), ("layer_kinds", c_void_p), ("embed_scale", c_int32),
+                ("final_softcap", c_float), ("tied", c_int32)]
+
+
+class FkLayerWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "post_attn_norm",
+                                        "ffn_norm", "w_gate", "w_up", "w_down", "post_ffn_norm")]
+
+
+class FkWeights(ctypes.Structure):
+    _fields_ = [("embed", c_void_p), ("lm_head", c_void_p), ("final_norm", c_void_p),
+                ("layers", POINTER(FkLayerWeights))]
+
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "fk_status_string": (ctypes.c_char_p, [c_int32]),
+    "fk_last_error": (ctypes.c_char_p, []),
+    "fk_version": (ctypes.c_char_p, []),
+    "fk_model_arena_bytes": (c_size_t, [POINTER(FkConfig), c_int32]),
+    "fk_model_create": (c_int32, [POINTER(FkConfig), POINTER(FkWeights), c_int32, c_void_p, c_size_t,
+                                  POINTER(c_void_p)]),
+    "fk_model_free": (None, [c_void_p]),
+    "fk_forward_workspace_bytes": (c_size_t, [c_void_p, c_int32, c_int32]),
+    "fk_forward": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p,
+                             c_void_p, c_void_p]),
+    "fk_session_bytes": (c_size_t, [c_void_p, c_int32, c_int32, c_int32]),
+    "fk_session_create": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_size_t, POINTER(c_void_p)]),
+    "fk_session_free": (None, [c_void_p]),
+    "fk_session_prefill": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
+    "fk_decode_step": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fk_session_reset": (c_int32, [c_void_p]),
+    "fk_session_length": (c_int32, [c_void_p]),
+    "fk_sync_status": (c_int32, [c_void_p, c_void_p, c_int32, POINTER(c_uint32)]),
+    "fk_gemm_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p]),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_stale: bool = True):
+    """Load libfk.so (building it first if it is missing or older than its
+    sources). Raises if it cannot be built or loaded: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_stale and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(_build.LIB_PATH):
+                raise RuntimeError(f"libfk.so is missing at {_build.LIB_PATH}; run build()")
+            lib = ctypes.CDLL(_build.LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                if not hasattr(lib, name):
+                    continue
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != FK_OK:
+        raise FkError(status, where, load().fk_last_error().decode())
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+# raw C entry points, same names as the header
+# ---------------------------------------------------------------------------
+def fk_gemm_bf16(x_ptr, w_ptr, P, K, N, y_ptr, y_fp32, stream_ptr) -> int:
+    return load().fk_gemm_bf16(x_ptr, w_ptr, P, K, N, y_ptr, y_fp32, stream_ptr)
+
+
+def fk_forward(model_ptr, ids_ptr, ids_on_device, batch, seq, ws_ptr, ws_bytes, hidden_ptr, logits_ptr,
+               argmax_ptr, stream_ptr) -> int:
+    return load().fk_forward(model_ptr, ids_ptr, ids_on_device, batch, seq, ws_ptr, ws_bytes, hidden_ptr,
+                             logits_ptr, argmax_ptr, stream_ptr)
+
+
+def fk_session_prefill(sess_ptr, ids_ptr, ids_on_device, seq, logits_ptr, next_ptr, stream_ptr) -> int:
+    return load().fk_session_prefill(sess_ptr, ids_ptr, ids_on_device, seq, logits_ptr, next_ptr, stream_ptr)
+
+
+def fk_decode_step(sess_ptr, ids_ptr, logits_ptr, next_ptr, stream_ptr) -> int:
+    return load().fk_decode_step(sess_ptr, ids_ptr, logits_ptr, next_ptr, stream_ptr)
+
+
+def fk_sync_status(model_ptr, stream_ptr, timeout_ms):
+    flags = c_uint32(0)
+    st = load().fk_sync_status(model_ptr, stream_ptr, timeout_ms, ctypes.byref(flags))
+    return st, flags.value
+
+
+# ---------------------------------------------------------------------------
+# torch conveniences
+# ---------------------------------------------------------------------------
+def gemm(x, w, out_fp32: bool = False, out=None, stream=None):
+    """Y = X · Wᵀ on the tensor cores (bf16 in, fp32 accumulate)."""
+    import torch
+    P, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((P, N), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=x.device)
+    _check(fk_gemm_bf16(_ptr(x), _ptr(w), P, K, N, _ptr(out), 1 if out_fp32 else 0, _stream_ptr(stream)),
+           "fk_gemm_bf16")
+    return out
+
+
+def config_to_c(cfg) -> tuple:
+    """Fill an FkConfig from any object with the ModelConfig fields; returns
+    (struct, kinds buffer) -- keep the buffer alive while the struct is used."""
+    kinds = cfg.kinds() if hasattr(cfg, "kinds") else tuple(cfg.layer_kinds)
+    kbuf = (ctypes.c_uint8 * max(1, len(kinds)))(*kinds)
+    c = FkConfig(
+        n_layers=cfg.n_layers, hidden=cfg.hidden, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+        head_dim=cfg.head_dim, intermediate=cfg.intermediate, vocab=cfg.vocab, rms_eps=cfg.rms_eps,
+        rope_theta_global=cfg.rope_theta_global, rope_theta_local=cfg.rope_theta_local,
+        rope_scaling={"none": 0, "llama3": 1}[cfg.rope_scaling], rope_factor=cfg.rope_factor,
+        rope_low_freq_factor=cfg.rope_low_freq_factor, rope_high_freq_factor=cfg.rope_high_freq_factor,
+        rope_orig_max_pos=cfg.rope_orig_max_pos, act={"silu": 0, "gelu_tanh": 1}[cfg.act],
+        norm_layout={"pre": 0, "sandwich": 1}[cfg.norm_layout], qk_norm=int(cfg.qk_norm),
+        sliding_window=cfg.sliding_window, layer_kinds=ctypes.cast(kbuf, c_void_p) if len(kinds) else None,
+        embed_scale={"none": 0, "sqrt_hidden_bf16": 1}[cfg.embed_scale], final_softcap=cfg.final_softcap,
+        tied=int(cfg.tied))
+    return c, kbuf
+
+
+class Model:
+    """A model bound to device weights (a dict name -> bf16 CUDA tensor, names
+    as in ``fk_layer_weights``, prefixed ``L{l}.`` per layer)."""
+
+    def __init__(self, cfg, weights: dict, max_positions: int):
+        import torch
+        lib = load()
+        self.cfg = cfg
+        self.weights = weights  # keep the tensors alive: the library borrows them
+        self._ccfg, self._kinds = config_to_c(cfg)
+        n = cfg.n_layers
+        self._layers = (FkLayerWeights * n)()
+        for l in range(n):
+            for f, _ in FkLayerWeights._fields_:
+                t = weights.get(f"L{l}.{f}")
+                setattr(self._layers[l], f, _ptr(t) if t is not None else None)
+        self._cw = FkWeights(embed=_ptr(weights["embed"]), lm_head=_ptr(weights.get("lm_head")) or None,
+                             final_norm=_ptr(weights["final_norm"]), layers=self._layers)
+        nbytes = lib.fk_model_arena_bytes(ctypes.byref(self._ccfg), max_positions)
+        if nbytes == 0:
+            raise FkError(2, "fk_model_arena_bytes", lib.fk_last_error().decode())
+        dev = weights["embed"].device
+        self.arena = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        h = c_void_p()
+        _check(lib.fk_model_create(ctypes.byref(self._ccfg), ctypes.byref(self._cw), max_positions,
+                                   _ptr(self.arena), nbytes, ctypes.byref(h)), "fk_model_create")
+        self.handle = h.value
+        self.max_positions = max_positions
+        self._ws = None
+
+    def close(self):
+        if self.handle:
+            load().fk_model_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, ids, hidden: bool = True, logits: bool = True, argmax: bool = True, stream=None) -> dict:
+        """Cacheless forward over ids [B, S] (numpy/CPU int32 = host ids, CUDA
+        int32 tensor = device ids). Returns torch tensors on the device."""
+        import numpy as np
+        import torch
+        lib = load()
+        on_dev = isinstance(ids, torch.Tensor) and ids.is_cuda
+        if not on_dev:
+            ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        B, S = ids.shape
+        dev = self.arena.device
+        cfg = self.cfg
+        T = B * S
+        wsb = lib.fk_forward_workspace_bytes(self.handle, B, S)
+        if self._ws is None or self._ws.numel() < wsb:
+            self._ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        out = {
+            "hidden": torch.empty((cfg.n_layers + 2, T, cfg.hidden), dtype=torch.float32, device=dev) if hidden else None,
+            "logits": torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev) if logits else None,
+            "argmax": torch.empty((T,), dtype=torch.int32, device=dev) if argmax else None,
+        }
+        ids_ptr = _ptr(ids) if on_dev else ids.ctypes.data
+        _check(fk_forward(self.handle, ids_ptr, 1 if on_dev else 0, B, S, _ptr(self._ws), self._ws.numel(),
+                          _ptr(out["hidden"]), _ptr(out["logits"]), _ptr(out["argmax"]), _stream_ptr(stream)),
+               "fk_forward")
+        return out
+
+    def session(self, batch: int, max_seq: int, max_chunk: int | None = None) -> "Session":
+        return Session(self, batch, max_seq, max_chunk or max_seq)
+
+    def sync_status(self, stream=None, timeout_ms: int = 10000):
+        return fk_sync_status(self.handle, _stream_ptr(stream), timeout_ms)
+
+
+class Session:
+    """KV-cached prefill + greedy decode for `batch` sequences."""
+
+    def __init__(self, model: Model, batch: int, max_seq: int, max_chunk: int):
+        import torch
+        lib = load()
+        self.model = model
+        self.batch = batch
+        nbytes = lib.fk_session_bytes(model.handle, batch, max_seq, max_chunk)
+        if nbytes == 0:
+            raise FkError(1, "fk_session_bytes", lib.fk_last_error().decode())
+        self.mem = torch.empty(nbytes, dtype=torch.uint8, device=model.arena.device)
+        h = c_void_p()
+        _check(lib.fk_session_create(model.handle, batch, max_seq, max_chunk, _ptr(self.mem), nbytes,
+                                     ctypes.byref(h)), "fk_session_create")
+        self.handle = h.value
+
+    def close(self):
+        if self.handle:
+            load().fk_session_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, ids, logits=None, next_ids=None, stream=None):
+        import numpy as np
+        import torch
+        on_dev = isinstance(ids, torch.Tensor) and ids.is_cuda
+        if not on_dev:
+            ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        S = ids.shape[1]
+        ids_ptr = _ptr(ids) if on_dev else ids.ctypes.data
+        _check(fk_session_prefill(self.handle, ids_ptr, 1 if on_dev else 0, S, _ptr(logits), _ptr(next_ids),
+                                  _stream_ptr(stream)), "fk_session_prefill")
+
+    def decode(self, ids=None, logits=None, next_ids=None, stream=None):
+        _check(fk_decode_step(self.handle, _ptr(ids), _ptr(logits), _ptr(next_ids), _stream_ptr(stream)),
+               "fk_decode_step")
+
+    def reset(self):
+        _check(load().fk_session_reset(self.handle), "fk_session_reset")
+
+    @property
+    def length(self) -> int:
+        return load().fk_session_length(self.handle)
+
+
+def build_library(force: bool = False) -> str:
+    """Compile libfk.so for sm_103a (in-tree)."""
+    return _build.build(force=force)

@@ -1,0 +1,440 @@
+// Causal GQA attention over the bf16 KV cache ("N7 · model/forward-parity",
+// Thm 1: causal multi-head/GQA attention; Thm 2 and "pegainfer #878":
+// sliding-window local layers).
+//
+// Prefill: flash-style, one CTA per (64 queries, head, sequence), 4 warps x 16
+// query rows, 64-key blocks double-buffered in shared memory with cp.async,
+// QKᵀ and PV on tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate), online
+// softmax in fp32 (exp2 domain), P rounded to bf16 for the PV product.
+// Only the key blocks inside the causal (and window) range are visited.
+//
+// Decode: split-KV. Each CTA takes one (sequence, kv head, key chunk), scores
+// all query heads of its group against the chunk with 16-byte loads, and
+// writes an unnormalised partial (max, sum, output); a combine kernel merges
+// the partials in split order, so the result does not depend on scheduling.
+#include <algorithm>
+#include <mutex>
+
+#include "fk_common.cuh"
+#include "fk_ops.h"
+
+namespace fk {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+FK_DEVICE void cp_async16(void* smem_dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+FK_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+FK_DEVICE void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+FK_DEVICE void ldsm_x4(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+FK_DEVICE void ldsm_x4_t(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+FK_DEVICE void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// element (r, c) of a [rows][HD] bf16 tile, 16-byte chunks XOR-swizzled by row
+template <int HD>
+FK_DEVICE int swz(int r, int c) {
+  return r * HD + ((((c >> 3) ^ (r & 7))) << 3) + (c & 7);
+}
+
+constexpr int BQ = 64, BKV = 64;
+
+template <int HD>
+__global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, int ldq,
+                                                           const __nv_bfloat16* __restrict__ kc,
+                                                           const __nv_bfloat16* __restrict__ vc, int cap, int S,
+                                                           int pos0, int Hq, int Hkv, int window, float scale_log2,
+                                                           __nv_bfloat16* __restrict__ o) {
+  extern __shared__ uint4 smem_u4[];
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_u4);
+  __nv_bfloat16* sK = sQ + BQ * HD;
+  __nv_bfloat16* sV = sK + 2 * BKV * HD;
+  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (Hq / Hkv);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kv_len = pos0 + S;
+  const int q_lo = qb * BQ;
+  const int q_hi = min(S, q_lo + BQ) - 1;
+  const int qp_lo = pos0 + q_lo, qp_hi = pos0 + q_hi;
+  const int k_lo = window > 0 ? max(0, qp_lo - window + 1) : 0;
+  const int kb_lo = k_lo / BKV, kb_hi = qp_hi / BKV;
+  const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
+  const __nv_bfloat16* kbase = kc + head_off;
+  const __nv_bfloat16* vbase = vc + head_off;
+  constexpr int CPR = HD / 8;  // 16-byte chunks per row
+
+  for (int i = tid; i < BQ * CPR; i += 128) {
+    const int r = i / CPR, cc = i % CPR;
+    const int qi = q_lo + r;
+    const __nv_bfloat16* src = q + (size_t)(b * S + min(qi, S - 1)) * ldq + (size_t)h * HD + cc * 8;
+    cp_async16(sQ + swz<HD>(r, cc * 8), src, qi < S ? 16 : 0);
+  }
+  auto load_kv = [&](int kb, int buf) {
+    __nv_bfloat16* dk = sK + buf * BKV * HD;
+    __nv_bfloat16* dv = sV + buf * BKV * HD;
+    for (int i = tid; i < BKV * CPR; i += 128) {
+      const int r = i / CPR, cc = i % CPR;
+      const int kp = kb * BKV + r;
+      const int ok = kp < kv_len ? 16 : 0;
+      const size_t off = (size_t)min(kp, kv_len - 1) * HD + cc * 8;
+      cp_async16(dk + swz<HD>(r, cc * 8), kbase + off, ok);
+      cp_async16(dv + swz<HD>(r, cc * 8), vbase + off, ok);
+    }
+  };
+  load_kv(kb_lo, 0);
+  cp_async_commit();
+
+  float oacc[HD / 8][4];
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int qr0 = qp_lo + warp * 16 + (lane >> 2);  // positions of this thread's two rows
+  const int qr1 = qr0 + 8;
+  const int mat = lane >> 3, mr = lane & 7;
+
+  for (int kb = kb_lo; kb <= kb_hi; ++kb) {
+    const int buf = (kb - kb_lo) & 1;
+    if (kb < kb_hi) {
+      load_kv(kb + 1, buf ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const __nv_bfloat16* tK = sK + buf * BKV * HD;
+    const __nv_bfloat16* tV = sV + buf * BKV * HD;
+
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < HD; k0 += 16) {
+      uint32_t a[4];
+      ldsm_x4(a, sQ + swz<HD>(warp * 16 + mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t bb[4];
+        ldsm_x4(bb, tK + swz<HD>(np * 16 + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
+        mma_bf16_16816(s[2 * np], a, bb[0], bb[1]);
+        mma_bf16_16816(s[2 * np + 1], a, bb[2], bb[3]);
+      }
+    }
+    // mask (causal, window, cache end) and move to the exp2 domain
+    const int key0 = kb * BKV + 2 * (lane & 3);
+    const bool edge = (kb * BKV + BKV - 1 > qp_lo + warp * 16) || (kb * BKV + BKV > kv_len) ||
+                      (window > 0 && qp_hi - kb * BKV >= window);
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = s[nt][e] * scale_log2;
+        if (edge) {
+          const int key = key0 + nt * 8 + (e & 1);
+          const int qp = e < 2 ? qr0 : qr1;
+          const bool ok = key <= qp && key < kv_len && (window == 0 || qp - key < window);
+          v = ok ? v : -INFINITY;
+        }
+        s[nt][e] = v;
+      }
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
+    m0 = mn0;
+    m1 = mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - base0);
+      s[nt][1] = exp2f(s[nt][1] - base0);
+      s[nt][2] = exp2f(s[nt][2] - base1);
+      s[nt][3] = exp2f(s[nt][3] - base1);
+      rs0 += s[nt][0] + s[nt][1];
+      rs1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * corr0 + rs0;
+    l1 = l1 * corr1 + rs1;
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) {
+      oacc[i][0] *= corr0;
+      oacc[i][1] *= corr0;
+      oacc[i][2] *= corr1;
+      oacc[i][3] *= corr1;
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t a[4];
+      a[0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
+      a[1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
+      a[2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+      a[3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < HD / 16; ++dp) {
+        uint32_t bb[4];
+        ldsm_x4_t(bb, tV + swz<HD>(ks * 16 + mr + (mat & 1) * 8, dp * 16 + (mat >> 1) * 8));
+        mma_bf16_16816(oacc[2 * dp], a, bb[0], bb[1]);
+        mma_bf16_16816(oacc[2 * dp + 1], a, bb[2], bb[3]);
+      }
+    }
+    __syncthreads();
+  }
+
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const int qi0 = q_lo + warp * 16 + (lane >> 2), qi1 = qi0 + 8;
+  const size_t ldo = (size_t)Hq * HD;
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) {
+    const int col = h * HD + dt * 8 + 2 * (lane & 3);
+    if (qi0 < S)
+      *reinterpret_cast<uint32_t*>(o + (size_t)(b * S + qi0) * ldo + col) =
+          pack_bf16x2(oacc[dt][0] * inv0, oacc[dt][1] * inv0);
+    if (qi1 < S)
+      *reinterpret_cast<uint32_t*>(o + (size_t)(b * S + qi1) * ldo + col) =
+          pack_bf16x2(oacc[dt][2] * inv1, oacc[dt][3] * inv1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+constexpr int kDecThreads = 128;
+constexpr int kMaxChunk = 1024;
+constexpr int kMaxGroup = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
+    const __nv_bfloat16* __restrict__ q, int ldq, const __nv_bfloat16* __restrict__ kc,
+    const __nv_bfloat16* __restrict__ vc, int cap, int ctx_host, const int* d_ctx, int Hq, int Hkv, int window,
+    float scale_log2, int chunk, int n_splits, float* __restrict__ part_o, float* __restrict__ part_ml) {
+  constexpr int TPK = HD / 8;               // threads per key row (16-byte loads)
+  constexpr int KPP = kDecThreads / TPK;    // keys per pass
+  __shared__ float sq[kMaxGroup][HD];
+  __shared__ float sc[kMaxGroup][kMaxChunk];
+  __shared__ float sred[KPP][HD];
+  __shared__ float sm_m[kMaxGroup], sm_l[kMaxGroup];
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int group = Hq / Hkv;
+  const int tid = threadIdx.x;
+  const int ctx = d_ctx ? *d_ctx : ctx_host;
+  const int qpos = ctx - 1;
+  int lo = split * chunk;
+  const int hi = min(ctx, lo + chunk);
+  if (window > 0) lo = max(lo, qpos - window + 1);
+  const int n = max(0, hi - lo);
+  const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
+
+  for (int i = tid; i < group * HD; i += kDecThreads) {
+    const int hh = i / HD, d = i % HD;
+    sq[hh][d] = __bfloat162float(q[(size_t)b * ldq + (size_t)(g * group + hh) * HD + d]);
+  }
+  __syncthreads();
+
+  // scores
+  const int part = tid % TPK, kk = tid / TPK;
+  for (int j0 = 0; j0 < n; j0 += KPP) {  // uniform trip count: every lane joins the shuffles
+    const int j = j0 + kk;
+    const bool valid = j < n;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) u = *reinterpret_cast<const uint4*>(kc + head_off + (size_t)(lo + j) * HD + part * 8);
+    float kv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                   bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+    for (int hh = 0; hh < group; ++hh) {
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc += sq[hh][part * 8 + e] * kv[e];
+#pragma unroll
+      for (int off = TPK / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (part == 0 && valid) sc[hh][j] = acc * scale_log2;
+    }
+  }
+  __syncthreads();
+  // softmax statistics per head (one warp per head)
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int hh = warp; hh < group; hh += kDecThreads / 32) {
+    float mx = -INFINITY;
+    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sc[hh][j]);
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int j = lane; j < n; j += 32) {
+      const float p = exp2f(sc[hh][j] - mx);
+      sc[hh][j] = p;
+      sum += p;
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) {
+      sm_m[hh] = n > 0 ? mx : -INFINITY;
+      sm_l[hh] = sum;
+    }
+  }
+  __syncthreads();
+  // weighted values: thread (key slot kk, column chunk part)
+  for (int hh = 0; hh < group; ++hh) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = kk; j < n; j += KPP) {
+      const uint4 u = *reinterpret_cast<const uint4*>(vc + head_off + (size_t)(lo + j) * HD + part * 8);
+      const float p = sc[hh][j];
+      acc[0] += p * bf16_lo(u.x);
+      acc[1] += p * bf16_hi(u.x);
+      acc[2] += p * bf16_lo(u.y);
+      acc[3] += p * bf16_hi(u.y);
+      acc[4] += p * bf16_lo(u.z);
+      acc[5] += p * bf16_hi(u.z);
+      acc[6] += p * bf16_lo(u.w);
+      acc[7] += p * bf16_hi(u.w);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sred[kk][part * 8 + e] = acc[e];
+    __syncthreads();
+    const int h = g * group + hh;
+    const size_t base = (((size_t)b * Hq + h) * n_splits + split);
+    for (int d = tid; d < HD; d += kDecThreads) {
+      float s = 0.f;
+      for (int r = 0; r < KPP; ++r) s += sred[r][d];
+      part_o[base * HD + d] = s;
+    }
+    if (tid == 0) {
+      part_ml[base * 2] = sm_m[hh];
+      part_ml[base * 2 + 1] = sm_l[hh];
+    }
+    __syncthreads();
+  }
+}
+
+template <int HD>
+__global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hq,
+                                    int n_splits, __nv_bfloat16* __restrict__ o) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const size_t base = ((size_t)b * Hq + h) * n_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, part_ml[(base + s) * 2]);
+  float L = 0.f;
+  for (int s = 0; s < n_splits; ++s) {
+    const float m = part_ml[(base + s) * 2];
+    if (m != -INFINITY) L += part_ml[(base + s) * 2 + 1] * exp2f(m - M);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  for (int d = threadIdx.x; d < HD; d += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+      const float m = part_ml[(base + s) * 2];
+      if (m != -INFINITY) acc += part_o[(base + s) * HD + d] * exp2f(m - M);
+    }
+    o[((size_t)b * Hq + h) * HD + d] = __float2bfloat16_rn(acc * inv);
+  }
+}
+
+template <int HD>
+cudaError_t prefill_hd(const void* q, int ldq, const void* kc, const void* vc, int cap, int B, int S, int pos0, int Hq,
+                       int Hkv, int window, float scale, void* o, cudaStream_t st) {
+  constexpr int smem = (BQ + 4 * BKV) * HD * 2;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(attn_prefill_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (err != cudaSuccess) return err;
+  dim3 grid((S + BQ - 1) / BQ, Hq, B);
+  attn_prefill_kernel<HD><<<grid, 128, smem, st>>>(
+      static_cast<const __nv_bfloat16*>(q), ldq, static_cast<const __nv_bfloat16*>(kc),
+      static_cast<const __nv_bfloat16*>(vc), cap, S, pos0, Hq, Hkv, window, scale * kLog2e,
+      static_cast<__nv_bfloat16*>(o));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_prefill(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
+                                     int S, int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
+                                     cudaStream_t st) {
+  if (B == 0 || S == 0) return cudaSuccess;
+  switch (hd) {
+    case 64: return prefill_hd<64>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, st);
+    case 128: return prefill_hd<128>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, st);
+    case 256: return prefill_hd<256>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+size_t decode_attention_scratch_bytes(int B, int Hq, int hd, int max_splits) {
+  return (size_t)B * Hq * max_splits * (hd + 2) * sizeof(float) + 256;
+}
+
+int decode_attention_splits(int B, int Hkv, int max_ctx, int sm_count, int* chunk) {
+  long target = 2L * sm_count;
+  long c = ((long)max_ctx * B * Hkv + target - 1) / target;
+  c = (c + 63) / 64 * 64;
+  c = std::max(64L, std::min((long)kMaxChunk, c));
+  *chunk = (int)c;
+  return (int)((max_ctx + c - 1) / c);
+}
+
+cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
+                                    int ctx, const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
+                                    int chunk, int n_splits, void* scratch, void* o, cudaStream_t st) {
+  if (B == 0) return cudaSuccess;
+  if (Hq / Hkv > kMaxGroup || chunk > kMaxChunk) return cudaErrorInvalidValue;
+  float* part_o = static_cast<float*>(scratch);
+  float* part_ml = part_o + (size_t)B * Hq * n_splits * hd;
+  dim3 grid(n_splits, Hkv, B);
+  auto* qq = static_cast<const __nv_bfloat16*>(q);
+  auto* kc = static_cast<const __nv_bfloat16*>(kcache);
+  auto* vc = static_cast<const __nv_bfloat16*>(vcache);
+  auto* oo = static_cast<__nv_bfloat16*>(o);
+  const float sl = scale * kLog2e;
+  switch (hd) {
+    case 64:
+      attn_decode_kernel<64><<<grid, kDecThreads, 0, st>>>(qq, ldq, kc, vc, cap, ctx, d_ctx, Hq, Hkv, window, sl,
+                                                           chunk, n_splits, part_o, part_ml);
+      attn_combine_kernel<64><<<dim3(Hq, B), 64, 0, st>>>(part_o, part_ml, Hq, n_splits, oo);
+      break;
+    case 128:
+      attn_decode_kernel<128><<<grid, kDecThreads, 0, st>>>(qq, ldq, kc, vc, cap, ctx, d_ctx, Hq, Hkv, window, sl,
+                                                            chunk, n_splits, part_o, part_ml);
+      attn_combine_kernel<128><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, Hq, n_splits, oo);
+      break;
+    case 256:
+      attn_decode_kernel<256><<<grid, kDecThreads, 0, st>>>(qq, ldq, kc, vc, cap, ctx, d_ctx, Hq, Hkv, window, sl,
+                                                            chunk, n_splits, part_o, part_ml);
+      attn_combine_kernel<256><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, Hq, n_splits, oo);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fk

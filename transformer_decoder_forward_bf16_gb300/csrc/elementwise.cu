@@ -1,0 +1,399 @@
+// Bandwidth-bound kernels of the forward pass: embedding gather (+scale) with
+// the first RMSNorm fused, RMSNorm, the sandwich post-norm + residual +
+// next-norm fusion, QK-norm + RoPE + KV-cache write, and the per-row argmax.
+//
+// Every row kernel assigns one warp per row, reads with 16-byte vector loads
+// and reduces with warp shuffles; nothing here needs shared memory.
+#include "fk_common.cuh"
+#include "fk_ops.h"
+
+namespace fk {
+
+namespace {
+
+// 8 bf16 values from a 16-byte load, widened to fp32
+FK_DEVICE void load8_bf16(const __nv_bfloat16* p, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(u.x);
+  v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y);
+  v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z);
+  v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w);
+  v[7] = bf16_hi(u.w);
+}
+FK_DEVICE void store8_bf16(__nv_bfloat16* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// ---------------------------------------------------------------------------
+// embedding: x[t] = E[id_t] * scale (fp32), u[t] = RMSNorm(x[t]) * w (bf16)
+// ("N7 · model/forward-parity", Thm 1: embedding lookup; "pegainfer #878":
+// scaled embedding; the first pre-attention RMSNorm is fused in).
+// ---------------------------------------------------------------------------
+__global__ void embed_norm_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ E, int T, int H,
+                                  int V, float scale, const __nv_bfloat16* __restrict__ w, float eps,
+                                  float* __restrict__ x, __nv_bfloat16* __restrict__ u, unsigned* dev_err) {
+  const int warps = blockDim.x >> 5;
+  const int t = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int id = ids[t];
+  if (id < 0 || id >= V) {
+    if (lane == 0 && dev_err) atomicOr(dev_err, FK_DEVERR_TOKEN_RANGE);
+    id = id < 0 ? 0 : V - 1;
+  }
+  const __nv_bfloat16* e = E + (size_t)id * H;
+  float* xr = x + (size_t)t * H;
+  float ss = 0.f;
+  for (int c = lane * 8; c < H; c += 256) {
+    float v[8];
+    load8_bf16(e + c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] *= scale;
+      ss += v[j] * v[j];
+    }
+    *reinterpret_cast<float4*>(xr + c) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(xr + c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / H + eps);
+  __nv_bfloat16* ur = u + (size_t)t * H;
+  for (int c = lane * 8; c < H; c += 256) {
+    float v[8], wv[8];
+    load8_bf16(e + c, v);
+    load8_bf16(w + c, wv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = v[j] * scale * r * wv[j];
+    store8_bf16(ur + c, v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// u[t] = RMSNorm(x[t]) * w  ("N7", Thm 1: RMSNorm), fp32 in, bf16 out
+// ---------------------------------------------------------------------------
+__global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, int T, int H, const __nv_bfloat16* __restrict__ w,
+                               float eps, __nv_bfloat16* __restrict__ u, int ldu) {
+  const int warps = blockDim.x >> 5;
+  const int t = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* xr = x + (size_t)t * ldx;
+  float ss = 0.f;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / H + eps);
+  __nv_bfloat16* ur = u + (size_t)t * ldu;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    const uint2 wp = *reinterpret_cast<const uint2*>(w + c);
+    *reinterpret_cast<uint2*>(ur + c) =
+        make_uint2(pack_bf16x2(v.x * r * bf16_lo(wp.x), v.y * r * bf16_hi(wp.x)),
+                   pack_bf16x2(v.z * r * bf16_lo(wp.y), v.w * r * bf16_hi(wp.y)));
+  }
+}
+
+// fp32-output variant for the final-norm hidden slot
+__global__ void rmsnorm_f32_kernel(const float* __restrict__ x, int T, int H, const __nv_bfloat16* __restrict__ w,
+                                   float eps, float* __restrict__ y) {
+  const int warps = blockDim.x >> 5;
+  const int t = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* xr = x + (size_t)t * H;
+  float ss = 0.f;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / H + eps);
+  float* yr = y + (size_t)t * H;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    const uint2 wp = *reinterpret_cast<const uint2*>(w + c);
+    *reinterpret_cast<float4*>(yr + c) =
+        make_float4(v.x * r * bf16_lo(wp.x), v.y * r * bf16_hi(wp.x), v.z * r * bf16_lo(wp.y), v.w * r * bf16_hi(wp.y));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Sandwich norm: x_out = x_in + RMSNorm(a) * w_post, then
+// u = RMSNorm(x_out) * w_next ("N7", Thm 2: gemma3 sandwich norm).
+// x_out may alias x_in.
+// ---------------------------------------------------------------------------
+__global__ void post_norm_residual_kernel(const float* __restrict__ a, const float* x_in, float* x_out, int T, int H,
+                                          const __nv_bfloat16* __restrict__ w_post,
+                                          const __nv_bfloat16* __restrict__ w_next, float eps,
+                                          __nv_bfloat16* __restrict__ u) {
+  const int warps = blockDim.x >> 5;
+  const int t = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* ar = a + (size_t)t * H;
+  const float* xi = x_in + (size_t)t * H;
+  float* xo = x_out + (size_t)t * H;
+  float ss = 0.f;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(ar + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / H + eps);
+  float ss2 = 0.f;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(ar + c);
+    const float4 xv = *reinterpret_cast<const float4*>(xi + c);
+    const uint2 wp = *reinterpret_cast<const uint2*>(w_post + c);
+    float4 o;
+    o.x = xv.x + v.x * r * bf16_lo(wp.x);
+    o.y = xv.y + v.y * r * bf16_hi(wp.x);
+    o.z = xv.z + v.z * r * bf16_lo(wp.y);
+    o.w = xv.w + v.w * r * bf16_hi(wp.y);
+    ss2 += o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+    *reinterpret_cast<float4*>(xo + c) = o;
+  }
+  ss2 = warp_sum(ss2);
+  const float r2 = rsqrtf(ss2 / H + eps);
+  __syncwarp();
+  __nv_bfloat16* ur = u + (size_t)t * H;
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xo + c);
+    const uint2 wp = *reinterpret_cast<const uint2*>(w_next + c);
+    *reinterpret_cast<uint2*>(ur + c) =
+        make_uint2(pack_bf16x2(v.x * r2 * bf16_lo(wp.x), v.y * r2 * bf16_hi(wp.x)),
+                   pack_bf16x2(v.z * r2 * bf16_lo(wp.y), v.w * r2 * bf16_hi(wp.y)));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// QK-norm + RoPE + KV-cache write ("N7", Thm 1: RoPE on q and k; Thm 2: qwen3
+// / gemma3 QK-norm). One warp per (token, head). Head element j pairs with
+// j + hd/2; lane owns C = hd/64 consecutive elements of each half.
+//   q: rotated in place inside the qkv rows;
+//   k: rotated and written to kcache[b][g][pos][:]; v: copied to vcache.
+// rope: float2 (cos, sin) table [positions][hd/2].
+// ---------------------------------------------------------------------------
+template <int C>
+__global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq,
+                                int Hkv, const float2* __restrict__ rope, int qk_norm,
+                                const __nv_bfloat16* __restrict__ q_norm, const __nv_bfloat16* __restrict__ k_norm,
+                                float eps, __nv_bfloat16* kcache, __nv_bfloat16* vcache, int cap) {
+  constexpr int HD = C * 64;
+  constexpr int HALF = HD / 2;
+  const int warps = blockDim.x >> 5;
+  const long gw = (long)blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int nh = Hq + 2 * Hkv;
+  if (gw >= (long)T * nh) return;
+  const int t = (int)(gw / nh);
+  const int h = (int)(gw % nh);
+  const int b = t / S, s = t % S;
+  const int pos = (d_pos0 ? *d_pos0 : pos0) + s;
+  __nv_bfloat16* row = qkv + (size_t)t * ldqkv + (size_t)h * HD;
+  float lo[C], hi[C];
+  const int e0 = lane * C;  // within each half of size 32*C = HALF
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    lo[i] = __bfloat162float(row[e0 + i]);
+    hi[i] = __bfloat162float(row[HALF + e0 + i]);
+  }
+  if (h >= Hq + Hkv) {  // v: copy into the cache
+    const int g = h - Hq - Hkv;
+    __nv_bfloat16* dst = vcache + (((size_t)b * Hkv + g) * cap + pos) * HD;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      dst[e0 + i] = __float2bfloat16_rn(lo[i]);
+      dst[HALF + e0 + i] = __float2bfloat16_rn(hi[i]);
+    }
+    return;
+  }
+  const bool is_q = h < Hq;
+  if (qk_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < C; ++i) ss += lo[i] * lo[i] + hi[i] * hi[i];
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / HD + eps);
+    const __nv_bfloat16* nw = is_q ? q_norm : k_norm;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      lo[i] = lo[i] * r * __bfloat162float(nw[e0 + i]);
+      hi[i] = hi[i] * r * __bfloat162float(nw[HALF + e0 + i]);
+    }
+  }
+  const float2* cs = rope + (size_t)pos * HALF + e0;
+  float olo[C], ohi[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const float2 c = cs[i];
+    olo[i] = lo[i] * c.x - hi[i] * c.y;
+    ohi[i] = hi[i] * c.x + lo[i] * c.y;
+  }
+  __nv_bfloat16* dst;
+  if (is_q) {
+    dst = row;
+  } else {
+    const int g = h - Hq;
+    dst = kcache + (((size_t)b * Hkv + g) * cap + pos) * HD;
+  }
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    dst[e0 + i] = __float2bfloat16_rn(olo[i]);
+    dst[HALF + e0 + i] = __float2bfloat16_rn(ohi[i]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// argmax per row over V fp32 values (lowest index wins ties).
+// One block of 256 threads per row.
+// ---------------------------------------------------------------------------
+FK_DEVICE void better(float& m, int& i, float m2, int i2) {
+  if (m2 > m || (m2 == m && i2 < i)) {
+    m = m2;
+    i = i2;
+  }
+}
+
+__global__ void argmax_kernel(const float* __restrict__ z, int R, int V, int ldz, int32_t* __restrict__ out) {
+  const int r = blockIdx.x;
+  if (r >= R) return;
+  const float* row = z + (size_t)r * ldz;
+  float m = -INFINITY;
+  int idx = 0x7fffffff;
+  if ((V & 3) == 0 && (ldz & 3) == 0) {
+    for (int c = threadIdx.x * 4; c < V; c += blockDim.x * 4) {
+      const float4 v = *reinterpret_cast<const float4*>(row + c);
+      better(m, idx, v.x, c);
+      better(m, idx, v.y, c + 1);
+      better(m, idx, v.z, c + 2);
+      better(m, idx, v.w, c + 3);
+    }
+  } else {
+    for (int c = threadIdx.x; c < V; c += blockDim.x) better(m, idx, row[c], c);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    better(m, idx, m2, i2);
+  }
+  __shared__ float sm[32];
+  __shared__ int si[32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm[w] = m;
+    si[w] = idx;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    m = lane < nw ? sm[lane] : -INFINITY;
+    idx = lane < nw ? si[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+      better(m, idx, m2, i2);
+    }
+    if (lane == 0) out[r] = idx == 0x7fffffff ? 0 : idx;
+  }
+}
+
+// copy the last position of each sequence: dst[b] = src[b*S + S-1]
+__global__ void gather_last_rows_kernel(const __nv_bfloat16* src, int ld, int S, int H, int B,
+                                        __nv_bfloat16* dst) {
+  const int b = blockIdx.x;
+  if (b >= B) return;
+  const __nv_bfloat16* s = src + ((size_t)b * S + S - 1) * ld;
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8)
+    *reinterpret_cast<uint4*>(dst + (size_t)b * H + c) = *reinterpret_cast<const uint4*>(s + c);
+}
+
+constexpr int kRowThreads = 256;  // 8 rows per block
+inline int row_blocks(long rows) { return (int)((rows + 7) / 8); }
+
+}  // namespace
+
+cudaError_t launch_embed_norm(const int32_t* ids, const void* E, int T, int H, int V, float scale, const void* w,
+                              float eps, float* x, void* u, unsigned* dev_err, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  embed_norm_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(ids, static_cast<const __nv_bfloat16*>(E), T, H, V, scale,
+                                                         static_cast<const __nv_bfloat16*>(w), eps, x,
+                                                         static_cast<__nv_bfloat16*>(u), dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float* x, int ldx, int T, int H, const void* w, float eps, void* u, int ldu,
+                           cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  rmsnorm_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(x, ldx, T, H, static_cast<const __nv_bfloat16*>(w), eps,
+                                                      static_cast<__nv_bfloat16*>(u), ldu);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, float eps, float* y, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  rmsnorm_f32_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(x, T, H, static_cast<const __nv_bfloat16*>(w), eps, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* x_out, int T, int H,
+                                      const void* w_post, const void* w_next, float eps, void* u, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  post_norm_residual_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(
+      a, x_in, x_out, T, H, static_cast<const __nv_bfloat16*>(w_post), static_cast<const __nv_bfloat16*>(w_next), eps,
+      static_cast<__nv_bfloat16*>(u));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
+                            const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
+                            void* kcache, void* vcache, int cap, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const long warps = (long)T * (Hq + 2 * Hkv);
+  const int blocks = (int)((warps + 7) / 8);
+  auto* q = static_cast<__nv_bfloat16*>(qkv);
+  auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
+  auto* kn = static_cast<const __nv_bfloat16*>(k_norm);
+  auto* kc = static_cast<__nv_bfloat16*>(kcache);
+  auto* vc = static_cast<__nv_bfloat16*>(vcache);
+  switch (hd) {
+    case 64:
+      rope_qkv_kernel<1><<<blocks, 256, 0, st>>>(q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn, kn, eps, kc,
+                                                 vc, cap);
+      break;
+    case 128:
+      rope_qkv_kernel<2><<<blocks, 256, 0, st>>>(q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn, kn, eps, kc,
+                                                 vc, cap);
+      break;
+    case 256:
+      rope_qkv_kernel<4><<<blocks, 256, 0, st>>>(q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn, kn, eps, kc,
+                                                 vc, cap);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  argmax_kernel<<<R, 256, 0, st>>>(z, R, V, ldz, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_last_rows(const void* src, int ld, int S, int H, int B, void* dst, cudaStream_t st) {
+  if (B == 0) return cudaSuccess;
+  gather_last_rows_kernel<<<B, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), ld, S, H, B,
+                                             static_cast<__nv_bfloat16*>(dst));
+  return cudaGetLastError();
+}
+
+}  // namespace fk

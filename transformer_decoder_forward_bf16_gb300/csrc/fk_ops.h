@@ -1,0 +1,41 @@
+// Launchers of the non-GEMM kernels (host side, internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fk {
+
+cudaError_t launch_embed_norm(const int32_t* ids, const void* E, int T, int H, int V, float scale, const void* w,
+                              float eps, float* x, void* u, unsigned* dev_err, cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* x, int ldx, int T, int H, const void* w, float eps, void* u, int ldu,
+                           cudaStream_t st);
+cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, float eps, float* y, cudaStream_t st);
+cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* x_out, int T, int H,
+                                      const void* w_post, const void* w_next, float eps, void* u, cudaStream_t st);
+// pos0 (host) or *d_pos0 (device, if non-null) is the position of the first of S tokens per sequence.
+cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
+                            const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
+                            void* kcache, void* vcache, int cap, cudaStream_t st);
+cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st);
+cudaError_t launch_gather_last_rows(const void* src, int ld, int S, int H, int B, void* dst, cudaStream_t st);
+
+// Causal GQA attention of S new queries per sequence (positions pos0..pos0+S-1)
+// over the cached keys 0..pos0+S-1 (window > 0: only the last `window`).
+//   q: bf16 rows of the qkv buffer, q[b*S+s][h*hd + d], row stride ldq
+//   k/v cache: bf16 [B][Hkv][cap][hd]
+//   o: bf16 [B*S][Hq*hd]
+cudaError_t launch_attention_prefill(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
+                                     int S, int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
+                                     cudaStream_t st);
+
+// One query per sequence at position ctx-1 (ctx = keys in the cache,
+// *d_ctx if non-null, else ctx). Split-KV: partial results in `scratch`
+// (fk::decode_attention_scratch_bytes), combined in a fixed order.
+size_t decode_attention_scratch_bytes(int B, int Hq, int hd, int max_splits);
+int decode_attention_splits(int B, int Hkv, int max_ctx, int sm_count, int* chunk);
+cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
+                                    int ctx, const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
+                                    int chunk, int n_splits, void* scratch, void* o, cudaStream_t st);
+
+}  // namespace fk

@@ -1,0 +1,441 @@
+// bf16 GEMM on the 5th-generation tensor cores: out = epilogue(A · Bᵀ).
+//
+// "N9 · metalgemm", Theorem 1 defines the operation (Y = X·Wᵀ with float
+// accumulation; the Apple MPS lane there is prior art, not the design).
+//
+// Design (sm_103a):
+//   * persistent kernel, one CTA per SM, 128 x BN output tiles walked in
+//     groups of 16 M-blocks so that a wave of CTAs shares A and B tiles in L2;
+//   * warp 0: TMA producer (128-byte swizzled 128x64 A boxes and 64x64 B
+//     boxes into a STAGES-deep ring, completion on mbarriers);
+//   * warp 1: TMEM allocator and single-thread tcgen05.mma issuer
+//     (M=128, N=BN, K=16 per instruction, fp32 accumulators in TMEM, two
+//     accumulator buffers so the epilogue of tile i overlaps the MMAs of
+//     tile i+1);
+//   * warps 2-5: epilogue, tcgen05.ld 32x32b (one TMEM lane = one output
+//     row per thread) then a fused store: bf16, fp32 (+softcap), fp32
+//     residual add, or the gated activation act(gate)*up of the FFN.
+//   * the weight operand may be up to three matrices stacked along N (Q|K|V
+//     without a repacked copy) or a gate/up pair interleaved per tile.
+#include <algorithm>
+#include <mutex>
+
+#include "fk_common.cuh"
+#include "fk_internal.h"
+
+namespace fk {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
+
+struct GemmArgs {
+  int M, K, n_virtual;  // n_virtual: rows of the (virtual) B operand
+  int nseg, glu;
+  int seg_start[4];
+  int seg_rows[3];
+  int n_out;
+  int epi, act;
+  void* out;
+  int ldo;
+  const float* res;
+  int ldr;
+  float softcap;
+  unsigned* dev_err;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+};
+
+FK_DEVICE void tile_coords(int t, int m_blocks, int n_blocks, int& mb, int& nb) {
+  constexpr int G = 16;
+  const int group = t / (G * n_blocks);
+  const int first_m = group * G;
+  const int gsize = min(m_blocks - first_m, G);
+  const int r = t - group * G * n_blocks;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
+FK_DEVICE float act_gelu_tanh(float g) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+}
+
+// Source of the i-th 64-row box of B for output block nb.
+template <int BN>
+FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int& map, int& row, bool& valid) {
+  if (a.glu) {
+    constexpr int half = BN / 128;  // boxes per half tile
+    map = (i < half) ? 0 : 1;
+    row = nb * (BN / 2) + (i % half) * 64;
+    valid = row < a.seg_rows[map];
+  } else {
+    const int v = nb * BN + i * 64;
+    map = 0;
+    if (a.nseg > 1 && v >= a.seg_start[1]) map = 1;
+    if (a.nseg > 2 && v >= a.seg_start[2]) map = 2;
+    row = v - a.seg_start[map];
+    valid = v < a.n_virtual;
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_blocks = (args.M + BM - 1) / BM;
+  const int n_blocks = args.glu ? (args.n_out + BN / 2 - 1) / (BN / 2) : (args.n_virtual + BN - 1) / BN;
+  const int tiles = m_blocks * n_blocks;
+  const int nk = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    if (args.nseg > 1) tma_prefetch_desc(&tmB1);
+    if (args.nseg > 2) tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      const CUtensorMap* maps[3] = {&tmB0, &tmB1, &tmB2};
+      int fills[C::STAGES];
+      for (int s = 0; s < C::STAGES; ++s) fills[s] = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, m_blocks, n_blocks, mb, nb);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.dev_err)) {
+            ok = false;
+            break;
+          }
+          uint32_t bytes = A_BYTES;
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) {
+            int map, row;
+            bool valid;
+            b_box_source<BN>(args, nb, i, map, row, valid);
+            if (valid) bytes += 64 * BK * 2;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(&tmA, &full[stage], sA + stage * A_BYTES, kb * BK, mb * BM);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) {
+            int map, row;
+            bool valid;
+            b_box_source<BN>(args, nb, i, map, row, valid);
+            if (valid) tma_load_2d(maps[map], &full[stage], sB + stage * C::B_BYTES + i * 64 * BK * 2, kb * BK, row);
+          }
+          ++fills[stage];
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy this thread issued land before the CTA unwinds
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (fills[s] == 0) continue;
+          const uint32_t a = smem_u32(&full[s]);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(a, (fills[s] - 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t aphase = (local >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aphase ^ 1, abort_flag, args.dev_err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, args.dev_err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(sA + stage * A_BYTES);
+          const uint64_t bd = smem_desc_sw128(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d, ad + 2 * k, bd + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) umma_commit(&tfull[acc]);
+      }
+      // every MMA issued by this thread has completed once mma_done fires
+      umma_commit(mma_done);
+      const uint32_t a = smem_u32(mma_done);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(t, m_blocks, n_blocks, mb, nb);
+      const int acc = local & 1;
+      const uint32_t aphase = (local >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aphase, abort_flag, args.dev_err)) break;
+      tc_fence_after();
+      const int row = mb * BM + q * 32 + lane;
+      const bool row_ok = row < args.M;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      float v[32];
+      if (args.epi == EPI_GLU_BF16) {
+        for (int c = 0; c < BN / 64; ++c) {
+          float u[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld32(taddr + BN / 2 + c * 32, u);
+          const int col0 = nb * (BN / 2) + c * 32;
+          if (!row_ok) continue;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = (args.act ? act_gelu_tanh(v[j]) : act_silu(v[j])) * u[j];
+          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + (size_t)row * args.ldo + col0;
+          if (col0 + 32 <= args.n_out) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 pk = make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
+                                    pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
+              *reinterpret_cast<uint4*>(o + j) = pk;
+            }
+          } else {
+            for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) o[j] = __float2bfloat16_rn(v[j]);
+          }
+        }
+      } else {
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_ld32(taddr + c * 32, v);
+          const int col0 = nb * BN + c * 32;
+          if (!row_ok || col0 >= args.n_out) continue;
+          const bool full_chunk = col0 + 32 <= args.n_out;
+          if (args.epi == EPI_BF16) {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + (size_t)row * args.ldo + col0;
+            if (full_chunk) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                uint4 pk = make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
+                                      pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
+                *reinterpret_cast<uint4*>(o + j) = pk;
+              }
+            } else {
+              for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) o[j] = __float2bfloat16_rn(v[j]);
+            }
+          } else {
+            float* o = reinterpret_cast<float*>(args.out) + (size_t)row * args.ldo + col0;
+            if (args.epi == EPI_ADD_F32) {
+              const float* r = args.res + (size_t)row * args.ldr + col0;
+              if (full_chunk) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                  float4 rv = *reinterpret_cast<const float4*>(r + j);
+                  v[j] += rv.x;
+                  v[j + 1] += rv.y;
+                  v[j + 2] += rv.z;
+                  v[j + 3] += rv.w;
+                }
+              } else {
+                for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) v[j] += r[j];
+              }
+            } else if (args.softcap > 0.f) {
+              const float c_ = args.softcap, inv = 1.0f / args.softcap;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = c_ * tanhf(v[j] * inv);
+            }
+            if (full_chunk) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(o + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            } else {
+              for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) o[j] = v[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN>
+fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st) {
+  using C = Cfg<BN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
+  const int m_blocks = (a.M + BM - 1) / BM;
+  const int n_blocks = a.glu ? (a.n_out + BN / 2 - 1) / (BN / 2) : (a.n_virtual + BN - 1) / BN;
+  const int tiles = m_blocks * n_blocks;
+  const int grid = std::min(tiles, sm_count);
+  gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, st>>>(tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0],
+                                                       w.nseg > 2 ? w.map[2] : w.map[0], a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
+  return FK_OK;
+}
+
+}  // namespace
+
+fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* rows, int nseg, int K, int glu) {
+  if (nseg < 1 || nseg > 3 || (glu && nseg != 2) || K <= 0 || K % 8) return fail(FK_ERR_INVALID_ARG, "gemm weights");
+  *g = GemmWeights();
+  g->nseg = nseg;
+  g->glu = glu;
+  g->K = K;
+  int start = 0;
+  for (int s = 0; s < nseg; ++s) {
+    if (!mats[s] || rows[s] <= 0) return fail(FK_ERR_INVALID_ARG, "gemm weights: null or empty matrix");
+    if (nseg > 1 && !glu && s < nseg - 1 && rows[s] % 64)
+      return fail(FK_ERR_INVALID_ARG, "stacked weight matrices need row counts that are multiples of 64");
+    fk_status st = make_tmap_bf16(&g->map[s], mats[s], rows[s], K, K, 64);
+    if (st != FK_OK) return st;
+    g->seg_start[s] = start;
+    g->seg_rows[s] = rows[s];
+    start += rows[s];
+  }
+  g->seg_start[nseg] = start;
+  if (glu) {
+    if (rows[0] != rows[1]) return fail(FK_ERR_INVALID_ARG, "gate/up row counts differ");
+    g->n_out = rows[0];
+  } else {
+    g->n_out = start;
+  }
+  return FK_OK;
+}
+
+fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
+                   cudaStream_t st) {
+  if (M == 0) return FK_OK;
+  if (!A || !o.out || M < 0 || lda < w.K || lda % 8 || o.ldo % (o.epi == EPI_BF16 || o.epi == EPI_GLU_BF16 ? 8 : 4))
+    return fail(FK_ERR_INVALID_ARG, "gemm_run: bad operand");
+  if (o.epi == EPI_ADD_F32 && (!o.res || o.ldr % 4)) return fail(FK_ERR_INVALID_ARG, "gemm_run: residual");
+  int sm_count = 0;
+  fk_status s = check_device(&sm_count);
+  if (s != FK_OK) return s;
+  CUtensorMap tA;
+  s = make_tmap_bf16(&tA, A, M, w.K, lda, BM);
+  if (s != FK_OK) return s;
+  GemmArgs a{};
+  a.M = M;
+  a.K = w.K;
+  a.n_virtual = w.seg_start[w.nseg];
+  a.nseg = w.nseg;
+  a.glu = w.glu;
+  for (int i = 0; i < 4; ++i) a.seg_start[i] = w.seg_start[i];
+  for (int i = 0; i < 3; ++i) a.seg_rows[i] = w.seg_rows[i];
+  a.n_out = w.n_out;
+  a.epi = o.epi;
+  a.act = o.act;
+  a.out = o.out;
+  a.ldo = o.ldo;
+  a.res = o.res;
+  a.ldr = o.ldr;
+  a.softcap = o.softcap;
+  a.dev_err = dev_err;
+  // 256-wide tiles when they still give every SM a tile; else 128-wide.
+  const int m_blocks = (M + BM - 1) / BM;
+  const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
+  if (m_blocks * nb256 >= sm_count) return launch_bn<256>(tA, w, a, sm_count, st);
+  return launch_bn<128>(tA, w, a, sm_count, st);
+}
+
+}  // namespace fk
+
+extern "C" fk_status fk_gemm_bf16(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
+                                  int32_t y_fp32, void* stream) {
+  using namespace fk;
+  if (!d_x || !d_w || !d_y || P < 0 || K <= 0 || N <= 0) return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16: bad argument");
+  if (K % 8 || N % 8) return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16: K and N must be multiples of 8");
+  if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_w) | reinterpret_cast<uintptr_t>(d_y)) & 15)
+    return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16: buffers must be 16-byte aligned");
+  int sm = 0;
+  fk_status s = check_device(&sm);
+  if (s != FK_OK) return s;
+  GemmWeights w;
+  const void* mats[1] = {d_w};
+  int rows[1] = {N};
+  s = gemm_weights_init(&w, mats, rows, 1, K, 0);
+  if (s != FK_OK) return s;
+  GemmOut o;
+  o.epi = y_fp32 ? EPI_F32 : EPI_BF16;
+  o.out = d_y;
+  o.ldo = N;
+  return gemm_run(d_x, P, K, w, o, nullptr, static_cast<cudaStream_t>(stream));
+}

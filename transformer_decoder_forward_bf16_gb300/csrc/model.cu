@@ -1,0 +1,650 @@
+// The forward pass behind the C ABI: model binding, the layer loop shared by
+// the cacheless forward, session prefill and decode, and the LM head.
+//
+// Per layer, pre-norm layout ("N7 · model/forward-parity", Thm 1):
+//   qkv = u·[Wq;Wk;Wv]ᵀ          GEMM, stacked weights, bf16 out
+//   q,k <- [QK-norm] RoPE        k, v -> KV cache
+//   o   = attention(q, K, V)     causal GQA [sliding window]
+//   x'  = x + o·Woᵀ              GEMM, fp32 residual epilogue
+//   u   = RMSNorm(x')·w_ffn
+//   h   = act(u·Wgᵀ) ⊙ (u·Wuᵀ)   GEMM, gate/up interleaved, fused activation
+//   x'' = x' + h·Wdᵀ             GEMM, fp32 residual epilogue
+//   u   = RMSNorm(x'')·w_next    (next layer's attn norm, or the final norm)
+// Sandwich layout ("N7", Thm 2, gemma3): the O and down GEMMs write fp32 and a
+// fused kernel adds RMSNorm(a)·w_post to the residual and normalises the sum.
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include <cuda_bf16.h>
+
+#include "fk_internal.h"
+#include "fk_ops.h"
+
+using namespace fk;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Scratch {
+  int32_t* ids = nullptr;  // [T]
+  float* x0 = nullptr;     // [T, H] residual
+  float* x1 = nullptr;     // [T, H] residual (mid-layer)
+  float* a = nullptr;      // [T, H] sandwich pre-norm outputs
+  void* u = nullptr;       // [T, H] bf16 normalised rows
+  void* qkv = nullptr;     // [T, Nq + 2 Nkv] bf16
+  void* ao = nullptr;      // [T, Nq] bf16 attention output
+  void* h = nullptr;       // [T, I] bf16 gated FFN activations
+};
+
+}  // namespace
+
+struct fk_model {
+  fk_config cfg{};
+  std::vector<uint8_t> kinds;
+  std::vector<fk_layer_weights> layers;
+  const void* embed = nullptr;
+  const void* head = nullptr;
+  const void* final_norm = nullptr;
+  int max_pos = 0;
+  unsigned* dev_err = nullptr;
+  float2* rope[2] = {nullptr, nullptr};  // cos/sin tables per layer kind
+  std::vector<GemmWeights> g_qkv, g_o, g_gu, g_down;
+  GemmWeights g_head;
+  int Nq = 0, Nkv = 0, Nqkv = 0;
+  float embed_scale = 1.f;
+  float attn_scale = 1.f;
+  int sm_count = 0;
+  bool has_local = false;
+};
+
+struct fk_session {
+  fk_model* m = nullptr;
+  int B = 0, max_seq = 0, max_chunk = 0;
+  int len = 0;
+  __nv_bfloat16* kcache = nullptr;  // [L][B][Hkv][max_seq][hd]
+  __nv_bfloat16* vcache = nullptr;
+  size_t layer_kv = 0;  // elements per layer
+  Scratch sc;
+  int32_t* next_ids = nullptr;  // [B]
+  float* logits = nullptr;      // [B, V]
+  void* u_last = nullptr;       // [B, H] bf16
+  void* dec_scratch = nullptr;
+  int dec_chunk = 0, dec_splits = 0;
+};
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+fk_status validate_config(const fk_config* c) {
+  if (!c) return fail(FK_ERR_INVALID_ARG, "config is NULL");
+  auto bad = [](const char* m) { return fail(FK_ERR_INVALID_CONFIG, m); };
+  if (c->n_layers < 1) return bad("n_layers must be >= 1");
+  if (c->hidden < 64 || c->hidden % 64) return bad("hidden must be a positive multiple of 64");
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads)
+    return bad("n_q_heads must be a positive multiple of n_kv_heads");
+  if (c->n_q_heads / c->n_kv_heads > 8) return bad("more than 8 query heads per kv head");
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return bad("head_dim must be 64, 128 or 256");
+  if (c->intermediate < 64 || c->intermediate % 64) return bad("intermediate must be a positive multiple of 64");
+  if (c->vocab < 8 || c->vocab % 8) return bad("vocab must be a positive multiple of 8");
+  if (!(c->rms_eps > 0.f) || !std::isfinite(c->rms_eps)) return bad("rms_eps must be > 0");
+  if (!(c->rope_theta_global > 1.0) || !(c->rope_theta_local > 1.0)) return bad("rope thetas must be > 1");
+  if (c->rope_scaling != FK_ROPE_NONE && c->rope_scaling != FK_ROPE_LLAMA3) return bad("unknown rope_scaling");
+  if (c->rope_scaling == FK_ROPE_LLAMA3 &&
+      (!(c->rope_factor >= 1.f) || !(c->rope_low_freq_factor > 0.f) ||
+       !(c->rope_high_freq_factor > c->rope_low_freq_factor) || c->rope_orig_max_pos <= 0))
+    return bad("llama3 rope scaling parameters out of range");
+  if (c->act != FK_ACT_SILU && c->act != FK_ACT_GELU_TANH) return bad("unknown act");
+  if (c->norm_layout != FK_NORM_PRE && c->norm_layout != FK_NORM_SANDWICH) return bad("unknown norm_layout");
+  if (c->qk_norm != 0 && c->qk_norm != 1) return bad("qk_norm must be 0 or 1");
+  if (c->sliding_window < 0) return bad("sliding_window must be >= 0");
+  if (c->embed_scale != FK_EMBED_SCALE_NONE && c->embed_scale != FK_EMBED_SCALE_SQRT_HIDDEN_BF16)
+    return bad("unknown embed_scale");
+  // "pegainfer #878": the final-logit softcap is validated positive at parse
+  if (!std::isfinite(c->final_softcap) || c->final_softcap < 0.f) return bad("final_softcap must be 0 (off) or > 0");
+  if (c->tied != 0 && c->tied != 1) return bad("tied must be 0 or 1");
+  if (c->layer_kinds) {
+    for (int l = 0; l < c->n_layers; ++l) {
+      if (c->layer_kinds[l] > 1) return bad("layer_kinds entries must be 0 (global) or 1 (local)");
+      if (c->layer_kinds[l] == 1 && c->sliding_window == 0) return bad("local layer without a sliding_window");
+    }
+  }
+  return FK_OK;
+}
+
+bool has_local(const fk_config* c) {
+  if (!c->layer_kinds) return false;
+  for (int l = 0; l < c->n_layers; ++l)
+    if (c->layer_kinds[l] == 1) return true;
+  return false;
+}
+
+// Arena: [error word | rope table global | rope table local]
+size_t rope_table_bytes(const fk_config* c, int max_pos) {
+  return align_up((size_t)max_pos * (c->head_dim / 2) * sizeof(float2));
+}
+
+// bf16(sqrt(hidden)) by round-to-nearest-even on the float bits ("pegainfer
+// #878": derive the embedding scale and assert its recorded bf16 value)
+float bf16_round(float v) {
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  u &= 0xFFFF0000u;
+  float r;
+  std::memcpy(&r, &u, 4);
+  return r;
+}
+
+// RoPE frequencies f_j (j < hd/2) of one layer kind, in double. llama3
+// scaling: wavelength lam = 2*pi/f; lam < C/b keeps f; lam > C/a gives f/s;
+// between, t = (C/lam - a)/(b - a) blends f/s and f as (1-t) f/s + t f.
+void rope_freqs(const fk_config* c, int kind, std::vector<double>& f) {
+  const int half = c->head_dim / 2;
+  const double theta = kind == 1 ? c->rope_theta_local : c->rope_theta_global;
+  f.resize(half);
+  for (int j = 0; j < half; ++j) {
+    double fj = std::pow(theta, -2.0 * j / c->head_dim);
+    if (c->rope_scaling == FK_ROPE_LLAMA3) {
+      const double C = c->rope_orig_max_pos, a = c->rope_low_freq_factor, b = c->rope_high_freq_factor,
+                   s = c->rope_factor;
+      const double lam = 2.0 * M_PI / fj;
+      if (lam > C / a) {
+        fj = fj / s;
+      } else if (lam >= C / b) {
+        const double t = (C / lam - a) / (b - a);
+        fj = (1.0 - t) * fj / s + t * fj;
+      }
+    }
+    f[j] = fj;
+  }
+}
+
+size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
+  const fk_config& c = m->cfg;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> uint8_t* {
+    uint8_t* p = base ? base + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  };
+  Scratch t;
+  t.ids = reinterpret_cast<int32_t*>(take((size_t)T * 4));
+  t.x0 = reinterpret_cast<float*>(take((size_t)T * c.hidden * 4));
+  t.x1 = reinterpret_cast<float*>(take((size_t)T * c.hidden * 4));
+  if (c.norm_layout == FK_NORM_SANDWICH) t.a = reinterpret_cast<float*>(take((size_t)T * c.hidden * 4));
+  t.u = take((size_t)T * c.hidden * 2);
+  t.qkv = take((size_t)T * m->Nqkv * 2);
+  t.ao = take((size_t)T * m->Nq * 2);
+  t.h = take((size_t)T * c.intermediate * 2);
+  if (s) *s = t;
+  return off;
+}
+
+struct KV {
+  __nv_bfloat16* k;
+  __nv_bfloat16* v;
+  size_t layer_stride;  // elements between layers (0: one buffer reused by every layer)
+  int cap;              // positions per (sequence, kv head)
+};
+
+#define FK_LAUNCH(expr)                                 \
+  do {                                                  \
+    cudaError_t _e = (expr);                            \
+    if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
+  } while (0)
+#define FK_TRY(expr)                \
+  do {                              \
+    fk_status _s = (expr);          \
+    if (_s != FK_OK) return _s;     \
+  } while (0)
+
+// The decoder stack over T = B*S tokens at positions pos0 .. pos0+S-1 of
+// each sequence. Reads sc.ids; leaves the final-normed rows (bf16) in sc.u.
+// slots (optional): fp32 [L+2][T][H] hidden states. decode: S == 1, attention
+// through the split-KV kernel with dscratch.
+fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, const KV& kv, float* slots,
+                    bool decode, void* dscratch, int dchunk, int dsplits, cudaStream_t st) {
+  const fk_config& c = m->cfg;
+  const int H = c.hidden, L = c.n_layers, hd = c.head_dim;
+  const long T = (long)B * S;
+  const bool sandwich = c.norm_layout == FK_NORM_SANDWICH;
+  float* x_in = slots ? slots : sc.x0;
+  FK_LAUNCH(launch_embed_norm(sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
+                              x_in, sc.u, m->dev_err, st));
+  for (int l = 0; l < L; ++l) {
+    const fk_layer_weights& w = m->layers[l];
+    const int kind = m->kinds[l];
+    const int window = kind == 1 ? c.sliding_window : 0;
+    float* x_out = slots ? slots + (size_t)(l + 1) * T * H : sc.x0;
+    float* x_mid = sc.x1;
+    const void* next_norm = l + 1 < L ? m->layers[l + 1].attn_norm : m->final_norm;
+    __nv_bfloat16* kl = kv.k + kv.layer_stride * l;
+    __nv_bfloat16* vl = kv.v + kv.layer_stride * l;
+
+    GemmOut o;
+    o.epi = EPI_BF16;
+    o.out = sc.qkv;
+    o.ldo = m->Nqkv;
+    FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st));
+    FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
+                              m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st));
+    if (decode) {
+      FK_LAUNCH(launch_attention_decode(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, pos0 + 1, nullptr, c.n_q_heads,
+                                        c.n_kv_heads, hd, window, m->attn_scale, dchunk, dsplits, dscratch, sc.ao,
+                                        st));
+    } else {
+      FK_LAUNCH(launch_attention_prefill(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
+                                         window, m->attn_scale, sc.ao, st));
+    }
+    // attention output projection + residual
+    if (sandwich) {
+      o.epi = EPI_F32;
+      o.out = sc.a;
+      o.ldo = H;
+      o.softcap = 0.f;
+      FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st));
+      FK_LAUNCH(launch_post_norm_residual(sc.a, x_in, x_mid, (int)T, H, w.post_attn_norm, w.ffn_norm, c.rms_eps, sc.u,
+                                          st));
+    } else {
+      o.epi = EPI_ADD_F32;
+      o.out = x_mid;
+      o.ldo = H;
+      o.res = x_in;
+      o.ldr = H;
+      FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st));
+      FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st));
+    }
+    // gated FFN
+    GemmOut og;
+    og.epi = EPI_GLU_BF16;
+    og.out = sc.h;
+    og.ldo = c.intermediate;
+    og.act = c.act;
+    FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st));
+    if (sandwich) {
+      GemmOut od;
+      od.epi = EPI_F32;
+      od.out = sc.a;
+      od.ldo = H;
+      FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st));
+      FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps, sc.u,
+                                          st));
+    } else {
+      GemmOut od;
+      od.epi = EPI_ADD_F32;
+      od.out = x_out;
+      od.ldo = H;
+      od.res = x_mid;
+      od.ldr = H;
+      FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st));
+      FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st));
+    }
+    x_in = x_out;
+  }
+  if (slots) FK_LAUNCH(launch_rmsnorm_f32(x_in, (int)T, H, m->final_norm, c.rms_eps, slots + (size_t)(L + 1) * T * H, st));
+  return FK_OK;
+}
+
+fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* argmax, cudaStream_t st) {
+  GemmOut o;
+  o.epi = EPI_F32;
+  o.out = logits;
+  o.ldo = m->cfg.vocab;
+  o.softcap = m->cfg.final_softcap;
+  FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st));
+  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st));
+  return FK_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+fk_status check_ids_host(const int32_t* ids, long n, int vocab) {
+  for (long i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= vocab) {
+      char buf[128];
+      snprintf(buf, sizeof buf, "token id %d at index %ld is outside [0, %d)", ids[i], i, vocab);
+      return fail(FK_ERR_TOKEN_RANGE, buf);
+    }
+  return FK_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// model
+// ===========================================================================
+extern "C" size_t fk_model_arena_bytes(const fk_config* cfg, int32_t max_positions) {
+  if (validate_config(cfg) != FK_OK || max_positions < 1) {
+    if (max_positions < 1) set_error("max_positions must be >= 1");
+    return 0;
+  }
+  return kAlign + rope_table_bytes(cfg, max_positions) * (has_local(cfg) ? 2 : 1);
+}
+
+extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, int32_t max_positions, void* d_arena,
+                                     size_t arena_bytes, fk_model** out) {
+  if (!out) return fail(FK_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  FK_TRY(validate_config(cfg));
+  if (!w || !w->embed || !w->final_norm || !w->layers) return fail(FK_ERR_INVALID_ARG, "weights incomplete");
+  if (!cfg->tied && !w->lm_head) return fail(FK_ERR_INVALID_ARG, "untied model without lm_head");
+  if (max_positions < 1) return fail(FK_ERR_INVALID_ARG, "max_positions must be >= 1");
+  const size_t need = fk_model_arena_bytes(cfg, max_positions);
+  if (!d_arena || arena_bytes < need) return fail(FK_ERR_WORKSPACE, "model arena too small");
+  if (reinterpret_cast<uintptr_t>(d_arena) % kAlign) return fail(FK_ERR_INVALID_ARG, "arena must be 256-byte aligned");
+  int sms = 0;
+  FK_TRY(check_device(&sms));
+
+  fk_model* m = new fk_model();
+  m->cfg = *cfg;
+  m->kinds.assign(cfg->n_layers, 0);
+  if (cfg->layer_kinds) m->kinds.assign(cfg->layer_kinds, cfg->layer_kinds + cfg->n_layers);
+  m->cfg.layer_kinds = m->kinds.data();
+  m->has_local = has_local(cfg);
+  m->layers.assign(w->layers, w->layers + cfg->n_layers);
+  m->embed = w->embed;
+  m->head = cfg->tied ? w->embed : w->lm_head;
+  m->final_norm = w->final_norm;
+  m->max_pos = max_positions;
+  m->sm_count = sms;
+  m->Nq = cfg->n_q_heads * cfg->head_dim;
+  m->Nkv = cfg->n_kv_heads * cfg->head_dim;
+  m->Nqkv = m->Nq + 2 * m->Nkv;
+  m->embed_scale = cfg->embed_scale == FK_EMBED_SCALE_SQRT_HIDDEN_BF16 ? bf16_round(std::sqrt((float)cfg->hidden)) : 1.f;
+  m->attn_scale = 1.0f / std::sqrt((float)cfg->head_dim);
+
+  auto cleanup = [&](fk_status s) {
+    delete m;
+    return s;
+  };
+  // weights: pointers present and 16-byte aligned
+  const void* top[3] = {m->embed, m->head, m->final_norm};
+  for (const void* p : top)
+    if (!aligned16(p)) return cleanup(fail(FK_ERR_INVALID_ARG, "weights must be 16-byte aligned"));
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const fk_layer_weights& lw = m->layers[l];
+    const void* need_ptrs[] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo, lw.ffn_norm, lw.w_gate, lw.w_up, lw.w_down};
+    for (const void* p : need_ptrs)
+      if (!p || !aligned16(p)) return cleanup(fail(FK_ERR_INVALID_ARG, "layer weight missing or misaligned"));
+    if (cfg->qk_norm && (!lw.q_norm || !lw.k_norm || !aligned16(lw.q_norm) || !aligned16(lw.k_norm)))
+      return cleanup(fail(FK_ERR_INVALID_ARG, "qk_norm weights missing"));
+    if (cfg->norm_layout == FK_NORM_SANDWICH &&
+        (!lw.post_attn_norm || !lw.post_ffn_norm || !aligned16(lw.post_attn_norm) || !aligned16(lw.post_ffn_norm)))
+      return cleanup(fail(FK_ERR_INVALID_ARG, "sandwich norm weights missing"));
+  }
+  // GEMM operands (TMA descriptors of the weights)
+  const int H = cfg->hidden, I = cfg->intermediate;
+  m->g_qkv.resize(cfg->n_layers);
+  m->g_o.resize(cfg->n_layers);
+  m->g_gu.resize(cfg->n_layers);
+  m->g_down.resize(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const fk_layer_weights& lw = m->layers[l];
+    const void* qkv[3] = {lw.wq, lw.wk, lw.wv};
+    int rq[3] = {m->Nq, m->Nkv, m->Nkv};
+    fk_status s = gemm_weights_init(&m->g_qkv[l], qkv, rq, 3, H, 0);
+    const void* wo[1] = {lw.wo};
+    int ro[1] = {H};
+    if (s == FK_OK) s = gemm_weights_init(&m->g_o[l], wo, ro, 1, m->Nq, 0);
+    const void* gu[2] = {lw.w_gate, lw.w_up};
+    int rg[2] = {I, I};
+    if (s == FK_OK) s = gemm_weights_init(&m->g_gu[l], gu, rg, 2, H, 1);
+    const void* wd[1] = {lw.w_down};
+    int rd[1] = {H};
+    if (s == FK_OK) s = gemm_weights_init(&m->g_down[l], wd, rd, 1, I, 0);
+    if (s != FK_OK) return cleanup(s);
+  }
+  {
+    const void* hw[1] = {m->head};
+    int rv[1] = {cfg->vocab};
+    fk_status s = gemm_weights_init(&m->g_head, hw, rv, 1, H, 0);
+    if (s != FK_OK) return cleanup(s);
+  }
+  // arena: error word + RoPE tables (host double precision -> fp32 cos/sin)
+  uint8_t* arena = static_cast<uint8_t*>(d_arena);
+  m->dev_err = reinterpret_cast<unsigned*>(arena);
+  const size_t tb = rope_table_bytes(cfg, max_positions);
+  m->rope[0] = reinterpret_cast<float2*>(arena + kAlign);
+  m->rope[1] = m->has_local ? reinterpret_cast<float2*>(arena + kAlign + tb) : m->rope[0];
+  const int half = cfg->head_dim / 2;
+  std::vector<float2> table((size_t)max_positions * half);
+  std::vector<double> f;
+  for (int kind = 0; kind < (m->has_local ? 2 : 1); ++kind) {
+    rope_freqs(cfg, kind, f);
+    for (int p = 0; p < max_positions; ++p)
+      for (int j = 0; j < half; ++j) {
+        const double ang = (double)p * f[j];
+        table[(size_t)p * half + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    cudaError_t e = cudaMemcpy(m->rope[kind], table.data(), table.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "upload rope table"));
+  }
+  cudaError_t e = cudaMemset(m->dev_err, 0, sizeof(unsigned));
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "clear error word"));
+  *out = m;
+  return FK_OK;
+}
+
+extern "C" void fk_model_free(fk_model* m) { delete m; }
+
+// ===========================================================================
+// cacheless forward
+// ===========================================================================
+static size_t forward_layout(const fk_model* m, int B, int S, uint8_t* base, Scratch* sc, KV* kv, float** logits) {
+  const fk_config& c = m->cfg;
+  const long T = (long)B * S;
+  size_t off = scratch_bytes(m, T, sc, base);
+  const size_t kv_elems = (size_t)B * c.n_kv_heads * S * c.head_dim;
+  if (kv) {
+    kv->k = base ? reinterpret_cast<__nv_bfloat16*>(base + off) : nullptr;
+    kv->v = base ? reinterpret_cast<__nv_bfloat16*>(base + off + align_up(kv_elems * 2)) : nullptr;
+    kv->layer_stride = 0;
+    kv->cap = S;
+  }
+  off += 2 * align_up(kv_elems * 2);
+  if (logits) *logits = base ? reinterpret_cast<float*>(base + off) : nullptr;
+  off += align_up((size_t)T * c.vocab * 4);
+  return off;
+}
+
+extern "C" size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, int32_t seq) {
+  if (!m || batch < 1 || seq < 1) return 0;
+  return forward_layout(m, batch, seq, nullptr, nullptr, nullptr, nullptr);
+}
+
+extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
+                                void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
+                                void* stream) {
+  if (!m || !ids || batch < 1 || seq < 1) return fail(FK_ERR_INVALID_ARG, "fk_forward: bad argument");
+  if (seq > m->max_pos) return fail(FK_ERR_CONTEXT_FULL, "seq exceeds the model's max_positions");
+  const long T = (long)batch * seq;
+  if (!ids_on_device) FK_TRY(check_ids_host(ids, T, m->cfg.vocab));
+  const size_t need = fk_forward_workspace_bytes(m, batch, seq);
+  if (!d_ws || ws_bytes < need) return fail(FK_ERR_WORKSPACE, "forward workspace too small");
+  if (reinterpret_cast<uintptr_t>(d_ws) % kAlign) return fail(FK_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if ((d_hidden && !aligned16(d_hidden)) || (d_logits && !aligned16(d_logits)))
+    return fail(FK_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  FK_TRY(check_device(nullptr));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Scratch sc;
+  KV kv;
+  float* ws_logits = nullptr;
+  forward_layout(m, batch, seq, static_cast<uint8_t*>(d_ws), &sc, &kv, &ws_logits);
+  FK_CUDA_TRY(cudaMemcpyAsync(sc.ids, ids, T * sizeof(int32_t),
+                              ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+  FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, nullptr, 0, 0, st));
+  if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, st));
+  return FK_OK;
+}
+
+// ===========================================================================
+// sessions
+// ===========================================================================
+static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chunk, uint8_t* base, fk_session* s) {
+  const fk_config& c = m->cfg;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> uint8_t* {
+    uint8_t* p = base ? base + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  };
+  const size_t layer_kv = (size_t)B * c.n_kv_heads * max_seq * c.head_dim;
+  uint8_t* k = take(layer_kv * c.n_layers * 2);
+  uint8_t* v = take(layer_kv * c.n_layers * 2);
+  const long T = (long)B * max_chunk;
+  Scratch sc;
+  const size_t sb = scratch_bytes(m, T, &sc, base ? base + off : nullptr);
+  off += sb;
+  uint8_t* next = take((size_t)B * 4);
+  uint8_t* logits = take((size_t)B * c.vocab * 4);
+  uint8_t* ul = take((size_t)B * c.hidden * 2);
+  int chunk = 0;
+  const int splits = decode_attention_splits(B, c.n_kv_heads, max_seq, m->sm_count, &chunk);
+  uint8_t* ds = take(decode_attention_scratch_bytes(B, c.n_q_heads, c.head_dim, splits));
+  if (s) {
+    s->kcache = reinterpret_cast<__nv_bfloat16*>(k);
+    s->vcache = reinterpret_cast<__nv_bfloat16*>(v);
+    s->layer_kv = layer_kv;
+    s->sc = sc;
+    s->next_ids = reinterpret_cast<int32_t*>(next);
+    s->logits = reinterpret_cast<float*>(logits);
+    s->u_last = ul;
+    s->dec_scratch = ds;
+    s->dec_chunk = chunk;
+    s->dec_splits = splits;
+  }
+  return off;
+}
+
+extern "C" size_t fk_session_bytes(const fk_model* m, int32_t batch, int32_t max_seq, int32_t max_chunk) {
+  if (!m || batch < 1 || max_seq < 1 || max_chunk < 1 || max_seq > m->max_pos) {
+    set_error("fk_session_bytes: bad argument (batch, max_seq <= max_positions, max_chunk >= 1)");
+    return 0;
+  }
+  return session_layout(m, batch, max_seq, std::min(max_chunk, max_seq), nullptr, nullptr);
+}
+
+extern "C" fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_seq, int32_t max_chunk, void* d_mem,
+                                       size_t bytes, fk_session** out) {
+  if (!out) return fail(FK_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  const size_t need = fk_session_bytes(m, batch, max_seq, max_chunk);
+  if (need == 0) return FK_ERR_INVALID_ARG;
+  if (!d_mem || bytes < need) return fail(FK_ERR_WORKSPACE, "session memory too small");
+  if (reinterpret_cast<uintptr_t>(d_mem) % kAlign) return fail(FK_ERR_INVALID_ARG, "session memory must be 256-byte aligned");
+  FK_TRY(check_device(nullptr));
+  fk_session* s = new fk_session();
+  s->m = m;
+  s->B = batch;
+  s->max_seq = max_seq;
+  s->max_chunk = std::min(max_chunk, max_seq);
+  session_layout(m, batch, max_seq, s->max_chunk, static_cast<uint8_t*>(d_mem), s);
+  *out = s;
+  return FK_OK;
+}
+
+extern "C" void fk_session_free(fk_session* s) { delete s; }
+
+extern "C" fk_status fk_session_reset(fk_session* s) {
+  if (!s) return fail(FK_ERR_INVALID_ARG, "session is NULL");
+  s->len = 0;
+  return FK_OK;
+}
+
+extern "C" int32_t fk_session_length(const fk_session* s) { return s ? s->len : -1; }
+
+static fk_status session_head(fk_session* s, const void* u_rows, float* d_logits, int32_t* d_next, cudaStream_t st) {
+  fk_model* m = s->m;
+  float* logits = d_logits ? d_logits : s->logits;
+  FK_TRY(run_head(m, u_rows, s->B, logits, s->next_ids, st));
+  if (d_next) FK_CUDA_TRY(cudaMemcpyAsync(d_next, s->next_ids, s->B * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+  return FK_OK;
+}
+
+extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32_t ids_on_device, int32_t seq,
+                                        float* d_last_logits, int32_t* d_next, void* stream) {
+  if (!s || !ids || seq < 1) return fail(FK_ERR_INVALID_ARG, "fk_session_prefill: bad argument");
+  if (s->len + seq > s->max_seq) return fail(FK_ERR_CONTEXT_FULL, "prefill would exceed the session's max_seq");
+  if (d_last_logits && !aligned16(d_last_logits)) return fail(FK_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+  fk_model* m = s->m;
+  if (!ids_on_device) FK_TRY(check_ids_host(ids, (long)s->B * seq, m->cfg.vocab));
+  FK_TRY(check_device(nullptr));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  KV kv{s->kcache, s->vcache, s->layer_kv, s->max_seq};
+  int C = 0;
+  for (int c0 = 0; c0 < seq; c0 += C) {
+    C = std::min(s->max_chunk, seq - c0);
+    FK_CUDA_TRY(cudaMemcpy2DAsync(s->sc.ids, C * sizeof(int32_t), ids + c0, seq * sizeof(int32_t),
+                                  C * sizeof(int32_t), s->B,
+                                  ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    FK_TRY(run_stack(m, s->sc, s->B, C, s->len, kv, nullptr, false, nullptr, 0, 0, st));
+    s->len += C;
+  }
+  FK_LAUNCH(launch_gather_last_rows(s->sc.u, m->cfg.hidden, C, m->cfg.hidden, s->B, s->u_last, st));
+  return session_head(s, s->u_last, d_last_logits, d_next, st);
+}
+
+extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next,
+                                    void* stream) {
+  if (!s) return fail(FK_ERR_INVALID_ARG, "session is NULL");
+  if (s->len + 1 > s->max_seq) return fail(FK_ERR_CONTEXT_FULL, "decode would exceed the session's max_seq");
+  if (s->len == 0 && !d_ids) return fail(FK_ERR_INVALID_ARG, "no previous greedy ids: prefill first or pass d_ids");
+  if (d_logits && !aligned16(d_logits)) return fail(FK_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+  FK_TRY(check_device(nullptr));
+  fk_model* m = s->m;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FK_CUDA_TRY(cudaMemcpyAsync(s->sc.ids, d_ids ? d_ids : s->next_ids, s->B * sizeof(int32_t),
+                              cudaMemcpyDeviceToDevice, st));
+  KV kv{s->kcache, s->vcache, s->layer_kv, s->max_seq};
+  FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_scratch, s->dec_chunk, s->dec_splits, st));
+  s->len += 1;
+  return session_head(s, s->sc.u, d_logits, d_next, st);
+}
+
+// ===========================================================================
+// status
+// ===========================================================================
+extern "C" fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t* flags) {
+  if (flags) *flags = 0;
+  if (!m) return fail(FK_ERR_INVALID_ARG, "model is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t ev;
+  FK_CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+  cudaError_t e = cudaEventRecord(ev, st);
+  if (e != cudaSuccess) {
+    cudaEventDestroy(ev);
+    return cuda_fail(e, "cudaEventRecord");
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    e = cudaEventQuery(ev);
+    if (e == cudaSuccess) break;
+    if (e != cudaErrorNotReady) {
+      cudaEventDestroy(ev);
+      return cuda_fail(e, "stream reported an error");
+    }
+    if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms)) {
+      cudaEventDestroy(ev);
+      return fail(FK_ERR_TIMEOUT, "stream did not drain before the deadline");
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  cudaEventDestroy(ev);
+  unsigned h = 0;
+  FK_CUDA_TRY(cudaMemcpy(&h, m->dev_err, sizeof h, cudaMemcpyDeviceToHost));
+  if (h) {
+    FK_CUDA_TRY(cudaMemset(m->dev_err, 0, sizeof h));
+    if (flags) *flags = h;
+    char buf[96];
+    snprintf(buf, sizeof buf, "device error word 0x%x", h);
+    return fail(FK_ERR_DEVICE_FLAG, buf);
+  }
+  return FK_OK;
+}

@@ -1,0 +1,119 @@
+// Host runtime shared by the entry points: error reporting, device checks and
+// TMA descriptor encoding.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "fk_internal.h"
+
+namespace fk {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+fk_status fail(fk_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+fk_status cuda_fail(cudaError_t e, const char* what) {
+  char buf[512];
+  snprintf(buf, sizeof buf, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  g_last_error = buf;
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return FK_ERR_NO_DEVICE;
+  return FK_ERR_CUDA;
+}
+
+fk_status check_device(int* sm_count) {
+  static std::mutex mu;
+  static int cached_dev = -1, cached_sms = 0;
+  static fk_status cached = FK_OK;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e == cudaErrorInvalidDevice ? cudaErrorNoDevice : e, "cudaGetDevice");
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev != cached_dev) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(FK_ERR_NO_DEVICE, "cannot query the CUDA device");
+    }
+    cached_dev = dev;
+    cached_sms = sms;
+    if (major != 10 || minor != 3) {
+      char buf[160];
+      snprintf(buf, sizeof buf, "device %d is sm_%d%d; this library is built for sm_103a (GB300) only", dev, major,
+               minor);
+      set_error(buf);
+      cached = FK_ERR_NO_DEVICE;
+    } else {
+      cached = FK_OK;
+    }
+  }
+  if (cached != FK_OK) return fail(cached, "device is not sm_103 (GB300)");
+  if (sm_count) *sm_count = cached_sms;
+  return FK_OK;
+}
+
+fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  if (!encode) return fail(FK_ERR_NO_DEVICE, "cuTensorMapEncodeTiled is unavailable (no CUDA driver)");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld * 2) % 16 || rows <= 0 || cols <= 0 || box_rows > 256)
+    return fail(FK_ERR_INVALID_ARG, "tensor map: base must be 16-byte aligned, rows 16-byte multiples");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return fail(FK_ERR_CUDA, buf);
+  }
+  return FK_OK;
+}
+
+}  // namespace fk
+
+extern "C" const char* fk_status_string(fk_status s) {
+  switch (s) {
+    case FK_OK: return "ok";
+    case FK_ERR_INVALID_ARG: return "invalid argument";
+    case FK_ERR_INVALID_CONFIG: return "invalid config";
+    case FK_ERR_TOKEN_RANGE: return "token id out of range";
+    case FK_ERR_CONTEXT_FULL: return "session context full";
+    case FK_ERR_NO_DEVICE: return "no sm_103 CUDA device";
+    case FK_ERR_CUDA: return "CUDA error";
+    case FK_ERR_DEVICE_FLAG: return "device error flag set";
+    case FK_ERR_TIMEOUT: return "timeout";
+    case FK_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* fk_last_error(void) { return fk::g_last_error.c_str(); }
+
+extern "C" const char* fk_version(void) { return "fk 0.1 sm_103a"; }
