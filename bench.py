@@ -1,0 +1,390 @@
+#!/usr/bin/env python
+"""Prefill and decode throughput of the decoder forward pass on GB300.
+
+Workload (Llama-3-8B-shaped GQA model: 32 layers, hidden 4096, 32 query / 8
+kv heads, head_dim 128, FFN 14336, vocab 128256 untied, RoPE base 500000 with
+llama3 scaling; seeded N(0, 0.02^2) bf16 weights, norm weights 1.0, uniform
+random token ids):
+  * prefill: a KV-cached session prefill of 4 sequences x 4096 tokens,
+    greedy next id from the last position of each (the timed "value");
+  * decode: 32 sequences prefilled to 2048 tokens once (untimed), then G
+    greedy decode steps per timed step (context 2048 -> 2048 + G*(W+K)).
+One step = one prefill of the 4 x 4096 batch + G decode steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fk|reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
+path has no cross-sequence exchange, so there is no data-path collective.
+``--impl reference`` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "prefill tok/s & decode tok/s on 1 GB300; % of bf16 TC / HBM roofline"
+WORKLOAD = "llama3-8b-shaped: session prefill 4x4096 + greedy decode batch 32 at context 2048"
+PREFILL_B, PREFILL_S = 4, 4096
+DECODE_B, DECODE_CTX = 32, 2048
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fk", choices=["fk", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=16, help="greedy decode steps per bench step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="truncate the model to this many layers (profiling of a small case only)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_hash(*rel_paths) -> str:
+    h = hashlib.sha256()
+    for r in rel_paths:
+        h.update(open(os.path.join(ROOT, r), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(f"{kernel}@{workload}")
+        if e and e.get("source_hash") == source_hash(*e["sources"]):
+            return e["bytes_per_launch"]
+    except Exception:
+        return None
+    return None
+
+
+def host_weights(cfg, seed: int = synth.SEED_WEIGHTS) -> dict:
+    return synth.make_weights(cfg, seed=seed)
+
+
+def upload(wbits: dict, device) -> dict:
+    import torch
+    out = {}
+    for k, v in wbits.items():
+        out[k] = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(device, non_blocking=False)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_prefill_rate(cfg, wbits, n_tokens: int = 8) -> dict:
+    """Oracle prefill tok/s for the full model, from timing the oracle on the
+    same weights with 1 and 2 decoder layers (embedding + final norm + head
+    included in both) and scaling the per-layer time to cfg.n_layers."""
+    import oracle
+    ids = synth.make_ids(cfg, 1, n_tokens, stream=77)
+    times = {}
+    for nl in (1, 2):
+        c = cfg.with_(n_layers=nl)
+        sub = {k: v for k, v in wbits.items() if not k.startswith("L") or int(k[1:].split(".")[0]) < nl}
+        t0 = time.perf_counter()
+        oracle.Session(c, sub, 1).prefill(ids)
+        times[nl] = time.perf_counter() - t0
+    per_layer = max(times[2] - times[1], 1e-9)
+    fixed = max(times[1] - per_layer, 0.0)
+    full = fixed + per_layer * cfg.n_layers
+    return {"tok_s": n_tokens / full, "seconds_measured": times[1] + times[2], "full_forward_s": full,
+            "sample": f"oracle session prefill of 1x{n_tokens} tokens on the full-size weights with 1 and 2 "
+                      f"decoder layers (+embedding, final norm, LM head), per-layer time scaled to "
+                      f"{cfg.n_layers} layers"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS["llama3-8b"]
+    nl = 2
+    wbits = synth.make_weights(cfg.with_(n_layers=nl))
+    wbits["lm_head"] = synth.make_tensor(cfg, "lm_head")
+    for _ in range(args.warmup):
+        oracle_prefill_rate(cfg, wbits, 4)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = oracle_prefill_rate(cfg, wbits, 4)
+        secs.append(time.perf_counter() - t0)
+        vals.append(r["tok_s"])
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(secs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": PREFILL_B, "seq_len": PREFILL_S,
+                       "parallelism": "replicas", "l2": "inputs larger than L2 (16 GB of weights)"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+    import transformer_decoder_forward_bf16_gb300 as fk
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = fk.load()
+    peaks = load_peaks()
+
+    cfg = synth.CONFIGS["llama3-8b"]
+    if args.layers:
+        cfg = cfg.with_(n_layers=args.layers)
+    G = args.decode_steps
+    t0 = time.time()
+    wbits = host_weights(cfg)
+    wdev = upload(wbits, dev)
+    setup_gen_s = time.time() - t0
+    max_pos = max(PREFILL_S, DECODE_CTX + G * (args.warmup + args.steps) + 8)
+    model = fk.Model(cfg, wdev, max_positions=max_pos)
+    sp = model.session(PREFILL_B, PREFILL_S, max_chunk=PREFILL_S)
+    sd = model.session(DECODE_B, max_pos, max_chunk=1024)
+    ids_p = torch.from_numpy(synth.make_ids(cfg, PREFILL_B, PREFILL_S, stream=10 + rank)).to(dev)
+    ids_d = torch.from_numpy(synth.make_ids(cfg, DECODE_B, DECODE_CTX, stream=50 + rank)).to(dev)
+    z_p = torch.empty((PREFILL_B, cfg.vocab), dtype=torch.float32, device=dev)
+    n_p = torch.empty((PREFILL_B,), dtype=torch.int32, device=dev)
+    z_d = torch.empty((DECODE_B, cfg.vocab), dtype=torch.float32, device=dev)
+    n_d = torch.empty((DECODE_B,), dtype=torch.int32, device=dev)
+    sd.prefill(ids_d)  # context for the decode batch (untimed set-up)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    def step(events=None):
+        sp.reset()
+        if events:
+            events[0].record(stream)
+        sp.prefill(ids_p, logits=z_p, next_ids=n_p)
+        if events:
+            events[1].record(stream)
+        for _ in range(G):
+            sd.decode(None, logits=z_d, next_ids=n_d)
+        if events:
+            events[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    lib.fk_profile_reset()
+    lib.fk_profile_enable(1)
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    lib.fk_profile_enable(0)
+    total_ms = start.elapsed_time(stop)
+    pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    prof = {}
+    import ctypes
+    for i in range(lib.fk_profile_count()):
+        name = ctypes.c_char_p()
+        n = ctypes.c_int64()
+        ms = ctypes.c_double()
+        lib.fk_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms))
+        prof[name.value.decode()] = (n.value, ms.value)
+    lib.fk_profile_reset()
+    st, flags = model.sync_status()
+    if st != 0:
+        raise RuntimeError(f"device error word set: {flags:#x}")
+
+    times = torch.tensor([total_ms, pre_ms, dec_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, pre_ms, dec_ms = times.tolist()
+    prefill_tok = world * PREFILL_B * PREFILL_S * args.steps
+    decode_tok = world * DECODE_B * G * args.steps
+    prefill_tps = prefill_tok / (pre_ms / 1e3)
+    decode_tps = decode_tok / (dec_ms / 1e3)
+
+    # ---- roofline of the dominant kernels (algorithmic work / device time)
+    H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
+    Nq, Nkv = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    T = PREFILL_B * PREFILL_S
+    flops_per_launch = {"gemm_gate_up": 2.0 * T * H * 2 * I, "gemm_down": 2.0 * T * I * H,
+                        "gemm_qkv": 2.0 * T * H * (Nq + 2 * Nkv), "gemm_o": 2.0 * T * Nq * H}
+    pre_k = max(flops_per_launch, key=lambda k: prof.get(k, (0, 0.0))[1])
+    n, ms = prof.get(pre_k, (0, 0.0))
+    achieved_tf = flops_per_launch[pre_k] * n / (ms / 1e3) / 1e12 if ms > 0 else None
+    peak_tf = peaks["bf16_sustained"]
+    bytes_per_launch_dec = {"gemm_gate_up_dec": 2.0 * 2 * I * H, "gemm_down_dec": 2.0 * I * H,
+                            "gemm_qkv_dec": 2.0 * (Nq + 2 * Nkv) * H, "gemm_o_dec": 2.0 * Nq * H}
+    dec_k = max(bytes_per_launch_dec, key=lambda k: prof.get(k, (0, 0.0))[1])
+    n2, ms2 = prof.get(dec_k, (0, 0.0))
+    achieved_gbs = bytes_per_launch_dec[dec_k] * n2 / (ms2 / 1e3) / 1e9 if ms2 > 0 else None
+    launches = sum(c * (2 if k == "attn_decode" else 1) for k, (c, _) in prof.items())
+    gpu_launches = launches
+
+    line = {
+        "metric": METRIC, "value": prefill_tps, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) bf16 weights, uniform ids)",
+        "config": {"workload": WORKLOAD, "global_batch": PREFILL_B * world, "seq_len": PREFILL_S,
+                   "decode_batch": DECODE_B * world, "decode_context": DECODE_CTX, "decode_steps_per_step": G,
+                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (16 GB of weights)"},
+        "decode": {"value": decode_tps, "unit": "tok/s", "ms_per_token_step": dec_ms / (G * args.steps)},
+        "roofline": {"kernel": pre_k, "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": (achieved_tf / peak_tf) if achieved_tf else None,
+                     "peak_src": f"{peaks['src']} bf16 sustained",
+                     "traffic": measured_traffic(pre_k, "llama3-8b prefill 4x4096")},
+        "roofline_decode": {"kernel": dec_k, "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"],
+                            "unit": "GB/s", "frac": (achieved_gbs / peaks["hbm"]) if achieved_gbs else None,
+                            "peak_src": f"{peaks['src']} hbm",
+                            "traffic": measured_traffic(dec_k, "llama3-8b decode b32")},
+        "step_fraction": {"prefill_tc_frac": (2.0 * T * (H * (Nq + 2 * Nkv) + Nq * H + 3 * H * I) * cfg.n_layers
+                                              / (pre_ms / args.steps / 1e3) / 1e12 / peak_tf)},
+        "kernels": {k: {"launches": c, "ms": round(m, 3)} for k, (c, m) in sorted(prof.items())},
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "setup_s": round(setup_gen_s, 1),
+    }
+
+    # ---- end to end through the public API: host ids in, host result out
+    if not args.no_e2e:
+        ids_host = synth.make_ids(cfg, PREFILL_B, PREFILL_S, stream=10 + rank)
+        res_host = torch.empty((PREFILL_B,), dtype=torch.int32, pin_memory=True)
+        zl_host = torch.empty((PREFILL_B, V), dtype=torch.float32, pin_memory=True)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        ke = max(1, min(3, args.steps))
+        e0.record(stream)
+        for _ in range(ke):
+            sp.reset()
+            sp.prefill(ids_host, logits=z_p, next_ids=n_p)  # host ids: copied in by the call
+            res_host.copy_(n_p, non_blocking=True)
+            zl_host.copy_(z_p, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
+        line["e2e"] = {"value": world * PREFILL_B * PREFILL_S / (e2e_ms / 1e3), "unit": "tok/s",
+                       "h2d_bytes_per_step": int(ids_host.nbytes),
+                       "d2h_bytes_per_step": int(res_host.numel() * 4 + zl_host.numel() * 4)}
+
+    # ---- CPU oracle on the host cores (rank 0, N = 1 only)
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        nl = 2
+        sub = {k: v for k, v in wbits.items() if not k.startswith("L") or int(k[1:].split(".")[0]) < nl}
+        r = oracle_prefill_rate(cfg, sub, 8)
+        line["cpu_baseline"] = {"value": r["tok_s"], "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": r["sample"], "seconds": round(r["seconds_measured"], 1)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -222,6 +222,22 @@ fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t
 fk_status fk_gemm_bf16(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
                        int32_t y_fp32, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Kernel timing (tracing)
+ * When enabled, every kernel launch of the entry points above is bracketed by
+ * CUDA events on its stream and filed under a kernel-class name ("gemm_qkv",
+ * "attn_prefill", ...). Not for use while a stream is being captured into a
+ * CUDA graph. Process-wide; thread-safe.
+ * ------------------------------------------------------------------------- */
+void fk_profile_enable(int32_t on);
+/* Drop every recorded launch. */
+void fk_profile_reset(void);
+/* Wait for the recorded events, then return the number of kernel classes. */
+int32_t fk_profile_count(void);
+/* Class i (0 <= i < fk_profile_count()): name (static storage until the next
+ * reset), launches and their summed device time in milliseconds. */
+fk_status fk_profile_get(int32_t i, const char** name, int64_t* launches, double* total_ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,6 +76,10 @@ _SIGS = {
     "fk_session_length": (c_int32, [c_void_p]),
     "fk_sync_status": (c_int32, [c_void_p, c_void_p, c_int32, POINTER(c_uint32)]),
     "fk_gemm_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p]),
+    "fk_profile_enable": (None, [c_int32]),
+    "fk_profile_reset": (None, []),
+    "fk_profile_count": (c_int32, []),
+    "fk_profile_get": (c_int32, [c_int32, POINTER(ctypes.c_char_p), POINTER(ctypes.c_int64), POINTER(c_double)]),
 }
 
 
@@ -95,8 +99,6 @@ def load(build_if_stale: bool = True):
                 raise RuntimeError(f"libfk.so is missing at {_build.LIB_PATH}; run build()")
             lib = ctypes.CDLL(_build.LIB_PATH)
             for name, (res, args) in _SIGS.items():
-                if not hasattr(lib, name):
-                    continue
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args

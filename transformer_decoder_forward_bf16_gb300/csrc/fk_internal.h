@@ -27,6 +27,17 @@ fk_status cuda_fail(cudaError_t e, const char* what);
 fk_status check_device(int* sm_count);
 
 // ---------------------------------------------------------------------------
+// kernel timing: RAII scope recording events around the launches inside it
+// ---------------------------------------------------------------------------
+bool profiling_enabled();
+struct ProfScope {
+  int slot = -1;
+  cudaStream_t st = nullptr;
+  ProfScope(const char* name, cudaStream_t stream);
+  ~ProfScope();
+};
+
+// ---------------------------------------------------------------------------
 // TMA descriptors
 // ---------------------------------------------------------------------------
 // 2-D bf16 row-major tensor [rows, cols] with row stride ld (elements), boxes

@@ -216,8 +216,9 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   const long T = (long)B * S;
   const bool sandwich = c.norm_layout == FK_NORM_SANDWICH;
   float* x_in = slots ? slots : sc.x0;
+  { ProfScope ps(decode ? "embed_norm_dec" : "embed_norm", st);
   FK_LAUNCH(launch_embed_norm(sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
-                              x_in, sc.u, m->dev_err, st));
+                              x_in, sc.u, m->dev_err, st)); }
   for (int l = 0; l < L; ++l) {
     const fk_layer_weights& w = m->layers[l];
     const int kind = m->kinds[l];
@@ -232,14 +233,17 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     o.epi = EPI_BF16;
     o.out = sc.qkv;
     o.ldo = m->Nqkv;
-    FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st));
+    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st)); }
+    { ProfScope ps(decode ? "rope_qkv_dec" : "rope_qkv", st);
     FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
-                              m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st));
+                              m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
     if (decode) {
+      ProfScope ps("attn_decode", st);
       FK_LAUNCH(launch_attention_decode(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, pos0 + 1, nullptr, c.n_q_heads,
                                         c.n_kv_heads, hd, window, m->attn_scale, dchunk, dsplits, dscratch, sc.ao,
                                         st));
     } else {
+      ProfScope ps("attn_prefill", st);
       FK_LAUNCH(launch_attention_prefill(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
                                          window, m->attn_scale, sc.ao, st));
     }
@@ -249,7 +253,8 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.out = sc.a;
       o.ldo = H;
       o.softcap = 0.f;
-      FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st));
+      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st)); }
+      ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_in, x_mid, (int)T, H, w.post_attn_norm, w.ffn_norm, c.rms_eps, sc.u,
                                           st));
     } else {
@@ -258,7 +263,8 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.ldo = H;
       o.res = x_in;
       o.ldr = H;
-      FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st));
+      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st)); }
+      ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st));
     }
     // gated FFN
@@ -267,13 +273,14 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     og.out = sc.h;
     og.ldo = c.intermediate;
     og.act = c.act;
-    FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st));
+    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st)); }
     if (sandwich) {
       GemmOut od;
       od.epi = EPI_F32;
       od.out = sc.a;
       od.ldo = H;
-      FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st));
+      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st)); }
+      ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps, sc.u,
                                           st));
     } else {
@@ -283,7 +290,8 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       od.ldo = H;
       od.res = x_mid;
       od.ldr = H;
-      FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st));
+      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st)); }
+      ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st));
     }
     x_in = x_out;
@@ -298,7 +306,8 @@ fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* ar
   o.out = logits;
   o.ldo = m->cfg.vocab;
   o.softcap = m->cfg.final_softcap;
-  FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st));
+  { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st)); }
+  ProfScope ps("argmax", st);
   if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st));
   return FK_OK;
 }

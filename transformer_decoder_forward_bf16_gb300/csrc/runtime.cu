@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "fk_internal.h"
 
@@ -96,7 +97,104 @@ fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64
   return FK_OK;
 }
 
+// ---------------------------------------------------------------------------
+// kernel timing
+// ---------------------------------------------------------------------------
+namespace {
+struct ProfClass {
+  std::string name;
+  int64_t launches = 0;
+  double ms = 0.0;
+};
+struct Pending {
+  int cls;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfClass> g_prof_classes;
+std::vector<Pending> g_prof_pending;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void prof_drain_locked() {
+  for (const Pending& p : g_prof_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.b) == cudaSuccess && cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      g_prof_classes[p.cls].launches += 1;
+      g_prof_classes[p.cls].ms += ms;
+    } else {
+      cudaGetLastError();
+    }
+    g_prof_pool.push_back(p.a);
+    g_prof_pool.push_back(p.b);
+  }
+  g_prof_pending.clear();
+}
+}  // namespace
+
+bool profiling_enabled() { return g_prof_on; }
+
+ProfScope::ProfScope(const char* name, cudaStream_t stream) : st(stream) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  int cls = -1;
+  for (size_t i = 0; i < g_prof_classes.size(); ++i)
+    if (g_prof_classes[i].name == name) cls = (int)i;
+  if (cls < 0) {
+    g_prof_classes.push_back(ProfClass{name});
+    cls = (int)g_prof_classes.size() - 1;
+  }
+  Pending p{cls, prof_event(), prof_event()};
+  cudaEventRecord(p.a, st);
+  g_prof_pending.push_back(p);
+  slot = (int)g_prof_pending.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (slot < (int)g_prof_pending.size()) cudaEventRecord(g_prof_pending[slot].b, st);
+}
+
 }  // namespace fk
+
+extern "C" void fk_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(fk::g_prof_mu);
+  fk::g_prof_on = on != 0;
+}
+
+extern "C" void fk_profile_reset(void) {
+  std::lock_guard<std::mutex> lock(fk::g_prof_mu);
+  fk::prof_drain_locked();
+  fk::g_prof_classes.clear();
+}
+
+extern "C" int32_t fk_profile_count(void) {
+  std::lock_guard<std::mutex> lock(fk::g_prof_mu);
+  fk::prof_drain_locked();
+  return (int32_t)fk::g_prof_classes.size();
+}
+
+extern "C" fk_status fk_profile_get(int32_t i, const char** name, int64_t* launches, double* total_ms) {
+  std::lock_guard<std::mutex> lock(fk::g_prof_mu);
+  fk::prof_drain_locked();
+  if (i < 0 || i >= (int32_t)fk::g_prof_classes.size()) return fk::fail(FK_ERR_INVALID_ARG, "profile index");
+  if (name) *name = fk::g_prof_classes[i].name.c_str();
+  if (launches) *launches = fk::g_prof_classes[i].launches;
+  if (total_ms) *total_ms = fk::g_prof_classes[i].ms;
+  return FK_OK;
+}
 
 extern "C" const char* fk_status_string(fk_status s) {
   switch (s) {
