@@ -222,6 +222,24 @@ fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t
 fk_status fk_gemm_bf16(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
                        int32_t y_fp32, void* stream);
 
+/* Decode attention of one query per sequence ("N7 · model/forward-parity",
+ * Thm 1: causal GQA attention; "pegainfer #878": sliding-window layers).
+ *   d_q:      bf16 [batch][n_q_heads*head_dim], the query at position ctx-1
+ *   d_kcache, d_vcache: bf16 [batch][n_kv_heads][cap][head_dim], keys/values
+ *             at positions 0..ctx-1 (RoPE already applied to the keys)
+ *   window:   0 = attend to all ctx keys; W > 0 = only the last W
+ *   d_out:    bf16 [batch][n_q_heads*head_dim]
+ * Query head h reads kv head h / (n_q_heads/n_kv_heads); scale 1/sqrt(head_dim).
+ * Split-KV: partial results go to d_scratch (fp32, at least
+ * fk_attention_decode_scratch_bytes(...) bytes, 16-byte aligned) and are
+ * merged in a fixed order, so results are bitwise reproducible.
+ * head_dim is 64, 128 or 256; 1..8 query heads per kv head; 1 <= ctx <= cap. */
+size_t fk_attention_decode_scratch_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                         int32_t ctx);
+fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
+                              int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap, int32_t ctx,
+                              int32_t window, void* d_scratch, size_t scratch_bytes, void* d_out, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Kernel timing (tracing)
  * When enabled, every kernel launch of the entry points above is bracketed by

@@ -76,6 +76,9 @@ _SIGS = {
     "fk_session_length": (c_int32, [c_void_p]),
     "fk_sync_status": (c_int32, [c_void_p, c_void_p, c_int32, POINTER(c_uint32)]),
     "fk_gemm_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p]),
+    "fk_attention_decode_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
+    "fk_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                      c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
     "fk_profile_enable": (None, [c_int32]),
     "fk_profile_reset": (None, []),
     "fk_profile_count": (c_int32, []),
@@ -161,6 +164,23 @@ def gemm(x, w, out_fp32: bool = False, out=None, stream=None):
         out = torch.empty((P, N), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=x.device)
     _check(fk_gemm_bf16(_ptr(x), _ptr(w), P, K, N, _ptr(out), 1 if out_fp32 else 0, _stream_ptr(stream)),
            "fk_gemm_bf16")
+    return out
+
+
+def attention_decode(q, kcache, vcache, ctx: int, window: int = 0, out=None, scratch=None, stream=None):
+    """One decode-attention step (q [B, Hq*hd], caches [B, Hkv, cap, hd], bf16)."""
+    import torch
+    B, Hkv, cap, hd = kcache.shape
+    Hq = q.shape[1] // hd
+    lib = load()
+    nbytes = lib.fk_attention_decode_scratch_bytes(B, Hq, Hkv, hd, ctx)
+    if scratch is None:
+        scratch = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib.fk_attention_decode(_ptr(q), _ptr(kcache), _ptr(vcache), B, Hq, Hkv, hd, cap, ctx, window,
+                                   _ptr(scratch), scratch.numel(), _ptr(out), _stream_ptr(stream)),
+           "fk_attention_decode")
     return out
 
 

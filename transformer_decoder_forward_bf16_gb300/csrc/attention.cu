@@ -438,3 +438,70 @@ cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, 
 }
 
 }  // namespace fk
+
+// ---------------------------------------------------------------------------
+// op-level entry point: one decode-attention step over a caller's KV cache
+// ---------------------------------------------------------------------------
+#include "fk_internal.h"
+
+namespace {
+fk_status check_decode_args(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int hd, int cap,
+                            int ctx, int window, const void* out) {
+  using fk::fail;
+  if (!q || !kc || !vc || !out) return fail(FK_ERR_INVALID_ARG, "attention decode: null pointer");
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > 8)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: need batch >= 1 and 1..8 query heads per kv head");
+  if (hd != 64 && hd != 128 && hd != 256) return fail(FK_ERR_INVALID_ARG, "attention decode: head_dim 64/128/256");
+  if (ctx < 1 || ctx > cap || window < 0) return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: q and caches must be 16-byte aligned");
+  return FK_OK;
+}
+}  // namespace
+
+namespace fk {
+// shared by the scratch-taking and the allocation-free entry points
+fk_status attention_decode_plan(int B, int Hq, int Hkv, int hd, int ctx, int* chunk, int* splits, size_t* bytes) {
+  int sms = 0;
+  fk_status s = check_device(&sms);
+  if (s != FK_OK) return s;
+  *splits = decode_attention_splits(B, Hkv, ctx, sms, chunk);
+  *bytes = decode_attention_scratch_bytes(B, Hq, hd, *splits);
+  return FK_OK;
+}
+fk_status attention_decode_run(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int hd, int cap,
+                               int ctx, int window, int chunk, int splits, void* scratch, void* out,
+                               cudaStream_t st) {
+  cudaError_t e = launch_attention_decode(q, Hq * hd, kc, vc, cap, B, ctx, nullptr, Hq, Hkv, hd, window,
+                                          1.0f / sqrtf((float)hd), chunk, splits, scratch, out, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention decode launch");
+  return FK_OK;
+}
+}  // namespace fk
+
+extern "C" size_t fk_attention_decode_scratch_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
+                                                    int32_t head_dim, int32_t ctx) {
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || ctx < 1) return 0;
+  int chunk = 0, splits = 0;
+  size_t bytes = 0;
+  if (fk::attention_decode_plan(batch, n_q_heads, n_kv_heads, head_dim, ctx, &chunk, &splits, &bytes) != FK_OK)
+    return 0;
+  return bytes;
+}
+
+extern "C" fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
+                                         int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
+                                         int32_t ctx, int32_t window, void* d_scratch, size_t scratch_bytes,
+                                         void* d_out, void* stream) {
+  fk_status s = check_decode_args(d_q, d_kcache, d_vcache, batch, n_q_heads, n_kv_heads, head_dim, cap, ctx, window,
+                                  d_out);
+  if (s != FK_OK) return s;
+  int chunk = 0, splits = 0;
+  size_t need = 0;
+  s = fk::attention_decode_plan(batch, n_q_heads, n_kv_heads, head_dim, ctx, &chunk, &splits, &need);
+  if (s != FK_OK) return s;
+  if (!d_scratch || scratch_bytes < need) return fk::fail(FK_ERR_WORKSPACE, "attention decode: scratch too small");
+  if (reinterpret_cast<uintptr_t>(d_scratch) & 15) return fk::fail(FK_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
+  return fk::attention_decode_run(d_q, d_kcache, d_vcache, batch, n_q_heads, n_kv_heads, head_dim, cap, ctx, window,
+                                  chunk, splits, d_scratch, d_out, static_cast<cudaStream_t>(stream));
+}
