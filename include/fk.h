@@ -240,6 +240,24 @@ fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void*
                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap, int32_t ctx,
                               int32_t window, void* d_scratch, size_t scratch_bytes, void* d_out, void* stream);
 
+/* Allocation-free fk_attention_decode. The pages have no counterpart: this
+ * entry point serves callers that cannot provide a scratch buffer (their
+ * device memory belongs to another allocator, or their path must not enter
+ * the driver's allocation code). Arguments and results are those of
+ * fk_attention_decode; the split-KV partials live in a fixed array inside the
+ * library's device image, fk_attention_decode_noalloc_limit() bytes (4 MiB)
+ * per device, reserved by every GPU that loads the library until exit.
+ * Calls whose partials exceed it return FK_ERR_WORKSPACE before launching.
+ * The first call on a device looks up the array's address (make it before
+ * any stream capture on that device). All calls share the array and it keeps
+ * the previous call's contents (nothing needs to start at zero); calls whose
+ * kernels overlap on the GPU race on it and must be serialised. Calls no
+ * allocator of any kind. */
+size_t fk_attention_decode_noalloc_limit(void);
+fk_status fk_attention_decode_noalloc(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
+                                      int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
+                                      int32_t ctx, int32_t window, void* d_out, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Kernel timing (tracing)
  * When enabled, every kernel launch of the entry points above is bracketed by

@@ -79,6 +79,9 @@ _SIGS = {
     "fk_attention_decode_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "fk_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "fk_attention_decode_noalloc_limit": (c_size_t, []),
+    "fk_attention_decode_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                              c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "fk_profile_enable": (None, [c_int32]),
     "fk_profile_reset": (None, []),
     "fk_profile_count": (c_int32, []),
