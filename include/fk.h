@@ -222,6 +222,15 @@ fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t
 fk_status fk_gemm_bf16(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
                        int32_t y_fp32, void* stream);
 
+/* The same product for few rows (1 <= P <= 64, the decode and short-prompt
+ * regime) on the weight-streaming kernel: the weight tile is the 128-row side
+ * of the tensor-core MMA, K is split across CTAs, and the fp32 partial sums
+ * (d_scratch, fk_gemm_bf16_splitk_scratch_bytes(P, K, N) bytes) are added in
+ * a fixed order, so results are bitwise reproducible. */
+size_t fk_gemm_bf16_splitk_scratch_bytes(int32_t P, int32_t K, int32_t N);
+fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
+                              int32_t y_fp32, void* d_scratch, size_t scratch_bytes, void* stream);
+
 /* Decode attention of one query per sequence ("N7 · model/forward-parity",
  * Thm 1: causal GQA attention; "pegainfer #878": sliding-window layers).
  *   d_q:      bf16 [batch][n_q_heads*head_dim], the query at position ctx-1

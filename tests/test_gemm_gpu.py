@@ -79,3 +79,20 @@ def test_gemm_rejects_bad_args(fk):
     with pytest.raises(fk.FkError) as ei:
         fk.gemm(x, w)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("P,K,N", [(1, 64, 8), (9, 576, 960), (16, 64, 96), (32, 4096, 6144), (32, 14336, 4096),
+                                   (64, 512, 256), (5, 1000, 520), (33, 4096, 128256)])
+@pytest.mark.parametrize("fp32", [True, False])
+def test_gemm_splitk(fk, P, K, N, fp32):
+    """The few-row weight-streaming kernel (decode shapes), same gates as above."""
+    import torch
+    x, w = _inputs(P, K, N, s=3)
+    y = fk.gemm_splitk(to_dev_bf16(x), to_dev_bf16(w), out_fp32=fp32)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(oracle.bf16_to_f64(x), oracle.bf16_to_f64(w))
+    e = err_scale(y.float().cpu().numpy(), ref)
+    assert e < (2e-5 if fp32 else 6e-3), e
+    y2 = fk.gemm_splitk(to_dev_bf16(x), to_dev_bf16(w), out_fp32=fp32)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)  # ordered split reduction: bitwise replay

@@ -76,6 +76,9 @@ _SIGS = {
     "fk_session_length": (c_int32, [c_void_p]),
     "fk_sync_status": (c_int32, [c_void_p, c_void_p, c_int32, POINTER(c_uint32)]),
     "fk_gemm_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p]),
+    "fk_gemm_bf16_splitk_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
+    "fk_gemm_bf16_splitk": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p,
+                                      c_size_t, c_void_p]),
     "fk_attention_decode_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "fk_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -167,6 +170,21 @@ def gemm(x, w, out_fp32: bool = False, out=None, stream=None):
         out = torch.empty((P, N), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=x.device)
     _check(fk_gemm_bf16(_ptr(x), _ptr(w), P, K, N, _ptr(out), 1 if out_fp32 else 0, _stream_ptr(stream)),
            "fk_gemm_bf16")
+    return out
+
+
+def gemm_splitk(x, w, out_fp32: bool = False, out=None, stream=None):
+    """Y = X · Wᵀ for few rows (P <= 64) on the weight-streaming split-K kernel."""
+    import torch
+    P, K = x.shape
+    N = w.shape[0]
+    lib = load()
+    nbytes = lib.fk_gemm_bf16_splitk_scratch_bytes(P, K, N)
+    scratch = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((P, N), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=x.device)
+    _check(lib.fk_gemm_bf16_splitk(_ptr(x), _ptr(w), P, K, N, _ptr(out), 1 if out_fp32 else 0, _ptr(scratch),
+                                   scratch.numel(), _stream_ptr(stream)), "fk_gemm_bf16_splitk")
     return out
 
 

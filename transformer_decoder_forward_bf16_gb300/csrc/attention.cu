@@ -231,106 +231,202 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
 // ---------------------------------------------------------------------------
 // decode
 // ---------------------------------------------------------------------------
+// One CTA per (key chunk, kv head, sequence). The query heads of the GQA group
+// (<= 8) form the 16 MMA rows (rows >= group are zero); each of the 4 warps
+// takes 16 keys of every 64-key tile, keeps its own online-softmax state, and
+// the warps are merged in shared memory at the end. K/V tiles stream through
+// an NST-deep cp.async ring, so each CTA keeps NST-1 tiles in flight.
 constexpr int kDecThreads = 128;
-constexpr int kMaxChunk = 1024;
 constexpr int kMaxGroup = 8;
+constexpr int kDecTile = 64;
+
+template <int HD>
+struct DecCfg {
+  static constexpr int NST = HD == 256 ? 3 : (HD == 128 ? 3 : 4);
+  static constexpr int TILE_ELEMS = kDecTile * HD;
+  static constexpr int SMEM = (16 * HD + NST * 2 * TILE_ELEMS) * 2;
+};
 
 template <int HD>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ q, int ldq, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, int cap, int ctx_host, const int* d_ctx, int Hq, int Hkv, int window,
     float scale_log2, int chunk, int n_splits, float* __restrict__ part_o, float* __restrict__ part_ml) {
-  constexpr int TPK = HD / 8;               // threads per key row (16-byte loads)
-  constexpr int KPP = kDecThreads / TPK;    // keys per pass
-  __shared__ float sq[kMaxGroup][HD];
-  __shared__ float sc[kMaxGroup][kMaxChunk];
-  __shared__ float sred[KPP][HD];
-  __shared__ float sm_m[kMaxGroup], sm_l[kMaxGroup];
+  using C = DecCfg<HD>;
+  extern __shared__ uint4 smem_u4[];
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_u4);
+  __nv_bfloat16* sKV = sQ + 16 * HD;  // [NST][K tile, V tile]
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int group = Hq / Hkv;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ctx = d_ctx ? *d_ctx : ctx_host;
   const int qpos = ctx - 1;
   int lo = split * chunk;
   const int hi = min(ctx, lo + chunk);
   if (window > 0) lo = max(lo, qpos - window + 1);
   const int n = max(0, hi - lo);
+  const int ntiles = (n + kDecTile - 1) / kDecTile;
   const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
+  const __nv_bfloat16* kbase = kc + head_off;
+  const __nv_bfloat16* vbase = vc + head_off;
+  constexpr int CPR = HD / 8;
 
+  for (int i = tid; i < 16 * CPR; i += kDecThreads) {
+    const int r = i / CPR, cc = i % CPR;
+    const __nv_bfloat16* src = q + (size_t)b * ldq + (size_t)(g * group + min(r, group - 1)) * HD + cc * 8;
+    cp_async16(sQ + swz<HD>(r, cc * 8), src, r < group ? 16 : 0);
+  }
+  auto load_tile = [&](int t, int buf) {
+    __nv_bfloat16* dk = sKV + (size_t)buf * 2 * C::TILE_ELEMS;
+    __nv_bfloat16* dv = dk + C::TILE_ELEMS;
+    for (int i = tid; i < kDecTile * CPR; i += kDecThreads) {
+      const int r = i / CPR, cc = i % CPR;
+      const int kp = lo + t * kDecTile + r;
+      const int ok = kp < hi ? 16 : 0;
+      const size_t off = (size_t)min(kp, hi - 1) * HD + cc * 8;
+      cp_async16(dk + swz<HD>(r, cc * 8), kbase + off, ok);
+      cp_async16(dv + swz<HD>(r, cc * 8), vbase + off, ok);
+    }
+  };
+  cp_async_commit();  // Q
+#pragma unroll
+  for (int t = 0; t < C::NST - 1; ++t) {
+    if (t < ntiles) load_tile(t, t);
+    cp_async_commit();
+  }
+
+  float oacc[HD / 8][4];
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int mat = lane >> 3, mr = lane & 7;
+
+  for (int t = 0; t < ntiles; ++t) {
+    cp_async_wait<C::NST - 2>();
+    __syncthreads();
+    {
+      const int tn = t + C::NST - 1;
+      if (tn < ntiles) load_tile(tn, tn % C::NST);
+      cp_async_commit();
+    }
+    const __nv_bfloat16* tK = sKV + (size_t)(t % C::NST) * 2 * C::TILE_ELEMS;
+    const __nv_bfloat16* tV = tK + C::TILE_ELEMS;
+    const int kr = warp * 16;  // this warp's 16 keys of the tile
+    float s[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < HD; k0 += 16) {
+      uint32_t a[4], bb[4];
+      ldsm_x4(a, sQ + swz<HD>(mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
+      ldsm_x4(bb, tK + swz<HD>(kr + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
+      mma_bf16_16816(s[0], a, bb[0], bb[1]);
+      mma_bf16_16816(s[1], a, bb[2], bb[3]);
+    }
+    const int key0 = lo + t * kDecTile + kr + 2 * (lane & 3);
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = key0 + nt * 8 + (e & 1) < hi;
+        s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
+      }
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
+    m0 = mn0;
+    m1 = mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - base0);
+      s[nt][1] = exp2f(s[nt][1] - base0);
+      s[nt][2] = exp2f(s[nt][2] - base1);
+      s[nt][3] = exp2f(s[nt][3] - base1);
+      rs0 += s[nt][0] + s[nt][1];
+      rs1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * corr0 + rs0;
+    l1 = l1 * corr1 + rs1;
+    uint32_t a[4];
+    a[0] = pack_bf16x2(s[0][0], s[0][1]);
+    a[1] = pack_bf16x2(s[0][2], s[0][3]);
+    a[2] = pack_bf16x2(s[1][0], s[1][1]);
+    a[3] = pack_bf16x2(s[1][2], s[1][3]);
+#pragma unroll
+    for (int dp = 0; dp < HD / 16; ++dp) {
+      oacc[2 * dp][0] *= corr0;
+      oacc[2 * dp][1] *= corr0;
+      oacc[2 * dp][2] *= corr1;
+      oacc[2 * dp][3] *= corr1;
+      oacc[2 * dp + 1][0] *= corr0;
+      oacc[2 * dp + 1][1] *= corr0;
+      oacc[2 * dp + 1][2] *= corr1;
+      oacc[2 * dp + 1][3] *= corr1;
+      uint32_t bb[4];
+      ldsm_x4_t(bb, tV + swz<HD>(kr + mr + (mat & 1) * 8, dp * 16 + (mat >> 1) * 8));
+      mma_bf16_16816(oacc[2 * dp], a, bb[0], bb[1]);
+      mma_bf16_16816(oacc[2 * dp + 1], a, bb[2], bb[3]);
+    }
+  }
+  cp_async_wait<0>();
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  __syncthreads();  // the K/V ring is free: reuse it for the cross-warp merge
+  float* sO = reinterpret_cast<float*>(sKV);  // [4 warps][16 rows][HD]
+  float* sM = sO + 4 * 16 * HD;               // [4][16]
+  float* sL = sM + 64;
+  const int r0 = lane >> 2, r1 = r0 + 8;
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) {
+    const int col = dt * 8 + 2 * (lane & 3);
+    sO[(warp * 16 + r0) * HD + col] = oacc[dt][0];
+    sO[(warp * 16 + r0) * HD + col + 1] = oacc[dt][1];
+    sO[(warp * 16 + r1) * HD + col] = oacc[dt][2];
+    sO[(warp * 16 + r1) * HD + col + 1] = oacc[dt][3];
+  }
+  if ((lane & 3) == 0) {
+    sM[warp * 16 + r0] = m0;
+    sM[warp * 16 + r1] = m1;
+    sL[warp * 16 + r0] = l0;
+    sL[warp * 16 + r1] = l1;
+  }
+  __syncthreads();
   for (int i = tid; i < group * HD; i += kDecThreads) {
-    const int hh = i / HD, d = i % HD;
-    sq[hh][d] = __bfloat162float(q[(size_t)b * ldq + (size_t)(g * group + hh) * HD + d]);
-  }
-  __syncthreads();
-
-  // scores
-  const int part = tid % TPK, kk = tid / TPK;
-  for (int j0 = 0; j0 < n; j0 += KPP) {  // uniform trip count: every lane joins the shuffles
-    const int j = j0 + kk;
-    const bool valid = j < n;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) u = *reinterpret_cast<const uint4*>(kc + head_off + (size_t)(lo + j) * HD + part * 8);
-    float kv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                   bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
-    for (int hh = 0; hh < group; ++hh) {
-      float acc = 0.f;
+    const int r = i / HD, d = i % HD;
+    float M = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc += sq[hh][part * 8 + e] * kv[e];
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sM[w * 16 + r]);
+    float L = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
-      for (int off = TPK / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (part == 0 && valid) sc[hh][j] = acc * scale_log2;
+      for (int w = 0; w < 4; ++w) {
+        const float mw = sM[w * 16 + r];
+        if (mw != -INFINITY) {
+          const float f = exp2f(mw - M);
+          L += sL[w * 16 + r] * f;
+          acc += sO[(w * 16 + r) * HD + d] * f;
+        }
+      }
     }
-  }
-  __syncthreads();
-  // softmax statistics per head (one warp per head)
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int hh = warp; hh < group; hh += kDecThreads / 32) {
-    float mx = -INFINITY;
-    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sc[hh][j]);
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int j = lane; j < n; j += 32) {
-      const float p = exp2f(sc[hh][j] - mx);
-      sc[hh][j] = p;
-      sum += p;
+    const int h = g * group + r;
+    const size_t base = ((size_t)b * Hq + h) * n_splits + split;
+    part_o[base * HD + d] = acc;
+    if (d == 0) {
+      part_ml[base * 2] = M;
+      part_ml[base * 2 + 1] = L;
     }
-    sum = warp_sum(sum);
-    if (lane == 0) {
-      sm_m[hh] = n > 0 ? mx : -INFINITY;
-      sm_l[hh] = sum;
-    }
-  }
-  __syncthreads();
-  // weighted values: thread (key slot kk, column chunk part)
-  for (int hh = 0; hh < group; ++hh) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = kk; j < n; j += KPP) {
-      const uint4 u = *reinterpret_cast<const uint4*>(vc + head_off + (size_t)(lo + j) * HD + part * 8);
-      const float p = sc[hh][j];
-      acc[0] += p * bf16_lo(u.x);
-      acc[1] += p * bf16_hi(u.x);
-      acc[2] += p * bf16_lo(u.y);
-      acc[3] += p * bf16_hi(u.y);
-      acc[4] += p * bf16_lo(u.z);
-      acc[5] += p * bf16_hi(u.z);
-      acc[6] += p * bf16_lo(u.w);
-      acc[7] += p * bf16_hi(u.w);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sred[kk][part * 8 + e] = acc[e];
-    __syncthreads();
-    const int h = g * group + hh;
-    const size_t base = (((size_t)b * Hq + h) * n_splits + split);
-    for (int d = tid; d < HD; d += kDecThreads) {
-      float s = 0.f;
-      for (int r = 0; r < KPP; ++r) s += sred[r][d];
-      part_o[base * HD + d] = s;
-    }
-    if (tid == 0) {
-      part_ml[base * 2] = sm_m[hh];
-      part_ml[base * 2 + 1] = sm_l[hh];
-    }
-    __syncthreads();
   }
 }
 
@@ -394,49 +490,50 @@ size_t decode_attention_scratch_bytes(int B, int Hq, int hd, int max_splits) {
 }
 
 int decode_attention_splits(int B, int Hkv, int max_ctx, int sm_count, int* chunk) {
-  long target = 2L * sm_count;
+  const long target = 4L * sm_count;
   long c = ((long)max_ctx * B * Hkv + target - 1) / target;
-  c = (c + 63) / 64 * 64;
-  c = std::max(64L, std::min((long)kMaxChunk, c));
+  c = (c + kDecTile - 1) / kDecTile * kDecTile;
+  c = std::max((long)kDecTile, c);
   *chunk = (int)c;
   return (int)((max_ctx + c - 1) / c);
+}
+
+template <int HD>
+cudaError_t decode_hd(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int ctx,
+                      const int* d_ctx, int Hq, int Hkv, int window, float sl, int chunk, int n_splits, float* part_o,
+                      float* part_ml, void* o, cudaStream_t st) {
+  using C = DecCfg<HD>;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(attn_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (err != cudaSuccess) return err;
+  dim3 grid(n_splits, Hkv, B);
+  attn_decode_kernel<HD><<<grid, kDecThreads, C::SMEM, st>>>(
+      static_cast<const __nv_bfloat16*>(q), ldq, static_cast<const __nv_bfloat16*>(kcache),
+      static_cast<const __nv_bfloat16*>(vcache), cap, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o,
+      part_ml);
+  attn_combine_kernel<HD><<<dim3(Hq, B), HD < 128 ? HD : 128, 0, st>>>(part_o, part_ml, Hq, n_splits,
+                                                                      static_cast<__nv_bfloat16*>(o));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
                                     int ctx, const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
                                     int chunk, int n_splits, void* scratch, void* o, cudaStream_t st) {
   if (B == 0) return cudaSuccess;
-  if (Hq / Hkv > kMaxGroup || chunk > kMaxChunk) return cudaErrorInvalidValue;
+  if (Hq / Hkv > kMaxGroup || chunk % kDecTile) return cudaErrorInvalidValue;
   float* part_o = static_cast<float*>(scratch);
   float* part_ml = part_o + (size_t)B * Hq * n_splits * hd;
-  dim3 grid(n_splits, Hkv, B);
-  auto* qq = static_cast<const __nv_bfloat16*>(q);
-  auto* kc = static_cast<const __nv_bfloat16*>(kcache);
-  auto* vc = static_cast<const __nv_bfloat16*>(vcache);
-  auto* oo = static_cast<__nv_bfloat16*>(o);
   const float sl = scale * kLog2e;
   switch (hd) {
-    case 64:
-      attn_decode_kernel<64><<<grid, kDecThreads, 0, st>>>(qq, ldq, kc, vc, cap, ctx, d_ctx, Hq, Hkv, window, sl,
-                                                           chunk, n_splits, part_o, part_ml);
-      attn_combine_kernel<64><<<dim3(Hq, B), 64, 0, st>>>(part_o, part_ml, Hq, n_splits, oo);
-      break;
-    case 128:
-      attn_decode_kernel<128><<<grid, kDecThreads, 0, st>>>(qq, ldq, kc, vc, cap, ctx, d_ctx, Hq, Hkv, window, sl,
-                                                            chunk, n_splits, part_o, part_ml);
-      attn_combine_kernel<128><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, Hq, n_splits, oo);
-      break;
-    case 256:
-      attn_decode_kernel<256><<<grid, kDecThreads, 0, st>>>(qq, ldq, kc, vc, cap, ctx, d_ctx, Hq, Hkv, window, sl,
-                                                            chunk, n_splits, part_o, part_ml);
-      attn_combine_kernel<256><<<dim3(Hq, B), 128, 0, st>>>(part_o, part_ml, Hq, n_splits, oo);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+    case 64: return decode_hd<64>(q, ldq, kcache, vcache, cap, B, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml, o, st);
+    case 128: return decode_hd<128>(q, ldq, kcache, vcache, cap, B, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml, o, st);
+    case 256: return decode_hd<256>(q, ldq, kcache, vcache, cap, B, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml, o, st);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
-
 }  // namespace fk
 
 // ---------------------------------------------------------------------------

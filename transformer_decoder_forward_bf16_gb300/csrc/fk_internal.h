@@ -79,8 +79,21 @@ struct GemmOut {
   int act = 0;             // GLU activation: 0 SiLU, 1 GELU (tanh form)
 };
 
-// A: bf16 [M, K] with row stride lda (elements, multiple of 8).
+// A: bf16 [M, K] with row stride lda (elements, multiple of 8). With M <=
+// kSkinnyMaxTokens and a large enough scratch buffer (skinny_scratch_bytes)
+// the weight-streaming split-K kernel runs instead of the tiled one.
 fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
-                   cudaStream_t st);
+                   cudaStream_t st, void* scratch = nullptr, size_t scratch_bytes = 0);
+
+// Skinny (few-token) GEMM: swap-AB tcgen05 split-K + ordered reduction.
+constexpr int kSkinnyMaxTokens = 64;
+struct SkinnyPlan {
+  int splits = 1, kb_per_split = 1, n_tiles = 1, nk = 1;
+  size_t part_bytes = 0;
+};
+SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count);
+size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count);
+fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
+                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st);
 
 }  // namespace fk

@@ -1,0 +1,325 @@
+// Skinny GEMM for few tokens (decode, short prompts): out = epilogue(X · Wᵀ)
+// with X [M <= 64, K] and a weight operand of up to three stacked matrices.
+//
+// The contraction is the projection of "N7 · model/forward-parity", Thm 1 (and
+// "N9 · metalgemm", Thm 1: Y = X·Wᵀ); at M <= 64 it is bound by streaming the
+// weights from HBM, so the kernel is laid out for bandwidth:
+//   * operands swapped: the weight tile (128 output features x 64 K) is the
+//     M=128 side of tcgen05.mma and the tokens are the N side (16/32/64), so
+//     TMEM lane = output feature and column = token;
+//   * split-K over a 2-D grid (feature tiles x K splits) sized to put about
+//     four CTAs on every SM, each streaming its weight slab through a 4-deep
+//     TMA ring (2 CTAs per SM => ~128 KB of loads in flight per SM);
+//   * fp32 partial sums per split, then one reduction kernel that adds the
+//     splits in a fixed order (bitwise-reproducible) and applies the fused
+//     epilogue (bf16 store, fp32 + softcap, fp32 residual add, or the gated
+//     FFN activation act(gate) * up).
+#include <algorithm>
+#include <mutex>
+
+#include "fk_common.cuh"
+#include "fk_internal.h"
+
+namespace fk {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kStages = 4;
+constexpr int A_BYTES = 128 * 64 * 2;
+
+struct SkinnyArgs {
+  int M, K, n_rows, nseg;
+  int seg_start[4];
+  int kb_per_split, nk;
+  float* part;  // [splits][M][n_rows]
+  unsigned* dev_err;
+};
+
+template <int BT>
+struct SCfg {
+  static constexpr int B_BYTES = BT * 64 * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int SMEM = kStages * STAGE + 1024 + 256;
+  static constexpr uint32_t TMEM_COLS = BT < 32 ? 32 : BT;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(128, BT);
+};
+
+template <int BT>
+__global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                           const __grid_constant__ CUtensorMap tmW0,
+                                                           const __grid_constant__ CUtensorMap tmW1,
+                                                           const __grid_constant__ CUtensorMap tmW2,
+                                                           const SkinnyArgs args) {
+  using C = SCfg<BT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::STAGE);
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * 128;
+  const int split = blockIdx.y;
+  const int kb0 = split * args.kb_per_split;
+  const int kb1 = min(args.nk, kb0 + args.kb_per_split);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW0);
+    if (args.nseg > 1) tma_prefetch_desc(&tmW1);
+    if (args.nseg > 2) tma_prefetch_desc(&tmW2);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: two 64-row weight boxes + one token box per stage
+    const CUtensorMap* maps[3] = {&tmW0, &tmW1, &tmW2};
+    int map[2], row[2];
+    bool valid[2];
+    uint32_t bytes = C::B_BYTES;
+    for (int i = 0; i < 2; ++i) {
+      const int v = n0 + i * 64;
+      int m = 0;
+      if (args.nseg > 1 && v >= args.seg_start[1]) m = 1;
+      if (args.nseg > 2 && v >= args.seg_start[2]) m = 2;
+      map[i] = m;
+      row[i] = v - args.seg_start[m];
+      valid[i] = v < args.n_rows;
+      if (valid[i]) bytes += 64 * 64 * 2;
+    }
+    const uint64_t evict_first = l2_policy_evict_first();
+    int issued[kStages] = {0, 0, 0, 0};
+    bool ok = true;
+    for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
+      const int stage = it % kStages;
+      const uint32_t phase = (it / kStages) & 1;
+      if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.dev_err)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = smem + stage * C::STAGE;
+      mbar_arrive_expect_tx(&full[stage], bytes);
+      for (int i = 0; i < 2; ++i)
+        if (valid[i])
+          tma_load_2d_hint(maps[map[i]], &full[stage], sa + i * 64 * 128, kb * 64, row[i], evict_first);
+      tma_load_2d(&tmX, &full[stage], sa + A_BYTES, kb * 64, 0);
+      ++issued[stage];
+    }
+    if (!ok) {
+      for (int s = 0; s < kStages; ++s) {
+        if (issued[s] == 0) continue;
+        const uint32_t a = smem_u32(&full[s]);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(a, (issued[s] - 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
+      const int stage = it % kStages;
+      const uint32_t phase = (it / kStages) & 1;
+      if (!mbar_wait(&full[stage], phase, abort_flag, args.dev_err)) break;
+      tc_fence_after();
+      uint8_t* sa = smem + stage * C::STAGE;
+      const uint64_t ad = smem_desc_sw128(sa);
+      const uint64_t bd = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) umma_bf16(tmem, ad + 2 * k, bd + 2 * k, C::IDESC, (it | k) != 0 ? 1u : 0u);
+      umma_commit(&empty[stage]);
+    }
+    umma_commit(done);
+  }
+  __syncwarp();
+  // ---- epilogue: every warp drains its 32 TMEM lanes (= 32 output features)
+  const bool have = mbar_wait(done, 0, abort_flag, args.dev_err);
+  tc_fence_after();
+  const int feat = n0 + warp * 32 + lane;
+  float* part = args.part + (size_t)split * args.M * args.n_rows;
+#pragma unroll
+  for (int c0 = 0; c0 < (BT < 32 ? 32 : BT); c0 += 32) {
+    float v[32];
+    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+    if (have && feat < args.n_rows && kb1 > kb0) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < args.M) part[(size_t)(c0 + j) * args.n_rows + feat] = v[j];
+    } else if (have && feat < args.n_rows) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < args.M) part[(size_t)(c0 + j) * args.n_rows + feat] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
+FK_DEVICE float act_gelu_tanh(float g) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+}
+
+// Sum the splits in order and apply the epilogue; one thread per (token, 4 features).
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int S, int M, int n_rows, int n_out, int epi,
+                                     int act, void* out, int ldo, const float* res, int ldr, float softcap) {
+  const int per_row = (n_out + 3) / 4;
+  const long total = (long)M * per_row;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per_row);
+    const int f = (int)(i % per_row) * 4;
+    const int nf = min(4, n_out - f);
+    float v[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < S; ++s) {
+      const float* p = part + ((size_t)s * M + t) * n_rows;
+      for (int j = 0; j < nf; ++j) v[j] += p[f + j];
+      if (epi == EPI_GLU_BF16)
+        for (int j = 0; j < nf; ++j) u[j] += p[n_out + f + j];
+    }
+    if (epi == EPI_GLU_BF16) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + (size_t)t * ldo + f;
+      for (int j = 0; j < nf; ++j) o[j] = __float2bfloat16_rn((act ? act_gelu_tanh(v[j]) : act_silu(v[j])) * u[j]);
+    } else if (epi == EPI_BF16) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + (size_t)t * ldo + f;
+      for (int j = 0; j < nf; ++j) o[j] = __float2bfloat16_rn(v[j]);
+    } else if (epi == EPI_ADD_F32) {
+      float* o = static_cast<float*>(out) + (size_t)t * ldo + f;
+      const float* r = res + (size_t)t * ldr + f;
+      for (int j = 0; j < nf; ++j) o[j] = r[j] + v[j];
+    } else {
+      float* o = static_cast<float*>(out) + (size_t)t * ldo + f;
+      if (softcap > 0.f) {
+        const float inv = 1.0f / softcap;
+        for (int j = 0; j < nf; ++j) o[j] = softcap * tanhf(v[j] * inv);
+      } else {
+        for (int j = 0; j < nf; ++j) o[j] = v[j];
+      }
+    }
+  }
+}
+
+template <int BT>
+fk_status launch_bt(const CUtensorMap& tX, const GemmWeights& w, const SkinnyArgs& a, int n_tiles, int splits,
+                    cudaStream_t st) {
+  using C = SCfg<BT>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (attr != cudaSuccess) return cuda_fail(attr, "cudaFuncSetAttribute(gemv)");
+  gemv_tc_kernel<BT><<<dim3(n_tiles, splits), kThreads, C::SMEM, st>>>(
+      tX, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0], w.nseg > 2 ? w.map[2] : w.map[0], a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "gemv_tc_kernel launch");
+  return FK_OK;
+}
+
+}  // namespace
+
+SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count) {
+  SkinnyPlan p;
+  const int nk = (K + 63) / 64;
+  const int n_tiles = (n_rows + 127) / 128;
+  int splits = std::max(1, std::min(nk, (4 * sm_count + n_tiles - 1) / n_tiles));
+  p.kb_per_split = (nk + splits - 1) / splits;
+  p.splits = (nk + p.kb_per_split - 1) / p.kb_per_split;
+  p.n_tiles = n_tiles;
+  p.nk = nk;
+  p.part_bytes = (size_t)p.splits * M * n_rows * sizeof(float);
+  return p;
+}
+
+size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count) {
+  if (M <= 0 || M > kSkinnyMaxTokens) return 0;
+  return skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count).part_bytes;
+}
+
+fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
+                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st) {
+  int sms = 0;
+  fk_status s = check_device(&sms);
+  if (s != FK_OK) return s;
+  const int n_rows = w.seg_start[w.nseg];
+  const SkinnyPlan p = skinny_plan(M, w.K, n_rows, sms);
+  if (!scratch || scratch_bytes < p.part_bytes) return fail(FK_ERR_WORKSPACE, "skinny GEMM scratch too small");
+  const int BT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  CUtensorMap tX;
+  s = make_tmap_bf16(&tX, A, M, w.K, lda, BT);
+  if (s != FK_OK) return s;
+  SkinnyArgs a{};
+  a.M = M;
+  a.K = w.K;
+  a.n_rows = n_rows;
+  a.nseg = w.nseg;
+  for (int i = 0; i < 4; ++i) a.seg_start[i] = w.seg_start[i];
+  a.kb_per_split = p.kb_per_split;
+  a.nk = p.nk;
+  a.part = static_cast<float*>(scratch);
+  a.dev_err = dev_err;
+  if (BT == 16)
+    s = launch_bt<16>(tX, w, a, p.n_tiles, p.splits, st);
+  else if (BT == 32)
+    s = launch_bt<32>(tX, w, a, p.n_tiles, p.splits, st);
+  else
+    s = launch_bt<64>(tX, w, a, p.n_tiles, p.splits, st);
+  if (s != FK_OK) return s;
+  const int n_out = w.glu ? w.n_out : n_rows;
+  const long work = (long)M * ((n_out + 3) / 4);
+  const int blocks = (int)std::min<long>((work + 255) / 256, 8L * sms);
+  splitk_reduce_kernel<<<blocks, 256, 0, st>>>(static_cast<const float*>(scratch), p.splits, M, n_rows, n_out, o.epi,
+                                               o.act, o.out, o.ldo, o.res, o.ldr, o.softcap);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "splitk_reduce_kernel launch");
+  return FK_OK;
+}
+
+}  // namespace fk
+
+extern "C" size_t fk_gemm_bf16_splitk_scratch_bytes(int32_t P, int32_t K, int32_t N) {
+  if (P < 1 || P > fk::kSkinnyMaxTokens || K < 8 || N < 8) return 0;
+  int sms = 0;
+  if (fk::check_device(&sms) != FK_OK) return 0;
+  return fk::skinny_plan(P, K, N, sms).part_bytes;
+}
+
+extern "C" fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
+                                         int32_t y_fp32, void* d_scratch, size_t scratch_bytes, void* stream) {
+  using namespace fk;
+  if (!d_x || !d_w || !d_y || P < 1 || P > kSkinnyMaxTokens || K <= 0 || N <= 0)
+    return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16_splitk: bad argument (1 <= P <= 64)");
+  if (K % 8 || N % 8) return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16_splitk: K and N must be multiples of 8");
+  if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_w) | reinterpret_cast<uintptr_t>(d_y) |
+       reinterpret_cast<uintptr_t>(d_scratch)) & 15)
+    return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16_splitk: buffers must be 16-byte aligned");
+  GemmWeights w;
+  const void* mats[1] = {d_w};
+  int rows[1] = {N};
+  fk_status s = gemm_weights_init(&w, mats, rows, 1, K, 0);
+  if (s != FK_OK) return s;
+  GemmOut o;
+  o.epi = y_fp32 ? EPI_F32 : EPI_BF16;
+  o.out = d_y;
+  o.ldo = N;
+  return gemm_run_skinny(d_x, P, K, w, o, d_scratch, scratch_bytes, nullptr, static_cast<cudaStream_t>(stream));
+}

@@ -39,6 +39,8 @@ struct Scratch {
   void* qkv = nullptr;     // [T, Nq + 2 Nkv] bf16
   void* ao = nullptr;      // [T, Nq] bf16 attention output
   void* h = nullptr;       // [T, I] bf16 gated FFN activations
+  void* gemv = nullptr;    // split-K partial sums of the few-token GEMMs
+  size_t gemv_bytes = 0;
 };
 
 }  // namespace
@@ -183,6 +185,19 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
   t.qkv = take((size_t)T * m->Nqkv * 2);
   t.ao = take((size_t)T * m->Nq * 2);
   t.h = take((size_t)T * c.intermediate * 2);
+  // few-token GEMMs (T <= 64, or decode/short chunks up to that size) need
+  // split-K scratch: the largest of the layer and head GEMMs
+  const int Ms = (int)std::min<long>(T, kSkinnyMaxTokens);
+  size_t gb = 0;
+  if (!m->g_qkv.empty()) {
+    gb = std::max(gb, skinny_scratch_bytes(m->g_qkv[0], Ms, m->sm_count));
+    gb = std::max(gb, skinny_scratch_bytes(m->g_o[0], Ms, m->sm_count));
+    gb = std::max(gb, skinny_scratch_bytes(m->g_gu[0], Ms, m->sm_count));
+    gb = std::max(gb, skinny_scratch_bytes(m->g_down[0], Ms, m->sm_count));
+    gb = std::max(gb, skinny_scratch_bytes(m->g_head, Ms, m->sm_count));
+  }
+  t.gemv_bytes = gb;
+  t.gemv = gb ? take(gb) : nullptr;
   if (s) *s = t;
   return off;
 }
@@ -216,6 +231,12 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   const long T = (long)B * S;
   const bool sandwich = c.norm_layout == FK_NORM_SANDWICH;
   float* x_in = slots ? slots : sc.x0;
+  // Layer GEMMs of decode steps stream weights through the split-K kernel.
+  // Prefill (any chunk size) keeps the tiled kernel, whose per-element
+  // summation order does not depend on the row count: chunked cached prefill
+  // then rounds every bf16 activation exactly as the cacheless forward does.
+  void* gv = decode ? sc.gemv : nullptr;
+  const size_t gvb = decode ? sc.gemv_bytes : 0;
   { ProfScope ps(decode ? "embed_norm_dec" : "embed_norm", st);
   FK_LAUNCH(launch_embed_norm(sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
                               x_in, sc.u, m->dev_err, st)); }
@@ -233,7 +254,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     o.epi = EPI_BF16;
     o.out = sc.qkv;
     o.ldo = m->Nqkv;
-    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st)); }
+    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb)); }
     { ProfScope ps(decode ? "rope_qkv_dec" : "rope_qkv", st);
     FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
                               m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
@@ -253,7 +274,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.out = sc.a;
       o.ldo = H;
       o.softcap = 0.f;
-      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st)); }
+      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb)); }
       ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_in, x_mid, (int)T, H, w.post_attn_norm, w.ffn_norm, c.rms_eps, sc.u,
                                           st));
@@ -263,7 +284,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.ldo = H;
       o.res = x_in;
       o.ldr = H;
-      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st)); }
+      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st));
     }
@@ -273,13 +294,13 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     og.out = sc.h;
     og.ldo = c.intermediate;
     og.act = c.act;
-    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st)); }
+    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st, gv, gvb)); }
     if (sandwich) {
       GemmOut od;
       od.epi = EPI_F32;
       od.out = sc.a;
       od.ldo = H;
-      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st)); }
+      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb)); }
       ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps, sc.u,
                                           st));
@@ -290,7 +311,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       od.ldo = H;
       od.res = x_mid;
       od.ldr = H;
-      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st)); }
+      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st));
     }
@@ -300,13 +321,14 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   return FK_OK;
 }
 
-fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* argmax, cudaStream_t st) {
+fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* argmax, const Scratch& sc,
+                   cudaStream_t st) {
   GemmOut o;
   o.epi = EPI_F32;
   o.out = logits;
   o.ldo = m->cfg.vocab;
   o.softcap = m->cfg.final_softcap;
-  { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st)); }
+  { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st, sc.gemv, sc.gemv_bytes)); }
   ProfScope ps("argmax", st);
   if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st));
   return FK_OK;
@@ -489,7 +511,7 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   FK_CUDA_TRY(cudaMemcpyAsync(sc.ids, ids, T * sizeof(int32_t),
                               ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
   FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, nullptr, 0, 0, st));
-  if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, st));
+  if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st));
   return FK_OK;
 }
 
@@ -572,7 +594,7 @@ extern "C" int32_t fk_session_length(const fk_session* s) { return s ? s->len : 
 static fk_status session_head(fk_session* s, const void* u_rows, float* d_logits, int32_t* d_next, cudaStream_t st) {
   fk_model* m = s->m;
   float* logits = d_logits ? d_logits : s->logits;
-  FK_TRY(run_head(m, u_rows, s->B, logits, s->next_ids, st));
+  FK_TRY(run_head(m, u_rows, s->B, logits, s->next_ids, s->sc, st));
   if (d_next) FK_CUDA_TRY(cudaMemcpyAsync(d_next, s->next_ids, s->B * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
   return FK_OK;
 }
