@@ -25,6 +25,13 @@ listed in the design notes):
 * Softcap z -> c * tanh(z / c) on the float logits, before argmax.
 * The embedding scale is bf16(sqrt(hidden)); the product stays in float.
 * Argmax ties go to the lowest index.
+
+``storage="bf16"`` evaluates the same definition with the values that the
+numerics contract stores in bf16 rounded to bf16 where they are stored (every
+norm output that feeds a projection, the projected q, k, v, q and k after
+QK-norm and RoPE, the attention output, the gated FFN activation and the LM
+head input). Arithmetic stays float64 and the attention probabilities stay
+unrounded. ``storage="exact"`` (the default) rounds nothing.
 """
 from __future__ import annotations
 
@@ -35,7 +42,7 @@ import numpy as np
 __all__ = [
     "bf16_to_f64", "round_to_bf16", "embed_scale", "rmsnorm", "rope_inv_freq", "rope_apply",
     "attention", "silu", "gelu_tanh", "softcap", "gemm", "OracleWeights", "forward", "Session",
-    "argmax_first", "top2_margin", "log_softmax", "topk_ids", "greedy",
+    "argmax_first", "top2_margin", "log_softmax", "topk_ids", "greedy", "store_bf16",
 ]
 
 
@@ -57,6 +64,22 @@ def round_to_bf16(v: float) -> float:
         return 0.0
     m, e = math.frexp(v)
     return math.ldexp(round(m * 256.0), e - 8)
+
+
+def store_bf16(x: np.ndarray) -> np.ndarray:
+    """Value of x after being stored as bf16: float64 -> float32 (nearest),
+    then the float32 bits rounded to the top 16 (nearest, ties to even)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _rounder(storage: str):
+    if storage == "exact":
+        return lambda x: x
+    if storage == "bf16":
+        return store_bf16
+    raise ValueError(storage)
 
 
 # ---------------------------------------------------------------------------
@@ -211,7 +234,7 @@ class OracleWeights:
 # ---------------------------------------------------------------------------
 # Decoder layer and forward
 # ---------------------------------------------------------------------------
-def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k, past_v, past_pos):
+def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k, past_v, past_pos, R=lambda v: v):
     """One decoder layer on x [B, S, H] at positions pos [B, S].
 
     past_k/past_v [B, P, Hkv, hd] (P may be 0) are this layer's cached keys and
@@ -225,16 +248,16 @@ def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k
     kind = cfg.kinds()[l]
     window = cfg.sliding_window if kind == 1 else 0
 
-    u = rmsnorm(x, W[p + "attn_norm"], cfg.rms_eps)
-    q = W.linear(u, p + "wq").reshape(B, S, Hq, hd)
-    k = W.linear(u, p + "wk").reshape(B, S, Hkv, hd)
-    v = W.linear(u, p + "wv").reshape(B, S, Hkv, hd)
+    u = R(rmsnorm(x, W[p + "attn_norm"], cfg.rms_eps))
+    q = R(W.linear(u, p + "wq")).reshape(B, S, Hq, hd)
+    k = R(W.linear(u, p + "wk")).reshape(B, S, Hkv, hd)
+    v = R(W.linear(u, p + "wv")).reshape(B, S, Hkv, hd)
     if cfg.qk_norm:
         q = rmsnorm(q, W[p + "q_norm"], cfg.rms_eps)
         k = rmsnorm(k, W[p + "k_norm"], cfg.rms_eps)
     f = rope_inv_freq(cfg, kind)
-    q = rope_apply(q, pos, f)
-    k = rope_apply(k, pos, f)
+    q = R(rope_apply(q, pos, f))
+    k = R(rope_apply(k, pos, f))
 
     keys = np.concatenate([past_k, k], axis=1)
     vals = np.concatenate([past_v, v], axis=1)
@@ -242,16 +265,16 @@ def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k
     o = np.empty((B, S, Hq, hd), dtype=np.float64)
     for b in range(B):
         o[b] = attention(q[b], keys[b], vals[b], pos[b], kpos[b], window, 1.0 / math.sqrt(hd))
-    a = W.linear(o.reshape(B, S, Hq * hd), p + "wo")
+    a = W.linear(R(o).reshape(B, S, Hq * hd), p + "wo")
     if cfg.norm_layout == "sandwich":
         a = rmsnorm(a, W[p + "post_attn_norm"], cfg.rms_eps)
     x = x + a
 
-    u = rmsnorm(x, W[p + "ffn_norm"], cfg.rms_eps)
+    u = R(rmsnorm(x, W[p + "ffn_norm"], cfg.rms_eps))
     g = W.linear(u, p + "w_gate")
     up = W.linear(u, p + "w_up")
     act = silu(g) if cfg.act == "silu" else gelu_tanh(g)
-    d = W.linear(act * up, p + "w_down")
+    d = W.linear(R(act * up), p + "w_down")
     if cfg.norm_layout == "sandwich":
         d = rmsnorm(d, W[p + "post_ffn_norm"], cfg.rms_eps)
     x = x + d
@@ -274,7 +297,7 @@ def _head(cfg, W: OracleWeights, y: np.ndarray) -> np.ndarray:
     return z
 
 
-def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "all") -> dict:
+def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "all", storage: str = "exact") -> dict:
     """Cacheless forward over ids [B, S] ("N7 · model/forward-parity", Thm 1:
     embedding lookup, decoder stack appending one hidden slot per layer, final
     norm, head matmul to logits).
@@ -282,6 +305,7 @@ def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "a
     Returns {"hidden": [L+2, B, S, H] or None, "logits": [B, S, V] ("all") or
     [B, V] ("last") or None ("none")}.
     """
+    R = _rounder(storage)
     W = weights if isinstance(weights, OracleWeights) else OracleWeights(weights)
     ids = np.asarray(ids)
     B, S = ids.shape
@@ -292,7 +316,7 @@ def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "a
     empty_kv = np.zeros((B, 0, Hkv, hd))
     empty_pos = np.zeros((B, 0), dtype=np.int64)
     for l in range(cfg.n_layers):
-        x, _, _ = _layer(cfg, W, l, x, pos, empty_kv, empty_kv, empty_pos)
+        x, _, _ = _layer(cfg, W, l, x, pos, empty_kv, empty_kv, empty_pos, R)
         if hidden:
             slots.append(x)
     y = rmsnorm(x, W["final_norm"], cfg.rms_eps)
@@ -300,9 +324,9 @@ def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "a
         slots.append(y)
     out = {"hidden": np.stack(slots) if hidden else None}
     if logits == "all":
-        out["logits"] = _head(cfg, W, y)
+        out["logits"] = _head(cfg, W, R(y))
     elif logits == "last":
-        out["logits"] = _head(cfg, W, y[:, -1, :])
+        out["logits"] = _head(cfg, W, R(y[:, -1, :]))
     else:
         out["logits"] = None
     return out
@@ -313,7 +337,8 @@ class Session:
     Thm 1: NewSession().Prefill last-position logits agree with the cacheless
     Forward; greedy Generate feeds each argmax back as the next token)."""
 
-    def __init__(self, cfg, weights, batch: int):
+    def __init__(self, cfg, weights, batch: int, storage: str = "exact"):
+        self.R = _rounder(storage)
         self.cfg = cfg
         self.W = weights if isinstance(weights, OracleWeights) else OracleWeights(weights)
         self.B = batch
@@ -330,11 +355,11 @@ class Session:
         past_pos = np.broadcast_to(np.arange(self.length), (self.B, self.length))
         x = _embed(cfg, W, ids)
         for l in range(cfg.n_layers):
-            x, k, v = _layer(cfg, W, l, x, pos, self.k[l], self.v[l], past_pos)
+            x, k, v = _layer(cfg, W, l, x, pos, self.k[l], self.v[l], past_pos, self.R)
             self.k[l] = np.concatenate([self.k[l], k], axis=1)
             self.v[l] = np.concatenate([self.v[l], v], axis=1)
         self.length += S
-        y = rmsnorm(x[:, -1, :], W["final_norm"], cfg.rms_eps)
+        y = self.R(rmsnorm(x[:, -1, :], W["final_norm"], cfg.rms_eps))
         return _head(cfg, W, y)
 
     def prefill(self, ids: np.ndarray) -> np.ndarray:
@@ -373,21 +398,23 @@ def topk_ids(z: np.ndarray, k: int) -> np.ndarray:
     return order[..., :k]
 
 
-def greedy(cfg, weights, prompt: np.ndarray, n_steps: int, forced: np.ndarray | None = None) -> dict:
+def greedy(cfg, weights, prompt: np.ndarray, n_steps: int, forced: np.ndarray | None = None,
+           storage: str = "exact") -> dict:
     """Greedy generation: prefill the prompt [B, S], take next = argmax, then
     n_steps decode steps each feeding the previous id ("N7", Thm 1 witness:
     Generate's greedy ids). With ``forced`` [n_steps, B] the fed ids are those
     instead (teacher forcing) and the argmax of each step is still recorded.
 
     Returns {"ids": [n_steps + 1, B] argmax per call, "margins": same shape,
-    "last_logits": logits of the final call}.
+    "first_logits": logits of the prefill, "last_logits": logits of the final call}.
     """
-    sess = Session(cfg, weights, np.asarray(prompt).shape[0])
+    sess = Session(cfg, weights, np.asarray(prompt).shape[0], storage)
     z = sess.prefill(prompt)
+    first = z
     ids, margins = [argmax_first(z)], [top2_margin(z)]
     for t in range(n_steps):
         feed = ids[-1] if forced is None else np.asarray(forced[t])
         z = sess.decode(feed)
         ids.append(argmax_first(z))
         margins.append(top2_margin(z))
-    return {"ids": np.stack(ids), "margins": np.stack(margins), "last_logits": z}
+    return {"ids": np.stack(ids), "margins": np.stack(margins), "first_logits": first, "last_logits": z}

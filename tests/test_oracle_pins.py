@@ -447,3 +447,23 @@ def test_greedy_feeds_argmax():
     seq = np.concatenate([prompt, g["ids"][:-1].T], axis=1)
     full = oracle.forward(cfg, wb, seq)
     np.testing.assert_array_equal(np.argmax(full["logits"][:, 3:], axis=-1), g["ids"].T)
+
+
+def test_store_bf16_matches_scalar_rounding():
+    x = RNG.standard_normal(3000) * 37.0
+    got = oracle.store_bf16(x)
+    want = np.array([oracle.round_to_bf16(float(np.float32(v))) for v in x])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_storage_mode_is_close_but_not_exact():
+    cfg = tiny_config("gemma")
+    wb = synth.make_weights(cfg, seed=2, sigma=0.3, norm_mode="random")
+    ids = synth.make_ids(cfg, 1, 8, seed=3)
+    ex = oracle.forward(cfg, wb, ids)
+    st = oracle.forward(cfg, wb, ids, storage="bf16")
+    again = oracle.forward(cfg, wb, ids, storage="exact")
+    np.testing.assert_array_equal(ex["logits"], again["logits"])
+    d = np.abs(st["logits"] - ex["logits"]).max()
+    assert 0 < d < 0.05 * np.abs(ex["logits"]).max()
+    np.testing.assert_array_equal(st["hidden"][0], ex["hidden"][0])  # the embedding is not a stored activation
