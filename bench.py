@@ -9,7 +9,10 @@ random token ids):
     greedy next id from the last position of each (the timed "value");
   * decode: 32 sequences prefilled to 2048 tokens once (untimed), then G
     greedy decode steps per timed step (context 2048 -> 2048 + G*(W+K)).
-One step = one prefill of the 4 x 4096 batch + G decode steps.
+  * decode at batch 1 from the same context length (the per-sequence
+    latency case), G greedy steps per timed step.
+One step = one prefill of the 4 x 4096 batch + G decode steps at batch 32 + G
+at batch 1; decode steps replay the session's captured CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fk|reference]
 
@@ -237,29 +240,41 @@ def main():
     model = fk.Model(cfg, wdev, max_positions=max_pos)
     sp = model.session(PREFILL_B, PREFILL_S, max_chunk=PREFILL_S)
     sd = model.session(DECODE_B, max_pos, max_chunk=1024)
+    s1 = model.session(1, max_pos, max_chunk=1024)
     ids_p = torch.from_numpy(synth.make_ids(cfg, PREFILL_B, PREFILL_S, stream=10 + rank)).to(dev)
     ids_d = torch.from_numpy(synth.make_ids(cfg, DECODE_B, DECODE_CTX, stream=50 + rank)).to(dev)
     z_p = torch.empty((PREFILL_B, cfg.vocab), dtype=torch.float32, device=dev)
     n_p = torch.empty((PREFILL_B,), dtype=torch.int32, device=dev)
     z_d = torch.empty((DECODE_B, cfg.vocab), dtype=torch.float32, device=dev)
     n_d = torch.empty((DECODE_B,), dtype=torch.int32, device=dev)
-    sd.prefill(ids_d)  # context for the decode batch (untimed set-up)
+    z_1 = torch.empty((1, cfg.vocab), dtype=torch.float32, device=dev)
+    n_1 = torch.empty((1,), dtype=torch.int32, device=dev)
+    sd.prefill(ids_d)  # contexts for the decode batches (untimed set-up)
+    s1.prefill(ids_d[:1].contiguous())
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
-    def step(events=None):
+    def step(events=None, profile_prefill=False):
         sp.reset()
         if events:
             events[0].record(stream)
+        if profile_prefill:
+            lib.fk_profile_enable(1)
         sp.prefill(ids_p, logits=z_p, next_ids=n_p)
+        if profile_prefill:
+            lib.fk_profile_enable(0)
         if events:
             events[1].record(stream)
-        for _ in range(G):
+        for _ in range(G):  # greedy steps, replayed from the captured decode graph
             sd.decode(None, logits=z_d, next_ids=n_d)
         if events:
             events[2].record(stream)
+        for _ in range(G):
+            s1.decode(None, logits=z_1, next_ids=n_1)
+        if events:
+            events[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -267,7 +282,6 @@ def main():
     if world > 1:
         dist.barrier()
     lib.fk_profile_reset()
-    lib.fk_profile_enable(1)
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
@@ -277,37 +291,53 @@ def main():
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for k in range(args.steps):
-        step(ev[k])
+        step(ev[k], profile_prefill=True)
     stop.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    lib.fk_profile_enable(0)
     total_ms = start.elapsed_time(stop)
     pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
-    prof = {}
+    dec1_ms = sum(e[2].elapsed_time(e[3]) for e in ev)
     import ctypes
-    for i in range(lib.fk_profile_count()):
-        name = ctypes.c_char_p()
-        n = ctypes.c_int64()
-        ms = ctypes.c_double()
-        lib.fk_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms))
-        prof[name.value.decode()] = (n.value, ms.value)
-    lib.fk_profile_reset()
+
+    def read_profile():
+        prof = {}
+        for i in range(lib.fk_profile_count()):
+            name = ctypes.c_char_p()
+            n = ctypes.c_int64()
+            ms = ctypes.c_double()
+            lib.fk_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms))
+            prof[name.value.decode()] = (n.value, ms.value)
+        lib.fk_profile_reset()
+        return prof
+
+    prof = read_profile()
+    # per-kernel decode timing: one profiled pass (launched one by one, outside the timed region)
+    lib.fk_profile_enable(1)
+    for _ in range(2):
+        sd.decode(None, logits=z_d, next_ids=n_d)
+    lib.fk_profile_enable(0)
+    prof_dec = read_profile()
+    lib.fk_profile_enable(1)
+    for _ in range(2):
+        s1.decode(None, logits=z_1, next_ids=n_1)
+    lib.fk_profile_enable(0)
+    prof_dec1 = read_profile()
     st, flags = model.sync_status()
     if st != 0:
         raise RuntimeError(f"device error word set: {flags:#x}")
 
-    times = torch.tensor([total_ms, pre_ms, dec_ms], dtype=torch.float64, device=dev)
+    times = torch.tensor([total_ms, pre_ms, dec_ms, dec1_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, pre_ms, dec_ms = times.tolist()
+    total_ms, pre_ms, dec_ms, dec1_ms = times.tolist()
     prefill_tok = world * PREFILL_B * PREFILL_S * args.steps
-    decode_tok = world * DECODE_B * G * args.steps
     prefill_tps = prefill_tok / (pre_ms / 1e3)
-    decode_tps = decode_tok / (dec_ms / 1e3)
+    decode_tps = world * DECODE_B * G * args.steps / (dec_ms / 1e3)
+    decode1_tps = world * G * args.steps / (dec1_ms / 1e3)
 
     # ---- roofline of the dominant kernels (algorithmic work / device time)
     H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
@@ -321,11 +351,18 @@ def main():
     peak_tf = peaks["bf16_sustained"]
     bytes_per_launch_dec = {"gemm_gate_up_dec": 2.0 * 2 * I * H, "gemm_down_dec": 2.0 * I * H,
                             "gemm_qkv_dec": 2.0 * (Nq + 2 * Nkv) * H, "gemm_o_dec": 2.0 * Nq * H}
-    dec_k = max(bytes_per_launch_dec, key=lambda k: prof.get(k, (0, 0.0))[1])
-    n2, ms2 = prof.get(dec_k, (0, 0.0))
+    dec_k = max(bytes_per_launch_dec, key=lambda k: prof_dec.get(k, (0, 0.0))[1])
+    n2, ms2 = prof_dec.get(dec_k, (0, 0.0))
     achieved_gbs = bytes_per_launch_dec[dec_k] * n2 / (ms2 / 1e3) / 1e9 if ms2 > 0 else None
+    # whole decode step: every weight once + the KV cache read + the new K/V written
+    L = cfg.n_layers
+    w_bytes = 2.0 * (L * (H * (Nq + 2 * Nkv) + Nq * H + 3 * H * I) + V * H)
+    ctx_mid = DECODE_CTX + G * (args.warmup + args.steps // 2)
+    kv_bytes = lambda B: 2.0 * 2 * L * Nkv * B * ctx_mid + 2.0 * 2 * L * Nkv * B
+    step_gbs = lambda B, ms_tot: (w_bytes + kv_bytes(B)) * G * args.steps / (ms_tot / 1e3) / 1e9
     launches = sum(c * (2 if k == "attn_decode" else 1) for k, (c, _) in prof.items())
-    gpu_launches = launches
+    per_dec_step = sum(c * (2 if k == "attn_decode" else 1) for k, (c, _) in prof_dec.items()) // 2 + 1
+    gpu_launches = launches + 2 * G * args.steps * per_dec_step
 
     line = {
         "metric": METRIC, "value": prefill_tps, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -334,18 +371,23 @@ def main():
         "config": {"workload": WORKLOAD, "global_batch": PREFILL_B * world, "seq_len": PREFILL_S,
                    "decode_batch": DECODE_B * world, "decode_context": DECODE_CTX, "decode_steps_per_step": G,
                    "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (16 GB of weights)"},
-        "decode": {"value": decode_tps, "unit": "tok/s", "ms_per_token_step": dec_ms / (G * args.steps)},
+        "decode": {"value": decode_tps, "unit": "tok/s", "batch": DECODE_B, "ms_per_token_step": dec_ms / (G * args.steps),
+                   "hbm_gbs": step_gbs(DECODE_B, dec_ms), "hbm_frac": step_gbs(DECODE_B, dec_ms) / peaks["hbm"]},
+        "decode_b1": {"value": decode1_tps, "unit": "tok/s", "batch": 1, "ms_per_token_step": dec1_ms / (G * args.steps),
+                      "hbm_gbs": step_gbs(1, dec1_ms), "hbm_frac": step_gbs(1, dec1_ms) / peaks["hbm"]},
         "roofline": {"kernel": pre_k, "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": (achieved_tf / peak_tf) if achieved_tf else None,
                      "peak_src": f"{peaks['src']} bf16 sustained",
                      "traffic": measured_traffic(pre_k, "llama3-8b prefill 4x4096")},
         "roofline_decode": {"kernel": dec_k, "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"],
                             "unit": "GB/s", "frac": (achieved_gbs / peaks["hbm"]) if achieved_gbs else None,
-                            "peak_src": f"{peaks['src']} hbm",
+                            "peak_src": f"{peaks['src']} hbm", "timing": "separate profiled pass (launched one by one)",
                             "traffic": measured_traffic(dec_k, "llama3-8b decode b32")},
         "step_fraction": {"prefill_tc_frac": (2.0 * T * (H * (Nq + 2 * Nkv) + Nq * H + 3 * H * I) * cfg.n_layers
                                               / (pre_ms / args.steps / 1e3) / 1e12 / peak_tf)},
         "kernels": {k: {"launches": c, "ms": round(m, 3)} for k, (c, m) in sorted(prof.items())},
+        "kernels_decode_b32_per_2_steps": {k: {"launches": c, "ms": round(m, 3)} for k, (c, m) in sorted(prof_dec.items())},
+        "kernels_decode_b1_per_2_steps": {k: {"launches": c, "ms": round(m, 3)} for k, (c, m) in sorted(prof_dec1.items())},
         "gpu_launches": gpu_launches,
         "clocks": clk,
         "setup_s": round(setup_gen_s, 1),

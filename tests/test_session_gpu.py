@@ -55,3 +55,24 @@ def test_decode_matches_oracle(fk, kind):
     decided = ref["margins"] > 1e-2
     np.testing.assert_array_equal(got[decided], ref["ids"][decided])
     np.testing.assert_allclose(z.cpu().numpy(), ref["last_logits"], atol=0.05)
+
+
+def test_graph_decode_equals_launched_decode(fk):
+    """Steps fed back from the previous argmax replay a captured CUDA graph;
+    feeding the same ids explicitly launches kernel by kernel. Same bits."""
+    import torch
+    cfg = synth.small_config("llama")
+    wb, model = _setup(fk, cfg)
+    prompt = synth.make_ids(cfg, 2, 30)
+    a, b = model.session(2, 64), model.session(2, 64)
+    za, zb = (torch.empty((2, cfg.vocab), dtype=torch.float32, device="cuda") for _ in range(2))
+    na, nb = (torch.empty((2,), dtype=torch.int32, device="cuda") for _ in range(2))
+    a.prefill(prompt, logits=za, next_ids=na)
+    b.prefill(prompt, logits=zb, next_ids=nb)
+    for _ in range(8):
+        feed = nb.clone()
+        a.decode(None, logits=za, next_ids=na)        # graph
+        b.decode(feed, logits=zb, next_ids=nb)        # one by one
+        torch.cuda.synchronize()
+        assert torch.equal(za, zb) and torch.equal(na, nb)
+    assert a.length == b.length == 38

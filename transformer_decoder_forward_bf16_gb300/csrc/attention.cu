@@ -252,6 +252,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
     const __nv_bfloat16* __restrict__ q, int ldq, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, int cap, int ctx_host, const int* d_ctx, int Hq, int Hkv, int window,
     float scale_log2, int chunk, int n_splits, float* __restrict__ part_o, float* __restrict__ part_ml) {
+  pdl_trigger();
+  pdl_wait();
   using C = DecCfg<HD>;
   extern __shared__ uint4 smem_u4[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_u4);
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int group = Hq / Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ctx = d_ctx ? *d_ctx : ctx_host;
+  const int ctx = d_ctx ? *d_ctx + 1 : ctx_host;  // *d_ctx: tokens before the new one
   const int qpos = ctx - 1;
   int lo = split * chunk;
   const int hi = min(ctx, lo + chunk);
@@ -433,6 +435,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
 template <int HD>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hq,
                                     int n_splits, __nv_bfloat16* __restrict__ o) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   const size_t base = ((size_t)b * Hq + h) * n_splits;
   float M = -INFINITY;
@@ -510,13 +514,12 @@ cudaError_t decode_hd(const void* q, int ldq, const void* kcache, const void* vc
   });
   if (err != cudaSuccess) return err;
   dim3 grid(n_splits, Hkv, B);
-  attn_decode_kernel<HD><<<grid, kDecThreads, C::SMEM, st>>>(
-      static_cast<const __nv_bfloat16*>(q), ldq, static_cast<const __nv_bfloat16*>(kcache),
-      static_cast<const __nv_bfloat16*>(vcache), cap, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o,
-      part_ml);
-  attn_combine_kernel<HD><<<dim3(Hq, B), HD < 128 ? HD : 128, 0, st>>>(part_o, part_ml, Hq, n_splits,
-                                                                      static_cast<__nv_bfloat16*>(o));
-  return cudaGetLastError();
+  cudaError_t e = fk_launch(attn_decode_kernel<HD>, grid, kDecThreads, C::SMEM, st, static_cast<const __nv_bfloat16*>(q),
+                            ldq, static_cast<const __nv_bfloat16*>(kcache), static_cast<const __nv_bfloat16*>(vcache),
+                            cap, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml);
+  if (e != cudaSuccess) return e;
+  return fk_launch(attn_combine_kernel<HD>, dim3(Hq, B), HD < 128 ? HD : 128, 0, st, (const float*)part_o,
+                   (const float*)part_ml, Hq, n_splits, static_cast<__nv_bfloat16*>(o));
 }
 
 cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,

@@ -36,6 +36,8 @@ FK_DEVICE void store8_bf16(__nv_bfloat16* p, const float* v) {
 __global__ void embed_norm_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ E, int T, int H,
                                   int V, float scale, const __nv_bfloat16* __restrict__ w, float eps,
                                   float* __restrict__ x, __nv_bfloat16* __restrict__ u, unsigned* dev_err) {
+  pdl_trigger();
+  pdl_wait();
   const int warps = blockDim.x >> 5;
   const int t = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -77,6 +79,8 @@ __global__ void embed_norm_kernel(const int32_t* __restrict__ ids, const __nv_bf
 // ---------------------------------------------------------------------------
 __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, int T, int H, const __nv_bfloat16* __restrict__ w,
                                float eps, __nv_bfloat16* __restrict__ u, int ldu) {
+  pdl_trigger();
+  pdl_wait();
   const int warps = blockDim.x >> 5;
   const int t = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -96,6 +100,46 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, int T, int 
     *reinterpret_cast<uint2*>(ur + c) =
         make_uint2(pack_bf16x2(v.x * r * bf16_lo(wp.x), v.y * r * bf16_hi(wp.x)),
                    pack_bf16x2(v.z * r * bf16_lo(wp.y), v.w * r * bf16_hi(wp.y)));
+  }
+}
+
+// The same normalisation for few rows: one 256-thread block per row, the row
+// held in registers (16-byte loads, one read of x), block-wide reduction.
+constexpr int kRowsThreads = 256;
+constexpr int kRowsMaxVec = 8;  // float4 per thread: H <= 8192
+__global__ void __launch_bounds__(kRowsThreads) rmsnorm_rows_kernel(const float* __restrict__ x, int ldx, int H,
+                                                                    const __nv_bfloat16* __restrict__ w, float eps,
+                                                                    __nv_bfloat16* __restrict__ u, int ldu) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[kRowsThreads / 32];
+  const int t = blockIdx.x;
+  const float* xr = x + (size_t)t * ldx;
+  float4 v[kRowsMaxVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowsMaxVec; ++i) {
+    const int c = (i * kRowsThreads + threadIdx.x) * 4;
+    v[i] = c < H ? *reinterpret_cast<const float4*>(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowsThreads / 32; ++i) tot += red[i];
+  const float r = rsqrtf(tot / H + eps);
+  __nv_bfloat16* ur = u + (size_t)t * ldu;
+#pragma unroll
+  for (int i = 0; i < kRowsMaxVec; ++i) {
+    const int c = (i * kRowsThreads + threadIdx.x) * 4;
+    if (c < H) {
+      const uint2 wp = *reinterpret_cast<const uint2*>(w + c);
+      *reinterpret_cast<uint2*>(ur + c) =
+          make_uint2(pack_bf16x2(v[i].x * r * bf16_lo(wp.x), v[i].y * r * bf16_hi(wp.x)),
+                     pack_bf16x2(v[i].z * r * bf16_lo(wp.y), v[i].w * r * bf16_hi(wp.y)));
+    }
   }
 }
 
@@ -132,6 +176,8 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
                                           const __nv_bfloat16* __restrict__ w_post,
                                           const __nv_bfloat16* __restrict__ w_next, float eps,
                                           __nv_bfloat16* __restrict__ u) {
+  pdl_trigger();
+  pdl_wait();
   const int warps = blockDim.x >> 5;
   const int t = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -185,6 +231,8 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
                                 int Hkv, const float2* __restrict__ rope, int qk_norm,
                                 const __nv_bfloat16* __restrict__ q_norm, const __nv_bfloat16* __restrict__ k_norm,
                                 float eps, __nv_bfloat16* kcache, __nv_bfloat16* vcache, int cap) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int HD = C * 64;
   constexpr int HALF = HD / 2;
   const int warps = blockDim.x >> 5;
@@ -261,7 +309,10 @@ FK_DEVICE void better(float& m, int& i, float m2, int i2) {
   }
 }
 
-__global__ void argmax_kernel(const float* __restrict__ z, int R, int V, int ldz, int32_t* __restrict__ out) {
+__global__ void argmax_kernel(const float* __restrict__ z, int R, int V, int ldz, int32_t* __restrict__ out,
+                              int32_t* __restrict__ out2) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   if (r >= R) return;
   const float* row = z + (size_t)r * ldz;
@@ -302,7 +353,11 @@ __global__ void argmax_kernel(const float* __restrict__ z, int R, int V, int ldz
       const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
       better(m, idx, m2, i2);
     }
-    if (lane == 0) out[r] = idx == 0x7fffffff ? 0 : idx;
+    if (lane == 0) {
+      const int best = idx == 0x7fffffff ? 0 : idx;
+      out[r] = best;
+      if (out2) out2[r] = best;
+    }
   }
 }
 
@@ -316,6 +371,12 @@ __global__ void gather_last_rows_kernel(const __nv_bfloat16* src, int ld, int S,
     *reinterpret_cast<uint4*>(dst + (size_t)b * H + c) = *reinterpret_cast<const uint4*>(s + c);
 }
 
+__global__ void set_int_kernel(int* p, int value) { *p = value; }
+__global__ void inc_int_kernel(int* p) {
+  pdl_wait();
+  *p += 1;
+}
+
 constexpr int kRowThreads = 256;  // 8 rows per block
 inline int row_blocks(long rows) { return (int)((rows + 7) / 8); }
 
@@ -324,18 +385,19 @@ inline int row_blocks(long rows) { return (int)((rows + 7) / 8); }
 cudaError_t launch_embed_norm(const int32_t* ids, const void* E, int T, int H, int V, float scale, const void* w,
                               float eps, float* x, void* u, unsigned* dev_err, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  embed_norm_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(ids, static_cast<const __nv_bfloat16*>(E), T, H, V, scale,
-                                                         static_cast<const __nv_bfloat16*>(w), eps, x,
-                                                         static_cast<__nv_bfloat16*>(u), dev_err);
-  return cudaGetLastError();
+  return fk_launch(embed_norm_kernel, row_blocks(T), kRowThreads, 0, st, ids, static_cast<const __nv_bfloat16*>(E), T, H,
+                   V, scale, static_cast<const __nv_bfloat16*>(w), eps, x, static_cast<__nv_bfloat16*>(u), dev_err);
 }
 
 cudaError_t launch_rmsnorm(const float* x, int ldx, int T, int H, const void* w, float eps, void* u, int ldu,
                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(x, ldx, T, H, static_cast<const __nv_bfloat16*>(w), eps,
-                                                      static_cast<__nv_bfloat16*>(u), ldu);
-  return cudaGetLastError();
+  if (T <= 512 && H <= kRowsThreads * 4 * kRowsMaxVec) {
+    return fk_launch(rmsnorm_rows_kernel, T, kRowsThreads, 0, st, x, ldx, H, static_cast<const __nv_bfloat16*>(w), eps,
+                     static_cast<__nv_bfloat16*>(u), ldu);
+  }
+  return fk_launch(rmsnorm_kernel, row_blocks(T), kRowThreads, 0, st, x, ldx, T, H, static_cast<const __nv_bfloat16*>(w),
+                   eps, static_cast<__nv_bfloat16*>(u), ldu);
 }
 
 cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, float eps, float* y, cudaStream_t st) {
@@ -347,10 +409,9 @@ cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, floa
 cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* x_out, int T, int H,
                                       const void* w_post, const void* w_next, float eps, void* u, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  post_norm_residual_kernel<<<row_blocks(T), kRowThreads, 0, st>>>(
-      a, x_in, x_out, T, H, static_cast<const __nv_bfloat16*>(w_post), static_cast<const __nv_bfloat16*>(w_next), eps,
-      static_cast<__nv_bfloat16*>(u));
-  return cudaGetLastError();
+  return fk_launch(post_norm_residual_kernel, row_blocks(T), kRowThreads, 0, st, a, x_in, x_out, T, H,
+                   static_cast<const __nv_bfloat16*>(w_post), static_cast<const __nv_bfloat16*>(w_next), eps,
+                   static_cast<__nv_bfloat16*>(u));
 }
 
 cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
@@ -366,27 +427,32 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const 
   auto* vc = static_cast<__nv_bfloat16*>(vcache);
   switch (hd) {
     case 64:
-      rope_qkv_kernel<1><<<blocks, 256, 0, st>>>(q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn, kn, eps, kc,
-                                                 vc, cap);
-      break;
+      return fk_launch(rope_qkv_kernel<1>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn,
+                       kn, eps, kc, vc, cap);
     case 128:
-      rope_qkv_kernel<2><<<blocks, 256, 0, st>>>(q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn, kn, eps, kc,
-                                                 vc, cap);
-      break;
+      return fk_launch(rope_qkv_kernel<2>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn,
+                       kn, eps, kc, vc, cap);
     case 256:
-      rope_qkv_kernel<4><<<blocks, 256, 0, st>>>(q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn, kn, eps, kc,
-                                                 vc, cap);
-      break;
+      return fk_launch(rope_qkv_kernel<4>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn,
+                       kn, eps, kc, vc, cap);
     default:
       return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st) {
+cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st, int32_t* out2) {
   if (R == 0) return cudaSuccess;
-  argmax_kernel<<<R, 256, 0, st>>>(z, R, V, ldz, out);
+  return fk_launch(argmax_kernel, R, 256, 0, st, z, R, V, ldz, out, out2);
+}
+
+cudaError_t launch_set_int(int* p, int value, cudaStream_t st) {
+  set_int_kernel<<<1, 1, 0, st>>>(p, value);
   return cudaGetLastError();
+}
+
+cudaError_t launch_inc_int(int* p, cudaStream_t st) {
+  return fk_launch(inc_int_kernel, 1, 1, 0, st, p);
 }
 
 cudaError_t launch_gather_last_rows(const void* src, int ld, int S, int H, int B, void* dst, cudaStream_t st) {

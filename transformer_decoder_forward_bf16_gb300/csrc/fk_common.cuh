@@ -180,6 +180,14 @@ FK_DEVICE void tmem_ld32(uint32_t taddr, float* v) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with the PDL attribute may
+// start while its predecessor drains; pdl_wait() blocks until the predecessor
+// has completed and its writes are visible (a no-op without the attribute).
+// ---------------------------------------------------------------------------
+FK_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+FK_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // numerics
 // ---------------------------------------------------------------------------
 FK_DEVICE float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
@@ -200,3 +208,5 @@ FK_DEVICE float warp_max(float v) {
 }
 
 }  // namespace fk
+
+#include "fk_launch.h"

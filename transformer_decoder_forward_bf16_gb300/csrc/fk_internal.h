@@ -89,11 +89,14 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
 constexpr int kSkinnyMaxTokens = 64;
 struct SkinnyPlan {
   int splits = 1, kb_per_split = 1, n_tiles = 1, nk = 1;
-  size_t part_bytes = 0;
+  size_t counter_bytes = 0;  // per-group arrival counters at the start of the scratch
+  size_t part_bytes = 0;     // whole scratch: counters + fp32 partial sums
 };
 SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count);
 size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count);
+// counters_zeroed: the scratch's leading counters are known to be zero (a
+// session clears them once; every launch leaves them zero again).
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
-                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st);
+                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed = true);
 
 }  // namespace fk

@@ -17,7 +17,12 @@ cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* 
 cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
                             const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
                             void* kcache, void* vcache, int cap, cudaStream_t st);
-cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st);
+// out2 (optional): a second copy of the ids
+cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st,
+                          int32_t* out2 = nullptr);
+// *p = value (one thread), and *p += 1
+cudaError_t launch_set_int(int* p, int value, cudaStream_t st);
+cudaError_t launch_inc_int(int* p, cudaStream_t st);
 cudaError_t launch_gather_last_rows(const void* src, int ld, int S, int H, int B, void* dst, cudaStream_t st);
 
 // Causal GQA attention of S new queries per sequence (positions pos0..pos0+S-1)
@@ -29,8 +34,9 @@ cudaError_t launch_attention_prefill(const void* q, int ldq, const void* kcache,
                                      int S, int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
                                      cudaStream_t st);
 
-// One query per sequence at position ctx-1 (ctx = keys in the cache,
-// *d_ctx if non-null, else ctx). Split-KV: partial results in `scratch`
+// One query per sequence at position ctx-1 (ctx = keys in the cache; if
+// d_ctx is non-null, ctx = *d_ctx + 1, *d_ctx being the length before the
+// new token). Split-KV: partial results in `scratch`
 // (fk::decode_attention_scratch_bytes), combined in a fixed order.
 size_t decode_attention_scratch_bytes(int B, int Hq, int hd, int max_splits);
 int decode_attention_splits(int B, int Hkv, int max_ctx, int sm_count, int* chunk);

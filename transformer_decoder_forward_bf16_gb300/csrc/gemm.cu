@@ -384,6 +384,7 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
                    cudaStream_t st, void* scratch, size_t scratch_bytes) {
   if (M == 0) return FK_OK;
   if (M <= kSkinnyMaxTokens && scratch) return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st);
+
   if (!A || !o.out || M < 0 || lda < w.K || lda % 8 || o.ldo % (o.epi == EPI_BF16 || o.epi == EPI_GLU_BF16 ? 8 : 4))
     return fail(FK_ERR_INVALID_ARG, "gemm_run: bad operand");
   if (o.epi == EPI_ADD_F32 && (!o.res || o.ldr % 4)) return fail(FK_ERR_INVALID_ARG, "gemm_run: residual");

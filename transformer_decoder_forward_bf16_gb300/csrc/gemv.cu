@@ -34,7 +34,44 @@ struct SkinnyArgs {
   int kb_per_split, nk;
   float* part;  // [splits][M][n_rows]
   unsigned* dev_err;
+  // fused reduction: the last CTA to finish a feature group sums the splits
+  unsigned* counters;  // one per group, zero between launches (the last CTA resets it)
+  int fused, glu_tiles;  // glu_tiles: feature tiles of one half of a gate|up pair (0 = not GLU)
+  int epi, act, n_out, ldo, ldr;
+  void* out;
+  const float* res;
+  float softcap;
 };
+
+FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
+FK_DEVICE float act_gelu_tanh(float g) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+}
+
+// Sum the splits of one feature for every token (fixed split order) and store
+// the epilogue's result. v: gate (or plain) feature f, u: up feature (GLU).
+FK_DEVICE void reduce_store(const SkinnyArgs& a, int S, int f) {
+  for (int t = 0; t < a.M; ++t) {
+    float v = 0.f, u = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float* p = a.part + ((size_t)s * a.M + t) * a.n_rows;
+      v += __ldcg(p + f);
+      if (a.glu_tiles) u += __ldcg(p + a.n_out + f);
+    }
+    if (a.epi == EPI_GLU_BF16) {
+      static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] =
+          __float2bfloat16_rn((a.act ? act_gelu_tanh(v) : act_silu(v)) * u);
+    } else if (a.epi == EPI_BF16) {
+      static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] = __float2bfloat16_rn(v);
+    } else if (a.epi == EPI_ADD_F32) {
+      float* o = static_cast<float*>(a.out) + (size_t)t * a.ldo + f;
+      *o = a.res[(size_t)t * a.ldr + f] + v;
+    } else {
+      static_cast<float*>(a.out)[(size_t)t * a.ldo + f] = a.softcap > 0.f ? a.softcap * tanhf(v / a.softcap) : v;
+    }
+  }
+}
 
 template <int BT>
 struct SCfg {
@@ -87,8 +124,12 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  pdl_trigger();
+  if (!(warp == 0 && lane == 0)) pdl_wait();
   if (warp == 0 && lane == 0) {
-    // ---- producer: two 64-row weight boxes + one token box per stage
+    // ---- producer: two 64-row weight boxes + one token box per stage. The
+    // weights do not depend on the previous kernel, so the first stages are
+    // requested before waiting for it; the token rows only after.
     const CUtensorMap* maps[3] = {&tmW0, &tmW1, &tmW2};
     int map[2], row[2];
     bool valid[2];
@@ -106,7 +147,20 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     const uint64_t evict_first = l2_policy_evict_first();
     int issued[kStages] = {0, 0, 0, 0};
     bool ok = true;
-    for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
+    const int npre = min(kStages, kb1 - kb0);
+    for (int it = 0; it < npre; ++it) {  // fresh ring: every stage is free
+      uint8_t* sa = smem + it * C::STAGE;
+      mbar_arrive_expect_tx(&full[it], bytes);
+      for (int i = 0; i < 2; ++i)
+        if (valid[i])
+          tma_load_2d_hint(maps[map[i]], &full[it], sa + i * 64 * 128, (kb0 + it) * 64, row[i], evict_first);
+    }
+    pdl_wait();
+    for (int it = 0; it < npre; ++it) {
+      tma_load_2d(&tmX, &full[it], smem + it * C::STAGE + A_BYTES, (kb0 + it) * 64, 0);
+      ++issued[it];
+    }
+    for (int kb = kb0 + npre, it = npre; kb < kb1; ++kb, ++it) {
       const int stage = it % kStages;
       const uint32_t phase = (it / kStages) & 1;
       if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.dev_err)) {
@@ -172,17 +226,27 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-}
-
-FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
-FK_DEVICE float act_gelu_tanh(float g) {
-  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+  if (!args.fused || !have) return;
+  // ---- fused split-K reduction: the last CTA of this feature group finishes it
+  volatile int* last = abort_flag + 1;
+  const int group = args.glu_tiles ? (int)blockIdx.x % args.glu_tiles : (int)blockIdx.x;
+  const unsigned expect = gridDim.y * (args.glu_tiles ? 2u : 1u);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *last = atomicAdd(&args.counters[group], 1u) == expect - 1 ? 1 : 0;
+  __syncthreads();
+  if (!*last) return;
+  __threadfence();
+  const int f = group * 128 + threadIdx.x;
+  if (f < args.n_out) reduce_store(args, gridDim.y, f);
+  if (threadIdx.x == 0) args.counters[group] = 0;
 }
 
 // Sum the splits in order and apply the epilogue; one thread per (token, 4 features).
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int S, int M, int n_rows, int n_out, int epi,
                                      int act, void* out, int ldo, const float* res, int ldr, float softcap) {
+  pdl_trigger();
+  pdl_wait();
   const int per_row = (n_out + 3) / 4;
   const long total = (long)M * per_row;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
@@ -219,36 +283,73 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int S, int 
 }
 
 template <int BT>
-fk_status launch_bt(const CUtensorMap& tX, const GemmWeights& w, const SkinnyArgs& a, int n_tiles, int splits,
-                    cudaStream_t st) {
-  using C = SCfg<BT>;
+cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfg<BT>::SMEM);
   });
+  return attr;
+}
+
+template <int BT>
+fk_status launch_bt(const CUtensorMap& tX, const GemmWeights& w, const SkinnyArgs& a, int n_tiles, int splits,
+                    cudaStream_t st) {
+  using C = SCfg<BT>;
+  cudaError_t attr = set_smem_attr<BT>();
   if (attr != cudaSuccess) return cuda_fail(attr, "cudaFuncSetAttribute(gemv)");
-  gemv_tc_kernel<BT><<<dim3(n_tiles, splits), kThreads, C::SMEM, st>>>(
-      tX, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0], w.nseg > 2 ? w.map[2] : w.map[0], a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = fk_launch(gemv_tc_kernel<BT>, dim3(n_tiles, splits), kThreads, C::SMEM, st, tX, w.map[0],
+                            w.nseg > 1 ? w.map[1] : w.map[0], w.nseg > 2 ? w.map[2] : w.map[0], a);
   if (e != cudaSuccess) return cuda_fail(e, "gemv_tc_kernel launch");
   return FK_OK;
 }
 
 }  // namespace
 
+// CTAs of the skinny kernel that fit on one SM at once (shared memory bound).
+static int resident_per_sm(int M) {
+  static int cached[3] = {0, 0, 0};
+  const int i = M <= 16 ? 0 : (M <= 32 ? 1 : 2);
+  if (!cached[i]) {
+    int n = 0;
+    cudaError_t e;
+    set_smem_attr<16>();
+    set_smem_attr<32>();
+    set_smem_attr<64>();
+    if (i == 0)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_tc_kernel<16>, kThreads, SCfg<16>::SMEM);
+    else if (i == 1)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_tc_kernel<32>, kThreads, SCfg<32>::SMEM);
+    else
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_tc_kernel<64>, kThreads, SCfg<64>::SMEM);
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 2;
+    }
+    cached[i] = n;
+  }
+  return cached[i];
+}
+
+
+// Split K so that the whole grid is one wave of resident CTAs: every CTA
+// starts at once (and, in the decode step, requests its first weight tiles
+// while the previous kernel drains), and none waits for a second wave.
 SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count) {
   SkinnyPlan p;
   const int nk = (K + 63) / 64;
   const int n_tiles = (n_rows + 127) / 128;
-  int splits = std::max(1, std::min(nk, (4 * sm_count + n_tiles - 1) / n_tiles));
+  const int wave = resident_per_sm(M) * sm_count;
+  int splits = std::max(1, std::min(nk, wave / n_tiles));
   p.kb_per_split = (nk + splits - 1) / splits;
   p.splits = (nk + p.kb_per_split - 1) / p.kb_per_split;
   p.n_tiles = n_tiles;
   p.nk = nk;
-  p.part_bytes = (size_t)p.splits * M * n_rows * sizeof(float);
+  p.counter_bytes = ((size_t)n_tiles * sizeof(unsigned) + 255) / 256 * 256;
+  p.part_bytes = p.counter_bytes + (size_t)p.splits * M * n_rows * sizeof(float);
   return p;
 }
+
 
 size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count) {
   if (M <= 0 || M > kSkinnyMaxTokens) return 0;
@@ -256,7 +357,7 @@ size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count) {
 }
 
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
-                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st) {
+                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed) {
   int sms = 0;
   fk_status s = check_device(&sms);
   if (s != FK_OK) return s;
@@ -267,6 +368,7 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   CUtensorMap tX;
   s = make_tmap_bf16(&tX, A, M, w.K, lda, BT);
   if (s != FK_OK) return s;
+  const int n_out = w.glu ? w.n_out : n_rows;
   SkinnyArgs a{};
   a.M = M;
   a.K = w.K;
@@ -275,21 +377,33 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   for (int i = 0; i < 4; ++i) a.seg_start[i] = w.seg_start[i];
   a.kb_per_split = p.kb_per_split;
   a.nk = p.nk;
-  a.part = static_cast<float*>(scratch);
+  a.counters = static_cast<unsigned*>(scratch);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + p.counter_bytes);
   a.dev_err = dev_err;
+  // a gate|up pair fuses only when each half is a whole number of 128-row tiles
+  // (the last CTA sums M x splits values per feature: worth it only for few tokens)
+  a.fused = M <= 8 && !(w.glu && n_out % 128);
+  a.glu_tiles = w.glu ? n_out / 128 : 0;
+  a.epi = o.epi;
+  a.act = o.act;
+  a.n_out = n_out;
+  a.out = o.out;
+  a.ldo = o.ldo;
+  a.res = o.res;
+  a.ldr = o.ldr;
+  a.softcap = o.softcap;
+  if (a.fused && !counters_zeroed) FK_CUDA_TRY(cudaMemsetAsync(a.counters, 0, p.counter_bytes, st));
   if (BT == 16)
     s = launch_bt<16>(tX, w, a, p.n_tiles, p.splits, st);
   else if (BT == 32)
     s = launch_bt<32>(tX, w, a, p.n_tiles, p.splits, st);
   else
     s = launch_bt<64>(tX, w, a, p.n_tiles, p.splits, st);
-  if (s != FK_OK) return s;
-  const int n_out = w.glu ? w.n_out : n_rows;
+  if (s != FK_OK || a.fused) return s;
   const long work = (long)M * ((n_out + 3) / 4);
   const int blocks = (int)std::min<long>((work + 255) / 256, 8L * sms);
-  splitk_reduce_kernel<<<blocks, 256, 0, st>>>(static_cast<const float*>(scratch), p.splits, M, n_rows, n_out, o.epi,
-                                               o.act, o.out, o.ldo, o.res, o.ldr, o.softcap);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = fk_launch(splitk_reduce_kernel, blocks, 256, 0, st, (const float*)a.part, p.splits, M, n_rows, n_out,
+                            o.epi, o.act, o.out, o.ldo, o.res, o.ldr, o.softcap);
   if (e != cudaSuccess) return cuda_fail(e, "splitk_reduce_kernel launch");
   return FK_OK;
 }
@@ -321,5 +435,6 @@ extern "C" fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32
   o.epi = y_fp32 ? EPI_F32 : EPI_BF16;
   o.out = d_y;
   o.ldo = N;
-  return gemm_run_skinny(d_x, P, K, w, o, d_scratch, scratch_bytes, nullptr, static_cast<cudaStream_t>(stream));
+  return gemm_run_skinny(d_x, P, K, w, o, d_scratch, scratch_bytes, nullptr, static_cast<cudaStream_t>(stream),
+                         false);
 }

@@ -13,6 +13,7 @@
 // Sandwich layout ("N7", Thm 2, gemma3): the O and down GEMMs write fp32 and a
 // fused kernel adds RMSNorm(a)·w_post to the residual and normalises the sum.
 #include <chrono>
+#include <cstdlib>
 #include <cmath>
 #include <cstring>
 #include <thread>
@@ -22,6 +23,7 @@
 
 #include "fk_internal.h"
 #include "fk_ops.h"
+#include "fk_launch.h"
 
 using namespace fk;
 
@@ -39,8 +41,9 @@ struct Scratch {
   void* qkv = nullptr;     // [T, Nq + 2 Nkv] bf16
   void* ao = nullptr;      // [T, Nq] bf16 attention output
   void* h = nullptr;       // [T, I] bf16 gated FFN activations
-  void* gemv = nullptr;    // split-K partial sums of the few-token GEMMs
+  void* gemv = nullptr;    // split-K counters + partial sums of the few-token GEMMs
   size_t gemv_bytes = 0;
+  size_t gemv_counter_bytes = 0;  // leading counters, zero between launches
 };
 
 }  // namespace
@@ -77,6 +80,13 @@ struct fk_session {
   void* u_last = nullptr;       // [B, H] bf16
   void* dec_scratch = nullptr;
   int dec_chunk = 0, dec_splits = 0;
+  int* d_len = nullptr;          // device copy of len (read by decode kernels)
+  bool d_len_valid = false;      // false after reset until the next prefill
+  // captured decode step (feeds the previous greedy ids), keyed by outputs
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t graph = nullptr;
+  float* graph_logits = nullptr;
+  int32_t* graph_next = nullptr;
 };
 
 namespace {
@@ -196,7 +206,14 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
     gb = std::max(gb, skinny_scratch_bytes(m->g_down[0], Ms, m->sm_count));
     gb = std::max(gb, skinny_scratch_bytes(m->g_head, Ms, m->sm_count));
   }
+  size_t cb = 0;
+  if (gb) {
+    const GemmWeights* all[5] = {&m->g_qkv[0], &m->g_o[0], &m->g_gu[0], &m->g_down[0], &m->g_head};
+    for (const GemmWeights* g : all)
+      cb = std::max(cb, skinny_plan(Ms, g->K, g->seg_start[g->nseg], m->sm_count).counter_bytes);
+  }
   t.gemv_bytes = gb;
+  t.gemv_counter_bytes = cb;
   t.gemv = gb ? take(gb) : nullptr;
   if (s) *s = t;
   return off;
@@ -225,7 +242,8 @@ struct KV {
 // slots (optional): fp32 [L+2][T][H] hidden states. decode: S == 1, attention
 // through the split-KV kernel with dscratch.
 fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, const KV& kv, float* slots,
-                    bool decode, void* dscratch, int dchunk, int dsplits, cudaStream_t st) {
+                    bool decode, void* dscratch, int dchunk, int dsplits, cudaStream_t st,
+                    const int* d_len = nullptr, const int32_t* ids = nullptr) {
   const fk_config& c = m->cfg;
   const int H = c.hidden, L = c.n_layers, hd = c.head_dim;
   const long T = (long)B * S;
@@ -238,7 +256,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   void* gv = decode ? sc.gemv : nullptr;
   const size_t gvb = decode ? sc.gemv_bytes : 0;
   { ProfScope ps(decode ? "embed_norm_dec" : "embed_norm", st);
-  FK_LAUNCH(launch_embed_norm(sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
+  FK_LAUNCH(launch_embed_norm(ids ? ids : sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
                               x_in, sc.u, m->dev_err, st)); }
   for (int l = 0; l < L; ++l) {
     const fk_layer_weights& w = m->layers[l];
@@ -256,11 +274,11 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     o.ldo = m->Nqkv;
     { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb)); }
     { ProfScope ps(decode ? "rope_qkv_dec" : "rope_qkv", st);
-    FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
+    FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, d_len, c.n_q_heads, c.n_kv_heads, hd,
                               m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
     if (decode) {
       ProfScope ps("attn_decode", st);
-      FK_LAUNCH(launch_attention_decode(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, pos0 + 1, nullptr, c.n_q_heads,
+      FK_LAUNCH(launch_attention_decode(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, pos0 + 1, d_len, c.n_q_heads,
                                         c.n_kv_heads, hd, window, m->attn_scale, dchunk, dsplits, dscratch, sc.ao,
                                         st));
     } else {
@@ -322,7 +340,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
 }
 
 fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* argmax, const Scratch& sc,
-                   cudaStream_t st) {
+                   cudaStream_t st, int32_t* argmax2 = nullptr) {
   GemmOut o;
   o.epi = EPI_F32;
   o.out = logits;
@@ -330,7 +348,7 @@ fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* ar
   o.softcap = m->cfg.final_softcap;
   { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st, sc.gemv, sc.gemv_bytes)); }
   ProfScope ps("argmax", st);
-  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st));
+  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st, argmax2));
   return FK_OK;
 }
 
@@ -510,6 +528,7 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   forward_layout(m, batch, seq, static_cast<uint8_t*>(d_ws), &sc, &kv, &ws_logits);
   FK_CUDA_TRY(cudaMemcpyAsync(sc.ids, ids, T * sizeof(int32_t),
                               ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+  if (sc.gemv_counter_bytes) FK_CUDA_TRY(cudaMemsetAsync(sc.gemv, 0, sc.gemv_counter_bytes, st));
   FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, nullptr, 0, 0, st));
   if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st));
   return FK_OK;
@@ -539,7 +558,9 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
   int chunk = 0;
   const int splits = decode_attention_splits(B, c.n_kv_heads, max_seq, m->sm_count, &chunk);
   uint8_t* ds = take(decode_attention_scratch_bytes(B, c.n_q_heads, c.head_dim, splits));
+  uint8_t* dl = take(sizeof(int));
   if (s) {
+    s->d_len = reinterpret_cast<int*>(dl);
     s->kcache = reinterpret_cast<__nv_bfloat16*>(k);
     s->vcache = reinterpret_cast<__nv_bfloat16*>(v);
     s->layer_kv = layer_kv;
@@ -577,15 +598,28 @@ extern "C" fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_s
   s->max_seq = max_seq;
   s->max_chunk = std::min(max_chunk, max_seq);
   session_layout(m, batch, max_seq, s->max_chunk, static_cast<uint8_t*>(d_mem), s);
+  if (s->sc.gemv_counter_bytes) {
+    cudaError_t e = cudaMemset(s->sc.gemv, 0, s->sc.gemv_counter_bytes);
+    if (e != cudaSuccess) {
+      delete s;
+      return cuda_fail(e, "clear split-K counters");
+    }
+  }
   *out = s;
   return FK_OK;
 }
 
-extern "C" void fk_session_free(fk_session* s) { delete s; }
+extern "C" void fk_session_free(fk_session* s) {
+  if (!s) return;
+  if (s->graph) cudaGraphExecDestroy(s->graph);
+  if (s->cap_stream) cudaStreamDestroy(s->cap_stream);
+  delete s;
+}
 
 extern "C" fk_status fk_session_reset(fk_session* s) {
   if (!s) return fail(FK_ERR_INVALID_ARG, "session is NULL");
   s->len = 0;
+  s->d_len_valid = false;
   return FK_OK;
 }
 
@@ -594,9 +628,7 @@ extern "C" int32_t fk_session_length(const fk_session* s) { return s ? s->len : 
 static fk_status session_head(fk_session* s, const void* u_rows, float* d_logits, int32_t* d_next, cudaStream_t st) {
   fk_model* m = s->m;
   float* logits = d_logits ? d_logits : s->logits;
-  FK_TRY(run_head(m, u_rows, s->B, logits, s->next_ids, s->sc, st));
-  if (d_next) FK_CUDA_TRY(cudaMemcpyAsync(d_next, s->next_ids, s->B * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
-  return FK_OK;
+  return run_head(m, u_rows, s->B, logits, s->next_ids, s->sc, st, d_next);
 }
 
 extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32_t ids_on_device, int32_t seq,
@@ -619,7 +651,33 @@ extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32
     s->len += C;
   }
   FK_LAUNCH(launch_gather_last_rows(s->sc.u, m->cfg.hidden, C, m->cfg.hidden, s->B, s->u_last, st));
+  FK_LAUNCH(launch_set_int(s->d_len, s->len, st));
+  s->d_len_valid = true;
   return session_head(s, s->u_last, d_last_logits, d_next, st);
+}
+
+// Enqueue one decode step whose positions come from s->d_len (so the same
+// launches serve every step, captured or not).
+static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next,
+                                cudaStream_t st) {
+  fk_model* m = s->m;
+  // every launch of the step may overlap its predecessor's tail (each kernel
+  // waits for its predecessor before touching data the predecessor writes)
+  PdlScope pdl(true);
+  KV kv{s->kcache, s->vcache, s->layer_kv, s->max_seq};
+  FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_scratch, s->dec_chunk, s->dec_splits, st,
+                   s->d_len, d_ids ? d_ids : s->next_ids));
+  FK_TRY(session_head(s, s->sc.u, d_logits, d_next, st));
+  FK_LAUNCH(launch_inc_int(s->d_len, st));
+  return FK_OK;
+}
+
+static bool graphs_disabled() {
+  static const bool off = [] {
+    const char* e = getenv("FK_NO_GRAPH");
+    return e && *e && *e != '0';
+  }();
+  return off;
 }
 
 extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next,
@@ -629,14 +687,47 @@ extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* 
   if (s->len == 0 && !d_ids) return fail(FK_ERR_INVALID_ARG, "no previous greedy ids: prefill first or pass d_ids");
   if (d_logits && !aligned16(d_logits)) return fail(FK_ERR_INVALID_ARG, "logits must be 16-byte aligned");
   FK_TRY(check_device(nullptr));
-  fk_model* m = s->m;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  FK_CUDA_TRY(cudaMemcpyAsync(s->sc.ids, d_ids ? d_ids : s->next_ids, s->B * sizeof(int32_t),
-                              cudaMemcpyDeviceToDevice, st));
-  KV kv{s->kcache, s->vcache, s->layer_kv, s->max_seq};
-  FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_scratch, s->dec_chunk, s->dec_splits, st));
+  if (!s->d_len_valid) {
+    FK_LAUNCH(launch_set_int(s->d_len, s->len, st));
+    s->d_len_valid = true;
+  }
+  // Steps that feed back the previous greedy ids are replayed from a CUDA
+  // graph captured on the first such call (re-captured if the output
+  // buffers change). Steps with caller ids, and steps while kernel timing is
+  // on, are launched one by one.
+  if (d_ids || profiling_enabled() || graphs_disabled()) {
+    FK_TRY(enqueue_decode(s, d_ids, d_logits, d_next, st));
+    s->len += 1;
+    return FK_OK;
+  }
+  if (!s->graph || s->graph_logits != d_logits || s->graph_next != d_next) {
+    if (s->graph) {
+      cudaGraphExecDestroy(s->graph);
+      s->graph = nullptr;
+    }
+    if (!s->cap_stream) FK_CUDA_TRY(cudaStreamCreateWithFlags(&s->cap_stream, cudaStreamNonBlocking));
+    FK_CUDA_TRY(cudaStreamBeginCapture(s->cap_stream, cudaStreamCaptureModeThreadLocal));
+    fk_status es = enqueue_decode(s, nullptr, d_logits, d_next, s->cap_stream);
+    cudaGraph_t g = nullptr;
+    cudaError_t ce = cudaStreamEndCapture(s->cap_stream, &g);
+    if (es != FK_OK) {
+      if (g) cudaGraphDestroy(g);
+      return es;
+    }
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamEndCapture(decode step)");
+    ce = cudaGraphInstantiate(&s->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (ce != cudaSuccess) {
+      s->graph = nullptr;
+      return cuda_fail(ce, "cudaGraphInstantiate(decode step)");
+    }
+    s->graph_logits = d_logits;
+    s->graph_next = d_next;
+  }
+  FK_CUDA_TRY(cudaGraphLaunch(s->graph, st));
   s->len += 1;
-  return session_head(s, s->sc.u, d_logits, d_next, st);
+  return FK_OK;
 }
 
 // ===========================================================================

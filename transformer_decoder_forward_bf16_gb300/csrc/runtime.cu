@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "fk_internal.h"
+#include "fk_launch.h"
 
 namespace fk {
 
@@ -144,6 +145,13 @@ void prof_drain_locked() {
 }  // namespace
 
 bool profiling_enabled() { return g_prof_on; }
+
+namespace {
+thread_local bool g_pdl = false;
+}
+bool pdl_enabled() { return g_pdl; }
+PdlScope::PdlScope(bool on) : prev(g_pdl) { g_pdl = on; }
+PdlScope::~PdlScope() { g_pdl = prev; }
 
 ProfScope::ProfScope(const char* name, cudaStream_t stream) : st(stream) {
   if (!g_prof_on) return;
