@@ -184,7 +184,9 @@ fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int
 
 /* ---------------------------------------------------------------------------
  * KV-cached session ("N7", Thm 1: NewSession().Prefill and greedy Generate)
- * batch sequences of equal length; K/V cache bf16 [layer][batch][kv_head][max_seq][head_dim].
+ * batch sequences of equal length; bf16 K cache [layer][batch][kv_head][cap][head_dim]
+ * and transposed V cache [layer][batch][kv_head][head_dim][cap], cap = max_seq
+ * rounded up to 64, both cleared when the session is created.
  * Prefill is processed in chunks of at most max_chunk tokens per sequence.
  * ------------------------------------------------------------------------- */
 size_t fk_session_bytes(const fk_model* m, int32_t batch, int32_t max_seq, int32_t max_chunk);
@@ -234,8 +236,11 @@ fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32
 /* Decode attention of one query per sequence ("N7 · model/forward-parity",
  * Thm 1: causal GQA attention; "pegainfer #878": sliding-window layers).
  *   d_q:      bf16 [batch][n_q_heads*head_dim], the query at position ctx-1
- *   d_kcache, d_vcache: bf16 [batch][n_kv_heads][cap][head_dim], keys/values
- *             at positions 0..ctx-1 (RoPE already applied to the keys)
+ *   d_kcache: bf16 [batch][n_kv_heads][cap][head_dim], keys at positions
+ *             0..ctx-1 (RoPE already applied)
+ *   d_vcache: bf16 [batch][n_kv_heads][head_dim][cap], values transposed
+ *             (position fastest); cap a multiple of 64, and every position
+ *             below the next multiple of 64 above ctx must hold finite values
  *   window:   0 = attend to all ctx keys; W > 0 = only the last W
  *   d_out:    bf16 [batch][n_q_heads*head_dim]
  * Query head h reads kv head h / (n_q_heads/n_kv_heads); scale 1/sqrt(head_dim).

@@ -36,10 +36,10 @@ def test_noalloc_matches_scratch_entry_point(fk, B, Hq, Hkv, hd, ctx, window):
     lib = fk.load()
     assert lib.fk_attention_decode_noalloc_limit() == 4 << 20
     for call, seed in enumerate((11, 12)):  # two calls in a row, different inputs
-        cap = ctx + 3
+        cap = (ctx + 3 + 63) // 64 * 64
         q = to_dev_bf16(synth.normal_bf16(seed, 1, (B, Hq * hd), 1.0))
         k = to_dev_bf16(synth.normal_bf16(seed, 2, (B, Hkv, cap, hd), 1.0))
-        v = to_dev_bf16(synth.normal_bf16(seed, 3, (B, Hkv, cap, hd), 1.0))
+        v = to_dev_bf16(synth.normal_bf16(seed, 3, (B, Hkv, hd, cap), 1.0))  # transposed values
         want = fk.attention_decode(q, k, v, ctx - call, window)
         got = torch.empty_like(q)
         _call_noalloc(fk, q, k, v, ctx - call, window, got)

@@ -189,7 +189,8 @@ def gemm_splitk(x, w, out_fp32: bool = False, out=None, stream=None):
 
 
 def attention_decode(q, kcache, vcache, ctx: int, window: int = 0, out=None, scratch=None, stream=None):
-    """One decode-attention step (q [B, Hq*hd], caches [B, Hkv, cap, hd], bf16)."""
+    """One decode-attention step: q [B, Hq*hd], kcache [B, Hkv, cap, hd],
+    vcache transposed [B, Hkv, hd, cap] (bf16, cap a multiple of 64)."""
     import torch
     B, Hkv, cap, hd = kcache.shape
     Hq = q.shape[1] // hd

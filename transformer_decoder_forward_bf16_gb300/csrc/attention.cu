@@ -52,10 +52,10 @@ FK_DEVICE void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// element (r, c) of a [rows][HD] bf16 tile, 16-byte chunks XOR-swizzled by row
-template <int HD>
+// element (r, c) of a [rows][COLS] bf16 tile, 16-byte chunks XOR-swizzled by row
+template <int COLS>
 FK_DEVICE int swz(int r, int c) {
-  return r * HD + ((((c >> 3) ^ (r & 7))) << 3) + (c & 7);
+  return r * COLS + ((((c >> 3) ^ (r & 7))) << 3) + (c & 7);
 }
 
 constexpr int BQ = 64, BKV = 64;
@@ -81,8 +81,9 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
   const int kb_lo = k_lo / BKV, kb_hi = qp_hi / BKV;
   const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
   const __nv_bfloat16* kbase = kc + head_off;
-  const __nv_bfloat16* vbase = vc + head_off;
-  constexpr int CPR = HD / 8;  // 16-byte chunks per row
+  const __nv_bfloat16* vbase = vc + head_off;  // V^T: [HD][cap]
+  constexpr int CPR = HD / 8;  // 16-byte chunks per K row
+  constexpr int CPV = BKV / 8;  // 16-byte chunks per V^T row of a tile
 
   for (int i = tid; i < BQ * CPR; i += 128) {
     const int r = i / CPR, cc = i % CPR;
@@ -97,9 +98,13 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
       const int r = i / CPR, cc = i % CPR;
       const int kp = kb * BKV + r;
       const int ok = kp < kv_len ? 16 : 0;
-      const size_t off = (size_t)min(kp, kv_len - 1) * HD + cc * 8;
-      cp_async16(dk + swz<HD>(r, cc * 8), kbase + off, ok);
-      cp_async16(dv + swz<HD>(r, cc * 8), vbase + off, ok);
+      cp_async16(dk + swz<HD>(r, cc * 8), kbase + (size_t)min(kp, kv_len - 1) * HD + cc * 8, ok);
+    }
+    // V^T rows: keys [kb*BKV, kb*BKV + BKV) are inside the cache (cap is a
+    // multiple of 64); keys past kv_len hold finite values and get p = 0
+    for (int i = tid; i < HD * CPV; i += 128) {
+      const int d = i / CPV, cc = i % CPV;
+      cp_async16(dv + swz<BKV>(d, cc * 8), vbase + (size_t)d * cap + kb * BKV + cc * 8, 16);
     }
   };
   load_kv(kb_lo, 0);
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
 #pragma unroll
       for (int dp = 0; dp < HD / 16; ++dp) {
         uint32_t bb[4];
-        ldsm_x4_t(bb, tV + swz<HD>(ks * 16 + mr + (mat & 1) * 8, dp * 16 + (mat >> 1) * 8));
+        ldsm_x4(bb, tV + swz<BKV>(dp * 16 + mr + (mat >> 1) * 8, ks * 16 + (mat & 1) * 8));
         mma_bf16_16816(oacc[2 * dp], a, bb[0], bb[1]);
         mma_bf16_16816(oacc[2 * dp + 1], a, bb[2], bb[3]);
       }
@@ -266,12 +271,15 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
   int lo = split * chunk;
   const int hi = min(ctx, lo + chunk);
   if (window > 0) lo = max(lo, qpos - window + 1);
-  const int n = max(0, hi - lo);
-  const int ntiles = (n + kDecTile - 1) / kDecTile;
+  // tiles start on a 64-key boundary (16-byte aligned V^T rows); keys outside
+  // [lo, hi) inside a tile are masked
+  const int t0 = lo & ~(kDecTile - 1);
+  const int ntiles = hi > lo ? (hi - t0 + kDecTile - 1) / kDecTile : 0;
   const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
   const __nv_bfloat16* kbase = kc + head_off;
-  const __nv_bfloat16* vbase = vc + head_off;
+  const __nv_bfloat16* vbase = vc + head_off;  // V^T: [HD][cap]
   constexpr int CPR = HD / 8;
+  constexpr int CPV = kDecTile / 8;
 
   for (int i = tid; i < 16 * CPR; i += kDecThreads) {
     const int r = i / CPR, cc = i % CPR;
@@ -283,11 +291,13 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
     __nv_bfloat16* dv = dk + C::TILE_ELEMS;
     for (int i = tid; i < kDecTile * CPR; i += kDecThreads) {
       const int r = i / CPR, cc = i % CPR;
-      const int kp = lo + t * kDecTile + r;
-      const int ok = kp < hi ? 16 : 0;
-      const size_t off = (size_t)min(kp, hi - 1) * HD + cc * 8;
-      cp_async16(dk + swz<HD>(r, cc * 8), kbase + off, ok);
-      cp_async16(dv + swz<HD>(r, cc * 8), vbase + off, ok);
+      const int kp = t0 + t * kDecTile + r;
+      const int ok = (kp >= lo && kp < hi) ? 16 : 0;
+      cp_async16(dk + swz<HD>(r, cc * 8), kbase + (size_t)min(max(kp, lo), hi - 1) * HD + cc * 8, ok);
+    }
+    for (int i = tid; i < HD * CPV; i += kDecThreads) {
+      const int d = i / CPV, cc = i % CPV;
+      cp_async16(dv + swz<kDecTile>(d, cc * 8), vbase + (size_t)d * cap + t0 + t * kDecTile + cc * 8, 16);
     }
   };
   cp_async_commit();  // Q
@@ -325,13 +335,14 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
       mma_bf16_16816(s[0], a, bb[0], bb[1]);
       mma_bf16_16816(s[1], a, bb[2], bb[3]);
     }
-    const int key0 = lo + t * kDecTile + kr + 2 * (lane & 3);
+    const int key0 = t0 + t * kDecTile + kr + 2 * (lane & 3);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool ok = key0 + nt * 8 + (e & 1) < hi;
+        const int key = key0 + nt * 8 + (e & 1);
+        const bool ok = key >= lo && key < hi;
         s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
       }
       mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
       oacc[2 * dp + 1][2] *= corr1;
       oacc[2 * dp + 1][3] *= corr1;
       uint32_t bb[4];
-      ldsm_x4_t(bb, tV + swz<HD>(kr + mr + (mat & 1) * 8, dp * 16 + (mat >> 1) * 8));
+      ldsm_x4(bb, tV + swz<kDecTile>(dp * 16 + mr + (mat >> 1) * 8, kr + (mat & 1) * 8));
       mma_bf16_16816(oacc[2 * dp], a, bb[0], bb[1]);
       mma_bf16_16816(oacc[2 * dp + 1], a, bb[2], bb[3]);
     }
@@ -552,7 +563,8 @@ fk_status check_decode_args(const void* q, const void* kc, const void* vc, int B
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > 8)
     return fail(FK_ERR_INVALID_ARG, "attention decode: need batch >= 1 and 1..8 query heads per kv head");
   if (hd != 64 && hd != 128 && hd != 256) return fail(FK_ERR_INVALID_ARG, "attention decode: head_dim 64/128/256");
-  if (ctx < 1 || ctx > cap || window < 0) return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap");
+  if (ctx < 1 || ctx > cap || window < 0 || cap % 64)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap, cap a multiple of 64");
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15)
     return fail(FK_ERR_INVALID_ARG, "attention decode: q and caches must be 16-byte aligned");
   return FK_OK;

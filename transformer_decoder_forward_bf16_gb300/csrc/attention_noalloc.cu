@@ -72,7 +72,8 @@ extern "C" fk_status fk_attention_decode_noalloc(const void* d_q, const void* d_
     return fail(FK_ERR_INVALID_ARG, "attention decode: need batch >= 1 and 1..8 query heads per kv head");
   if (head_dim != 64 && head_dim != 128 && head_dim != 256)
     return fail(FK_ERR_INVALID_ARG, "attention decode: head_dim 64/128/256");
-  if (ctx < 1 || ctx > cap || window < 0) return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap");
+  if (ctx < 1 || ctx > cap || window < 0 || cap % 64)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap, cap a multiple of 64");
   if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_kcache) |
        reinterpret_cast<uintptr_t>(d_vcache)) & 15)
     return fail(FK_ERR_INVALID_ARG, "attention decode: q and caches must be 16-byte aligned");

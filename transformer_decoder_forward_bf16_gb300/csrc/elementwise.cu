@@ -223,7 +223,8 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
 // / gemma3 QK-norm). One warp per (token, head). Head element j pairs with
 // j + hd/2; lane owns C = hd/64 consecutive elements of each half.
 //   q: rotated in place inside the qkv rows;
-//   k: rotated and written to kcache[b][g][pos][:]; v: copied to vcache.
+//   k: rotated and written to kcache[b][g][pos][:]; v: copied to the
+//   transposed value cache vcache[b][g][d][pos] (cap a multiple of 64).
 // rope: float2 (cos, sin) table [positions][hd/2].
 // ---------------------------------------------------------------------------
 template <int C>
@@ -252,13 +253,13 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
     lo[i] = __bfloat162float(row[e0 + i]);
     hi[i] = __bfloat162float(row[HALF + e0 + i]);
   }
-  if (h >= Hq + Hkv) {  // v: copy into the cache
+  if (h >= Hq + Hkv) {  // v: copy into the transposed cache vcache[b][g][d][pos]
     const int g = h - Hq - Hkv;
-    __nv_bfloat16* dst = vcache + (((size_t)b * Hkv + g) * cap + pos) * HD;
+    __nv_bfloat16* dst = vcache + ((size_t)b * Hkv + g) * HD * cap + pos;
 #pragma unroll
     for (int i = 0; i < C; ++i) {
-      dst[e0 + i] = __float2bfloat16_rn(lo[i]);
-      dst[HALF + e0 + i] = __float2bfloat16_rn(hi[i]);
+      dst[(size_t)(e0 + i) * cap] = __float2bfloat16_rn(lo[i]);
+      dst[(size_t)(HALF + e0 + i) * cap] = __float2bfloat16_rn(hi[i]);
     }
     return;
   }

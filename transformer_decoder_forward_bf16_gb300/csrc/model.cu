@@ -74,6 +74,7 @@ struct fk_session {
   __nv_bfloat16* kcache = nullptr;  // [L][B][Hkv][max_seq][hd]
   __nv_bfloat16* vcache = nullptr;
   size_t layer_kv = 0;  // elements per layer
+  int cap = 0;          // cache positions per (sequence, kv head): max_seq rounded up to 64
   Scratch sc;
   int32_t* next_ids = nullptr;  // [B]
   float* logits = nullptr;      // [B, V]
@@ -220,10 +221,11 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
 }
 
 struct KV {
-  __nv_bfloat16* k;
-  __nv_bfloat16* v;
+  __nv_bfloat16* k;     // [B][Hkv][cap][hd]
+  __nv_bfloat16* v;     // transposed: [B][Hkv][hd][cap]
   size_t layer_stride;  // elements between layers (0: one buffer reused by every layer)
-  int cap;              // positions per (sequence, kv head)
+  int cap;              // positions per (sequence, kv head), a multiple of 64
+  size_t bytes = 0;     // bytes of one of k / v (all layers)
 };
 
 #define FK_LAUNCH(expr)                                 \
@@ -490,12 +492,14 @@ static size_t forward_layout(const fk_model* m, int B, int S, uint8_t* base, Scr
   const fk_config& c = m->cfg;
   const long T = (long)B * S;
   size_t off = scratch_bytes(m, T, sc, base);
-  const size_t kv_elems = (size_t)B * c.n_kv_heads * S * c.head_dim;
+  const int cap = (S + 63) / 64 * 64;  // attention tiles read whole 64-position blocks
+  const size_t kv_elems = (size_t)B * c.n_kv_heads * cap * c.head_dim;
   if (kv) {
     kv->k = base ? reinterpret_cast<__nv_bfloat16*>(base + off) : nullptr;
     kv->v = base ? reinterpret_cast<__nv_bfloat16*>(base + off + align_up(kv_elems * 2)) : nullptr;
     kv->layer_stride = 0;
-    kv->cap = S;
+    kv->cap = cap;
+    kv->bytes = kv_elems * 2;
   }
   off += 2 * align_up(kv_elems * 2);
   if (logits) *logits = base ? reinterpret_cast<float*>(base + off) : nullptr;
@@ -529,6 +533,8 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   FK_CUDA_TRY(cudaMemcpyAsync(sc.ids, ids, T * sizeof(int32_t),
                               ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
   if (sc.gemv_counter_bytes) FK_CUDA_TRY(cudaMemsetAsync(sc.gemv, 0, sc.gemv_counter_bytes, st));
+  // attention reads V in 64-position blocks: positions past seq must hold finite values
+  if (seq % 64) FK_CUDA_TRY(cudaMemsetAsync(kv.v, 0, kv.bytes, st));
   FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, nullptr, 0, 0, st));
   if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st));
   return FK_OK;
@@ -545,7 +551,8 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
     off += align_up(bytes);
     return p;
   };
-  const size_t layer_kv = (size_t)B * c.n_kv_heads * max_seq * c.head_dim;
+  const int cap = (max_seq + 63) / 64 * 64;
+  const size_t layer_kv = (size_t)B * c.n_kv_heads * cap * c.head_dim;
   uint8_t* k = take(layer_kv * c.n_layers * 2);
   uint8_t* v = take(layer_kv * c.n_layers * 2);
   const long T = (long)B * max_chunk;
@@ -564,6 +571,7 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
     s->kcache = reinterpret_cast<__nv_bfloat16*>(k);
     s->vcache = reinterpret_cast<__nv_bfloat16*>(v);
     s->layer_kv = layer_kv;
+    s->cap = cap;
     s->sc = sc;
     s->next_ids = reinterpret_cast<int32_t*>(next);
     s->logits = reinterpret_cast<float*>(logits);
@@ -598,6 +606,16 @@ extern "C" fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_s
   s->max_seq = max_seq;
   s->max_chunk = std::min(max_chunk, max_seq);
   session_layout(m, batch, max_seq, s->max_chunk, static_cast<uint8_t*>(d_mem), s);
+  {
+    // attention reads whole 64-position blocks of the cache: positions never
+    // written must hold finite values
+    cudaError_t e = cudaMemset(s->kcache, 0, s->layer_kv * m->cfg.n_layers * 2);
+    if (e == cudaSuccess) e = cudaMemset(s->vcache, 0, s->layer_kv * m->cfg.n_layers * 2);
+    if (e != cudaSuccess) {
+      delete s;
+      return cuda_fail(e, "clear KV cache");
+    }
+  }
   if (s->sc.gemv_counter_bytes) {
     cudaError_t e = cudaMemset(s->sc.gemv, 0, s->sc.gemv_counter_bytes);
     if (e != cudaSuccess) {
@@ -640,7 +658,7 @@ extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32
   if (!ids_on_device) FK_TRY(check_ids_host(ids, (long)s->B * seq, m->cfg.vocab));
   FK_TRY(check_device(nullptr));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  KV kv{s->kcache, s->vcache, s->layer_kv, s->max_seq};
+  KV kv{s->kcache, s->vcache, s->layer_kv, s->cap};
   int C = 0;
   for (int c0 = 0; c0 < seq; c0 += C) {
     C = std::min(s->max_chunk, seq - c0);
@@ -664,7 +682,7 @@ static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_lo
   // every launch of the step may overlap its predecessor's tail (each kernel
   // waits for its predecessor before touching data the predecessor writes)
   PdlScope pdl(true);
-  KV kv{s->kcache, s->vcache, s->layer_kv, s->max_seq};
+  KV kv{s->kcache, s->vcache, s->layer_kv, s->cap};
   FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_scratch, s->dec_chunk, s->dec_splits, st,
                    s->d_len, d_ids ? d_ids : s->next_ids));
   FK_TRY(session_head(s, s->sc.u, d_logits, d_next, st));
