@@ -233,6 +233,21 @@ size_t fk_gemm_bf16_splitk_scratch_bytes(int32_t P, int32_t K, int32_t N);
 fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
                               int32_t y_fp32, void* d_scratch, size_t scratch_bytes, void* stream);
 
+/* Prefill attention: seq new queries per sequence at positions
+ * pos0..pos0+seq-1 over cached keys/values at positions 0..pos0+seq-1
+ * ("N7 · model/forward-parity", Thm 1: causal GQA attention; "pegainfer
+ * #878": sliding window, query i sees key j iff 0 <= i-j < window).
+ *   d_q:   bf16 [batch*seq][n_q_heads*head_dim] (RoPE applied)
+ *   caches as for fk_attention_decode (K [batch][n_kv_heads][cap][head_dim],
+ *          V transposed [batch][n_kv_heads][head_dim][cap], cap % 64 == 0,
+ *          positions up to the next multiple of 128 finite)
+ *   d_out: bf16 [batch*seq][n_q_heads*head_dim]
+ * head_dim 64 and 128 run on the tensor-core (tcgen05) kernel, 256 on the
+ * mma.sync kernel. No scratch. */
+fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch, int32_t seq,
+                               int32_t pos0, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
+                               int32_t window, void* d_out, void* stream);
+
 /* Decode attention of one query per sequence ("N7 · model/forward-parity",
  * Thm 1: causal GQA attention; "pegainfer #878": sliding-window layers).
  *   d_q:      bf16 [batch][n_q_heads*head_dim], the query at position ctx-1

@@ -37,3 +37,32 @@ def test_decode_attention_vs_oracle(fk, B, Hq, Hkv, hd, ctx, window):
                                1.0 / math.sqrt(hd))[0]
         # bf16 output rounding (2^-9 relative) on values of size <= max|v|
         np.testing.assert_allclose(got[b], ref, atol=1e-3, rtol=4e-3)
+
+
+@pytest.mark.parametrize("B,S,pos0,Hq,Hkv,hd,window,ramp", [
+    (1, 1024, 0, 4, 1, 128, 0, True), (2, 600, 0, 8, 2, 128, 0, False), (1, 700, 0, 4, 2, 64, 0, True),
+    (1, 300, 200, 4, 1, 128, 0, True), (1, 900, 0, 4, 1, 128, 256, True), (1, 260, 0, 2, 1, 256, 64, False)])
+def test_prefill_attention_vs_oracle(fk, B, S, pos0, Hq, Hkv, hd, window, ramp):
+    """Prefill attention against the oracle. With ``ramp`` the keys grow along
+    the sequence, so each query row's running maximum keeps rising from one
+    key block to the next and the lazy O rescale of the tensor-core kernel runs
+    many times."""
+    import torch
+    kv_len = pos0 + S
+    cap = (kv_len + 63) // 64 * 64
+    q = synth.normal_bf16(7, 11, (B * S, Hq * hd), 1.0)
+    kf = synth.bf16_bits_to_f32(synth.normal_bf16(7, 12, (B, Hkv, cap, hd), 1.0))
+    if ramp:  # scores grow ~linearly with the key position
+        kf = kf * 0.25 + (np.arange(cap) / 64.0)[None, None, :, None].astype(np.float32)
+    k = synth.f32_to_bf16_bits(kf)
+    v = synth.normal_bf16(7, 13, (B, Hkv, hd, cap), 1.0)
+    out = fk.attention_prefill(to_dev_bf16(q), to_dev_bf16(k), to_dev_bf16(v), S, pos0, window)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().reshape(B, S, Hq, hd)
+    qf, kk, vv = (oracle.bf16_to_f64(a) for a in (q, k, v))
+    qf = qf.reshape(B, S, Hq, hd)
+    for b in range(B):
+        ref = oracle.attention(qf[b], kk[b, :, :kv_len].transpose(1, 0, 2), vv[b, :, :, :kv_len].transpose(2, 0, 1),
+                               pos0 + np.arange(S), np.arange(kv_len), window, 1.0 / math.sqrt(hd))
+        # P is rounded to bf16 for the PV product (2^-9 relative) and the output to bf16
+        np.testing.assert_allclose(got[b], ref, atol=1e-2, rtol=1e-2)

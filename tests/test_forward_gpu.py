@@ -44,11 +44,21 @@ def check_forward(fk, cfg, B, S, norm_mode="ones", sigma=0.02, seed=7):
             "logit_err": float(np.max(np.abs(z - zr)))}
 
 
-@pytest.mark.parametrize("kind", ["llama", "llama3", "gemma"])
-@pytest.mark.parametrize("B,S", [(1, 9), (2, 70), (1, 130)])
+SMALL_KINDS = {
+    "llama": synth.small_config("llama"),
+    "llama3": synth.small_config("llama3"),
+    "gemma": synth.small_config("gemma"),
+    # sliding window on a head_dim-64 model (the tensor-core prefill attention path)
+    "llama-window": synth.small_config("llama", sliding_window=24, layer_kinds=(1, 0)),
+    "llama3-window": synth.small_config("llama3", sliding_window=40, layer_kinds=(0, 1)),
+}
+
+
+@pytest.mark.parametrize("kind", sorted(SMALL_KINDS))
+@pytest.mark.parametrize("B,S", [(1, 9), (2, 70), (1, 130), (2, 300)])
 def test_small_models(fk, kind, B, S):
-    cfg = synth.small_config(kind)
-    r = check_forward(fk, cfg, B, S, norm_mode="random", sigma=0.05)
+    cfg = SMALL_KINDS[kind]
+    r = check_forward(fk, cfg, B, S, norm_mode="random", sigma=0.02)
     print(kind, B, S, r)
 
 
@@ -61,7 +71,7 @@ def test_smollm2_shape_9_tokens(fk):
 def test_bitwise_replay(fk):
     import torch
     cfg = synth.small_config("gemma")
-    wb = synth.make_weights(cfg, norm_mode="random", sigma=0.05)
+    wb = synth.make_weights(cfg, norm_mode="random", sigma=0.02)
     model = fk.Model(cfg, weights_to_dev(wb), max_positions=64)
     ids = synth.make_ids(cfg, 2, 40)
     a = model.forward(ids)

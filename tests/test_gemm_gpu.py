@@ -41,6 +41,17 @@ def test_gemm_full(fk, P, K, N, fp32):
     assert e < (2e-5 if fp32 else 6e-3), e
 
 
+@pytest.mark.parametrize("P,K,N", [(4160, 1024, 8192), (3000, 512, 9000)])
+def test_gemm_dual_tile_ragged(fk, P, K, N):
+    """Shapes that take the 256-row tiles with a partial or empty second half."""
+    import torch
+    x, w = _inputs(P, K, N, s=2)
+    y = fk.gemm(to_dev_bf16(x), to_dev_bf16(w), out_fp32=True)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(oracle.bf16_to_f64(x), oracle.bf16_to_f64(w))
+    assert err_scale(y.cpu().numpy(), ref) < 2e-5
+
+
 def test_gemm_exact_integers(fk):
     import torch
     P, K, N = 130, 128, 264

@@ -10,7 +10,7 @@ from helpers import weights_to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _setup(fk, cfg, norm_mode="random", sigma=0.05):
+def _setup(fk, cfg, norm_mode="random", sigma=0.02):
     wb = synth.make_weights(cfg, norm_mode=norm_mode, sigma=sigma)
     return wb, fk.Model(cfg, weights_to_dev(wb), max_positions=512)
 

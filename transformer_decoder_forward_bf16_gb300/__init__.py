@@ -79,6 +79,8 @@ _SIGS = {
     "fk_gemm_bf16_splitk_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
     "fk_gemm_bf16_splitk": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                       c_size_t, c_void_p]),
+    "fk_attention_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                       c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "fk_attention_decode_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "fk_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -185,6 +187,19 @@ def gemm_splitk(x, w, out_fp32: bool = False, out=None, stream=None):
         out = torch.empty((P, N), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=x.device)
     _check(lib.fk_gemm_bf16_splitk(_ptr(x), _ptr(w), P, K, N, _ptr(out), 1 if out_fp32 else 0, _ptr(scratch),
                                    scratch.numel(), _stream_ptr(stream)), "fk_gemm_bf16_splitk")
+    return out
+
+
+def attention_prefill(q, kcache, vcache, seq: int, pos0: int = 0, window: int = 0, out=None, stream=None):
+    """Prefill attention: q [B*seq, Hq*hd]; kcache [B, Hkv, cap, hd]; vcache
+    transposed [B, Hkv, hd, cap] (bf16)."""
+    import torch
+    B, Hkv, cap, hd = kcache.shape
+    Hq = q.shape[1] // hd
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().fk_attention_prefill(_ptr(q), _ptr(kcache), _ptr(vcache), B, seq, pos0, Hq, Hkv, hd, cap, window,
+                                       _ptr(out), _stream_ptr(stream)), "fk_attention_prefill")
     return out
 
 

@@ -99,4 +99,11 @@ size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count);
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
                           size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed = true);
 
+// tcgen05 flash attention for prefill (head_dim 64 or 128; caches as in the
+// session layout, V transposed, cap a multiple of 64).
+bool attention_prefill_tc_supported(int hd, int ldq, int cap);
+fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
+                               int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
+                               unsigned* dev_err, cudaStream_t st);
+
 }  // namespace fk

@@ -18,6 +18,7 @@
 //   * the weight operand may be up to three matrices stacked along N (Q|K|V
 //     without a repacked copy) or a gate/up pair interleaved per tile.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "fk_common.cuh"
@@ -47,12 +48,18 @@ struct GemmArgs {
   unsigned* dev_err;
 };
 
-template <int BN>
+// MT = 128-row sub-tiles per CTA tile. MT == 2 makes a 256 x BN tile: two
+// M=128 accumulators share every B tile, a third fewer L2->SM bytes per FLOP
+// than MT == 1, at the price of a single accumulator set (the epilogue of a
+// tile no longer overlaps the next tile's MMAs).
+template <int BN, int MT = 1>
 struct Cfg {
+  static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int STAGES = MT == 2 ? 3 : ((BN == 256) ? 4 : 6);
+  static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator sets (double buffer when they fit)
+  static constexpr uint32_t TMEM_COLS = NACC * MT * BN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 };
 
@@ -90,16 +97,17 @@ FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int& map, int& row
   }
 }
 
-template <int BN>
+template <int BN, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                    const GemmArgs args) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MT>;
+  constexpr int TM = BM * MT;  // rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + C::STAGES * A_BYTES;
+  uint8_t* sB = smem + C::STAGES * C::A_STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
@@ -109,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_blocks = (args.M + BM - 1) / BM;
+  const int m_blocks = (args.M + TM - 1) / TM;
   const int n_blocks = args.glu ? (args.n_out + BN / 2 - 1) / (BN / 2) : (args.n_virtual + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int nk = (args.K + BK - 1) / BK;
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint32_t bytes = A_BYTES;
+          uint32_t bytes = C::A_STAGE;
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i) {
             int map, row;
@@ -165,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid) bytes += 64 * BK * 2;
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(&tmA, &full[stage], sA + stage * A_BYTES, kb * BK, mb * BM);
+#pragma unroll
+          for (int sub = 0; sub < MT; ++sub)
+            tma_load_2d(&tmA, &full[stage], sA + stage * C::A_STAGE + sub * A_BYTES, kb * BK, mb * TM + sub * BM);
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i) {
             int map, row;
@@ -199,25 +209,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       int local = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t aphase = (local >> 1) & 1;
+        const int acc = local % C::NACC;
+        const uint32_t aphase = (local / C::NACC) & 1;
         if (!mbar_wait(&tempty[acc], aphase ^ 1, abort_flag, args.dev_err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * BN;
+        const uint32_t d = tmem_base + acc * MT * BN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, args.dev_err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sA + stage * A_BYTES);
           const uint64_t bd = smem_desc_sw128(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d, ad + 2 * k, bd + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int sub = 0; sub < MT; ++sub) {
+              const uint64_t ad = smem_desc_sw128(sA + stage * C::A_STAGE + sub * A_BYTES);
+              umma_bf16(d + sub * BN, ad + 2 * k, bd + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
           umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -240,13 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
       int mb, nb;
       tile_coords(t, m_blocks, n_blocks, mb, nb);
-      const int acc = local & 1;
-      const uint32_t aphase = (local >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], aphase, abort_flag, args.dev_err)) break;
+      const int acc = local % C::NACC;
+      const uint32_t aphase = (local / C::NACC) & 1;
+      // warp-uniform: the tcgen05.ld below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aphase, abort_flag, args.dev_err))) break;
       tc_fence_after();
-      const int row = mb * BM + q * 32 + lane;
+#pragma unroll 1
+      for (int sub = 0; sub < MT; ++sub) {
+      const int row = mb * TM + sub * BM + q * 32 + lane;
       const bool row_ok = row < args.M;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (acc * MT + sub) * BN;
       float v[32];
       if (args.epi == EPI_GLU_BF16) {
         for (int c = 0; c < BN / 64; ++c) {
@@ -318,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }  // sub-tiles
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
@@ -331,21 +348,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN>
+template <int BN, int MT>
 fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
-  const int m_blocks = (a.M + BM - 1) / BM;
+  const int m_blocks = (a.M + BM * MT - 1) / (BM * MT);
   const int n_blocks = a.glu ? (a.n_out + BN / 2 - 1) / (BN / 2) : (a.n_virtual + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int grid = std::min(tiles, sm_count);
-  gemm_tc_kernel<BN><<<grid, kThreads, C::SMEM, st>>>(tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0],
-                                                       w.nseg > 2 ? w.map[2] : w.map[0], a);
+  gemm_tc_kernel<BN, MT><<<grid, kThreads, C::SMEM, st>>>(tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0],
+                                                           w.nseg > 2 ? w.map[2] : w.map[0], a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
   return FK_OK;
@@ -411,11 +428,14 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
   a.ldr = o.ldr;
   a.softcap = o.softcap;
   a.dev_err = dev_err;
-  // 256-wide tiles when they still give every SM a tile; else 128-wide.
+  // 256x256 tiles while they give every SM at least two tiles; then 128x256;
+  // else 128-wide.
   const int m_blocks = (M + BM - 1) / BM;
   const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
-  if (m_blocks * nb256 >= sm_count) return launch_bn<256>(tA, w, a, sm_count, st);
-  return launch_bn<128>(tA, w, a, sm_count, st);
+  static const bool no_dual = getenv("FK_GEMM_NO_DUAL") != nullptr;
+  if (!no_dual && ((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count) return launch_bn<256, 2>(tA, w, a, sm_count, st);
+  if (m_blocks * nb256 >= sm_count) return launch_bn<256, 1>(tA, w, a, sm_count, st);
+  return launch_bn<128, 1>(tA, w, a, sm_count, st);
 }
 
 }  // namespace fk

@@ -285,8 +285,13 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
                                         st));
     } else {
       ProfScope ps("attn_prefill", st);
-      FK_LAUNCH(launch_attention_prefill(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
-                                         window, m->attn_scale, sc.ao, st));
+      if (attention_prefill_tc_supported(hd, m->Nqkv, kv.cap) && !getenv("FK_ATTN_MMA_SYNC")) {
+        FK_TRY(attention_prefill_tc(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd, window,
+                                    m->attn_scale, sc.ao, m->dev_err, st));
+      } else {
+        FK_LAUNCH(launch_attention_prefill(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
+                                           window, m->attn_scale, sc.ao, st));
+      }
     }
     // attention output projection + residual
     if (sandwich) {
