@@ -30,7 +30,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two warps per TMEM lane quarter, each taking half the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
 
 struct GemmArgs {
@@ -73,7 +74,13 @@ FK_DEVICE void tile_coords(int t, int m_blocks, int n_blocks, int& mb, int& nb) 
   nb = r / gsize;
 }
 
-FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
+// SiLU g * sigmoid(g) with the hardware 2^x (ex2.approx) and fast division:
+// both far more accurate than the bf16 rounding of the product that follows.
+FK_DEVICE float act_silu(float g) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-g * 1.4426950408889634f));
+  return __fdividef(g, 1.0f + e);
+}
 FK_DEVICE float act_gelu_tanh(float g) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
@@ -129,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * kEpiWarps);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -247,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ---------------- epilogue (warps 2..9) ----------------
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns it stores
     int local = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
       int mb, nb;
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (acc * MT + sub) * BN;
       float v[32];
       if (args.epi == EPI_GLU_BF16) {
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = half * (BN / 128); c < (half + 1) * (BN / 128); ++c) {
           float u[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld32(taddr + BN / 2 + c * 32, u);
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
           tmem_ld32(taddr + c * 32, v);
           const int col0 = nb * BN + c * 32;
           if (!row_ok || col0 >= args.n_out) continue;
