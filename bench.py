@@ -141,6 +141,23 @@ def measured_traffic(kernel: str, workload: str):
     return None
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings across the process group (the
+    slowest replica sets the job's time); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Units processed by all ranks / the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
 def host_weights(cfg, seed: int = synth.SEED_WEIGHTS) -> dict:
     return synth.make_weights(cfg, seed=seed)
 
@@ -187,11 +204,11 @@ def run_reference(args):
     wbits = synth.make_weights(cfg.with_(n_layers=nl))
     wbits["lm_head"] = synth.make_tensor(cfg, "lm_head")
     for _ in range(args.warmup):
-        oracle_prefill_rate(cfg, wbits, 4)
+        oracle_prefill_rate(cfg, wbits, 32)
     vals, secs = [], []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        r = oracle_prefill_rate(cfg, wbits, 4)
+        r = oracle_prefill_rate(cfg, wbits, 32)
         secs.append(time.perf_counter() - t0)
         vals.append(r["tok_s"])
     value = statistics.median(vals)
@@ -330,14 +347,10 @@ def main():
     if st != 0:
         raise RuntimeError(f"device error word set: {flags:#x}")
 
-    times = torch.tensor([total_ms, pre_ms, dec_ms, dec1_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, pre_ms, dec_ms, dec1_ms = times.tolist()
-    prefill_tok = world * PREFILL_B * PREFILL_S * args.steps
-    prefill_tps = prefill_tok / (pre_ms / 1e3)
-    decode_tps = world * DECODE_B * G * args.steps / (dec_ms / 1e3)
-    decode1_tps = world * G * args.steps / (dec1_ms / 1e3)
+    total_ms, pre_ms, dec_ms, dec1_ms = max_over_ranks([total_ms, pre_ms, dec_ms, dec1_ms], device=dev)
+    prefill_tps = job_throughput(PREFILL_B * PREFILL_S * args.steps, world, pre_ms)
+    decode_tps = job_throughput(DECODE_B * G * args.steps, world, dec_ms)
+    decode1_tps = job_throughput(G * args.steps, world, dec1_ms)
 
     # ---- roofline of the dominant kernels (algorithmic work / device time)
     H, I, V = cfg.hidden, cfg.intermediate, cfg.vocab
@@ -419,7 +432,7 @@ def main():
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         nl = 2
         sub = {k: v for k, v in wbits.items() if not k.startswith("L") or int(k[1:].split(".")[0]) < nl}
-        r = oracle_prefill_rate(cfg, sub, 8)
+        r = oracle_prefill_rate(cfg, sub, 256)
         line["cpu_baseline"] = {"value": r["tok_s"], "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": r["sample"], "seconds": round(r["seconds_measured"], 1)}
     if rank == 0:
