@@ -3,21 +3,22 @@
 // Thm 2 and "pegainfer #878": sliding-window local layers).
 //
 // One CTA per (128 queries, head, sequence); key blocks of 64 positions; two
-// CTAs per SM (shared memory and TMEM both sized for it) so each scheduler
-// runs two softmax warps.
-//   warp 0     TMA producer: the Q tile once, then K and Vᵀ tiles through a
-//              2-stage ring (all 128-byte swizzled, K-major).
+// CTAs per SM (96 KB of shared memory and 256 TMEM columns each).
+//   warp 0     TMA producers: lane 0 streams K tiles, lane 1 Vᵀ tiles, each
+//              through its own 2-deep ring (128-byte swizzled, K-major), so
+//              the K tile of block j+2 never waits behind the V tile of j.
 //   warp 1     TMEM allocator and single-thread MMA issuer:
-//                S_j = Q·K_jᵀ   (M=128 queries, N=64 keys) into one of two
-//                               TMEM S buffers, issued one block ahead;
-//                O  += P_j·V_j  (M=128, N=head_dim) into the TMEM O buffer.
-//   warps 2-5  softmax, one query row per thread (TMEM lane = row): read S_j,
-//              mask (causal, window, sequence end), running max in the exp2
-//              domain, P = exp2(S - m) rounded to bf16 into shared memory for
-//              the PV MMA. The running max is raised lazily: O and the row sum
-//              are rescaled (tcgen05.ld/st on O) only when the max grows by
-//              more than 2^8, so most blocks skip the rescale; P <= 2^8 keeps
-//              bf16 well inside range. At the end O / l is stored as bf16.
+//                S_j = Q·K_jᵀ   (M=128 queries, N=64 keys) into TMEM buffer j%2,
+//                               two blocks ahead of the softmax;
+//                O  += P_j·V_j  with P_j read from TMEM (it overwrites S_j)
+//                               and Vᵀ_j from shared memory; O in TMEM.
+//   warps 2-5  softmax, one query row per thread (TMEM lane = row): one TMEM
+//              read of S_j, mask (causal, window, sequence end), running max
+//              in the exp2 domain, P = exp2(S - m) packed to bf16 and stored
+//              back into the same TMEM columns for the PV MMA. The running
+//              max is raised lazily (only when it grows by more than 2^8), and
+//              only then does a warp wait for the previous PV and rescale its
+//              rows of O (tcgen05.ld/st); P <= 2^8 keeps bf16 in range.
 // Every mbarrier wait is bounded (FK_DEVERR_PIPE_TIMEOUT on expiry). Every
 // tcgen05.ld/st is executed by whole warps (they are warp-collective), so
 // per-row decisions that touch TMEM are taken warp-wide.
@@ -40,36 +41,41 @@ constexpr float kLazyRescale = 8.0f;  // log2 units
 template <int HD>
 struct FaCfg {
   static constexpr int Q_BYTES = BQ * HD * 2;   // HD/64 column blocks of [128 rows][128 B]
-  static constexpr int K_BYTES = BKV * HD * 2;  // HD/64 column blocks of [128 keys][128 B]
-  static constexpr int V_BYTES = HD * BKV * 2;  // BKV/64 column blocks of [HD rows][128 B]
-  static constexpr int P_BYTES = BQ * BKV * 2;  // BKV/64 column blocks of [128 rows][128 B]
+  static constexpr int K_BYTES = BKV * HD * 2;  // HD/64 column blocks of [64 keys][128 B]
+  static constexpr int V_BYTES = HD * BKV * 2;  // one column block of [HD rows][128 B]
   static constexpr int STAGES = 2;
-  // tiles then 128 bytes of barriers; no alignment slack (two CTAs must fit
-  // in an SM): the dynamic window starts 1024-byte aligned, checked on entry
-  static constexpr int SMEM = Q_BYTES + STAGES * (K_BYTES + V_BYTES) + P_BYTES + 128;
-  // S0 [0,BKV), S1 [BKV,2 BKV), O [2 BKV, 2 BKV + HD): 256 columns, two CTAs per SM
+  // tiles then 256 bytes for 16 barriers and two words; no alignment slack:
+  // the dynamic window starts 1024-byte aligned (checked on entry)
+  static constexpr int SMEM = Q_BYTES + STAGES * (K_BYTES + V_BYTES) + 256;
+  // S/P buffers [0, BKV) and [BKV, 2 BKV); O [2 BKV, 2 BKV + HD)
   static constexpr uint32_t TMEM_COLS = 2 * BKV + HD <= 256 ? 256 : 512;
   static constexpr uint32_t O_COL = 2 * BKV;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BQ, HD);
 };
 
-FK_DEVICE void tmem_st32(uint32_t taddr, const float* v) {
+FK_DEVICE void tmem_st32(uint32_t taddr, const uint32_t* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
       "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
-      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
-      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
-      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
-      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
-      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
-      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
-      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+FK_DEVICE void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] · B[smem]ᵀ (A operand read from TMEM: M lanes, K/2
+// columns of packed bf16 pairs, lower k in the low half).
+FK_DEVICE void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 2^x with the hardware approximation (ex2.approx, relative error ~2^-22,
 // far below the bf16 rounding P receives next).
 FK_DEVICE float fast_exp2(float x) {
@@ -77,8 +83,6 @@ FK_DEVICE float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-FK_DEVICE void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-FK_DEVICE void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -91,20 +95,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0 && dev_err) atomicOr(dev_err, FK_DEVERR_PIPE_TIMEOUT);
     return;
   }
-  uint8_t* smem = smem_raw;
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + C::Q_BYTES;                      // [STAGES][K_BYTES]
-  uint8_t* sV = sK + C::STAGES * C::K_BYTES;          // [STAGES][V_BYTES]
-  uint8_t* sP = sV + C::STAGES * C::V_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + C::P_BYTES);
+  uint8_t* sQ = smem_raw;
+  uint8_t* sK = sQ + C::Q_BYTES;              // [STAGES][K_BYTES]
+  uint8_t* sV = sK + C::STAGES * C::K_BYTES;  // [STAGES][V_BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::STAGES * C::V_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* pv_done = bars + 8;
-  uint64_t* mma_done = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* k_full = bars + 1;    // [2]
+  uint64_t* k_empty = bars + 3;   // [2]
+  uint64_t* v_full = bars + 5;    // [2]
+  uint64_t* v_empty = bars + 7;   // [2]
+  uint64_t* s_full = bars + 9;    // [2]
+  uint64_t* p_full = bars + 11;   // [2]
+  uint64_t* pv_done = bars + 13;  // [2]: PV_j commits to pv_done[j%2]
+  uint64_t* mma_done = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,12 +128,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -146,32 +152,39 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+    if (lane < 2) {
+      // ---------------- TMA producers: lane 0 K (and Q), lane 1 Vᵀ ----------------
+      const bool is_k = lane == 0;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-      for (int blk = 0; blk < HD / 64; ++blk)
-        tma_load_2d(&tmQ, q_full, sQ + blk * BQ * 128, h * HD + blk * 64, b * S + q_lo);
+        for (int blk = 0; blk < HD / 64; ++blk)
+          tma_load_2d(&tmQ, q_full, sQ + blk * BQ * 128, h * HD + blk * 64, b * S + q_lo);
+      }
       const int krow = (b * Hkv + g) * cap;
       const int vrow = (b * Hkv + g) * HD;
       int issued[2] = {0, 0};
       for (int j = 0; j < nkb; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, dev_err)) break;
-        mbar_arrive_expect_tx(&kv_full[st], C::K_BYTES + C::V_BYTES);
+        if (!mbar_wait(&empty[st], ((j >> 1) & 1) ^ 1, abort_flag, dev_err)) break;
         const int kb = kb_lo + j;
+        if (is_k) {
+          mbar_arrive_expect_tx(&full[st], C::K_BYTES);
 #pragma unroll
-        for (int blk = 0; blk < HD / 64; ++blk)
-          tma_load_2d(&tmK, &kv_full[st], sK + st * C::K_BYTES + blk * BKV * 128, blk * 64, krow + kb * BKV);
-#pragma unroll
-        for (int blk = 0; blk < BKV / 64; ++blk)
-          tma_load_2d(&tmV, &kv_full[st], sV + st * C::V_BYTES + blk * HD * 128, kb * BKV + blk * 64, vrow);
+          for (int blk = 0; blk < HD / 64; ++blk)
+            tma_load_2d(&tmK, &full[st], sK + st * C::K_BYTES + blk * BKV * 128, blk * 64, krow + kb * BKV);
+        } else {
+          mbar_arrive_expect_tx(&full[st], C::V_BYTES);
+          tma_load_2d(&tmV, &full[st], sV + st * C::V_BYTES, kb * BKV, vrow);
+        }
         ++issued[st];
       }
       if (*abort_flag) {  // let issued copies land before the CTA unwinds
         for (int st = 0; st < 2; ++st) {
           if (!issued[st]) continue;
-          const uint32_t a = smem_u32(&kv_full[st]);
+          const uint32_t a = smem_u32(&full[st]);
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(a, (issued[st] - 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
           }
@@ -184,32 +197,36 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = mbar_wait(q_full, 0, abort_flag, dev_err);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, dev_err)) return false;
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, dev_err)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(j & 1) * BKV;
+        const uint32_t d = tmem + (uint32_t)st * BKV;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t ad = smem_desc_sw128(sQ + (k >> 2) * BQ * 128) + 2 * (k & 3);
           const uint64_t bd = smem_desc_sw128(sK + st * C::K_BYTES + (k >> 2) * BKV * 128) + 2 * (k & 3);
           umma_bf16(d, ad, bd, C::IDESC_S, k > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j & 1]);
+        umma_commit(&s_full[st]);
+        umma_commit(&k_empty[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
+      if (ok && nkb > 1) ok = issue_s(1);
       for (int j = 0; j < nkb && ok; ++j) {
-        if (j + 1 < nkb && !issue_s(j + 1)) break;
-        if (!mbar_wait(p_full, j & 1, abort_flag, dev_err)) break;
-        tc_fence_after();
         const int st = j & 1;
+        if (!mbar_wait(&p_full[st], (j >> 1) & 1, abort_flag, dev_err)) break;
+        if (!mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, dev_err)) break;
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k) {
-          const uint64_t ad = smem_desc_sw128(sP + (k >> 2) * BQ * 128) + 2 * (k & 3);
-          const uint64_t bd = smem_desc_sw128(sV + st * C::V_BYTES + (k >> 2) * HD * 128) + 2 * (k & 3);
-          umma_bf16(tmem + C::O_COL, ad, bd, C::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+          const uint64_t bd = smem_desc_sw128(sV + st * C::V_BYTES) + 2 * k;
+          umma_bf16_ts(tmem + C::O_COL, tmem + (uint32_t)st * BKV + 8 * k, bd, C::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
         }
-        umma_commit(pv_done);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&pv_done[st]);
+        umma_commit(&v_empty[st]);
+        // S_{j+2} reuses this TMEM buffer: issued after PV_j, the tensor core
+        // reads P_j before it writes S_{j+2}
+        if (j + 2 < nkb && !issue_s(j + 2)) break;
       }
       umma_commit(mma_done);
       const uint32_t a = smem_u32(mma_done);
@@ -225,96 +242,84 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkb && ok; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, dev_err))) {
+    for (int j = 0; j < nkb; ++j) {
+      const int st = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[st], (j >> 1) & 1, abort_flag, dev_err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_addr = lane_base + (uint32_t)(j & 1) * BKV;
+      const uint32_t s_addr = lane_base + (uint32_t)st * BKV;
       const int key0 = (kb_lo + j) * BKV;
       const bool edge = (key0 + BKV - 1 > qp_lo) || (key0 + BKV > kv_len) || (window > 0 && qp_hi - key0 >= window);
-      float v[32];
-      float mx = -INFINITY;
+      float x[BKV];
+      tmem_ld32(s_addr, x);
+      tmem_ld32(s_addr + 32, x + 32);
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        tmem_ld32(s_addr + c * 32, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = v[e] * scale_log2;
-          if (edge) {
-            const int key = key0 + c * 32 + e;
-            if (!(key <= qp && key < kv_len && (window == 0 || qp - key < window))) x = -INFINITY;
-          }
-          mx = fmaxf(mx, x);
+      for (int e = 0; e < BKV; e += 2) {
+        float a0 = x[e] * scale_log2, a1 = x[e + 1] * scale_log2;
+        if (edge) {
+          const int k0 = key0 + e, k1 = k0 + 1;
+          if (!(k0 <= qp && k0 < kv_len && (window == 0 || qp - k0 < window))) a0 = -INFINITY;
+          if (!(k1 <= qp && k1 < kv_len && (window == 0 || qp - k1 < window))) a1 = -INFINITY;
         }
+        x[e] = a0;
+        x[e + 1] = a1;
+        mx0 = fmaxf(mx0, a0);
+        mx1 = fmaxf(mx1, a1);
       }
-      const float m_new = fmaxf(m, mx);
+      const float m_new = fmaxf(m, fmaxf(mx0, mx1));
       float m_use = m;
       bool rescale = false;
       if (m == -INFINITY) {
-        m_use = m_new;  // nothing accumulated yet in this row (O and l are 0)
+        m_use = m_new;  // nothing accumulated in this row yet (O and l are 0)
       } else if (m_new > m + kLazyRescale) {
         m_use = m_new;
         rescale = true;
       }
-      // P_j goes into the single P buffer and O may be rescaled: PV_{j-1} must be done
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_flag, dev_err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // tcgen05.ld/st are warp-collective: the whole warp rescales when any of
-      // its rows needs it, each lane with its own factor (1 for the others)
       if (__any_sync(0xffffffffu, rescale)) {
-        const float corr = rescale ? exp2f(m - m_use) : 1.f;
+        // O may only change after the last issued PV (PV_{j-1}) is done
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, dev_err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float corr = rescale ? fast_exp2(m - m_use) : 1.f;
         l *= corr;
+        float o[32];
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
-          tmem_ld32(lane_base + C::O_COL + c * 32, v);
+          tmem_ld32(lane_base + C::O_COL + c * 32, o);
+          uint32_t ob[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] *= corr;
-          tmem_st32(lane_base + C::O_COL + c * 32, v);
+          for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * corr);
+          tmem_st32(lane_base + C::O_COL + c * 32, ob);
         }
         tmem_st_wait();
       }
       m = m_use;
+      uint32_t pk[BKV / 2];
+      const bool live = m_use != -INFINITY;
+      float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        tmem_ld32(s_addr + c * 32, v);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0, p1;
-          {
-            float x = v[e] * scale_log2;
-            const int key = key0 + c * 32 + e;
-            const bool okk = !edge || (key <= qp && key < kv_len && (window == 0 || qp - key < window));
-            p0 = (okk && m_use != -INFINITY) ? fast_exp2(x - m_use) : 0.f;
-          }
-          {
-            float x = v[e + 1] * scale_log2;
-            const int key = key0 + c * 32 + e + 1;
-            const bool okk = !edge || (key <= qp && key < kv_len && (window == 0 || qp - key < window));
-            p1 = (okk && m_use != -INFINITY) ? fast_exp2(x - m_use) : 0.f;
-          }
-          l += p0 + p1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-        }
-        // 4 chunks of 8 keys; key chunk index ci = c*4 + i -> column block ci/8, chunk ci%8
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ci = c * 4 + i;
-          uint8_t* dst = sP + (ci >> 3) * BQ * 128 + r * 128 + (((ci & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+      for (int e = 0; e < BKV; e += 2) {
+        const float p0 = live ? fast_exp2(x[e] - m_use) : 0.f;
+        const float p1 = live ? fast_exp2(x[e + 1] - m_use) : 0.f;
+        l0 += p0;
+        l1 += p1;
+        pk[e >> 1] = pack_bf16x2(p0, p1);
       }
-      fence_async_smem();
+      l += l0 + l1;
+      tmem_st32(s_addr, pk);  // P_j over S_j: 32 columns of bf16 pairs
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[st]);
     }
     // epilogue: O / l -> bf16
-    const bool have = ok && mbar_wait(pv_done, (nkb - 1) & 1, abort_flag, dev_err);
+    const int jl = nkb - 1;
+    const bool have =
+        __all_sync(0xffffffffu, ok && mbar_wait(&pv_done[jl & 1], (jl >> 1) & 1, abort_flag, dev_err));
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const int qi = q_lo + r;
