@@ -362,6 +362,67 @@ __global__ void argmax_kernel(const float* __restrict__ z, int R, int V, int ldz
   }
 }
 
+// The same argmax for few rows split across blocks: block (s, r) scans one
+// column chunk of row r and records (max, index); the last block of a row
+// (arrival counter, reset after use) reduces the chunk results in chunk order
+// (lowest index on ties), so the result does not depend on scheduling.
+constexpr int kArgmaxSplits = 32;
+__global__ void argmax_split_kernel(const float* __restrict__ z, int V, int ldz, int32_t* __restrict__ out,
+                                    int32_t* __restrict__ out2, float* part_m, int* part_i, unsigned* counters) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.y, sp = blockIdx.x;
+  const int chunk = ((V + kArgmaxSplits - 1) / kArgmaxSplits + 1023) / 1024 * 1024;
+  const int c0 = sp * chunk, c1 = min(V, c0 + chunk);
+  const float* row = z + (size_t)r * ldz;
+  float m = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int c = c0 + threadIdx.x * 4; c < c1; c += blockDim.x * 4) {
+    if (c + 4 <= c1) {
+      const float4 v = *reinterpret_cast<const float4*>(row + c);
+      better(m, idx, v.x, c);
+      better(m, idx, v.y, c + 1);
+      better(m, idx, v.z, c + 2);
+      better(m, idx, v.w, c + 3);
+    } else {
+      for (int e = c; e < c1; ++e) better(m, idx, row[e], e);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    better(m, idx, m2, i2);
+  }
+  __shared__ float sm[32];
+  __shared__ int si[32];
+  __shared__ int last;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm[w] = m;
+    si[w] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) better(m, idx, sm[i], si[i]);
+    part_m[r * kArgmaxSplits + sp] = m;
+    part_i[r * kArgmaxSplits + sp] = idx;
+    __threadfence();
+    last = atomicAdd(&counters[r], 1u) == kArgmaxSplits - 1;
+  }
+  __syncthreads();
+  if (!last || threadIdx.x != 0) return;
+  __threadfence();
+  float bm = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = 0; i < kArgmaxSplits; ++i)
+    better(bm, bi, __ldcg(part_m + r * kArgmaxSplits + i), __ldcg(part_i + r * kArgmaxSplits + i));
+  const int best = bi == 0x7fffffff ? 0 : bi;
+  out[r] = best;
+  if (out2) out2[r] = best;
+  counters[r] = 0;
+}
+
 // copy the last position of each sequence: dst[b] = src[b*S + S-1]
 __global__ void gather_last_rows_kernel(const __nv_bfloat16* src, int ld, int S, int H, int B,
                                         __nv_bfloat16* dst) {
@@ -442,8 +503,15 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st, int32_t* out2) {
+cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st, int32_t* out2,
+                          void* scratch) {
   if (R == 0) return cudaSuccess;
+  if (scratch && R <= kArgmaxMaxSplitRows && (ldz & 3) == 0) {
+    float* pm = static_cast<float*>(scratch);
+    int* pi = reinterpret_cast<int*>(pm + kArgmaxMaxSplitRows * kArgmaxSplits);
+    unsigned* cnt = reinterpret_cast<unsigned*>(pi + kArgmaxMaxSplitRows * kArgmaxSplits);
+    return fk_launch(argmax_split_kernel, dim3(kArgmaxSplits, R), 256, 0, st, z, V, ldz, out, out2, pm, pi, cnt);
+  }
   return fk_launch(argmax_kernel, R, 256, 0, st, z, R, V, ldz, out, out2);
 }
 

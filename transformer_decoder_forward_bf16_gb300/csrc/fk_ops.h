@@ -17,9 +17,14 @@ cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* 
 cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
                             const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
                             void* kcache, void* vcache, int cap, cudaStream_t st);
-// out2 (optional): a second copy of the ids
+// out2 (optional): a second copy of the ids. With `scratch` (argmax_scratch_bytes,
+// its trailing counters zeroed once) and R <= kArgmaxMaxSplitRows, each row is
+// split across blocks.
+constexpr int kArgmaxMaxSplitRows = 64;
+inline size_t argmax_scratch_bytes() { return (size_t)kArgmaxMaxSplitRows * 32 * 8 + kArgmaxMaxSplitRows * 4; }
+inline size_t argmax_counter_offset() { return (size_t)kArgmaxMaxSplitRows * 32 * 8; }
 cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st,
-                          int32_t* out2 = nullptr);
+                          int32_t* out2 = nullptr, void* scratch = nullptr);
 // *p = value (one thread), and *p += 1
 cudaError_t launch_set_int(int* p, int value, cudaStream_t st);
 cudaError_t launch_inc_int(int* p, cudaStream_t st);

@@ -44,6 +44,7 @@ struct Scratch {
   void* gemv = nullptr;    // split-K counters + partial sums of the few-token GEMMs
   size_t gemv_bytes = 0;
   size_t gemv_counter_bytes = 0;  // leading counters, zero between launches
+  void* argmax = nullptr;         // split-row argmax partials + per-row counters (zero between launches)
 };
 
 }  // namespace
@@ -216,6 +217,7 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
   t.gemv_bytes = gb;
   t.gemv_counter_bytes = cb;
   t.gemv = gb ? take(gb) : nullptr;
+  t.argmax = take(argmax_scratch_bytes());
   if (s) *s = t;
   return off;
 }
@@ -355,7 +357,7 @@ fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* ar
   o.softcap = m->cfg.final_softcap;
   { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st, sc.gemv, sc.gemv_bytes)); }
   ProfScope ps("argmax", st);
-  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st, argmax2));
+  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st, argmax2, sc.argmax));
   return FK_OK;
 }
 
@@ -538,6 +540,8 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   FK_CUDA_TRY(cudaMemcpyAsync(sc.ids, ids, T * sizeof(int32_t),
                               ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
   if (sc.gemv_counter_bytes) FK_CUDA_TRY(cudaMemsetAsync(sc.gemv, 0, sc.gemv_counter_bytes, st));
+  FK_CUDA_TRY(cudaMemsetAsync(static_cast<uint8_t*>(sc.argmax) + argmax_counter_offset(), 0,
+                              argmax_scratch_bytes() - argmax_counter_offset(), st));
   // attention reads V in 64-position blocks: positions past seq must hold finite values
   if (seq % 64) FK_CUDA_TRY(cudaMemsetAsync(kv.v, 0, kv.bytes, st));
   FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, nullptr, 0, 0, st));
@@ -619,6 +623,14 @@ extern "C" fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_s
     if (e != cudaSuccess) {
       delete s;
       return cuda_fail(e, "clear KV cache");
+    }
+  }
+  {
+    cudaError_t e = cudaMemset(static_cast<uint8_t*>(s->sc.argmax) + argmax_counter_offset(), 0,
+                               argmax_scratch_bytes() - argmax_counter_offset());
+    if (e != cudaSuccess) {
+      delete s;
+      return cuda_fail(e, "clear argmax counters");
     }
   }
   if (s->sc.gemv_counter_bytes) {
