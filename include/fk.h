@@ -259,9 +259,11 @@ fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void
  *   window:   0 = attend to all ctx keys; W > 0 = only the last W
  *   d_out:    bf16 [batch][n_q_heads*head_dim]
  * Query head h reads kv head h / (n_q_heads/n_kv_heads); scale 1/sqrt(head_dim).
- * Split-KV: partial results go to d_scratch (fp32, at least
- * fk_attention_decode_scratch_bytes(...) bytes, 16-byte aligned) and are
- * merged in a fixed order, so results are bitwise reproducible.
+ * Split-KV: the splits of a (sequence, kv head) run as one thread-block
+ * cluster and merge their partials in the cluster's shared memory in a fixed
+ * order, so results are bitwise reproducible. d_scratch (at least
+ * fk_attention_decode_scratch_bytes(...) bytes, 16-byte aligned) is part of
+ * the interface but is not written by the current kernel.
  * head_dim is 64, 128 or 256; 1..8 query heads per kv head; 1 <= ctx <= cap. */
 size_t fk_attention_decode_scratch_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                          int32_t ctx);
@@ -273,15 +275,10 @@ fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void*
  * entry point serves callers that cannot provide a scratch buffer (their
  * device memory belongs to another allocator, or their path must not enter
  * the driver's allocation code). Arguments and results are those of
- * fk_attention_decode; the split-KV partials live in a fixed array inside the
- * library's device image, fk_attention_decode_noalloc_limit() bytes (4 MiB)
- * per device, reserved by every GPU that loads the library until exit.
- * Calls whose partials exceed it return FK_ERR_WORKSPACE before launching.
- * The first call on a device looks up the array's address (make it before
- * any stream capture on that device). All calls share the array and it keeps
- * the previous call's contents (nothing needs to start at zero); calls whose
- * kernels overlap on the GPU race on it and must be serialised. Calls no
- * allocator of any kind. */
+ * fk_attention_decode. The kernel keeps its split partials on chip, so the
+ * call touches no device memory beyond its arguments, reserves none
+ * (fk_attention_decode_noalloc_limit() returns 0), shares nothing between
+ * calls and calls no allocator of any kind. */
 size_t fk_attention_decode_noalloc_limit(void);
 fk_status fk_attention_decode_noalloc(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,

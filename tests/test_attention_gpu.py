@@ -22,7 +22,10 @@ def _case(B, Hq, Hkv, hd, cap, seed):
 
 @pytest.mark.parametrize("B,Hq,Hkv,hd,ctx,window", [
     (1, 4, 1, 64, 1, 0), (3, 9, 3, 64, 77, 0), (2, 32, 8, 128, 2049, 0), (32, 32, 8, 128, 300, 0),
-    (1, 16, 8, 256, 1500, 1024), (2, 2, 1, 256, 40, 16), (4, 8, 8, 128, 1025, 0)])
+    (1, 16, 8, 256, 1500, 1024), (2, 2, 1, 256, 40, 16), (4, 8, 8, 128, 1025, 0),
+    # a cluster of 16 splits with fewer tiles than splits (window start mid-tile),
+    # and a 2-split cluster over a ragged last tile
+    (1, 8, 1, 128, 3000, 700), (1, 4, 4, 64, 130, 0)])
 def test_decode_attention_vs_oracle(fk, B, Hq, Hkv, hd, ctx, window):
     import torch
     cap = (ctx + 5 + 63) // 64 * 64

@@ -8,10 +8,14 @@
 // softmax in fp32 (exp2 domain), P rounded to bf16 for the PV product.
 // Only the key blocks inside the causal (and window) range are visited.
 //
-// Decode: split-KV. Each CTA takes one (sequence, kv head, key chunk), scores
-// all query heads of its group against the chunk with 16-byte loads, and
-// writes an unnormalised partial (max, sum, output); a combine kernel merges
-// the partials in split order, so the result does not depend on scheduling.
+// Decode: split-KV over a thread-block cluster. The CTAs of one cluster share
+// one (sequence, kv head) and split its key range into equal runs of 64-key
+// tiles; each scores all query heads of the GQA group against its tiles with
+// 16-byte loads and keeps an unnormalised partial (max, sum, output) in its
+// shared memory. After a cluster barrier the CTAs merge the partials through
+// distributed shared memory, each CTA finishing a slice of the outputs and
+// adding the partials in rank order, so the result does not depend on
+// scheduling and no partial result leaves the chip.
 #include <algorithm>
 #include <mutex>
 
@@ -236,7 +240,8 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
 // ---------------------------------------------------------------------------
 // decode
 // ---------------------------------------------------------------------------
-// One CTA per (key chunk, kv head, sequence). The query heads of the GQA group
+// One CTA per (key split, kv head, sequence); the splits of a (sequence, kv
+// head) form one cluster of `gridDim.x` CTAs. The query heads of the GQA group
 // (<= 8) form the 16 MMA rows (rows >= group are zero); each of the 4 warps
 // takes 16 keys of every 64-key tile, keeps its own online-softmax state, and
 // the warps are merged in shared memory at the end. K/V tiles stream through
@@ -244,6 +249,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
 constexpr int kDecThreads = 128;
 constexpr int kMaxGroup = 8;
 constexpr int kDecTile = 64;
+constexpr int kMaxCluster = 16;
 
 template <int HD>
 struct DecCfg {
@@ -252,40 +258,118 @@ struct DecCfg {
   static constexpr int SMEM = (16 * HD + NST * 2 * TILE_ELEMS) * 2;
 };
 
+FK_DEVICE void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+FK_DEVICE uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+FK_DEVICE float dsmem_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Arguments of the decode kernel. With fused RoPE (a session's decode step),
+// q points at the token's qkv row [q heads | k heads | v heads] (ldq = the row
+// stride): the kernel applies [QK-norm and] RoPE at position ctx-1, writes
+// the new key and value into the caches and attends over them; otherwise q
+// holds the query heads with RoPE applied and the caches are complete.
+struct DecArgs {
+  const __nv_bfloat16* q;
+  int ldq;
+  const __nv_bfloat16* kc;  // [B][Hkv][cap][HD]
+  const __nv_bfloat16* vc;  // transposed: [B][Hkv][HD][cap]
+  int cap, ctx_host;
+  const int* d_ctx;  // non-null: ctx = *d_ctx + 1
+  int Hq, Hkv, window;
+  float scale_log2;
+  __nv_bfloat16* o;
+  // fused RoPE
+  const float2* rope;  // [positions][HD/2] (cos, sin) of frequency j
+  int qk_norm;
+  const __nv_bfloat16* q_norm;
+  const __nv_bfloat16* k_norm;
+  float eps;
+  __nv_bfloat16* kc_w;  // the caches again, written at position ctx-1
+  __nv_bfloat16* vc_w;
+};
+
+// [QK-norm and] RoPE of one head held by a warp: lane owns elements
+// e0..e0+C-1 of each half (pairs (j, j+HD/2)); returns the rotated values.
 template <int HD>
-__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
-    const __nv_bfloat16* __restrict__ q, int ldq, const __nv_bfloat16* __restrict__ kc,
-    const __nv_bfloat16* __restrict__ vc, int cap, int ctx_host, const int* d_ctx, int Hq, int Hkv, int window,
-    float scale_log2, int chunk, int n_splits, float* __restrict__ part_o, float* __restrict__ part_ml) {
-  pdl_trigger();
-  pdl_wait();
+FK_DEVICE void rope_head(const __nv_bfloat16* src, const DecArgs& a, const __nv_bfloat16* nw, int pos, int lane,
+                         float* olo, float* ohi) {
+  constexpr int C = HD / 64, HALF = HD / 2;
+  const int e0 = lane * C;
+  float lo[C], hi[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    lo[i] = __bfloat162float(src[e0 + i]);
+    hi[i] = __bfloat162float(src[HALF + e0 + i]);
+  }
+  if (a.qk_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < C; ++i) ss += lo[i] * lo[i] + hi[i] * hi[i];
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / HD + a.eps);
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      lo[i] = lo[i] * r * __bfloat162float(nw[e0 + i]);
+      hi[i] = hi[i] * r * __bfloat162float(nw[HALF + e0 + i]);
+    }
+  }
+  const float2* cs = a.rope + (size_t)pos * HALF + e0;
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const float2 c = cs[i];
+    olo[i] = lo[i] * c.x - hi[i] * c.y;
+    ohi[i] = hi[i] * c.x + lo[i] * c.y;
+  }
+}
+
+template <int HD, bool ROPE>
+__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const DecArgs a) {
   using C = DecCfg<HD>;
+  constexpr int NC = HD / 64, HALF = HD / 2;
   extern __shared__ uint4 smem_u4[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_u4);
   __nv_bfloat16* sKV = sQ + 16 * HD;  // [NST][K tile, V tile]
+  __shared__ __align__(16) __nv_bfloat16 sNew[2][HD];  // fused RoPE: the new key and value
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int n_splits = gridDim.x;  // = the cluster size: blockIdx.x is the rank
+  const int Hq = a.Hq, Hkv = a.Hkv, cap = a.cap, window = a.window;
   const int group = Hq / Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ctx = d_ctx ? *d_ctx + 1 : ctx_host;  // *d_ctx: tokens before the new one
+  pdl_trigger();
+  // Without fused RoPE everything below depends on the previous kernel. With
+  // it, the cache positions before the new token and the length were written
+  // by kernels that completed before the previous kernel (the QKV projection)
+  // passed its own wait, which precedes its trigger: the K/V tiles are
+  // requested first, and only the new token's q/k/v wait for the projection.
+  if (!ROPE) pdl_wait();
+  const int ctx = a.d_ctx ? *a.d_ctx + 1 : a.ctx_host;  // *d_ctx: tokens before the new one
   const int qpos = ctx - 1;
-  int lo = split * chunk;
-  const int hi = min(ctx, lo + chunk);
-  if (window > 0) lo = max(lo, qpos - window + 1);
-  // tiles start on a 64-key boundary (16-byte aligned V^T rows); keys outside
-  // [lo, hi) inside a tile are masked
-  const int t0 = lo & ~(kDecTile - 1);
-  const int ntiles = hi > lo ? (hi - t0 + kDecTile - 1) / kDecTile : 0;
+  // visible keys [lo, hi); tiles start on a 64-key boundary (16-byte aligned
+  // V^T rows) and the splits take equal runs of tiles; keys outside [lo, hi)
+  // inside a tile are masked
+  const int lo = window > 0 ? max(0, qpos - window + 1) : 0;
+  const int hi = ctx;
+  const int tfirst = lo / kDecTile, n_all = (hi + kDecTile - 1) / kDecTile - tfirst;
+  const int ta = tfirst + (int)((long)split * n_all / n_splits);
+  const int ntiles = tfirst + (int)((long)(split + 1) * n_all / n_splits) - ta;
+  const int t0 = ta * kDecTile;
+  const int t_new = ROPE ? qpos / kDecTile - ta : -1;  // this CTA's tile holding the new token, if any
   const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
-  const __nv_bfloat16* kbase = kc + head_off;
-  const __nv_bfloat16* vbase = vc + head_off;  // V^T: [HD][cap]
+  const __nv_bfloat16* kbase = a.kc + head_off;
+  const __nv_bfloat16* vbase = a.vc + head_off;  // V^T: [HD][cap]
   constexpr int CPR = HD / 8;
   constexpr int CPV = kDecTile / 8;
 
-  for (int i = tid; i < 16 * CPR; i += kDecThreads) {
-    const int r = i / CPR, cc = i % CPR;
-    const __nv_bfloat16* src = q + (size_t)b * ldq + (size_t)(g * group + min(r, group - 1)) * HD + cc * 8;
-    cp_async16(sQ + swz<HD>(r, cc * 8), src, r < group ? 16 : 0);
-  }
   auto load_tile = [&](int t, int buf) {
     __nv_bfloat16* dk = sKV + (size_t)buf * 2 * C::TILE_ELEMS;
     __nv_bfloat16* dv = dk + C::TILE_ELEMS;
@@ -300,12 +384,66 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
       cp_async16(dv + swz<kDecTile>(d, cc * 8), vbase + (size_t)d * cap + t0 + t * kDecTile + cc * 8, 16);
     }
   };
-  cp_async_commit();  // Q
+  if (ROPE) {
 #pragma unroll
-  for (int t = 0; t < C::NST - 1; ++t) {
-    if (t < ntiles) load_tile(t, t);
-    cp_async_commit();
+    for (int t = 0; t < C::NST - 1; ++t) {
+      if (t < ntiles) load_tile(t, t);
+      cp_async_commit();
+    }
+    pdl_wait();
+    const __nv_bfloat16* row = a.q + (size_t)b * a.ldq;
+    // roped query heads of the group -> sQ rows (rows >= group stay zero)
+    for (int r = warp; r < 16; r += kDecThreads / 32) {
+      float olo[NC], ohi[NC];
+      if (r < group) {
+        rope_head<HD>(row + (size_t)(g * group + r) * HD, a, a.q_norm, qpos, lane, olo, ohi);
+      } else {
+#pragma unroll
+        for (int i = 0; i < NC; ++i) olo[i] = ohi[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
+        sQ[swz<HD>(r, lane * NC + i)] = __float2bfloat16_rn(olo[i]);
+        sQ[swz<HD>(r, HALF + lane * NC + i)] = __float2bfloat16_rn(ohi[i]);
+      }
+    }
+    // the new key (roped) and value; the CTA whose tiles hold position qpos
+    // stores them in the caches
+    if (warp == 0) {
+      float olo[NC], ohi[NC];
+      rope_head<HD>(row + (size_t)(Hq + g) * HD, a, a.k_norm, qpos, lane, olo, ohi);
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
+        sNew[0][lane * NC + i] = __float2bfloat16_rn(olo[i]);
+        sNew[0][HALF + lane * NC + i] = __float2bfloat16_rn(ohi[i]);
+      }
+    } else if (warp == 1) {
+      const __nv_bfloat16* vs = row + (size_t)(Hq + Hkv + g) * HD;
+      for (int d = lane; d < HD; d += 32) sNew[1][d] = vs[d];
+    }
+    __syncthreads();
+    if (t_new >= 0 && t_new < ntiles) {
+      __nv_bfloat16* kw = a.kc_w + head_off + (size_t)qpos * HD;
+      __nv_bfloat16* vw = a.vc_w + head_off + qpos;
+      for (int d = tid; d < HD; d += kDecThreads) {
+        kw[d] = sNew[0][d];
+        vw[(size_t)d * cap] = sNew[1][d];
+      }
+    }
+  } else {
+    for (int i = tid; i < 16 * CPR; i += kDecThreads) {
+      const int r = i / CPR, cc = i % CPR;
+      const __nv_bfloat16* src = a.q + (size_t)b * a.ldq + (size_t)(g * group + min(r, group - 1)) * HD + cc * 8;
+      cp_async16(sQ + swz<HD>(r, cc * 8), src, r < group ? 16 : 0);
+    }
+    cp_async_commit();  // Q
+#pragma unroll
+    for (int t = 0; t < C::NST - 1; ++t) {
+      if (t < ntiles) load_tile(t, t);
+      cp_async_commit();
+    }
   }
+  const float scale_log2 = a.scale_log2;
 
   float oacc[HD / 8][4];
 #pragma unroll
@@ -316,6 +454,16 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
   for (int t = 0; t < ntiles; ++t) {
     cp_async_wait<C::NST - 2>();
     __syncthreads();
+    if (ROPE && t == t_new) {  // the cached copy of the new token is stale: patch the tile
+      __nv_bfloat16* dk = sKV + (size_t)(t % C::NST) * 2 * C::TILE_ELEMS;
+      __nv_bfloat16* dv = dk + C::TILE_ELEMS;
+      const int r = qpos - (t0 + t * kDecTile);
+      for (int d = tid; d < HD; d += kDecThreads) {
+        dk[swz<HD>(r, d)] = sNew[0][d];
+        dv[swz<kDecTile>(d, r)] = sNew[1][d];
+      }
+      __syncthreads();
+    }
     {
       const int tn = t + C::NST - 1;
       if (tn < ntiles) load_tile(tn, tn % C::NST);
@@ -416,6 +564,10 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
     sL[warp * 16 + r1] = l1;
   }
   __syncthreads();
+  // this CTA's partial per query head: sP [group][HD] (unnormalised), sPM, sPL
+  float* sP = sL + 64;
+  float* sPM = sP + kMaxGroup * HD;
+  float* sPL = sPM + kMaxGroup;
   for (int i = tid; i < group * HD; i += kDecThreads) {
     const int r = i / HD, d = i % HD;
     float M = -INFINITY;
@@ -433,39 +585,46 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
         }
       }
     }
-    const int h = g * group + r;
-    const size_t base = ((size_t)b * Hq + h) * n_splits + split;
-    part_o[base * HD + d] = acc;
+    sP[r * HD + d] = acc;
     if (d == 0) {
-      part_ml[base * 2] = M;
-      part_ml[base * 2 + 1] = L;
+      sPM[r] = M;
+      sPL[r] = L;
     }
   }
-}
-
-template <int HD>
-__global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hq,
-                                    int n_splits, __nv_bfloat16* __restrict__ o) {
-  pdl_trigger();
-  pdl_wait();
-  const int h = blockIdx.x, b = blockIdx.y;
-  const size_t base = ((size_t)b * Hq + h) * n_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, part_ml[(base + s) * 2]);
-  float L = 0.f;
-  for (int s = 0; s < n_splits; ++s) {
-    const float m = part_ml[(base + s) * 2];
-    if (m != -INFINITY) L += part_ml[(base + s) * 2 + 1] * exp2f(m - M);
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  for (int d = threadIdx.x; d < HD; d += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-      const float m = part_ml[(base + s) * 2];
-      if (m != -INFINITY) acc += part_o[(base + s) * HD + d] * exp2f(m - M);
+  cluster_sync();  // every split's partial is in its shared memory
+  // CTA `split` finishes outputs [split*per, (split+1)*per) of the group's
+  // group*HD values, reading the n_splits partials in rank order
+  const int total = group * HD;
+  const int per = (total + n_splits - 1) / n_splits;
+  const int i_end = min(total, (split + 1) * per);
+  for (int i = split * per + tid; i < i_end; i += kDecThreads) {
+    const int r = i / HD;
+    float m[kMaxCluster], v[kMaxCluster], l[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      m[c] = -INFINITY;
+      v[c] = l[c] = 0.f;
+      if (c < n_splits) {
+        m[c] = dsmem_ld(dsmem_addr(sPM + r, c));
+        l[c] = dsmem_ld(dsmem_addr(sPL + r, c));
+        v[c] = dsmem_ld(dsmem_addr(sP + i, c));
+      }
     }
-    o[((size_t)b * Hq + h) * HD + d] = __float2bfloat16_rn(acc * inv);
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) M = fmaxf(M, m[c]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      if (m[c] != -INFINITY) {
+        const float f = exp2f(m[c] - M);
+        L += l[c] * f;
+        acc += v[c] * f;
+      }
+    }
+    a.o[((size_t)b * Hq + g * group + r) * HD + (i - r * HD)] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
   }
+  cluster_sync();  // no CTA leaves while another may still read its partial
 }
 
 template <int HD>
@@ -500,53 +659,138 @@ cudaError_t launch_attention_prefill(const void* q, int ldq, const void* kcache,
   return cudaErrorInvalidValue;
 }
 
-size_t decode_attention_scratch_bytes(int B, int Hq, int hd, int max_splits) {
-  return (size_t)B * Hq * max_splits * (hd + 2) * sizeof(float) + 256;
-}
-
-int decode_attention_splits(int B, int Hkv, int max_ctx, int sm_count, int* chunk) {
-  const long target = 4L * sm_count;
-  long c = ((long)max_ctx * B * Hkv + target - 1) / target;
-  c = (c + kDecTile - 1) / kDecTile * kDecTile;
-  c = std::max((long)kDecTile, c);
-  *chunk = (int)c;
-  return (int)((max_ctx + c - 1) / c);
+// Largest cluster of decode CTAs the GPU co-schedules for this head_dim
+// (a cluster of 16 is beyond the portable size and is allowed explicitly).
+template <int HD, bool ROPE>
+cudaError_t decode_attrs() {
+  using C = DecCfg<HD>;
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<HD, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<HD, ROPE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 template <int HD>
-cudaError_t decode_hd(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int ctx,
-                      const int* d_ctx, int Hq, int Hkv, int window, float sl, int chunk, int n_splits, float* part_o,
-                      float* part_ml, void* o, cudaStream_t st) {
+int decode_max_cluster(cudaError_t* err) {
   using C = DecCfg<HD>;
   static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
+  static cudaError_t e0 = cudaSuccess;
+  static int n = 1;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(attn_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e0 = decode_attrs<HD, false>();
+    if (e0 == cudaSuccess) e0 = decode_attrs<HD, true>();
+    if (e0 != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxCluster, 1, 1);
+    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    int c = 0, c2 = 0;
+    if (cudaOccupancyMaxPotentialClusterSize(&c, attn_decode_kernel<HD, false>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxPotentialClusterSize(&c2, attn_decode_kernel<HD, true>, &cfg) != cudaSuccess || c < 1 ||
+        c2 < 1) {
+      cudaGetLastError();
+      c = c2 = 8;  // the portable size
+    }
+    n = std::min(std::min(c, c2), kMaxCluster);
   });
+  *err = e0;
+  return n;
+}
+
+template <int HD>
+int decode_resident_per_sm() {
+  int dev = 0, smem_sm = 0, reserved = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  return std::max(1, smem_sm / (DecCfg<HD>::SMEM + 2 * HD * 2 + reserved));
+}
+
+int decode_attention_splits(int B, int Hkv, int hd, int max_ctx, int sm_count) {
+  cudaError_t e = cudaSuccess;
+  int maxc = 1, res = 1;
+  switch (hd) {
+    case 64: maxc = decode_max_cluster<64>(&e); res = decode_resident_per_sm<64>(); break;
+    case 128: maxc = decode_max_cluster<128>(&e); res = decode_resident_per_sm<128>(); break;
+    case 256: maxc = decode_max_cluster<256>(&e); res = decode_resident_per_sm<256>(); break;
+    default: return 1;
+  }
+  if (e != cudaSuccess) return 1;
+  const long want = std::max(1L, (long)res * sm_count / ((long)B * Hkv));
+  const long lim = std::min<long>({(long)maxc, want, (max_ctx + kDecTile - 1L) / kDecTile});
+  int cs = 1;
+  while (cs * 2 <= lim) cs *= 2;
+  return cs;
+}
+
+template <int HD>
+cudaError_t decode_hd(const DecArgs& a, bool rope, int B, int n_splits, cudaStream_t st) {
+  using C = DecCfg<HD>;
+  cudaError_t err = cudaSuccess;
+  const int maxc = decode_max_cluster<HD>(&err);
   if (err != cudaSuccess) return err;
-  dim3 grid(n_splits, Hkv, B);
-  cudaError_t e = fk_launch(attn_decode_kernel<HD>, grid, kDecThreads, C::SMEM, st, static_cast<const __nv_bfloat16*>(q),
-                            ldq, static_cast<const __nv_bfloat16*>(kcache), static_cast<const __nv_bfloat16*>(vcache),
-                            cap, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml);
-  if (e != cudaSuccess) return e;
-  return fk_launch(attn_combine_kernel<HD>, dim3(Hq, B), HD < 128 ? HD : 128, 0, st, (const float*)part_o,
-                   (const float*)part_ml, Hq, n_splits, static_cast<__nv_bfloat16*>(o));
+  if (n_splits < 1 || n_splits > maxc) return cudaErrorInvalidValue;
+  const dim3 grid(n_splits, a.Hkv, B);
+  if (rope) return fk_launch_cluster(attn_decode_kernel<HD, true>, grid, kDecThreads, C::SMEM, st, n_splits, a);
+  return fk_launch_cluster(attn_decode_kernel<HD, false>, grid, kDecThreads, C::SMEM, st, n_splits, a);
+}
+
+cudaError_t decode_dispatch(const DecArgs& a, bool rope, int hd, int B, int n_splits, cudaStream_t st) {
+  if (B == 0) return cudaSuccess;
+  if (a.Hq / a.Hkv > kMaxGroup) return cudaErrorInvalidValue;
+  switch (hd) {
+    case 64: return decode_hd<64>(a, rope, B, n_splits, st);
+    case 128: return decode_hd<128>(a, rope, B, n_splits, st);
+    case 256: return decode_hd<256>(a, rope, B, n_splits, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
                                     int ctx, const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
-                                    int chunk, int n_splits, void* scratch, void* o, cudaStream_t st) {
-  if (B == 0) return cudaSuccess;
-  if (Hq / Hkv > kMaxGroup || chunk % kDecTile) return cudaErrorInvalidValue;
-  float* part_o = static_cast<float*>(scratch);
-  float* part_ml = part_o + (size_t)B * Hq * n_splits * hd;
-  const float sl = scale * kLog2e;
-  switch (hd) {
-    case 64: return decode_hd<64>(q, ldq, kcache, vcache, cap, B, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml, o, st);
-    case 128: return decode_hd<128>(q, ldq, kcache, vcache, cap, B, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml, o, st);
-    case 256: return decode_hd<256>(q, ldq, kcache, vcache, cap, B, ctx, d_ctx, Hq, Hkv, window, sl, chunk, n_splits, part_o, part_ml, o, st);
-  }
-  return cudaErrorInvalidValue;
+                                    int n_splits, void* o, cudaStream_t st) {
+  DecArgs a = {};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.ldq = ldq;
+  a.kc = static_cast<const __nv_bfloat16*>(kcache);
+  a.vc = static_cast<const __nv_bfloat16*>(vcache);
+  a.cap = cap;
+  a.ctx_host = ctx;
+  a.d_ctx = d_ctx;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.window = window;
+  a.scale_log2 = scale * kLog2e;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  return decode_dispatch(a, false, hd, B, n_splits, st);
+}
+
+cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcache, void* vcache, int cap, int B,
+                                         const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
+                                         const float2* rope, int qk_norm, const void* q_norm, const void* k_norm,
+                                         float eps, int n_splits, void* o, cudaStream_t st) {
+  if (!d_ctx) return cudaErrorInvalidValue;
+  DecArgs a = {};
+  a.q = static_cast<const __nv_bfloat16*>(qkv);
+  a.ldq = ldqkv;
+  a.kc = static_cast<const __nv_bfloat16*>(kcache);
+  a.vc = static_cast<const __nv_bfloat16*>(vcache);
+  a.kc_w = static_cast<__nv_bfloat16*>(kcache);
+  a.vc_w = static_cast<__nv_bfloat16*>(vcache);
+  a.cap = cap;
+  a.d_ctx = d_ctx;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.window = window;
+  a.scale_log2 = scale * kLog2e;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.rope = rope;
+  a.qk_norm = qk_norm;
+  a.q_norm = static_cast<const __nv_bfloat16*>(q_norm);
+  a.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
+  a.eps = eps;
+  return decode_dispatch(a, true, hd, B, n_splits, st);
 }
 }  // namespace fk
 
@@ -556,6 +800,10 @@ cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, 
 #include "fk_internal.h"
 
 namespace {
+// The scratch of fk_attention_decode is kept in the interface (a later kernel
+// may use it) but the cluster kernel writes nothing there.
+constexpr size_t kDecodeScratchBytes = 256;
+
 fk_status check_decode_args(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int hd, int cap,
                             int ctx, int window, const void* out) {
   using fk::fail;
@@ -572,20 +820,19 @@ fk_status check_decode_args(const void* q, const void* kc, const void* vc, int B
 }  // namespace
 
 namespace fk {
-// shared by the scratch-taking and the allocation-free entry points
-fk_status attention_decode_plan(int B, int Hq, int Hkv, int hd, int ctx, int* chunk, int* splits, size_t* bytes) {
+// shared by the scratch-taking and the allocation-free entry points: the
+// kernel keeps its split partials on chip, so neither needs device memory
+fk_status attention_decode_plan(int B, int Hkv, int hd, int ctx, int* splits) {
   int sms = 0;
   fk_status s = check_device(&sms);
   if (s != FK_OK) return s;
-  *splits = decode_attention_splits(B, Hkv, ctx, sms, chunk);
-  *bytes = decode_attention_scratch_bytes(B, Hq, hd, *splits);
+  *splits = decode_attention_splits(B, Hkv, hd, ctx, sms);
   return FK_OK;
 }
 fk_status attention_decode_run(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int hd, int cap,
-                               int ctx, int window, int chunk, int splits, void* scratch, void* out,
-                               cudaStream_t st) {
+                               int ctx, int window, int splits, void* out, cudaStream_t st) {
   cudaError_t e = launch_attention_decode(q, Hq * hd, kc, vc, cap, B, ctx, nullptr, Hq, Hkv, hd, window,
-                                          1.0f / sqrtf((float)hd), chunk, splits, scratch, out, st);
+                                          1.0f / sqrtf((float)hd), splits, out, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention decode launch");
   return FK_OK;
 }
@@ -594,11 +841,7 @@ fk_status attention_decode_run(const void* q, const void* kc, const void* vc, in
 extern "C" size_t fk_attention_decode_scratch_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
                                                     int32_t head_dim, int32_t ctx) {
   if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || ctx < 1) return 0;
-  int chunk = 0, splits = 0;
-  size_t bytes = 0;
-  if (fk::attention_decode_plan(batch, n_q_heads, n_kv_heads, head_dim, ctx, &chunk, &splits, &bytes) != FK_OK)
-    return 0;
-  return bytes;
+  return kDecodeScratchBytes;
 }
 
 extern "C" fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
@@ -608,12 +851,11 @@ extern "C" fk_status fk_attention_decode(const void* d_q, const void* d_kcache, 
   fk_status s = check_decode_args(d_q, d_kcache, d_vcache, batch, n_q_heads, n_kv_heads, head_dim, cap, ctx, window,
                                   d_out);
   if (s != FK_OK) return s;
-  int chunk = 0, splits = 0;
-  size_t need = 0;
-  s = fk::attention_decode_plan(batch, n_q_heads, n_kv_heads, head_dim, ctx, &chunk, &splits, &need);
+  if (!d_scratch || scratch_bytes < kDecodeScratchBytes)
+    return fk::fail(FK_ERR_WORKSPACE, "attention decode: scratch too small");
+  int splits = 1;
+  s = fk::attention_decode_plan(batch, n_kv_heads, head_dim, ctx, &splits);
   if (s != FK_OK) return s;
-  if (!d_scratch || scratch_bytes < need) return fk::fail(FK_ERR_WORKSPACE, "attention decode: scratch too small");
-  if (reinterpret_cast<uintptr_t>(d_scratch) & 15) return fk::fail(FK_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
   return fk::attention_decode_run(d_q, d_kcache, d_vcache, batch, n_q_heads, n_kv_heads, head_dim, cap, ctx, window,
-                                  chunk, splits, d_scratch, d_out, static_cast<cudaStream_t>(stream));
+                                  splits, d_out, static_cast<cudaStream_t>(stream));
 }

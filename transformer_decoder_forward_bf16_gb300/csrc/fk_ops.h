@@ -41,12 +41,22 @@ cudaError_t launch_attention_prefill(const void* q, int ldq, const void* kcache,
 
 // One query per sequence at position ctx-1 (ctx = keys in the cache; if
 // d_ctx is non-null, ctx = *d_ctx + 1, *d_ctx being the length before the
-// new token). Split-KV: partial results in `scratch`
-// (fk::decode_attention_scratch_bytes), combined in a fixed order.
-size_t decode_attention_scratch_bytes(int B, int Hq, int hd, int max_splits);
-int decode_attention_splits(int B, int Hkv, int max_ctx, int sm_count, int* chunk);
+// new token). Split-KV over a cluster of n_splits CTAs per (sequence, kv
+// head), merged on chip in a fixed order. decode_attention_splits picks
+// n_splits (a power of two <= 16) for a batch, head_dim and longest context.
+int decode_attention_splits(int B, int Hkv, int hd, int max_ctx, int sm_count);
 cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
                                     int ctx, const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
-                                    int chunk, int n_splits, void* scratch, void* o, cudaStream_t st);
+                                    int n_splits, void* o, cudaStream_t st);
+// A session's decode step (S == 1, length *d_ctx before the new token): takes
+// the token's qkv row (ldqkv = its stride), applies [QK-norm and] RoPE at
+// position *d_ctx to q and k as launch_rope_qkv does, writes k and v into the
+// caches and attends, all in one kernel. Launched after the QKV projection
+// with programmatic dependent launch, it reads the caches' earlier positions
+// before waiting for the projection.
+cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcache, void* vcache, int cap, int B,
+                                         const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
+                                         const float2* rope, int qk_norm, const void* q_norm, const void* k_norm,
+                                         float eps, int n_splits, void* o, cudaStream_t st);
 
 }  // namespace fk

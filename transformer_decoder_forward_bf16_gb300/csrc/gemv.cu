@@ -31,7 +31,7 @@ constexpr int A_BYTES = 128 * 64 * 2;
 struct SkinnyArgs {
   int M, K, n_rows, nseg;
   int seg_start[4];
-  int kb_per_split, nk;
+  int nk;  // k-blocks of 64; split s covers [s*nk/S, (s+1)*nk/S), S = gridDim.y
   float* part;  // [splits][M][n_rows]
   unsigned* dev_err;
   // fused reduction: the last CTA to finish a feature group sums the splits
@@ -52,12 +52,24 @@ FK_DEVICE float act_gelu_tanh(float g) {
 // Sum the splits of one feature for every token (fixed split order) and store
 // the epilogue's result. v: gate (or plain) feature f, u: up feature (GLU).
 FK_DEVICE void reduce_store(const SkinnyArgs& a, int S, int f) {
+  constexpr int U = 8;  // splits loaded per batch (all in flight before the in-order adds)
+  const size_t sstride = (size_t)a.M * a.n_rows;
   for (int t = 0; t < a.M; ++t) {
     float v = 0.f, u = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float* p = a.part + ((size_t)s * a.M + t) * a.n_rows;
-      v += __ldcg(p + f);
-      if (a.glu_tiles) u += __ldcg(p + a.n_out + f);
+    const float* p = a.part + (size_t)t * a.n_rows + f;
+    for (int s0 = 0; s0 < S; s0 += U) {
+      float tv[U], tu[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const bool in = s0 + j < S;
+        tv[j] = in ? __ldcg(p + (size_t)(s0 + j) * sstride) : 0.f;
+        tu[j] = in && a.glu_tiles ? __ldcg(p + (size_t)(s0 + j) * sstride + a.n_out) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        v += tv[j];
+        u += tu[j];
+      }
     }
     if (a.epi == EPI_GLU_BF16) {
       static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] =
@@ -100,8 +112,8 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * 128;
   const int split = blockIdx.y;
-  const int kb0 = split * args.kb_per_split;
-  const int kb1 = min(args.nk, kb0 + args.kb_per_split);
+  const int kb0 = (int)((long)split * args.nk / gridDim.y);
+  const int kb1 = (int)((long)(split + 1) * args.nk / gridDim.y);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -124,8 +136,14 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  pdl_trigger();
-  if (!(warp == 0 && lane == 0)) pdl_wait();
+  // The dependent kernel is released only after this grid's wait, i.e. once
+  // every kernel before this one has completed: a dependent may then read,
+  // before its own wait, anything those kernels wrote (the decode attention
+  // reads the KV cache's earlier positions while this projection runs).
+  if (!(warp == 0 && lane == 0)) {
+    pdl_wait();
+    pdl_trigger();
+  }
   if (warp == 0 && lane == 0) {
     // ---- producer: two 64-row weight boxes + one token box per stage. The
     // weights do not depend on the previous kernel, so the first stages are
@@ -156,6 +174,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
           tma_load_2d_hint(maps[map[i]], &full[it], sa + i * 64 * 128, (kb0 + it) * 64, row[i], evict_first);
     }
     pdl_wait();
+    pdl_trigger();
     for (int it = 0; it < npre; ++it) {
       tma_load_2d(&tmX, &full[it], smem + it * C::STAGE + A_BYTES, (kb0 + it) * 64, 0);
       ++issued[it];
@@ -288,6 +307,9 @@ cudaError_t set_smem_attr() {
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
     attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfg<BT>::SMEM);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared);
   });
   return attr;
 }
@@ -306,43 +328,33 @@ fk_status launch_bt(const CUtensorMap& tX, const GemmWeights& w, const SkinnyArg
 
 }  // namespace
 
-// CTAs of the skinny kernel that fit on one SM at once (shared memory bound).
+// CTAs of the skinny kernel that fit on one SM at once: shared memory bound
+// (the kernels ask for the largest shared-memory carveout, so this is the
+// SM's whole shared memory over each CTA's dynamic + reserved bytes).
 static int resident_per_sm(int M) {
   static int cached[3] = {0, 0, 0};
   const int i = M <= 16 ? 0 : (M <= 32 ? 1 : 2);
   if (!cached[i]) {
-    int n = 0;
-    cudaError_t e;
-    set_smem_attr<16>();
-    set_smem_attr<32>();
-    set_smem_attr<64>();
-    if (i == 0)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_tc_kernel<16>, kThreads, SCfg<16>::SMEM);
-    else if (i == 1)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_tc_kernel<32>, kThreads, SCfg<32>::SMEM);
-    else
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_tc_kernel<64>, kThreads, SCfg<64>::SMEM);
-    if (e != cudaSuccess || n < 1) {
-      cudaGetLastError();
-      n = 2;
-    }
-    cached[i] = n;
+    int dev = 0, smem_sm = 0, reserved = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    const int smem = i == 0 ? SCfg<16>::SMEM : (i == 1 ? SCfg<32>::SMEM : SCfg<64>::SMEM);
+    cached[i] = std::max(1, std::min(2048 / kThreads, smem_sm / (smem + reserved)));
   }
   return cached[i];
 }
 
-
-// Split K so that the whole grid is one wave of resident CTAs: every CTA
-// starts at once (and, in the decode step, requests its first weight tiles
-// while the previous kernel drains), and none waits for a second wave.
+// Split K so that the whole grid is one wave of resident CTAs, every SM
+// holding the same number: each CTA starts at once and streams an equal
+// share of the weights (splits differ by at most one k-block).
 SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count) {
   SkinnyPlan p;
   const int nk = (K + 63) / 64;
   const int n_tiles = (n_rows + 127) / 128;
   const int wave = resident_per_sm(M) * sm_count;
-  int splits = std::max(1, std::min(nk, wave / n_tiles));
-  p.kb_per_split = (nk + splits - 1) / splits;
-  p.splits = (nk + p.kb_per_split - 1) / p.kb_per_split;
+  p.splits = std::max(1, std::min(nk, wave / n_tiles));
+  p.kb_per_split = (nk + p.splits - 1) / p.splits;  // the longest split
   p.n_tiles = n_tiles;
   p.nk = nk;
   p.counter_bytes = ((size_t)n_tiles * sizeof(unsigned) + 255) / 256 * 256;
@@ -375,7 +387,6 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   a.n_rows = n_rows;
   a.nseg = w.nseg;
   for (int i = 0; i < 4; ++i) a.seg_start[i] = w.seg_start[i];
-  a.kb_per_split = p.kb_per_split;
   a.nk = p.nk;
   a.counters = static_cast<unsigned*>(scratch);
   a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + p.counter_bytes);

@@ -80,8 +80,7 @@ struct fk_session {
   int32_t* next_ids = nullptr;  // [B]
   float* logits = nullptr;      // [B, V]
   void* u_last = nullptr;       // [B, H] bf16
-  void* dec_scratch = nullptr;
-  int dec_chunk = 0, dec_splits = 0;
+  int dec_splits = 1;  // decode attention: CTAs per (sequence, kv head) cluster
   int* d_len = nullptr;          // device copy of len (read by decode kernels)
   bool d_len_valid = false;      // false after reset until the next prefill
   // captured decode step (feeds the previous greedy ids), keyed by outputs
@@ -244,9 +243,9 @@ struct KV {
 // The decoder stack over T = B*S tokens at positions pos0 .. pos0+S-1 of
 // each sequence. Reads sc.ids; leaves the final-normed rows (bf16) in sc.u.
 // slots (optional): fp32 [L+2][T][H] hidden states. decode: S == 1, attention
-// through the split-KV kernel with dscratch.
+// through the split-KV cluster kernel with dsplits CTAs per cluster.
 fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, const KV& kv, float* slots,
-                    bool decode, void* dscratch, int dchunk, int dsplits, cudaStream_t st,
+                    bool decode, int dsplits, cudaStream_t st,
                     const int* d_len = nullptr, const int32_t* ids = nullptr) {
   const fk_config& c = m->cfg;
   const int H = c.hidden, L = c.n_layers, hd = c.head_dim;
@@ -277,15 +276,15 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     o.out = sc.qkv;
     o.ldo = m->Nqkv;
     { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb)); }
-    { ProfScope ps(decode ? "rope_qkv_dec" : "rope_qkv", st);
-    FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, d_len, c.n_q_heads, c.n_kv_heads, hd,
-                              m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
-    if (decode) {
+    if (decode) {  // RoPE, cache write and attention in one kernel
       ProfScope ps("attn_decode", st);
-      FK_LAUNCH(launch_attention_decode(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, pos0 + 1, d_len, c.n_q_heads,
-                                        c.n_kv_heads, hd, window, m->attn_scale, dchunk, dsplits, dscratch, sc.ao,
-                                        st));
+      FK_LAUNCH(launch_attention_decode_rope(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, d_len, c.n_q_heads, c.n_kv_heads,
+                                             hd, window, m->attn_scale, m->rope[kind], c.qk_norm, w.q_norm, w.k_norm,
+                                             c.rms_eps, dsplits, sc.ao, st));
     } else {
+      { ProfScope ps("rope_qkv", st);
+      FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
+                                m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
       ProfScope ps("attn_prefill", st);
       if (attention_prefill_tc_supported(hd, m->Nqkv, kv.cap) && !getenv("FK_ATTN_MMA_SYNC")) {
         FK_TRY(attention_prefill_tc(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd, window,
@@ -544,7 +543,7 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
                               argmax_scratch_bytes() - argmax_counter_offset(), st));
   // attention reads V in 64-position blocks: positions past seq must hold finite values
   if (seq % 64) FK_CUDA_TRY(cudaMemsetAsync(kv.v, 0, kv.bytes, st));
-  FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, nullptr, 0, 0, st));
+  FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, 1, st));
   if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st));
   return FK_OK;
 }
@@ -571,9 +570,7 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
   uint8_t* next = take((size_t)B * 4);
   uint8_t* logits = take((size_t)B * c.vocab * 4);
   uint8_t* ul = take((size_t)B * c.hidden * 2);
-  int chunk = 0;
-  const int splits = decode_attention_splits(B, c.n_kv_heads, max_seq, m->sm_count, &chunk);
-  uint8_t* ds = take(decode_attention_scratch_bytes(B, c.n_q_heads, c.head_dim, splits));
+  const int splits = decode_attention_splits(B, c.n_kv_heads, c.head_dim, max_seq, m->sm_count);
   uint8_t* dl = take(sizeof(int));
   if (s) {
     s->d_len = reinterpret_cast<int*>(dl);
@@ -585,8 +582,6 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
     s->next_ids = reinterpret_cast<int32_t*>(next);
     s->logits = reinterpret_cast<float*>(logits);
     s->u_last = ul;
-    s->dec_scratch = ds;
-    s->dec_chunk = chunk;
     s->dec_splits = splits;
   }
   return off;
@@ -682,7 +677,7 @@ extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32
     FK_CUDA_TRY(cudaMemcpy2DAsync(s->sc.ids, C * sizeof(int32_t), ids + c0, seq * sizeof(int32_t),
                                   C * sizeof(int32_t), s->B,
                                   ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
-    FK_TRY(run_stack(m, s->sc, s->B, C, s->len, kv, nullptr, false, nullptr, 0, 0, st));
+    FK_TRY(run_stack(m, s->sc, s->B, C, s->len, kv, nullptr, false, 1, st));
     s->len += C;
   }
   FK_LAUNCH(launch_gather_last_rows(s->sc.u, m->cfg.hidden, C, m->cfg.hidden, s->B, s->u_last, st));
@@ -700,7 +695,7 @@ static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_lo
   // waits for its predecessor before touching data the predecessor writes)
   PdlScope pdl(true);
   KV kv{s->kcache, s->vcache, s->layer_kv, s->cap};
-  FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_scratch, s->dec_chunk, s->dec_splits, st,
+  FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_splits, st,
                    s->d_len, d_ids ? d_ids : s->next_ids));
   FK_TRY(session_head(s, s->sc.u, d_logits, d_next, st));
   FK_LAUNCH(launch_inc_int(s->d_len, st));
