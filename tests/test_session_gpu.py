@@ -57,6 +57,34 @@ def test_decode_matches_oracle(fk, kind):
     np.testing.assert_allclose(z.cpu().numpy(), ref["last_logits"], atol=0.05)
 
 
+@pytest.mark.parametrize("B", [1, 8, 24])
+def test_decode_with_wide_head_matches_cacheless_forward(fk, B):
+    """A vocabulary much wider than the layers: the LM head's split-K GEMM has
+    far more feature tiles than the layer GEMMs that share its scratch.
+    Several graph-replayed decode steps must each equal the cacheless forward
+    of the extended sequences at the new position (every logit written)."""
+    import torch
+    cfg = synth.small_config("llama", vocab=32768)
+    wb, model = _setup(fk, cfg)
+    S, steps = 40, 4
+    prompt = synth.make_ids(cfg, B, S)
+    sess = model.session(B, 64)
+    z = torch.empty((B, cfg.vocab), dtype=torch.float32, device="cuda")
+    nxt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    sess.prefill(prompt, logits=z, next_ids=nxt)
+    seq = [prompt, nxt.cpu().numpy().copy()[:, None]]
+    for _ in range(steps):
+        z.fill_(float("nan"))
+        sess.decode(None, logits=z, next_ids=nxt)
+        ext = np.concatenate(seq, axis=1).astype(np.int32)
+        full = model.forward(ext, hidden=False)
+        zf = full["logits"].view(B, ext.shape[1], -1)[:, -1]
+        torch.cuda.synchronize()
+        assert torch.isfinite(z).all()
+        assert torch.max(torch.abs(z - zf)).item() <= 1e-2
+        seq.append(nxt.cpu().numpy().copy()[:, None])
+
+
 def test_graph_decode_equals_launched_decode(fk):
     """Steps fed back from the previous argmax replay a captured CUDA graph;
     feeding the same ids explicitly launches kernel by kernel. Same bits."""

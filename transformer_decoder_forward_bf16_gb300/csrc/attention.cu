@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "fk_common.cuh"
+#include "fk_internal.h"
 #include "fk_ops.h"
 
 namespace fk {
@@ -241,36 +242,40 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* 
 // decode
 // ---------------------------------------------------------------------------
 // One CTA per (key split, kv head, sequence); the splits of a (sequence, kv
-// head) form one cluster of `gridDim.x` CTAs. The query heads of the GQA group
-// (<= 8) form the 16 MMA rows (rows >= group are zero); each of the 4 warps
-// takes 16 keys of every 64-key tile, keeps its own online-softmax state, and
-// the warps are merged in shared memory at the end. K/V tiles stream through
-// an NST-deep cp.async ring, so each CTA keeps NST-1 tiles in flight.
-constexpr int kDecThreads = 128;
+// head) form one cluster of `gridDim.x` CTAs. Warp 4 streams the CTA's 64-key
+// K and V^T tiles into an NST-deep shared-memory ring with TMA (mbarrier
+// completion; with fused RoPE it starts before the previous kernel has
+// finished, since it reads only earlier cache positions). Warps 0-3 consume
+// the ring: the query heads of the GQA group (<= 8) form the 16 MMA rows
+// (rows >= group are zero), each warp takes 16 keys of every tile, keeps its
+// own online-softmax state and releases the slot when done, so loads and
+// math overlap with no CTA-wide barrier per tile. The four warps are merged
+// in shared memory at the end.
+constexpr int kDecConsumers = 128;
+constexpr int kDecThreads = kDecConsumers + 32;
 constexpr int kMaxGroup = 8;
 constexpr int kDecTile = 64;
 constexpr int kMaxCluster = 16;
 
 template <int HD>
 struct DecCfg {
-  static constexpr int NST = HD == 256 ? 3 : (HD == 128 ? 3 : 4);
-  static constexpr int TILE_ELEMS = kDecTile * HD;
-  static constexpr int SMEM = (16 * HD + NST * 2 * TILE_ELEMS) * 2;
+  static constexpr int NST = HD == 64 ? 4 : (HD == 128 ? 3 : 2);
+  static constexpr int TILE_ELEMS = kDecTile * HD;          // K tile = V^T tile elements
+  static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;    // K + V^T
+  static constexpr int Q_BYTES = 16 * HD * 2;
+  static constexpr int RING_OFF = (Q_BYTES + 1023) / 1024 * 1024;
+  static constexpr int BAR_OFF = RING_OFF + NST * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + 128 + 1024;  // + barriers/flags, + base alignment slack
 };
 
-FK_DEVICE void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-FK_DEVICE uint32_t dsmem_addr(const void* local, uint32_t rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
-  return a;
-}
-FK_DEVICE float dsmem_ld(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+FK_DEVICE void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDecConsumers) : "memory"); }
+FK_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// element (r, c) of a K tile [64 keys][HD] stored as HD/64 TMA boxes of
+// [64][64] with the 128-byte swizzle
+template <int HD>
+FK_DEVICE int kswz(int r, int c) {
+  return (c >> 6) * (kDecTile * 64) + r * 64 + ((((c >> 3) & 7) ^ (r & 7)) << 3) + (c & 7);
 }
 
 // Arguments of the decode kernel. With fused RoPE (a session's decode step),
@@ -281,28 +286,27 @@ FK_DEVICE float dsmem_ld(uint32_t addr) {
 struct DecArgs {
   const __nv_bfloat16* q;
   int ldq;
-  const __nv_bfloat16* kc;  // [B][Hkv][cap][HD]
-  const __nv_bfloat16* vc;  // transposed: [B][Hkv][HD][cap]
   int cap, ctx_host;
   const int* d_ctx;  // non-null: ctx = *d_ctx + 1
   int Hq, Hkv, window;
   float scale_log2;
   __nv_bfloat16* o;
+  unsigned* dev_err;  // optional device error word (pipeline timeouts)
   // fused RoPE
   const float2* rope;  // [positions][HD/2] (cos, sin) of frequency j
   int qk_norm;
   const __nv_bfloat16* q_norm;
   const __nv_bfloat16* k_norm;
   float eps;
-  __nv_bfloat16* kc_w;  // the caches again, written at position ctx-1
+  __nv_bfloat16* kc_w;  // the caches, written at position ctx-1
   __nv_bfloat16* vc_w;
 };
 
 // [QK-norm and] RoPE of one head held by a warp: lane owns elements
-// e0..e0+C-1 of each half (pairs (j, j+HD/2)); returns the rotated values.
+// e0..e0+C-1 of each half (pairs (j, j+HD/2)); cs: this lane's (cos, sin).
 template <int HD>
-FK_DEVICE void rope_head(const __nv_bfloat16* src, const DecArgs& a, const __nv_bfloat16* nw, int pos, int lane,
-                         float* olo, float* ohi) {
+FK_DEVICE void rope_head(const __nv_bfloat16* src, const DecArgs& a, const __nv_bfloat16* nw, const float2* cs,
+                         int lane, float* olo, float* ohi) {
   constexpr int C = HD / 64, HALF = HD / 2;
   const int e0 = lane * C;
   float lo[C], hi[C];
@@ -323,28 +327,42 @@ FK_DEVICE void rope_head(const __nv_bfloat16* src, const DecArgs& a, const __nv_
       hi[i] = hi[i] * r * __bfloat162float(nw[HALF + e0 + i]);
     }
   }
-  const float2* cs = a.rope + (size_t)pos * HALF + e0;
 #pragma unroll
   for (int i = 0; i < C; ++i) {
-    const float2 c = cs[i];
-    olo[i] = lo[i] * c.x - hi[i] * c.y;
-    ohi[i] = hi[i] * c.x + lo[i] * c.y;
+    olo[i] = lo[i] * cs[i].x - hi[i] * cs[i].y;
+    ohi[i] = hi[i] * cs[i].x + lo[i] * cs[i].y;
   }
 }
 
 template <int HD, bool ROPE>
-__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                  const __grid_constant__ CUtensorMap tmV,
+                                                                  const DecArgs a) {
   using C = DecCfg<HD>;
   constexpr int NC = HD / 64, HALF = HD / 2;
-  extern __shared__ uint4 smem_u4[];
-  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_u4);
-  __nv_bfloat16* sKV = sQ + 16 * HD;  // [NST][K tile, V tile]
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint8_t* ring = smem + C::RING_OFF;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + C::NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NST);
   __shared__ __align__(16) __nv_bfloat16 sNew[2][HD];  // fused RoPE: the new key and value
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int n_splits = gridDim.x;  // = the cluster size: blockIdx.x is the rank
   const int Hq = a.Hq, Hkv = a.Hkv, cap = a.cap, window = a.window;
   const int group = Hq / Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecConsumers / 32);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_trigger();
   // Without fused RoPE everything below depends on the previous kernel. With
   // it, the cache positions before the new token and the length were written
@@ -354,9 +372,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const DecArgs 
   if (!ROPE) pdl_wait();
   const int ctx = a.d_ctx ? *a.d_ctx + 1 : a.ctx_host;  // *d_ctx: tokens before the new one
   const int qpos = ctx - 1;
-  // visible keys [lo, hi); tiles start on a 64-key boundary (16-byte aligned
-  // V^T rows) and the splits take equal runs of tiles; keys outside [lo, hi)
-  // inside a tile are masked
+  // visible keys [lo, hi); tiles start on a 64-key boundary and the splits
+  // take equal runs of tiles; keys outside [lo, hi) inside a tile are masked
   const int lo = window > 0 ? max(0, qpos - window + 1) : 0;
   const int hi = ctx;
   const int tfirst = lo / kDecTile, n_all = (hi + kDecTile - 1) / kDecTile - tfirst;
@@ -364,210 +381,219 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const DecArgs 
   const int ntiles = tfirst + (int)((long)(split + 1) * n_all / n_splits) - ta;
   const int t0 = ta * kDecTile;
   const int t_new = ROPE ? qpos / kDecTile - ta : -1;  // this CTA's tile holding the new token, if any
-  const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
-  const __nv_bfloat16* kbase = a.kc + head_off;
-  const __nv_bfloat16* vbase = a.vc + head_off;  // V^T: [HD][cap]
-  constexpr int CPR = HD / 8;
-  constexpr int CPV = kDecTile / 8;
+  const int head_row = (b * Hkv + g);                  // (sequence, kv head) index
 
-  auto load_tile = [&](int t, int buf) {
-    __nv_bfloat16* dk = sKV + (size_t)buf * 2 * C::TILE_ELEMS;
-    __nv_bfloat16* dv = dk + C::TILE_ELEMS;
-    for (int i = tid; i < kDecTile * CPR; i += kDecThreads) {
-      const int r = i / CPR, cc = i % CPR;
-      const int kp = t0 + t * kDecTile + r;
-      const int ok = (kp >= lo && kp < hi) ? 16 : 0;
-      cp_async16(dk + swz<HD>(r, cc * 8), kbase + (size_t)min(max(kp, lo), hi - 1) * HD + cc * 8, ok);
-    }
-    for (int i = tid; i < HD * CPV; i += kDecThreads) {
-      const int d = i / CPV, cc = i % CPV;
-      cp_async16(dv + swz<kDecTile>(d, cc * 8), vbase + (size_t)d * cap + t0 + t * kDecTile + cc * 8, 16);
-    }
-  };
-  if (ROPE) {
-#pragma unroll
-    for (int t = 0; t < C::NST - 1; ++t) {
-      if (t < ntiles) load_tile(t, t);
-      cp_async_commit();
-    }
-    pdl_wait();
-    const __nv_bfloat16* row = a.q + (size_t)b * a.ldq;
-    // roped query heads of the group -> sQ rows (rows >= group stay zero)
-    for (int r = warp; r < 16; r += kDecThreads / 32) {
-      float olo[NC], ohi[NC];
-      if (r < group) {
-        rope_head<HD>(row + (size_t)(g * group + r) * HD, a, a.q_norm, qpos, lane, olo, ohi);
-      } else {
-#pragma unroll
-        for (int i = 0; i < NC; ++i) olo[i] = ohi[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        sQ[swz<HD>(r, lane * NC + i)] = __float2bfloat16_rn(olo[i]);
-        sQ[swz<HD>(r, HALF + lane * NC + i)] = __float2bfloat16_rn(ohi[i]);
-      }
-    }
-    // the new key (roped) and value; the CTA whose tiles hold position qpos
-    // stores them in the caches
-    if (warp == 0) {
-      float olo[NC], ohi[NC];
-      rope_head<HD>(row + (size_t)(Hq + g) * HD, a, a.k_norm, qpos, lane, olo, ohi);
-#pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        sNew[0][lane * NC + i] = __float2bfloat16_rn(olo[i]);
-        sNew[0][HALF + lane * NC + i] = __float2bfloat16_rn(ohi[i]);
-      }
-    } else if (warp == 1) {
-      const __nv_bfloat16* vs = row + (size_t)(Hq + Hkv + g) * HD;
-      for (int d = lane; d < HD; d += 32) sNew[1][d] = vs[d];
-    }
-    __syncthreads();
-    if (t_new >= 0 && t_new < ntiles) {
-      __nv_bfloat16* kw = a.kc_w + head_off + (size_t)qpos * HD;
-      __nv_bfloat16* vw = a.vc_w + head_off + qpos;
-      for (int d = tid; d < HD; d += kDecThreads) {
-        kw[d] = sNew[0][d];
-        vw[(size_t)d * cap] = sNew[1][d];
-      }
-    }
-  } else {
-    for (int i = tid; i < 16 * CPR; i += kDecThreads) {
-      const int r = i / CPR, cc = i % CPR;
-      const __nv_bfloat16* src = a.q + (size_t)b * a.ldq + (size_t)(g * group + min(r, group - 1)) * HD + cc * 8;
-      cp_async16(sQ + swz<HD>(r, cc * 8), src, r < group ? 16 : 0);
-    }
-    cp_async_commit();  // Q
-#pragma unroll
-    for (int t = 0; t < C::NST - 1; ++t) {
-      if (t < ntiles) load_tile(t, t);
-      cp_async_commit();
-    }
-  }
-  const float scale_log2 = a.scale_log2;
-
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float oacc[HD / 8][4];
 #pragma unroll
   for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int mat = lane >> 3, mr = lane & 7;
 
-  for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<C::NST - 2>();
-    __syncthreads();
-    if (ROPE && t == t_new) {  // the cached copy of the new token is stale: patch the tile
-      __nv_bfloat16* dk = sKV + (size_t)(t % C::NST) * 2 * C::TILE_ELEMS;
-      __nv_bfloat16* dv = dk + C::TILE_ELEMS;
-      const int r = qpos - (t0 + t * kDecTile);
-      for (int d = tid; d < HD; d += kDecThreads) {
-        dk[swz<HD>(r, d)] = sNew[0][d];
-        dv[swz<kDecTile>(d, r)] = sNew[1][d];
+  if (warp == kDecConsumers / 32) {
+    // ---- producer: K tile = HD/64 boxes [64 keys][64], V^T tile = one box [HD][64 keys]
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int issued[C::NST];
+#pragma unroll
+      for (int s = 0; s < C::NST; ++s) issued[s] = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int stage = t % C::NST;
+        if (t >= C::NST && !mbar_wait(&empty[stage], ((t / C::NST) - 1) & 1, abort_flag, a.dev_err)) break;
+        uint8_t* sk = ring + stage * C::STAGE_BYTES;
+        uint8_t* sv = sk + C::TILE_ELEMS * 2;
+        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+        const int pos = t0 + t * kDecTile;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          tma_load_2d(&tmK, &full[stage], sk + c * kDecTile * 64 * 2, c * 64, head_row * cap + pos);
+        tma_load_2d(&tmV, &full[stage], sv, pos, head_row * HD);
+        ++issued[stage];
       }
-      __syncthreads();
-    }
-    {
-      const int tn = t + C::NST - 1;
-      if (tn < ntiles) load_tile(tn, tn % C::NST);
-      cp_async_commit();
-    }
-    const __nv_bfloat16* tK = sKV + (size_t)(t % C::NST) * 2 * C::TILE_ELEMS;
-    const __nv_bfloat16* tV = tK + C::TILE_ELEMS;
-    const int kr = warp * 16;  // this warp's 16 keys of the tile
-    float s[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int k0 = 0; k0 < HD; k0 += 16) {
-      uint32_t a[4], bb[4];
-      ldsm_x4(a, sQ + swz<HD>(mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
-      ldsm_x4(bb, tK + swz<HD>(kr + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
-      mma_bf16_16816(s[0], a, bb[0], bb[1]);
-      mma_bf16_16816(s[1], a, bb[2], bb[3]);
-    }
-    const int key0 = t0 + t * kDecTile + kr + 2 * (lane & 3);
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = key0 + nt * 8 + (e & 1);
-        const bool ok = key >= lo && key < hi;
-        s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
+      // leave only when every requested tile has landed
+      for (int s = 0; s < C::NST; ++s) {
+        if (!issued[s]) continue;
+        const uint32_t fa = smem_u32(&full[s]);
+        const uint64_t w0 = globaltimer_ns();
+        while (!mbar_try_wait(fa, (issued[s] - 1) & 1) && globaltimer_ns() - w0 < kWaitLimitNs) {
+        }
       }
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
+    __syncwarp();
+  } else {
+    // ---- consumers
+    if (ROPE) {
+      constexpr int CC = NC;
+      float2 cs[CC];  // this lane's (cos, sin) at the new position: no dependence on the projection
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - base0);
-      s[nt][1] = exp2f(s[nt][1] - base0);
-      s[nt][2] = exp2f(s[nt][2] - base1);
-      s[nt][3] = exp2f(s[nt][3] - base1);
-      rs0 += s[nt][0] + s[nt][1];
-      rs1 += s[nt][2] + s[nt][3];
-    }
-    l0 = l0 * corr0 + rs0;
-    l1 = l1 * corr1 + rs1;
-    uint32_t a[4];
-    a[0] = pack_bf16x2(s[0][0], s[0][1]);
-    a[1] = pack_bf16x2(s[0][2], s[0][3]);
-    a[2] = pack_bf16x2(s[1][0], s[1][1]);
-    a[3] = pack_bf16x2(s[1][2], s[1][3]);
+      for (int i = 0; i < CC; ++i) cs[i] = a.rope[(size_t)qpos * HALF + lane * CC + i];
+      pdl_wait();
+      const __nv_bfloat16* row = a.q + (size_t)b * a.ldq;
+      for (int r = warp; r < 16; r += kDecConsumers / 32) {
+        float olo[NC], ohi[NC];
+        if (r < group) {
+          rope_head<HD>(row + (size_t)(g * group + r) * HD, a, a.q_norm, cs, lane, olo, ohi);
+        } else {
 #pragma unroll
-    for (int dp = 0; dp < HD / 16; ++dp) {
-      oacc[2 * dp][0] *= corr0;
-      oacc[2 * dp][1] *= corr0;
-      oacc[2 * dp][2] *= corr1;
-      oacc[2 * dp][3] *= corr1;
-      oacc[2 * dp + 1][0] *= corr0;
-      oacc[2 * dp + 1][1] *= corr0;
-      oacc[2 * dp + 1][2] *= corr1;
-      oacc[2 * dp + 1][3] *= corr1;
-      uint32_t bb[4];
-      ldsm_x4(bb, tV + swz<kDecTile>(dp * 16 + mr + (mat >> 1) * 8, kr + (mat & 1) * 8));
-      mma_bf16_16816(oacc[2 * dp], a, bb[0], bb[1]);
-      mma_bf16_16816(oacc[2 * dp + 1], a, bb[2], bb[3]);
+          for (int i = 0; i < NC; ++i) olo[i] = ohi[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+          sQ[swz<HD>(r, lane * NC + i)] = __float2bfloat16_rn(olo[i]);
+          sQ[swz<HD>(r, HALF + lane * NC + i)] = __float2bfloat16_rn(ohi[i]);
+        }
+      }
+      if (warp == 0) {
+        float olo[NC], ohi[NC];
+        rope_head<HD>(row + (size_t)(Hq + g) * HD, a, a.k_norm, cs, lane, olo, ohi);
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+          sNew[0][lane * NC + i] = __float2bfloat16_rn(olo[i]);
+          sNew[0][HALF + lane * NC + i] = __float2bfloat16_rn(ohi[i]);
+        }
+      } else if (warp == 1) {
+        const __nv_bfloat16* vs = row + (size_t)(Hq + Hkv + g) * HD;
+        for (int d = lane; d < HD; d += 32) sNew[1][d] = vs[d];
+      }
+      consumers_sync();
+      if (t_new >= 0 && t_new < ntiles) {  // the one CTA whose tiles hold the new token stores it
+        __nv_bfloat16* kw = a.kc_w + ((size_t)head_row * cap + qpos) * HD;
+        __nv_bfloat16* vw = a.vc_w + (size_t)head_row * HD * cap + qpos;
+        for (int d = tid; d < HD; d += kDecConsumers) {
+          kw[d] = sNew[0][d];
+          vw[(size_t)d * cap] = sNew[1][d];
+        }
+      }
+    } else {
+      constexpr int CPR = HD / 8;
+      for (int i = tid; i < 16 * CPR; i += kDecConsumers) {
+        const int r = i / CPR, cc = i % CPR;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < group) v = *reinterpret_cast<const uint4*>(a.q + (size_t)b * a.ldq + (size_t)(g * group + r) * HD + cc * 8);
+        *reinterpret_cast<uint4*>(sQ + swz<HD>(r, cc * 8)) = v;
+      }
+      consumers_sync();
     }
+    const float scale_log2 = a.scale_log2;
+    const int mat = lane >> 3, mr = lane & 7;
+    const int kr = warp * 16;  // this warp's 16 keys of every tile
+    for (int t = 0; t < ntiles; ++t) {
+      const int stage = t % C::NST;
+      if (!mbar_wait(&full[stage], (t / C::NST) & 1, abort_flag, a.dev_err)) break;
+      __nv_bfloat16* tK = reinterpret_cast<__nv_bfloat16*>(ring + stage * C::STAGE_BYTES);
+      __nv_bfloat16* tV = tK + C::TILE_ELEMS;
+      const bool patch = ROPE && t == t_new && (qpos - (t0 + t * kDecTile)) / 16 == warp;
+      if (patch) {  // the cached copy of the new token is stale: this warp's key row
+        const int r = qpos - (t0 + t * kDecTile);
+        for (int d = lane; d < HD; d += 32) {
+          tK[kswz<HD>(r, d)] = sNew[0][d];
+          tV[swz<kDecTile>(d, r)] = sNew[1][d];
+        }
+        __syncwarp();
+      }
+      float s[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+      for (int k0 = 0; k0 < HD; k0 += 16) {
+        uint32_t qa[4], bb[4];
+        ldsm_x4(qa, sQ + swz<HD>(mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
+        ldsm_x4(bb, tK + kswz<HD>(kr + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
+        mma_bf16_16816(s[0], qa, bb[0], bb[1]);
+        mma_bf16_16816(s[1], qa, bb[2], bb[3]);
+      }
+      const int key0 = t0 + t * kDecTile + kr + 2 * (lane & 3);
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = key0 + nt * 8 + (e & 1);
+          const bool ok = key >= lo && key < hi;
+          s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
+        }
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
+      m0 = mn0;
+      m1 = mn1;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = exp2f(s[nt][0] - base0);
+        s[nt][1] = exp2f(s[nt][1] - base0);
+        s[nt][2] = exp2f(s[nt][2] - base1);
+        s[nt][3] = exp2f(s[nt][3] - base1);
+        rs0 += s[nt][0] + s[nt][1];
+        rs1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * corr0 + rs0;
+      l1 = l1 * corr1 + rs1;
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+      pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+      pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+      pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+#pragma unroll
+      for (int dp = 0; dp < HD / 16; ++dp) {
+        oacc[2 * dp][0] *= corr0;
+        oacc[2 * dp][1] *= corr0;
+        oacc[2 * dp][2] *= corr1;
+        oacc[2 * dp][3] *= corr1;
+        oacc[2 * dp + 1][0] *= corr0;
+        oacc[2 * dp + 1][1] *= corr0;
+        oacc[2 * dp + 1][2] *= corr1;
+        oacc[2 * dp + 1][3] *= corr1;
+        uint32_t bb[4];
+        ldsm_x4(bb, tV + swz<kDecTile>(dp * 16 + mr + (mat >> 1) * 8, kr + (mat & 1) * 8));
+        mma_bf16_16816(oacc[2 * dp], pa, bb[0], bb[1]);
+        mma_bf16_16816(oacc[2 * dp + 1], pa, bb[2], bb[3]);
+      }
+      if (patch) fence_proxy_async_smem();  // generic writes before the slot is refilled by TMA
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   }
-  cp_async_wait<0>();
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  __syncthreads();  // the K/V ring is free: reuse it for the cross-warp merge
-  float* sO = reinterpret_cast<float*>(sKV);  // [4 warps][16 rows][HD]
-  float* sM = sO + 4 * 16 * HD;               // [4][16]
+  __syncthreads();  // the ring is drained (the producer waited for its last tiles): reuse it
+  float* sO = reinterpret_cast<float*>(ring);  // [4 warps][16 rows][HD]
+  float* sM = sO + 4 * 16 * HD;                // [4][16]
   float* sL = sM + 64;
-  const int r0 = lane >> 2, r1 = r0 + 8;
-#pragma unroll
-  for (int dt = 0; dt < HD / 8; ++dt) {
-    const int col = dt * 8 + 2 * (lane & 3);
-    sO[(warp * 16 + r0) * HD + col] = oacc[dt][0];
-    sO[(warp * 16 + r0) * HD + col + 1] = oacc[dt][1];
-    sO[(warp * 16 + r1) * HD + col] = oacc[dt][2];
-    sO[(warp * 16 + r1) * HD + col + 1] = oacc[dt][3];
-  }
-  if ((lane & 3) == 0) {
-    sM[warp * 16 + r0] = m0;
-    sM[warp * 16 + r1] = m1;
-    sL[warp * 16 + r0] = l0;
-    sL[warp * 16 + r1] = l1;
-  }
-  __syncthreads();
-  // this CTA's partial per query head: sP [group][HD] (unnormalised), sPM, sPL
-  float* sP = sL + 64;
+  float* sP = sL + 64;  // this CTA's partial per query head: [group][HD] (unnormalised), sPM, sPL
   float* sPM = sP + kMaxGroup * HD;
   float* sPL = sPM + kMaxGroup;
+  if (warp < kDecConsumers / 32) {
+    const int r0 = lane >> 2, r1 = r0 + 8;
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) {
+      const int col = dt * 8 + 2 * (lane & 3);
+      if (r0 < group) {
+        sO[(warp * 16 + r0) * HD + col] = oacc[dt][0];
+        sO[(warp * 16 + r0) * HD + col + 1] = oacc[dt][1];
+      }
+      if (r1 < group) {
+        sO[(warp * 16 + r1) * HD + col] = oacc[dt][2];
+        sO[(warp * 16 + r1) * HD + col + 1] = oacc[dt][3];
+      }
+    }
+    if ((lane & 3) == 0) {
+      sM[warp * 16 + r0] = m0;
+      sM[warp * 16 + r1] = m1;
+      sL[warp * 16 + r0] = l0;
+      sL[warp * 16 + r1] = l1;
+    }
+  }
+  __syncthreads();
   for (int i = tid; i < group * HD; i += kDecThreads) {
     const int r = i / HD, d = i % HD;
     float M = -INFINITY;
@@ -707,6 +733,10 @@ int decode_resident_per_sm() {
   return std::max(1, smem_sm / (DecCfg<HD>::SMEM + 2 * HD * 2 + reserved));
 }
 
+// Splits per (sequence, kv head): the largest power of two that keeps the
+// grid within one wave of resident CTAs (the CTAs of a split then stream
+// their keys side by side), at most the co-schedulable cluster size and the
+// number of 64-key tiles.
 int decode_attention_splits(int B, int Hkv, int hd, int max_ctx, int sm_count) {
   cudaError_t e = cudaSuccess;
   int maxc = 1, res = 1;
@@ -725,24 +755,31 @@ int decode_attention_splits(int B, int Hkv, int hd, int max_ctx, int sm_count) {
 }
 
 template <int HD>
-cudaError_t decode_hd(const DecArgs& a, bool rope, int B, int n_splits, cudaStream_t st) {
+cudaError_t decode_hd(const void* kcache, const void* vcache, const DecArgs& a, bool rope, int B, int n_splits,
+                      cudaStream_t st) {
   using C = DecCfg<HD>;
   cudaError_t err = cudaSuccess;
   const int maxc = decode_max_cluster<HD>(&err);
   if (err != cudaSuccess) return err;
   if (n_splits < 1 || n_splits > maxc) return cudaErrorInvalidValue;
+  CUtensorMap tK, tV;
+  if (make_tmap_bf16(&tK, kcache, (int64_t)B * a.Hkv * a.cap, HD, HD, kDecTile) != FK_OK ||
+      make_tmap_bf16(&tV, vcache, (int64_t)B * a.Hkv * HD, a.cap, a.cap, HD) != FK_OK)
+    return cudaErrorInvalidValue;
   const dim3 grid(n_splits, a.Hkv, B);
-  if (rope) return fk_launch_cluster(attn_decode_kernel<HD, true>, grid, kDecThreads, C::SMEM, st, n_splits, a);
-  return fk_launch_cluster(attn_decode_kernel<HD, false>, grid, kDecThreads, C::SMEM, st, n_splits, a);
+  if (rope)
+    return fk_launch_cluster(attn_decode_kernel<HD, true>, grid, kDecThreads, C::SMEM, st, n_splits, tK, tV, a);
+  return fk_launch_cluster(attn_decode_kernel<HD, false>, grid, kDecThreads, C::SMEM, st, n_splits, tK, tV, a);
 }
 
-cudaError_t decode_dispatch(const DecArgs& a, bool rope, int hd, int B, int n_splits, cudaStream_t st) {
+cudaError_t decode_dispatch(const void* kcache, const void* vcache, const DecArgs& a, bool rope, int hd, int B,
+                            int n_splits, cudaStream_t st) {
   if (B == 0) return cudaSuccess;
-  if (a.Hq / a.Hkv > kMaxGroup) return cudaErrorInvalidValue;
+  if (a.Hq / a.Hkv > kMaxGroup || a.cap % kDecTile) return cudaErrorInvalidValue;
   switch (hd) {
-    case 64: return decode_hd<64>(a, rope, B, n_splits, st);
-    case 128: return decode_hd<128>(a, rope, B, n_splits, st);
-    case 256: return decode_hd<256>(a, rope, B, n_splits, st);
+    case 64: return decode_hd<64>(kcache, vcache, a, rope, B, n_splits, st);
+    case 128: return decode_hd<128>(kcache, vcache, a, rope, B, n_splits, st);
+    case 256: return decode_hd<256>(kcache, vcache, a, rope, B, n_splits, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -753,8 +790,6 @@ cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, 
   DecArgs a = {};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.ldq = ldq;
-  a.kc = static_cast<const __nv_bfloat16*>(kcache);
-  a.vc = static_cast<const __nv_bfloat16*>(vcache);
   a.cap = cap;
   a.ctx_host = ctx;
   a.d_ctx = d_ctx;
@@ -763,19 +798,17 @@ cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, 
   a.window = window;
   a.scale_log2 = scale * kLog2e;
   a.o = static_cast<__nv_bfloat16*>(o);
-  return decode_dispatch(a, false, hd, B, n_splits, st);
+  return decode_dispatch(kcache, vcache, a, false, hd, B, n_splits, st);
 }
 
 cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcache, void* vcache, int cap, int B,
                                          const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
                                          const float2* rope, int qk_norm, const void* q_norm, const void* k_norm,
-                                         float eps, int n_splits, void* o, cudaStream_t st) {
+                                         float eps, int n_splits, void* o, unsigned* dev_err, cudaStream_t st) {
   if (!d_ctx) return cudaErrorInvalidValue;
   DecArgs a = {};
   a.q = static_cast<const __nv_bfloat16*>(qkv);
   a.ldq = ldqkv;
-  a.kc = static_cast<const __nv_bfloat16*>(kcache);
-  a.vc = static_cast<const __nv_bfloat16*>(vcache);
   a.kc_w = static_cast<__nv_bfloat16*>(kcache);
   a.vc_w = static_cast<__nv_bfloat16*>(vcache);
   a.cap = cap;
@@ -785,19 +818,19 @@ cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcach
   a.window = window;
   a.scale_log2 = scale * kLog2e;
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.dev_err = dev_err;
   a.rope = rope;
   a.qk_norm = qk_norm;
   a.q_norm = static_cast<const __nv_bfloat16*>(q_norm);
   a.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
   a.eps = eps;
-  return decode_dispatch(a, true, hd, B, n_splits, st);
+  return decode_dispatch(kcache, vcache, a, true, hd, B, n_splits, st);
 }
 }  // namespace fk
 
 // ---------------------------------------------------------------------------
 // op-level entry point: one decode-attention step over a caller's KV cache
 // ---------------------------------------------------------------------------
-#include "fk_internal.h"
 
 namespace {
 // The scratch of fk_attention_decode is kept in the interface (a later kernel

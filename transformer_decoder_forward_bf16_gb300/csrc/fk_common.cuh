@@ -180,6 +180,30 @@ FK_DEVICE void tmem_ld32(uint32_t taddr, float* v) {
 }
 
 // ---------------------------------------------------------------------------
+// thread-block clusters: barrier over every thread of the cluster, and loads
+// from another CTA's shared memory (distributed shared memory)
+// ---------------------------------------------------------------------------
+FK_DEVICE void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+FK_DEVICE uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+FK_DEVICE uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+FK_DEVICE float dsmem_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
 // programmatic dependent launch: a kernel launched with the PDL attribute may
 // start while its predecessor drains; pdl_wait() blocks until the predecessor
 // has completed and its writes are visible (a no-op without the attribute).

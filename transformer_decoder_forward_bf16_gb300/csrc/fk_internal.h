@@ -82,8 +82,10 @@ struct GemmOut {
 // A: bf16 [M, K] with row stride lda (elements, multiple of 8). With M <=
 // kSkinnyMaxTokens and a large enough scratch buffer (skinny_scratch_bytes)
 // the weight-streaming split-K kernel runs instead of the tiled one.
+// counter_region: bytes at the start of the scratch reserved for the split-K
+// arrival counters of every GEMM sharing the scratch (0: this GEMM's own).
 fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
-                   cudaStream_t st, void* scratch = nullptr, size_t scratch_bytes = 0);
+                   cudaStream_t st, void* scratch = nullptr, size_t scratch_bytes = 0, size_t counter_region = 0);
 
 // Skinny (few-token) GEMM: swap-AB tcgen05 split-K + ordered reduction.
 constexpr int kSkinnyMaxTokens = 64;
@@ -93,11 +95,18 @@ struct SkinnyPlan {
   size_t part_bytes = 0;     // whole scratch: counters + fp32 partial sums
 };
 SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count);
-size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count);
-// counters_zeroed: the scratch's leading counters are known to be zero (a
-// session clears them once; every launch leaves them zero again).
+// Scratch of one skinny GEMM at up to M tokens: its arrival counters and its
+// fp32 partial sums (the partials of a smaller M never take more).
+size_t skinny_counter_bytes(const GemmWeights& w, int M, int sm_count);
+size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count);
+// The scratch holds [counters: counter_region bytes (0 = this GEMM's own)]
+// [partial sums]. GEMMs that share a scratch share one counter region, sized
+// for the one with the most tiles, so no GEMM's partials overlap another's
+// counters. counters_zeroed: the counters are known to be zero (a session
+// clears them once; every launch leaves them zero again).
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
-                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed = true);
+                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed = true,
+                          size_t counter_region = 0);
 
 // tcgen05 flash attention for prefill (head_dim 64 or 128; caches as in the
 // session layout, V transposed, cap a multiple of 64).

@@ -57,6 +57,6 @@ cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, 
 cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcache, void* vcache, int cap, int B,
                                          const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
                                          const float2* rope, int qk_norm, const void* q_norm, const void* k_norm,
-                                         float eps, int n_splits, void* o, cudaStream_t st);
+                                         float eps, int n_splits, void* o, unsigned* dev_err, cudaStream_t st);
 
 }  // namespace fk

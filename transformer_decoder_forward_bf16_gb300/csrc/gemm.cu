@@ -406,9 +406,10 @@ fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* 
 }
 
 fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
-                   cudaStream_t st, void* scratch, size_t scratch_bytes) {
+                   cudaStream_t st, void* scratch, size_t scratch_bytes, size_t counter_region) {
   if (M == 0) return FK_OK;
-  if (M <= kSkinnyMaxTokens && scratch) return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st);
+  if (M <= kSkinnyMaxTokens && scratch)
+    return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st, true, counter_region);
 
   if (!A || !o.out || M < 0 || lda < w.K || lda % 8 || o.ldo % (o.epi == EPI_BF16 || o.epi == EPI_GLU_BF16 ? 8 : 4))
     return fail(FK_ERR_INVALID_ARG, "gemm_run: bad operand");

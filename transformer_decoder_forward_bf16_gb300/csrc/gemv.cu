@@ -363,19 +363,35 @@ SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count) {
 }
 
 
-size_t skinny_scratch_bytes(const GemmWeights& w, int M, int sm_count) {
+size_t skinny_counter_bytes(const GemmWeights& w, int M, int sm_count) {
   if (M <= 0 || M > kSkinnyMaxTokens) return 0;
-  return skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count).part_bytes;
+  return skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count).counter_bytes;
+}
+
+size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count) {
+  if (M <= 0 || M > kSkinnyMaxTokens) return 0;
+  // splits depend on M only through the tile width (16/32/64 tokens): the
+  // largest product of splits and tokens is at the top of a width class
+  size_t b = 0;
+  for (int m : {std::min(M, 16), std::min(M, 32), M}) {
+    const SkinnyPlan p = skinny_plan(m, w.K, w.seg_start[w.nseg], sm_count);
+    b = std::max(b, p.part_bytes - p.counter_bytes);
+  }
+  return b;
 }
 
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
-                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed) {
+                          size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed,
+                          size_t counter_region) {
   int sms = 0;
   fk_status s = check_device(&sms);
   if (s != FK_OK) return s;
   const int n_rows = w.seg_start[w.nseg];
   const SkinnyPlan p = skinny_plan(M, w.K, n_rows, sms);
-  if (!scratch || scratch_bytes < p.part_bytes) return fail(FK_ERR_WORKSPACE, "skinny GEMM scratch too small");
+  const size_t creg = counter_region ? counter_region : p.counter_bytes;
+  if (creg < p.counter_bytes || creg % 256) return fail(FK_ERR_INVALID_ARG, "skinny GEMM: counter region too small");
+  if (!scratch || scratch_bytes < creg + (p.part_bytes - p.counter_bytes))
+    return fail(FK_ERR_WORKSPACE, "skinny GEMM scratch too small");
   const int BT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
   CUtensorMap tX;
   s = make_tmap_bf16(&tX, A, M, w.K, lda, BT);
@@ -389,7 +405,7 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   for (int i = 0; i < 4; ++i) a.seg_start[i] = w.seg_start[i];
   a.nk = p.nk;
   a.counters = static_cast<unsigned*>(scratch);
-  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + p.counter_bytes);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + creg);
   a.dev_err = dev_err;
   // a gate|up pair fuses only when each half is a whole number of 128-row tiles
   // (the last CTA sums M x splits values per feature: worth it only for few tokens)

@@ -197,21 +197,18 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
   t.ao = take((size_t)T * m->Nq * 2);
   t.h = take((size_t)T * c.intermediate * 2);
   // few-token GEMMs (T <= 64, or decode/short chunks up to that size) need
-  // split-K scratch: the largest of the layer and head GEMMs
+  // split-K scratch: one counter region sized for the GEMM with the most
+  // tiles, then room for the largest GEMM's partial sums
   const int Ms = (int)std::min<long>(T, kSkinnyMaxTokens);
-  size_t gb = 0;
+  size_t gb = 0, cb = 0;
   if (!m->g_qkv.empty()) {
-    gb = std::max(gb, skinny_scratch_bytes(m->g_qkv[0], Ms, m->sm_count));
-    gb = std::max(gb, skinny_scratch_bytes(m->g_o[0], Ms, m->sm_count));
-    gb = std::max(gb, skinny_scratch_bytes(m->g_gu[0], Ms, m->sm_count));
-    gb = std::max(gb, skinny_scratch_bytes(m->g_down[0], Ms, m->sm_count));
-    gb = std::max(gb, skinny_scratch_bytes(m->g_head, Ms, m->sm_count));
-  }
-  size_t cb = 0;
-  if (gb) {
     const GemmWeights* all[5] = {&m->g_qkv[0], &m->g_o[0], &m->g_gu[0], &m->g_down[0], &m->g_head};
-    for (const GemmWeights* g : all)
-      cb = std::max(cb, skinny_plan(Ms, g->K, g->seg_start[g->nseg], m->sm_count).counter_bytes);
+    size_t pb = 0;
+    for (const GemmWeights* g : all) {
+      cb = std::max(cb, skinny_counter_bytes(*g, Ms, m->sm_count));
+      pb = std::max(pb, skinny_partial_bytes(*g, Ms, m->sm_count));
+    }
+    gb = cb + pb;
   }
   t.gemv_bytes = gb;
   t.gemv_counter_bytes = cb;
@@ -275,12 +272,12 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     o.epi = EPI_BF16;
     o.out = sc.qkv;
     o.ldo = m->Nqkv;
-    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb)); }
+    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
     if (decode) {  // RoPE, cache write and attention in one kernel
       ProfScope ps("attn_decode", st);
       FK_LAUNCH(launch_attention_decode_rope(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, d_len, c.n_q_heads, c.n_kv_heads,
                                              hd, window, m->attn_scale, m->rope[kind], c.qk_norm, w.q_norm, w.k_norm,
-                                             c.rms_eps, dsplits, sc.ao, st));
+                                             c.rms_eps, dsplits, sc.ao, m->dev_err, st));
     } else {
       { ProfScope ps("rope_qkv", st);
       FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
@@ -300,7 +297,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.out = sc.a;
       o.ldo = H;
       o.softcap = 0.f;
-      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb)); }
+      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_in, x_mid, (int)T, H, w.post_attn_norm, w.ffn_norm, c.rms_eps, sc.u,
                                           st));
@@ -310,7 +307,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.ldo = H;
       o.res = x_in;
       o.ldr = H;
-      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb)); }
+      { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st));
     }
@@ -320,13 +317,13 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     og.out = sc.h;
     og.ldo = c.intermediate;
     og.act = c.act;
-    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st, gv, gvb)); }
+    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
     if (sandwich) {
       GemmOut od;
       od.epi = EPI_F32;
       od.out = sc.a;
       od.ldo = H;
-      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb)); }
+      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps, sc.u,
                                           st));
@@ -337,7 +334,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       od.ldo = H;
       od.res = x_mid;
       od.ldr = H;
-      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb)); }
+      { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st));
     }
@@ -354,7 +351,8 @@ fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* ar
   o.out = logits;
   o.ldo = m->cfg.vocab;
   o.softcap = m->cfg.final_softcap;
-  { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st, sc.gemv, sc.gemv_bytes)); }
+  { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st, sc.gemv, sc.gemv_bytes,
+                                                   sc.gemv_counter_bytes)); }
   ProfScope ps("argmax", st);
   if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st, argmax2, sc.argmax));
   return FK_OK;
