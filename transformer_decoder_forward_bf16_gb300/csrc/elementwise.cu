@@ -223,8 +223,8 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
 // / gemma3 QK-norm). One warp per (token, head). Head element j pairs with
 // j + hd/2; lane owns C = hd/64 consecutive elements of each half.
 //   q: rotated in place inside the qkv rows;
-//   k: rotated and written to kcache[b][g][pos][:]; v: copied to the
-//   transposed value cache vcache[b][g][d][pos] (cap a multiple of 64).
+//   k: rotated and written to kcache[b][g][pos][:]
+// (v goes to the transposed value cache through v_cache_kernel below).
 // rope: float2 (cos, sin) table [positions][hd/2].
 // ---------------------------------------------------------------------------
 template <int C>
@@ -239,7 +239,7 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
   const int warps = blockDim.x >> 5;
   const long gw = (long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int nh = Hq + 2 * Hkv;
+  const int nh = Hq + Hkv;  // q and k heads; v is moved by v_cache_kernel
   if (gw >= (long)T * nh) return;
   const int t = (int)(gw / nh);
   const int h = (int)(gw % nh);
@@ -252,16 +252,6 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
   for (int i = 0; i < C; ++i) {
     lo[i] = __bfloat162float(row[e0 + i]);
     hi[i] = __bfloat162float(row[HALF + e0 + i]);
-  }
-  if (h >= Hq + Hkv) {  // v: copy into the transposed cache vcache[b][g][d][pos]
-    const int g = h - Hq - Hkv;
-    __nv_bfloat16* dst = vcache + ((size_t)b * Hkv + g) * HD * cap + pos;
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      dst[(size_t)(e0 + i) * cap] = __float2bfloat16_rn(lo[i]);
-      dst[(size_t)(HALF + e0 + i) * cap] = __float2bfloat16_rn(hi[i]);
-    }
-    return;
   }
   const bool is_q = h < Hq;
   if (qk_norm) {
@@ -296,6 +286,59 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
   for (int i = 0; i < C; ++i) {
     dst[e0 + i] = __float2bfloat16_rn(olo[i]);
     dst[HALF + e0 + i] = __float2bfloat16_rn(ohi[i]);
+  }
+}
+
+// V rows of a prefill chunk into the transposed cache vcache[b][g][d][pos]:
+// one CTA per (64 positions, kv head, sequence) stages the [64][HD] tile in
+// shared memory and writes each cache row d as one run of 64 positions, so
+// both the reads and the writes are full 128-byte segments.
+constexpr int kVTile = 64;
+template <int HD>
+__global__ void __launch_bounds__(256) v_cache_kernel(const __nv_bfloat16* __restrict__ qkv, int ldqkv, int S, int pos0,
+                                                      int Hq, int Hkv, __nv_bfloat16* __restrict__ vcache, int cap) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int LD = HD + 2;  // padded row: the transposed reads of 8 positions hit distinct banks
+  __shared__ __align__(16) __nv_bfloat16 tile[kVTile * LD];
+  const int s0 = blockIdx.x * kVTile, g = blockIdx.y, b = blockIdx.z;
+  const int n = min(kVTile, S - s0);
+  constexpr int CPR = HD / 8;  // 16-byte chunks per row
+  for (int i = threadIdx.x; i < n * CPR; i += blockDim.x) {
+    const int r = i / CPR, c = i % CPR;
+    const uint4 v = *reinterpret_cast<const uint4*>(qkv + (size_t)(b * S + s0 + r) * ldqkv + (size_t)(Hq + Hkv + g) * HD +
+                                                    c * 8);
+    uint32_t* t32 = reinterpret_cast<uint32_t*>(tile + r * LD + c * 8);  // 4-byte aligned (LD even)
+    t32[0] = v.x;
+    t32[1] = v.y;
+    t32[2] = v.z;
+    t32[3] = v.w;
+  }
+  __syncthreads();
+  __nv_bfloat16* dst = vcache + ((size_t)b * Hkv + g) * HD * cap + pos0 + s0;
+  if (((pos0 + s0) & 7) == 0) {  // 16-byte aligned runs: 8 positions per store
+    constexpr int CPD = kVTile / 8;
+    for (int i = threadIdx.x; i < HD * CPD; i += blockDim.x) {
+      const int d = i / CPD, p = (i % CPD) * 8;
+      if (p >= n) continue;
+      if (p + 8 <= n) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint16_t lo = reinterpret_cast<const uint16_t&>(tile[(p + 2 * j) * LD + d]);
+          const uint16_t hi = reinterpret_cast<const uint16_t&>(tile[(p + 2 * j + 1) * LD + d]);
+          w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + (size_t)d * cap + p) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        for (int j = p; j < n; ++j) dst[(size_t)d * cap + j] = tile[j * LD + d];
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < HD * kVTile; i += blockDim.x) {
+      const int d = i / kVTile, p = i % kVTile;
+      if (p < n) dst[(size_t)d * cap + p] = tile[p * LD + d];
+    }
   }
 }
 
@@ -454,7 +497,7 @@ cudaError_t launch_embed_norm(const int32_t* ids, const void* E, int T, int H, i
 cudaError_t launch_rmsnorm(const float* x, int ldx, int T, int H, const void* w, float eps, void* u, int ldu,
                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  if (T <= 512 && H <= kRowsThreads * 4 * kRowsMaxVec) {
+  if (H <= kRowsThreads * 4 * kRowsMaxVec) {
     return fk_launch(rmsnorm_rows_kernel, T, kRowsThreads, 0, st, x, ldx, H, static_cast<const __nv_bfloat16*>(w), eps,
                      static_cast<__nv_bfloat16*>(u), ldu);
   }
@@ -480,7 +523,18 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const 
                             const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
                             void* kcache, void* vcache, int cap, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const long warps = (long)T * (Hq + 2 * Hkv);
+  if (d_pos0 || ldqkv % 8) return cudaErrorInvalidValue;  // chunks start at host positions; rows 16-byte aligned
+  {
+    const dim3 grid((S + kVTile - 1) / kVTile, Hkv, T / S);
+    const auto* src = static_cast<const __nv_bfloat16*>(qkv);
+    auto* vdst = static_cast<__nv_bfloat16*>(vcache);
+    cudaError_t e = cudaErrorInvalidValue;
+    if (hd == 64) e = fk_launch(v_cache_kernel<64>, grid, 256, 0, st, src, ldqkv, S, pos0, Hq, Hkv, vdst, cap);
+    if (hd == 128) e = fk_launch(v_cache_kernel<128>, grid, 256, 0, st, src, ldqkv, S, pos0, Hq, Hkv, vdst, cap);
+    if (hd == 256) e = fk_launch(v_cache_kernel<256>, grid, 256, 0, st, src, ldqkv, S, pos0, Hq, Hkv, vdst, cap);
+    if (e != cudaSuccess) return e;
+  }
+  const long warps = (long)T * (Hq + Hkv);
   const int blocks = (int)((warps + 7) / 8);
   auto* q = static_cast<__nv_bfloat16*>(qkv);
   auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
