@@ -15,15 +15,17 @@ def _setup(fk, cfg, norm_mode="random", sigma=0.02):
     return wb, fk.Model(cfg, weights_to_dev(wb), max_positions=512)
 
 
-@pytest.mark.parametrize("kind", ["llama", "llama3", "gemma"])
-def test_cached_prefill_matches_cacheless(fk, kind):
+@pytest.mark.parametrize("kind,chunk", [("llama", 48), ("llama3", 48), ("gemma", 48), ("llama", 45), ("llama3", 37)])
+def test_cached_prefill_matches_cacheless(fk, kind, chunk):
+    """Chunks of 48 start at positions that are multiples of 8 (the V cache
+    takes 16-byte runs); 45 and 37 exercise the unaligned element path."""
     import torch
     cfg = synth.small_config(kind)
     wb, model = _setup(fk, cfg)
     B, S = 2, 100
     ids = synth.make_ids(cfg, B, S)
     full = model.forward(ids, hidden=False)
-    sess = model.session(B, 256, max_chunk=48)  # three chunks
+    sess = model.session(B, 256, max_chunk=chunk)  # three chunks
     z = torch.empty((B, cfg.vocab), dtype=torch.float32, device="cuda")
     nxt = torch.empty((B,), dtype=torch.int32, device="cuda")
     sess.prefill(ids, logits=z, next_ids=nxt)
