@@ -59,14 +59,17 @@ def test_decode_matches_oracle(fk, kind):
     np.testing.assert_allclose(z.cpu().numpy(), ref["last_logits"], atol=0.05)
 
 
-@pytest.mark.parametrize("B", [1, 8, 24])
-def test_decode_with_wide_head_matches_cacheless_forward(fk, B):
+@pytest.mark.parametrize("B,hidden", [(1, 128), (8, 128), (24, 128), (1, 512), (8, 512)])
+def test_decode_with_wide_head_matches_cacheless_forward(fk, B, hidden):
     """A vocabulary much wider than the layers: the LM head's split-K GEMM has
     far more feature tiles than the layer GEMMs that share its scratch.
     Several graph-replayed decode steps must each equal the cacheless forward
-    of the extended sequences at the new position (every logit written)."""
+    of the extended sequences at the new position (every logit written).
+    Both sides round the same bf16 activations after different fp32
+    summation orders (split-K against tiled GEMMs), so the bound scales with
+    the logits' spread, about sqrt(hidden) * 0.02."""
     import torch
-    cfg = synth.small_config("llama", vocab=32768)
+    cfg = synth.small_config("llama", vocab=32768, hidden=hidden, intermediate=2 * hidden)
     wb, model = _setup(fk, cfg)
     S, steps = 40, 4
     prompt = synth.make_ids(cfg, B, S)
@@ -83,7 +86,7 @@ def test_decode_with_wide_head_matches_cacheless_forward(fk, B):
         zf = full["logits"].view(B, ext.shape[1], -1)[:, -1]
         torch.cuda.synchronize()
         assert torch.isfinite(z).all()
-        assert torch.max(torch.abs(z - zf)).item() <= 1e-2
+        assert torch.max(torch.abs(z - zf)).item() <= 1e-2 * max(1.0, (hidden / 128) ** 0.5)
         seq.append(nxt.cpu().numpy().copy()[:, None])
 
 

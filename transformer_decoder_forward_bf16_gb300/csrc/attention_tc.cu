@@ -3,7 +3,8 @@
 // Thm 2 and "pegainfer #878": sliding-window local layers).
 //
 // One CTA per (128 queries, head, sequence); key blocks of 64 positions; two
-// CTAs per SM (96 KB of shared memory and 256 TMEM columns each).
+// CTAs per SM at head_dim 128 (96 KB of shared memory and 256 TMEM columns
+// each), one at head_dim 256 (197 KB, 512 columns: O alone takes 256).
 //   warp 0     TMA producers: lane 0 streams K tiles, lane 1 Vᵀ tiles, each
 //              through its own 2-deep ring (128-byte swizzled, K-major), so
 //              the K tile of block j+2 never waits behind the V tile of j.
@@ -373,7 +374,7 @@ fk_status launch_tc(const void* q, int ldq, const void* kc, const void* vc, int 
 }  // namespace
 
 bool attention_prefill_tc_supported(int hd, int ldq, int cap) {
-  return (hd == 64 || hd == 128) && ldq % 8 == 0 && cap % 64 == 0;
+  return (hd == 64 || hd == 128 || hd == 256) && ldq % 8 == 0 && cap % 64 == 0;
 }
 
 fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
@@ -384,7 +385,9 @@ fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const
     return launch_tc<64>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st);
   if (hd == 128)
     return launch_tc<128>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st);
-  return fail(FK_ERR_INVALID_ARG, "tensor-core attention: head_dim 64 or 128");
+  if (hd == 256)
+    return launch_tc<256>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st);
+  return fail(FK_ERR_INVALID_ARG, "tensor-core attention: head_dim 64, 128 or 256");
 }
 
 }  // namespace fk
