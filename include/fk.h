@@ -73,13 +73,15 @@ typedef enum { FK_EMBED_SCALE_NONE = 0, FK_EMBED_SCALE_SQRT_HIDDEN_BF16 = 1 } fk
 /*
  * Model geometry ("pegainfer #878": one typed config is the single source of
  * every buffer size). Validation rules (FK_ERR_INVALID_CONFIG otherwise):
- *   n_layers >= 1; hidden, n_q_heads, n_kv_heads, head_dim, intermediate,
- *   vocab >= 1; n_q_heads % n_kv_heads == 0; head_dim even, a multiple of 8
- *   and <= 256; hidden, intermediate and n_q_heads*head_dim multiples of 64;
- *   rms_eps > 0; rope thetas > 1; llama3 scaling needs factor >= 1,
- *   high_freq_factor > low_freq_factor > 0 and orig_max_pos > 0;
- *   sliding_window >= 0 (0 = no local layers; local layer kinds then
- *   rejected); final_softcap == 0 (off) or > 0 and finite.
+ *   n_layers >= 1; hidden and intermediate positive multiples of 64;
+ *   n_q_heads, n_kv_heads >= 1 with n_q_heads a multiple of n_kv_heads and
+ *   at most 8 query heads per kv head; head_dim 64, 128 or 256; vocab a
+ *   positive multiple of 8; rms_eps > 0 and finite; rope thetas > 1; llama3
+ *   scaling needs factor >= 1, high_freq_factor > low_freq_factor > 0 and
+ *   orig_max_pos > 0; act, norm_layout and embed_scale one of their enums;
+ *   qk_norm and tied 0 or 1; sliding_window >= 0; layer_kinds entries 0
+ *   (global) or 1 (local), local layers only with sliding_window > 0;
+ *   final_softcap == 0 (off) or > 0 and finite.
  */
 typedef struct fk_config {
   int32_t n_layers;
@@ -242,8 +244,8 @@ fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32
  *          V transposed [batch][n_kv_heads][head_dim][cap], cap % 64 == 0,
  *          positions up to the next multiple of 128 finite)
  *   d_out: bf16 [batch*seq][n_q_heads*head_dim]
- * head_dim 64 and 128 run on the tensor-core (tcgen05) kernel, 256 on the
- * mma.sync kernel. No scratch. */
+ * head_dim 64, 128 and 256 run on the tensor-core (tcgen05) kernel. No
+ * scratch. */
 fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch, int32_t seq,
                                int32_t pos0, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
                                int32_t window, void* d_out, void* stream);
