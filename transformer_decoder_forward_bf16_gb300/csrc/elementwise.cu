@@ -228,7 +228,7 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
 // rope: float2 (cos, sin) table [positions][hd/2].
 // ---------------------------------------------------------------------------
 template <int C>
-__global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq,
+__global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int pos0, int Hq,
                                 int Hkv, const float2* __restrict__ rope, int qk_norm,
                                 const __nv_bfloat16* __restrict__ q_norm, const __nv_bfloat16* __restrict__ k_norm,
                                 float eps, __nv_bfloat16* kcache, __nv_bfloat16* vcache, int cap) {
@@ -244,7 +244,7 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
   const int t = (int)(gw / nh);
   const int h = (int)(gw % nh);
   const int b = t / S, s = t % S;
-  const int pos = (d_pos0 ? *d_pos0 : pos0) + s;
+  const int pos = pos0 + s;
   __nv_bfloat16* row = qkv + (size_t)t * ldqkv + (size_t)h * HD;
   float lo[C], hi[C];
   const int e0 = lane * C;  // within each half of size 32*C = HALF
@@ -519,11 +519,11 @@ cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* 
                    static_cast<__nv_bfloat16*>(u));
 }
 
-cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
+cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, int Hq, int Hkv, int hd,
                             const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
                             void* kcache, void* vcache, int cap, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  if (d_pos0 || ldqkv % 8) return cudaErrorInvalidValue;  // chunks start at host positions; rows 16-byte aligned
+  if (ldqkv % 8) return cudaErrorInvalidValue;  // rows 16-byte aligned
   {
     const dim3 grid((S + kVTile - 1) / kVTile, Hkv, T / S);
     const auto* src = static_cast<const __nv_bfloat16*>(qkv);
@@ -543,13 +543,13 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const 
   auto* vc = static_cast<__nv_bfloat16*>(vcache);
   switch (hd) {
     case 64:
-      return fk_launch(rope_qkv_kernel<1>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn,
+      return fk_launch(rope_qkv_kernel<1>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, Hq, Hkv, rope, qk_norm, qn,
                        kn, eps, kc, vc, cap);
     case 128:
-      return fk_launch(rope_qkv_kernel<2>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn,
+      return fk_launch(rope_qkv_kernel<2>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, Hq, Hkv, rope, qk_norm, qn,
                        kn, eps, kc, vc, cap);
     case 256:
-      return fk_launch(rope_qkv_kernel<4>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, d_pos0, Hq, Hkv, rope, qk_norm, qn,
+      return fk_launch(rope_qkv_kernel<4>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, Hq, Hkv, rope, qk_norm, qn,
                        kn, eps, kc, vc, cap);
     default:
       return cudaErrorInvalidValue;

@@ -14,9 +14,9 @@ cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, floa
 cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* x_out, int T, int H,
                                       const void* w_post, const void* w_next, float eps, void* u, cudaStream_t st);
 // Prefill chunks: pos0 is the position of the first of S tokens per sequence
-// (d_pos0 must be null: decode steps apply RoPE inside the attention kernel).
+// (decode steps apply RoPE inside the attention kernel).
 // q is rotated in place, k written to the cache, v transposed into the cache.
-cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, const int* d_pos0, int Hq, int Hkv, int hd,
+cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, int Hq, int Hkv, int hd,
                             const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
                             void* kcache, void* vcache, int cap, cudaStream_t st);
 // out2 (optional): a second copy of the ids. With `scratch` (argmax_scratch_bytes,

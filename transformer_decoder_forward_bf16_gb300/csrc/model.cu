@@ -280,7 +280,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
                                              c.rms_eps, dsplits, sc.ao, m->dev_err, st));
     } else {
       { ProfScope ps("rope_qkv", st);
-      FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, nullptr, c.n_q_heads, c.n_kv_heads, hd,
+      FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
                                 m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
       ProfScope ps("attn_prefill", st);
       if (attention_prefill_tc_supported(hd, m->Nqkv, kv.cap) && !getenv("FK_ATTN_MMA_SYNC")) {
