@@ -52,7 +52,7 @@ FK_DEVICE float act_gelu_tanh(float g) {
 // Sum the splits of one feature for every token (fixed split order) and store
 // the epilogue's result. v: gate (or plain) feature f, u: up feature (GLU).
 FK_DEVICE void reduce_store(const SkinnyArgs& a, int S, int f) {
-  constexpr int U = 8;  // splits loaded per batch (all in flight before the in-order adds)
+  constexpr int U = 16;  // splits loaded per batch (all in flight before the in-order adds)
   const size_t sstride = (size_t)a.M * a.n_rows;
   for (int t = 0; t < a.M; ++t) {
     float v = 0.f, u = 0.f;
@@ -250,12 +250,18 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   volatile int* last = abort_flag + 1;
   const int group = args.glu_tiles ? (int)blockIdx.x % args.glu_tiles : (int)blockIdx.x;
   const unsigned expect = gridDim.y * (args.glu_tiles ? 2u : 1u);
-  __threadfence();
+  // The CTA barrier orders every thread's partial stores before thread 0's
+  // arrival; thread 0's acquire-release atomic publishes them at GPU scope
+  // and, in the last CTA, acquires every other CTA's partials (the barrier
+  // after it extends that to all threads of the CTA).
   __syncthreads();
-  if (threadIdx.x == 0) *last = atomicAdd(&args.counters[group], 1u) == expect - 1 ? 1 : 0;
+  if (threadIdx.x == 0) {
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(&args.counters[group]) : "memory");
+    *last = prev == expect - 1 ? 1 : 0;
+  }
   __syncthreads();
   if (!*last) return;
-  __threadfence();
   const int f = group * 128 + threadIdx.x;
   if (f < args.n_out) reduce_store(args, gridDim.y, f);
   if (threadIdx.x == 0) args.counters[group] = 0;
