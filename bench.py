@@ -15,6 +15,17 @@ One step = one prefill of the 4 x 4096 batch + G decode steps at batch 32 + G
 at batch 1; decode steps replay the session's captured CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fk|reference]
+  python bench.py --all-configs     (one JSON line per other workload, below)
+
+``--all-configs`` times the other workloads of the parity suite through the
+same public API (CUDA events, after warm-up, L2 flushed between repeats):
+  A  SmolLM2-135M shape, cacheless forward of 1 x 9 ids with every hidden slot
+     and all logits (latency; weight bytes / latency);
+  B  op-level GEMM Y = X W^T at the five (P, in, out) shapes (TFLOP/s);
+  C  SmolLM2-135M shape with KV cache: 8 x 1024 session prefill (tok/s), then
+     64 greedy decode steps (tok/s);
+  E  Gemma3-style tower, cacheless forward at 1, 9 and 1024 ids (latency,
+     tok/s).
 
 N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
 path has no cross-sequence exchange, so there is no data-path collective.
@@ -57,6 +68,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (profiling of a small case only)")
+    ap.add_argument("--all-configs", action="store_true", help="time the other workloads (A, B, C, E)")
     return ap.parse_args()
 
 
@@ -226,10 +238,125 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+def _time_ms(fn, reps: int, flush=None) -> float:
+    """Median device time of fn over reps runs (CUDA events, L2 flushed
+    between runs)."""
+    import torch
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+def run_all_configs(args):
+    """One JSON line per workload A, B, C, E (see the module docstring)."""
+    import torch
+    import transformer_decoder_forward_bf16_gb300 as fk
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fk.load()
+    peaks = load_peaks()
+    hbm, tc = peaks["hbm"], peaks["bf16"]  # launches timed alone: the burst tensor-core figure
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2
+    reps = max(5, args.steps)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    def weight_bytes(wbits):
+        return sum(v.nbytes for v in wbits.values())
+
+    # A: SmolLM2-135M cacheless forward, 1 x 9, all slots and logits
+    cfg = synth.CONFIGS["smollm2-135m"]
+    wbits = host_weights(cfg)
+    model = fk.Model(cfg, upload(wbits, dev), max_positions=1100)
+    ids = synth.make_ids(cfg, 1, 9)
+    for _ in range(3):
+        model.forward(ids, hidden=True, logits=True, argmax=True)
+    ms = _time_ms(lambda: model.forward(ids, hidden=True, logits=True, argmax=True), reps, flush)
+    wb = weight_bytes(wbits) - cfg.vocab * cfg.hidden * 2 + 9 * cfg.hidden * 2  # embedding: 9 rows read
+    emit({"config": "A", "workload": "smollm2-135m cacheless forward 1x9, all hidden slots + logits",
+          "latency_ms": ms, "weight_gbs": wb / ms / 1e6, "hbm_frac": (wb / ms / 1e6) / hbm if hbm else None,
+          "note": "includes the host-to-device copy of the 9 ids and the per-call workspace set-up"})
+
+    # C: SmolLM2-135M with KV cache, 8 x 1024 prefill then 64 greedy steps
+    B, S, G = 8, 1024, 64
+    prompt = torch.from_numpy(synth.make_ids(cfg, B, S)).to(dev)
+    sess = model.session(B, S + G + 1, max_chunk=1024)
+    z = torch.empty((B, cfg.vocab), dtype=torch.float32, device=dev)
+    nxt = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def prefill():
+        sess.reset()
+        sess.prefill(prompt, logits=z, next_ids=nxt)
+    for _ in range(3):
+        prefill()
+    ms_p = _time_ms(prefill, reps, flush)
+
+    def decode_run():
+        sess.reset()
+        sess.prefill(prompt, logits=z, next_ids=nxt)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(G):
+            sess.decode(None, logits=z, next_ids=nxt)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+    decode_run()
+    ms_d = statistics.median(decode_run() for _ in range(3))
+    kv_bytes = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * cfg.n_layers * B * (S + G / 2)
+    step_bytes = wb - 9 * cfg.hidden * 2 + B * cfg.hidden * 2 + kv_bytes
+    emit({"config": "C", "workload": "smollm2-135m KV cache: 8x1024 prefill + 64 greedy steps",
+          "prefill_tok_s": B * S / ms_p * 1e3, "prefill_ms": ms_p,
+          "decode_tok_s": B * G / ms_d * 1e3, "decode_ms_per_step": ms_d / G,
+          "decode_hbm_frac": (step_bytes * G / ms_d / 1e6) / hbm if hbm else None})
+    del sess, model
+    torch.cuda.empty_cache()
+
+    # B: op-level GEMMs
+    rows = []
+    for (P, K, N) in ((16, 64, 96), (64, 512, 256), (256, 1536, 1536), (4096, 4096, 14336), (4096, 4096, 128256)):
+        x = torch.randn(P, K, device=dev).to(torch.bfloat16)
+        w = (0.02 * torch.randn(N, K, device=dev)).to(torch.bfloat16)
+        y = torch.empty((P, N), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            fk.gemm(x, w, out_fp32=True, out=y)
+        ms = _time_ms(lambda: fk.gemm(x, w, out_fp32=True, out=y), reps, flush)
+        tf = 2.0 * P * K * N / ms / 1e9
+        rows.append({"P": P, "in": K, "out": N, "ms": ms, "tflops": tf, "tc_frac": tf / tc if tc else None})
+        del x, w, y
+    emit({"config": "B", "workload": "op-level bf16 GEMM, fp32 out", "shapes": rows})
+
+    # E: Gemma3-style tower, cacheless forward at 1, 9, 1024 ids
+    cfg = synth.CONFIGS["gemma3-tower"]
+    wbits = host_weights(cfg)
+    model = fk.Model(cfg, upload(wbits, dev), max_positions=1100)
+    out = {"config": "E", "workload": "gemma3-style tower cacheless forward (logits, argmax)", "prompts": []}
+    for S in (1, 9, 1024):
+        ids = synth.make_ids(cfg, 1, S)
+        for _ in range(2):
+            model.forward(ids, hidden=False, logits=True, argmax=True)
+        ms = _time_ms(lambda: model.forward(ids, hidden=False, logits=True, argmax=True), reps, flush)
+        out["prompts"].append({"S": S, "latency_ms": ms, "tok_s": S / ms * 1e3})
+    emit(out)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.all_configs:
+        run_all_configs(args)
         return
     import torch
     import torch.distributed as dist

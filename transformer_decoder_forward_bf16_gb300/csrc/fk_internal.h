@@ -91,10 +91,13 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
 constexpr int kSkinnyMaxTokens = 64;
 struct SkinnyPlan {
   int splits = 1, kb_per_split = 1, n_tiles = 1, nk = 1;
+  bool direct = false;       // one split, epilogue straight from TMEM (small operands)
   size_t counter_bytes = 0;  // per-group arrival counters at the start of the scratch
   size_t part_bytes = 0;     // whole scratch: counters + fp32 partial sums
 };
-SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count);
+// allow_direct: the operand may take the single-split direct epilogue (not a
+// gate/up pair, whose halves are combined by the reduction).
+SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count, bool allow_direct);
 // Scratch of one skinny GEMM at up to M tokens: its arrival counters and its
 // fp32 partial sums (the partials of a smaller M never take more).
 size_t skinny_counter_bytes(const GemmWeights& w, int M, int sm_count);

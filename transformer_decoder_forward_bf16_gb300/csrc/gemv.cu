@@ -37,6 +37,7 @@ struct SkinnyArgs {
   // fused reduction: the last CTA to finish a feature group sums the splits
   unsigned* counters;  // one per group, zero between launches (the last CTA resets it)
   int fused, glu_tiles;  // glu_tiles: feature tiles of one half of a gate|up pair (0 = not GLU)
+  int direct;            // one split: the epilogue is applied straight from TMEM
   int epi, act, n_out, ldo, ldr;
   void* out;
   const float* res;
@@ -47,6 +48,21 @@ FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
 FK_DEVICE float act_gelu_tanh(float g) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+}
+
+// The epilogue for output feature f of token t: v = the sum over K (the gate
+// for GLU), u = the up projection (GLU only).
+FK_DEVICE void store_out(const SkinnyArgs& a, int t, int f, float v, float u) {
+  if (a.epi == EPI_GLU_BF16) {
+    static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] =
+        __float2bfloat16_rn((a.act ? act_gelu_tanh(v) : act_silu(v)) * u);
+  } else if (a.epi == EPI_BF16) {
+    static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] = __float2bfloat16_rn(v);
+  } else if (a.epi == EPI_ADD_F32) {
+    static_cast<float*>(a.out)[(size_t)t * a.ldo + f] = a.res[(size_t)t * a.ldr + f] + v;
+  } else {
+    static_cast<float*>(a.out)[(size_t)t * a.ldo + f] = a.softcap > 0.f ? a.softcap * tanhf(v / a.softcap) : v;
+  }
 }
 
 // Sum the splits of one feature for every token (fixed split order) and store
@@ -71,17 +87,7 @@ FK_DEVICE void reduce_store(const SkinnyArgs& a, int S, int f) {
         u += tu[j];
       }
     }
-    if (a.epi == EPI_GLU_BF16) {
-      static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] =
-          __float2bfloat16_rn((a.act ? act_gelu_tanh(v) : act_silu(v)) * u);
-    } else if (a.epi == EPI_BF16) {
-      static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] = __float2bfloat16_rn(v);
-    } else if (a.epi == EPI_ADD_F32) {
-      float* o = static_cast<float*>(a.out) + (size_t)t * a.ldo + f;
-      *o = a.res[(size_t)t * a.ldr + f] + v;
-    } else {
-      static_cast<float*>(a.out)[(size_t)t * a.ldo + f] = a.softcap > 0.f ? a.softcap * tanhf(v / a.softcap) : v;
-    }
+    store_out(a, t, f, v, u);
   }
 }
 
@@ -224,6 +230,25 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   const bool have = mbar_wait(done, 0, abort_flag, args.dev_err);
   tc_fence_after();
   const int feat = n0 + warp * 32 + lane;
+  if (args.direct) {  // one split: the epilogue straight from TMEM
+#pragma unroll
+    for (int c0 = 0; c0 < (BT < 32 ? 32 : BT); c0 += 32) {
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      if (have && feat < args.n_rows) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < args.M) store_out(args, c0 + j, feat, v[j], 0.f);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    return;
+  }
   float* part = args.part + (size_t)split * args.M * args.n_rows;
 #pragma unroll
   for (int c0 = 0; c0 < (BT < 32 ? 32 : BT); c0 += 32) {
@@ -351,27 +376,34 @@ static int resident_per_sm(int M) {
   return cached[i];
 }
 
+// Small operands (under kDirectBytes of weights, not a gate/up pair) take a
+// single split: the CTAs write the epilogue straight from TMEM, with no
+// partial sums, arrival counters or ordered reduction on the critical path,
+// which for so few bytes cost more than the split's extra bandwidth gains.
+constexpr size_t kDirectBytes = 8u << 20;
+
 // Split K so that the whole grid is one wave of resident CTAs, every SM
 // holding the same number: each CTA starts at once and streams an equal
 // share of the weights (splits differ by at most one k-block).
-SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count) {
+SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count, bool allow_direct) {
   SkinnyPlan p;
   const int nk = (K + 63) / 64;
   const int n_tiles = (n_rows + 127) / 128;
   const int wave = resident_per_sm(M) * sm_count;
-  p.splits = std::max(1, std::min(nk, wave / n_tiles));
+  p.direct = allow_direct && (size_t)n_rows * K * 2 < kDirectBytes;
+  p.splits = p.direct ? 1 : std::max(1, std::min(nk, wave / n_tiles));
   p.kb_per_split = (nk + p.splits - 1) / p.splits;  // the longest split
   p.n_tiles = n_tiles;
   p.nk = nk;
   p.counter_bytes = ((size_t)n_tiles * sizeof(unsigned) + 255) / 256 * 256;
-  p.part_bytes = p.counter_bytes + (size_t)p.splits * M * n_rows * sizeof(float);
+  p.part_bytes = p.counter_bytes + (p.direct ? 0 : (size_t)p.splits * M * n_rows * sizeof(float));
   return p;
 }
 
 
 size_t skinny_counter_bytes(const GemmWeights& w, int M, int sm_count) {
   if (M <= 0 || M > kSkinnyMaxTokens) return 0;
-  return skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count).counter_bytes;
+  return skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count, !w.glu).counter_bytes;
 }
 
 size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count) {
@@ -380,7 +412,7 @@ size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count) {
   // largest product of splits and tokens is at the top of a width class
   size_t b = 0;
   for (int m : {std::min(M, 16), std::min(M, 32), M}) {
-    const SkinnyPlan p = skinny_plan(m, w.K, w.seg_start[w.nseg], sm_count);
+    const SkinnyPlan p = skinny_plan(m, w.K, w.seg_start[w.nseg], sm_count, !w.glu);
     b = std::max(b, p.part_bytes - p.counter_bytes);
   }
   return b;
@@ -393,7 +425,7 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   fk_status s = check_device(&sms);
   if (s != FK_OK) return s;
   const int n_rows = w.seg_start[w.nseg];
-  const SkinnyPlan p = skinny_plan(M, w.K, n_rows, sms);
+  const SkinnyPlan p = skinny_plan(M, w.K, n_rows, sms, !w.glu);
   const size_t creg = counter_region ? counter_region : p.counter_bytes;
   if (creg < p.counter_bytes || creg % 256) return fail(FK_ERR_INVALID_ARG, "skinny GEMM: counter region too small");
   if (!scratch || scratch_bytes < creg + (p.part_bytes - p.counter_bytes))
@@ -415,7 +447,8 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   a.dev_err = dev_err;
   // a gate|up pair fuses only when each half is a whole number of 128-row tiles
   // (the last CTA sums M x splits values per feature: worth it only for few tokens)
-  a.fused = M <= 8 && !(w.glu && n_out % 128);
+  a.direct = p.direct;
+  a.fused = !p.direct && M <= 8 && !(w.glu && n_out % 128);
   a.glu_tiles = w.glu ? n_out / 128 : 0;
   a.epi = o.epi;
   a.act = o.act;
@@ -432,7 +465,7 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
     s = launch_bt<32>(tX, w, a, p.n_tiles, p.splits, st);
   else
     s = launch_bt<64>(tX, w, a, p.n_tiles, p.splits, st);
-  if (s != FK_OK || a.fused) return s;
+  if (s != FK_OK || a.fused || a.direct) return s;
   const long work = (long)M * ((n_out + 3) / 4);
   const int blocks = (int)std::min<long>((work + 255) / 256, 8L * sms);
   cudaError_t e = fk_launch(splitk_reduce_kernel, blocks, 256, 0, st, (const float*)a.part, p.splits, M, n_rows, n_out,
@@ -447,7 +480,7 @@ extern "C" size_t fk_gemm_bf16_splitk_scratch_bytes(int32_t P, int32_t K, int32_
   if (P < 1 || P > fk::kSkinnyMaxTokens || K < 8 || N < 8) return 0;
   int sms = 0;
   if (fk::check_device(&sms) != FK_OK) return 0;
-  return fk::skinny_plan(P, K, N, sms).part_bytes;
+  return fk::skinny_plan(P, K, N, sms, true).part_bytes;
 }
 
 extern "C" fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
