@@ -2,16 +2,18 @@
 // Thm 1: causal multi-head/GQA attention; Thm 2 and "pegainfer #878":
 // sliding-window local layers).
 //
-// Prefill: flash-style, one CTA per (64 queries, head, sequence), 4 warps x 16
-// query rows, 64-key blocks double-buffered in shared memory with cp.async,
-// QKᵀ and PV on tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate), online
-// softmax in fp32 (exp2 domain), P rounded to bf16 for the PV product.
-// Only the key blocks inside the causal (and window) range are visited.
+// Prefill (used where the tcgen05 kernel of attention_tc.cu does not apply:
+// row strides or caches without the 16-byte / 64-position alignment its TMA
+// tiles need): flash-style, one CTA per (64 queries, head, sequence), 4 warps
+// x 16 query rows, 64-key blocks double-buffered in shared memory with
+// cp.async, QKᵀ and PV on mma.sync m16n8k16 (bf16, fp32 accumulate), online
+// softmax in fp32 (exp2 domain), P rounded to bf16 for the PV product. Only
+// the key blocks inside the causal (and window) range are visited.
 //
 // Decode: split-KV over a thread-block cluster. The CTAs of one cluster share
 // one (sequence, kv head) and split its key range into equal runs of 64-key
-// tiles; each scores all query heads of the GQA group against its tiles with
-// 16-byte loads and keeps an unnormalised partial (max, sum, output) in its
+// tiles streamed by TMA; each scores all query heads of the GQA group against
+// its tiles and keeps an unnormalised partial (max, sum, output) in its
 // shared memory. After a cluster barrier the CTAs merge the partials through
 // distributed shared memory, each CTA finishing a slice of the outputs and
 // adding the partials in rank order, so the result does not depend on

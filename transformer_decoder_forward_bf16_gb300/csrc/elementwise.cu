@@ -1,9 +1,12 @@
 // Bandwidth-bound kernels of the forward pass: embedding gather (+scale) with
 // the first RMSNorm fused, RMSNorm, the sandwich post-norm + residual +
-// next-norm fusion, QK-norm + RoPE + KV-cache write, and the per-row argmax.
+// next-norm fusion, QK-norm + RoPE + K-cache write, the V-cache transpose of
+// a prefill chunk, and the per-row argmax.
 //
-// Every row kernel assigns one warp per row, reads with 16-byte vector loads
-// and reduces with warp shuffles; nothing here needs shared memory.
+// Row kernels read with 16-byte vector loads and reduce with warp shuffles
+// (one warp per row, or one block per row with the row held in registers);
+// the V transpose stages its tile in shared memory so that both sides move
+// 128-byte runs.
 #include "fk_common.cuh"
 #include "fk_ops.h"
 

@@ -7,13 +7,17 @@
 //   * operands swapped: the weight tile (128 output features x 64 K) is the
 //     M=128 side of tcgen05.mma and the tokens are the N side (16/32/64), so
 //     TMEM lane = output feature and column = token;
-//   * split-K over a 2-D grid (feature tiles x K splits) sized to put about
-//     four CTAs on every SM, each streaming its weight slab through a 4-deep
-//     TMA ring (2 CTAs per SM => ~128 KB of loads in flight per SM);
-//   * fp32 partial sums per split, then one reduction kernel that adds the
-//     splits in a fixed order (bitwise-reproducible) and applies the fused
-//     epilogue (bf16 store, fp32 + softcap, fp32 residual add, or the gated
-//     FFN activation act(gate) * up).
+//   * split-K over a 2-D grid (feature tiles x K splits) sized to one wave
+//     with the same number of CTAs on every SM (three at <= 16 tokens), each
+//     streaming its weight slab through a 4-deep TMA ring (~190 KB of loads
+//     in flight per SM);
+//   * fp32 partial sums per split, added in a fixed order (bitwise-
+//     reproducible) by the last CTA of each feature tile (<= 8 tokens) or by
+//     one reduction kernel, which applies the fused epilogue (bf16 store,
+//     fp32 + softcap, fp32 residual add, or the gated FFN activation
+//     act(gate) * up);
+//   * operands under 8 MB take a single split and apply the epilogue straight
+//     from TMEM.
 #include <algorithm>
 #include <mutex>
 
