@@ -26,8 +26,8 @@ _LIB_PATH = os.path.join(_HERE, "_gen.so")
 _lib = None
 _lock = threading.Lock()
 
-# Default seeds follow the page's test seeds (metalgemm proof ledger, Thm 1
-# verdict: "rand source 7; lcg seeds 99 and 0x1234567").
+# Default seeds follow the test seeds that "N9 · metalgemm", Thm 1 reports:
+# 7 for its random source, 99 and 0x1234567 for its LCG-generated inputs.
 SEED_WEIGHTS = 7
 SEED_IDS = 99
 SEED_GEMM_X = 0x1234567

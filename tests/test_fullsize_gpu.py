@@ -12,13 +12,13 @@
   Acceptance Criteria: tight gates and exact top-1 on the short cases, the
   distributional gate at the 1024-token window edge, bitwise replay).
 
-Greedy reading (spec margin rule): free-running ids must match until a
+Greedy reading (the margin rule of the parity gates): free-running ids must match until a
 step where the oracle's top-1/top-2 margin is <= 1e-2 (a near tie, recorded,
 not a failure); a teacher-forced pass then checks the argmax of every step
 whose margin exceeds 1e-2.
 
 The exact oracle (float64, nothing rounded) is the definition. On the
-SmolLM2 shape the device meets every spec gate against it. On the
+SmolLM2 shape the device meets every parity gate against it. On the
 Llama-3-8B and Gemma-style shapes (random weights with large hidden sizes make
 attention sharp, which amplifies rounding noise) the numerics contract itself
 -- bf16 storage of the norm outputs, q/k/v, attention output and FFN
@@ -152,7 +152,7 @@ def test_llama3_8b_slice_vs_oracle(fk):
           f"last logits max|d| device {z_dev:.4f} contract {z_ct:.4f}; worst cos device "
           f"{_worst_cos(h, ex['hidden'][:, 0], 3):.6f} contract {_worst_cos(ct['hidden'][:, 0], ex['hidden'][:, 0], 3):.6f}")
     assert e_dev <= 1.25 * e_ct and z_dev <= 1.25 * z_ct + 0.01
-    # embedding and layer-1 slots stay inside the spec cosine gate
+    # embedding and layer-1 slots stay inside the 0.9999 cosine gate
     assert _worst_cos(h[:2], ex["hidden"][:2, 0], 3) >= 0.9999
     thr = _noise_margin(z_ct)
     decided = ref["margins"] > thr
