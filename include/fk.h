@@ -70,6 +70,34 @@ typedef enum { FK_ACT_SILU = 0, FK_ACT_GELU_TANH = 1 } fk_act;
 typedef enum { FK_NORM_PRE = 0, FK_NORM_SANDWICH = 1 } fk_norm_layout;
 typedef enum { FK_EMBED_SCALE_NONE = 0, FK_EMBED_SCALE_SQRT_HIDDEN_BF16 = 1 } fk_embed_scale;
 
+/* Activation storage sites (bits of fk_config.f16_sites). Every activation
+ * the forward keeps in 16 bits between two kernels is stored as bf16 (8
+ * significant bits) unless its site's bit is set, in which case it is stored
+ * as IEEE f16 (11 significant bits, range +-65504). A GEMM whose input site is
+ * f16 runs on f16 tensor-core operands against an f16 copy of its bf16
+ * weights, made once in the model arena (exact for weights of magnitude in
+ * [2^-17, 65504]; smaller ones keep an absolute error below 2^-25). All
+ * accumulation stays fp32 and the residual stream fp32 either way. The bits:
+ *   FK_F16_QKV_IN   norm output feeding the Q/K/V projection
+ *   FK_F16_ATTN     q, k, v, the KV cache and the softmax probabilities
+ *   FK_F16_O_IN     attention output feeding the O projection
+ *   FK_F16_FFN_IN   norm output feeding the gate/up projection
+ *   FK_F16_FFN_ACT  gated activation feeding the down projection
+ *   FK_F16_HEAD_IN  final-norm output feeding the LM head
+ * f16 keeps 3 more significant bits than bf16: on deep models with large
+ * hidden sizes the rounding of these activations is what separates the
+ * result from the exact forward, so the finer format brings it inside the
+ * forward-parity gates ("N7 · model/forward-parity", Thm 1: hidden cosine
+ * >= 0.9999, last-position logits within 0.05) at the same tensor-core rate.
+ * The price is range: an activation above 65504 in magnitude overflows. */
+#define FK_F16_QKV_IN 0x01u
+#define FK_F16_ATTN 0x02u
+#define FK_F16_O_IN 0x04u
+#define FK_F16_FFN_IN 0x08u
+#define FK_F16_FFN_ACT 0x10u
+#define FK_F16_HEAD_IN 0x20u
+#define FK_F16_ALL 0x3Fu
+
 /*
  * Model geometry ("pegainfer #878": one typed config is the single source of
  * every buffer size). Validation rules (FK_ERR_INVALID_CONFIG otherwise):
@@ -81,7 +109,7 @@ typedef enum { FK_EMBED_SCALE_NONE = 0, FK_EMBED_SCALE_SQRT_HIDDEN_BF16 = 1 } fk
  *   orig_max_pos > 0; act, norm_layout and embed_scale one of their enums;
  *   qk_norm and tied 0 or 1; sliding_window >= 0; layer_kinds entries 0
  *   (global) or 1 (local), local layers only with sliding_window > 0;
- *   final_softcap == 0 (off) or > 0 and finite.
+ *   final_softcap == 0 (off) or > 0 and finite; f16_sites within FK_F16_ALL.
  */
 typedef struct fk_config {
   int32_t n_layers;
@@ -107,6 +135,7 @@ typedef struct fk_config {
   int32_t embed_scale;          /* fk_embed_scale */
   float final_softcap;          /* c of z -> c*tanh(z/c); 0 = off */
   int32_t tied;                 /* 1 = LM head is the embedding matrix */
+  uint32_t f16_sites;           /* FK_F16_* bits: activation sites stored as f16 (0 = all bf16) */
 } fk_config;
 
 /* Per-layer device weights, all bf16. Matrices are [out, in] row-major.
@@ -151,9 +180,10 @@ const char* fk_version(void);
 /* ---------------------------------------------------------------------------
  * Model
  * ------------------------------------------------------------------------- */
-/* Device arena the model needs (RoPE cos/sin tables for positions
- * [0, max_positions) of each layer kind, and the device error word).
- * Returns 0 if cfg is invalid. */
+/* Device arena the model needs (the device error word, RoPE cos/sin tables
+ * for positions [0, max_positions) of each layer kind, and the f16 copies of
+ * the weights of every GEMM whose input site is f16). Returns 0 if cfg is
+ * invalid. */
 size_t fk_model_arena_bytes(const fk_config* cfg, int32_t max_positions);
 
 /* Validate cfg, bind the caller's device weights (borrowed: they must outlive
@@ -179,10 +209,13 @@ size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, int32_t seq)
  *        n_layers+1 the final-norm output.
  *   d_logits: NULL, or fp32 [batch*seq][vocab] (after the softcap, if any).
  *   d_argmax: NULL, or int32 [batch*seq]: lowest index of the row maximum.
+ *   d_margin: NULL, or fp32 [batch*seq]: the row maximum minus the largest
+ *        other logit (0 on a tie) -- how far the argmax is from a flip ("N7 ·
+ *        model/forward-parity", Thm 3: near-tie argmax flips). Needs d_argmax.
  * A host `ids` buffer is copied synchronously before the call returns. */
 fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
                      void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
-                     void* stream);
+                     float* d_margin, void* stream);
 
 /* ---------------------------------------------------------------------------
  * KV-cached session ("N7", Thm 1: NewSession().Prefill and greedy Generate)
@@ -199,14 +232,17 @@ void fk_session_free(fk_session* s);
 /* Append ids [batch, seq] (host or device as in fk_forward) after the tokens
  * already in the session. d_last_logits: NULL or fp32 [batch][vocab] of the
  * last position; d_next: NULL or int32 [batch], the greedy next ids (also
- * kept in the session for fk_decode_step). FK_ERR_CONTEXT_FULL if the
- * session would exceed max_seq. */
+ * kept in the session for fk_decode_step); d_margin: NULL or fp32 [batch],
+ * the top-1 minus top-2 logit of each next id (as in fk_forward).
+ * FK_ERR_CONTEXT_FULL if the session would exceed max_seq. */
 fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32_t ids_on_device, int32_t seq,
-                             float* d_last_logits, int32_t* d_next, void* stream);
+                             float* d_last_logits, int32_t* d_next, float* d_margin, void* stream);
 
 /* One greedy decode step: feed d_ids [batch] (device int32), or the session's
- * last greedy ids when d_ids is NULL; write logits / next ids as in prefill. */
-fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next, void* stream);
+ * last greedy ids when d_ids is NULL; write logits / next ids / margins as in
+ * prefill. */
+fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next, float* d_margin,
+                         void* stream);
 
 /* Forget all tokens (length 0); the cache memory is reused. */
 fk_status fk_session_reset(fk_session* s);
@@ -214,11 +250,15 @@ int32_t fk_session_length(const fk_session* s);
 
 /* Wait up to timeout_ms for `stream` to drain, then read and clear the device
  * error word: FK_OK, FK_ERR_DEVICE_FLAG (bits in *flags if non-NULL), or
- * FK_ERR_TIMEOUT (the stream is still busy; nothing was read). */
+ * FK_ERR_TIMEOUT (the stream is still busy; nothing was read). m == NULL reads
+ * the current device's op-level word instead, which the op-level entry points
+ * below (GEMMs, attention, op hooks) set. */
 fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t* flags);
 
 /* ---------------------------------------------------------------------------
  * Op-level entry points (per-kernel parity; same kernels as the forward)
+ * A pipeline timeout inside one of them sets the current device's op-level
+ * error word, read with fk_sync_status(NULL, ...).
  * ------------------------------------------------------------------------- */
 /* Y[P,N] = X[P,K] · W[N,K]ᵀ, bf16 inputs, fp32 accumulation ("N9 · metalgemm",
  * Thm 1). Y is bf16 (y_fp32 == 0) or fp32. K % 8 == 0, N % 8 == 0 (16-byte
@@ -244,8 +284,7 @@ fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32
  *          V transposed [batch][n_kv_heads][head_dim][cap], cap % 64 == 0,
  *          positions up to the next multiple of 128 finite)
  *   d_out: bf16 [batch*seq][n_q_heads*head_dim]
- * head_dim 64, 128 and 256 run on the tensor-core (tcgen05) kernel. No
- * scratch. */
+ * head_dim 64, 128 or 256, on the tensor-core (tcgen05) kernel. No scratch. */
 fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch, int32_t seq,
                                int32_t pos0, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
                                int32_t window, void* d_out, void* stream);
@@ -263,28 +302,56 @@ fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void
  * Query head h reads kv head h / (n_q_heads/n_kv_heads); scale 1/sqrt(head_dim).
  * Split-KV: the splits of a (sequence, kv head) run as one thread-block
  * cluster and merge their partials in the cluster's shared memory in a fixed
- * order, so results are bitwise reproducible. d_scratch (at least
- * fk_attention_decode_scratch_bytes(...) bytes, 16-byte aligned) is part of
- * the interface but is not written by the current kernel.
+ * order, so results are bitwise reproducible and no scratch memory is used.
  * head_dim is 64, 128 or 256; 1..8 query heads per kv head; 1 <= ctx <= cap. */
-size_t fk_attention_decode_scratch_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                         int32_t ctx);
 fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap, int32_t ctx,
-                              int32_t window, void* d_scratch, size_t scratch_bytes, void* d_out, void* stream);
+                              int32_t window, void* d_out, void* stream);
 
-/* Allocation-free fk_attention_decode. The pages have no counterpart: this
- * entry point serves callers that cannot provide a scratch buffer (their
- * device memory belongs to another allocator, or their path must not enter
- * the driver's allocation code). Arguments and results are those of
- * fk_attention_decode. The kernel keeps its split partials on chip, so the
- * call touches no device memory beyond its arguments, reserves none
- * (fk_attention_decode_noalloc_limit() returns 0), shares nothing between
- * calls and calls no allocator of any kind. */
-size_t fk_attention_decode_noalloc_limit(void);
-fk_status fk_attention_decode_noalloc(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
-                                      int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
-                                      int32_t ctx, int32_t window, void* d_out, void* stream);
+/* Op hooks: one step of the path alone, on the kernels the forward uses, for
+ * per-step parity ("N9 · metalgemm", Thm 1: op-level parity of each device
+ * op, not only of the chain).
+ *
+ * fk_op_rmsnorm ("N7 · model/forward-parity", Thm 1: RMSNorm):
+ *   d_out[r] = d_x[r] / sqrt(mean(d_x[r]^2) + eps) * d_w, rounded to bf16.
+ *   d_x fp32 [rows][hidden], d_w bf16 [hidden], d_out bf16 [rows][hidden];
+ *   hidden a positive multiple of 8, eps > 0. */
+fk_status fk_op_rmsnorm(const float* d_x, int32_t rows, int32_t hidden, const void* d_w, float eps, void* d_out,
+                        void* stream);
+
+/* fk_op_rope ("N7", Thm 1: RoPE on q and k; Thm 2: QK-norm, llama3 scaling,
+ * local/global RoPE bases): for `layer` of model m, on d_qkv bf16
+ * [batch*seq][(n_q_heads + 2 n_kv_heads) head_dim] (rows of [q | k | v] heads,
+ * token t = b*seq + s at position pos0 + s): [QK-norm with the layer's
+ * q_norm/k_norm when the config has qk_norm, then] RoPE with the layer kind's
+ * base (and scaling) rotates q in place and writes the rotated k to d_kcache
+ * bf16 [batch][n_kv_heads][cap][head_dim] and v, transposed, to d_vcache bf16
+ * [batch][n_kv_heads][head_dim][cap] at positions pos0..pos0+seq-1. Other
+ * cache positions are untouched. pos0 + seq <= cap, cap % 64 == 0, and
+ * pos0 + seq <= the model's max_positions (FK_ERR_CONTEXT_FULL otherwise). */
+fk_status fk_op_rope(fk_model* m, int32_t layer, void* d_qkv, int32_t batch, int32_t seq, int32_t pos0,
+                     void* d_kcache, void* d_vcache, int32_t cap, void* stream);
+
+/* fk_op_head_argmax ("N7", Thm 1: head matmul to logits and per-position
+ * argmax; "pegainfer #878": final-logit softcap): d_logits fp32
+ * [rows][vocab] = softcap(d_u · headᵀ) with the model's (tied or untied)
+ * head, d_u bf16 [rows][hidden] (final-norm output); d_argmax (NULL or int32
+ * [rows]) the lowest index of each row maximum; d_margin (NULL or fp32 [rows],
+ * needs d_argmax) the row maximum minus the largest other logit. */
+fk_status fk_op_head_argmax(fk_model* m, const void* d_u, int32_t rows, float* d_logits, int32_t* d_argmax,
+                            float* d_margin, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Testing hook (failure detection)
+ * Sets the test controls of the current device's op-level control block:
+ * stall_first_stage != 0 makes fk_gemm_bf16_splitk leave its first pipeline
+ * stage unarmed, so the tensor-core issuer's bounded wait on it runs out;
+ * wait_limit_us > 0 replaces the 2 s limit of every bounded wait in op-level
+ * calls. The kernel then gives up, leaves its output undefined, sets
+ * FK_DEVERR_PIPE_TIMEOUT and returns; fk_sync_status(NULL, ...) reports it.
+ * (0, 0) restores normal operation. Not for production use.
+ * ------------------------------------------------------------------------- */
+fk_status fk_debug_set_op_pipe_fault(int32_t stall_first_stage, int32_t wait_limit_us);
 
 /* ---------------------------------------------------------------------------
  * Kernel timing (tracing)

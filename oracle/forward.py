@@ -27,10 +27,15 @@ listed in the design notes):
 * Argmax ties go to the lowest index.
 
 ``storage="bf16"`` evaluates the same definition with the values that the
-numerics contract stores in bf16 rounded to bf16 where they are stored (every
-norm output that feeds a projection, the projected q, k, v, q and k after
-QK-norm and RoPE, the attention output, the gated FFN activation and the LM
-head input). Arithmetic stays float64 and the attention probabilities stay
+numerics contract stores in 16 bits rounded where they are stored, to bf16.
+The storage sites are: ``qkv_in`` (the norm output feeding the Q/K/V
+projection), ``attn`` (the projected q, k, v and q, k after QK-norm and
+RoPE), ``o_in`` (the attention output feeding the O projection), ``ffn_in``
+(the norm output feeding gate/up), ``ffn_act`` (the gated activation feeding
+the down projection) and ``head_in`` (the final-norm output feeding the LM
+head). ``storage="f16"`` rounds the same sites to IEEE binary16 instead, and a
+dict {site: "exact" | "bf16" | "f16"} chooses per site (unnamed sites stay
+exact). Arithmetic stays float64 and the attention probabilities stay
 unrounded. ``storage="exact"`` (the default) rounds nothing.
 """
 from __future__ import annotations
@@ -42,7 +47,8 @@ import numpy as np
 __all__ = [
     "bf16_to_f64", "round_to_bf16", "embed_scale", "rmsnorm", "rope_inv_freq", "rope_apply",
     "attention", "silu", "gelu_tanh", "softcap", "gemm", "OracleWeights", "forward", "Session",
-    "argmax_first", "top2_margin", "log_softmax", "topk_ids", "greedy", "store_bf16",
+    "argmax_first", "top2_margin", "log_softmax", "topk_ids", "greedy", "store_bf16", "store_f16",
+    "STORAGE_SITES",
 ]
 
 
@@ -74,12 +80,37 @@ def store_bf16(x: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def _rounder(storage: str):
-    if storage == "exact":
-        return lambda x: x
-    if storage == "bf16":
-        return store_bf16
-    raise ValueError(storage)
+def store_f16(x: np.ndarray) -> np.ndarray:
+    """Value of x after being stored as IEEE binary16: float64 -> float32
+    (nearest), then float32 -> binary16 (nearest, ties to even; subnormals
+    kept, overflow to infinity)."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float64)
+
+
+STORAGE_SITES = ("qkv_in", "attn", "o_in", "ffn_in", "ffn_act", "head_in")
+_FORMATS = {"exact": lambda x: x, "bf16": store_bf16, "f16": store_f16}
+
+
+class _Rounder:
+    """Storage rounding per site (see the module docstring)."""
+
+    def __init__(self, storage):
+        if isinstance(storage, str):
+            if storage not in _FORMATS:
+                raise ValueError(storage)
+            storage = {site: storage for site in STORAGE_SITES}
+        unknown = set(storage) - set(STORAGE_SITES)
+        if unknown:
+            raise ValueError(f"unknown storage sites {sorted(unknown)}")
+        self.fn = {site: _FORMATS[storage.get(site, "exact")] for site in STORAGE_SITES}
+
+    def __call__(self, site: str, x: np.ndarray) -> np.ndarray:
+        return self.fn[site](x)
+
+
+def _rounder(storage):
+    return _Rounder(storage)
 
 
 # ---------------------------------------------------------------------------
@@ -234,7 +265,7 @@ class OracleWeights:
 # ---------------------------------------------------------------------------
 # Decoder layer and forward
 # ---------------------------------------------------------------------------
-def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k, past_v, past_pos, R=lambda v: v):
+def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k, past_v, past_pos, R=None):
     """One decoder layer on x [B, S, H] at positions pos [B, S].
 
     past_k/past_v [B, P, Hkv, hd] (P may be 0) are this layer's cached keys and
@@ -248,16 +279,18 @@ def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k
     kind = cfg.kinds()[l]
     window = cfg.sliding_window if kind == 1 else 0
 
-    u = R(rmsnorm(x, W[p + "attn_norm"], cfg.rms_eps))
-    q = R(W.linear(u, p + "wq")).reshape(B, S, Hq, hd)
-    k = R(W.linear(u, p + "wk")).reshape(B, S, Hkv, hd)
-    v = R(W.linear(u, p + "wv")).reshape(B, S, Hkv, hd)
+    if R is None:
+        R = _rounder("exact")
+    u = R("qkv_in", rmsnorm(x, W[p + "attn_norm"], cfg.rms_eps))
+    q = R("attn", W.linear(u, p + "wq")).reshape(B, S, Hq, hd)
+    k = R("attn", W.linear(u, p + "wk")).reshape(B, S, Hkv, hd)
+    v = R("attn", W.linear(u, p + "wv")).reshape(B, S, Hkv, hd)
     if cfg.qk_norm:
         q = rmsnorm(q, W[p + "q_norm"], cfg.rms_eps)
         k = rmsnorm(k, W[p + "k_norm"], cfg.rms_eps)
     f = rope_inv_freq(cfg, kind)
-    q = R(rope_apply(q, pos, f))
-    k = R(rope_apply(k, pos, f))
+    q = R("attn", rope_apply(q, pos, f))
+    k = R("attn", rope_apply(k, pos, f))
 
     keys = np.concatenate([past_k, k], axis=1)
     vals = np.concatenate([past_v, v], axis=1)
@@ -265,16 +298,16 @@ def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k
     o = np.empty((B, S, Hq, hd), dtype=np.float64)
     for b in range(B):
         o[b] = attention(q[b], keys[b], vals[b], pos[b], kpos[b], window, 1.0 / math.sqrt(hd))
-    a = W.linear(R(o).reshape(B, S, Hq * hd), p + "wo")
+    a = W.linear(R("o_in", o).reshape(B, S, Hq * hd), p + "wo")
     if cfg.norm_layout == "sandwich":
         a = rmsnorm(a, W[p + "post_attn_norm"], cfg.rms_eps)
     x = x + a
 
-    u = R(rmsnorm(x, W[p + "ffn_norm"], cfg.rms_eps))
+    u = R("ffn_in", rmsnorm(x, W[p + "ffn_norm"], cfg.rms_eps))
     g = W.linear(u, p + "w_gate")
     up = W.linear(u, p + "w_up")
     act = silu(g) if cfg.act == "silu" else gelu_tanh(g)
-    d = W.linear(R(act * up), p + "w_down")
+    d = W.linear(R("ffn_act", act * up), p + "w_down")
     if cfg.norm_layout == "sandwich":
         d = rmsnorm(d, W[p + "post_ffn_norm"], cfg.rms_eps)
     x = x + d
@@ -324,9 +357,9 @@ def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "a
         slots.append(y)
     out = {"hidden": np.stack(slots) if hidden else None}
     if logits == "all":
-        out["logits"] = _head(cfg, W, R(y))
+        out["logits"] = _head(cfg, W, R("head_in", y))
     elif logits == "last":
-        out["logits"] = _head(cfg, W, R(y[:, -1, :]))
+        out["logits"] = _head(cfg, W, R("head_in", y[:, -1, :]))
     else:
         out["logits"] = None
     return out
@@ -359,7 +392,7 @@ class Session:
             self.k[l] = np.concatenate([self.k[l], k], axis=1)
             self.v[l] = np.concatenate([self.v[l], v], axis=1)
         self.length += S
-        y = self.R(rmsnorm(x[:, -1, :], W["final_norm"], cfg.rms_eps))
+        y = self.R("head_in", rmsnorm(x[:, -1, :], W["final_norm"], cfg.rms_eps))
         return _head(cfg, W, y)
 
     def prefill(self, ids: np.ndarray) -> np.ndarray:

@@ -36,6 +36,7 @@ class ModelConfig:
     embed_scale: str = "none"           # "none" | "sqrt_hidden_bf16"
     final_softcap: float = 0.0          # 0 = off
     tied: bool = True
+    f16_sites: int = 0                  # activation storage sites kept as IEEE f16 (bit mask; 0 = all bf16)
 
     def kinds(self) -> tuple:
         return self.layer_kinds if self.layer_kinds else (0,) * self.n_layers

@@ -467,3 +467,75 @@ def test_bf16_storage_mode_is_close_but_not_exact():
     d = np.abs(st["logits"] - ex["logits"]).max()
     assert 0 < d < 0.05 * np.abs(ex["logits"]).max()
     np.testing.assert_array_equal(st["hidden"][0], ex["hidden"][0])  # the embedding is not a stored activation
+
+
+def test_oracle_weights_chunked_linear_matches_whole():
+    """OracleWeights.linear widens a large weight a block of output rows at a
+    time (the full-size Llama and Gemma heads and FFNs take that branch). Force
+    the branch on a small matrix with a ragged last block: every output must
+    equal the one-shot float64 product (each element is the same dot product
+    over the input), and a wrong block offset would move whole columns."""
+    rng = np.random.default_rng(17)
+    K, N = 96, 1000
+    bits = {"w": synth.normal_bf16(5, 77, (N, K), 0.02), "u": synth.normal_bf16(5, 78, (7, K), 1.0)}
+    x = oracle.bf16_to_f64(bits["u"]).reshape(1, 7, K)
+    chunked = oracle.OracleWeights(bits, cache_limit_bytes=0)
+    assert chunked.cache is None  # the widening-on-read path
+    whole = oracle.gemm(x, oracle.bf16_to_f64(bits["w"]))
+    for rows in (64, 333, 999, 1000):
+        got = chunked.linear(x, "w", rows_per_chunk=rows)
+        assert got.shape == (1, 7, N)
+        np.testing.assert_allclose(got, whole, rtol=1e-13, atol=1e-15)
+    # column j is the dot product with weight row j
+    j = int(rng.integers(0, N))
+    got = chunked.linear(x, "w", rows_per_chunk=64)
+    assert abs(got[0, 3, j] - float(np.dot(x[0, 3], oracle.bf16_to_f64(bits["w"][j])))) < 1e-13
+
+
+def _round_to_f16_scalar(v: float) -> float:
+    """IEEE binary16 rounding of a finite scalar written from the format's
+    definition: 11 significant bits for normal numbers (|v| >= 2^-14), a fixed
+    spacing of 2^-24 below, ties to even, overflow past 65504 to infinity."""
+    if v == 0.0:
+        return 0.0
+    m, e = math.frexp(v)            # v = m * 2^e, 0.5 <= |m| < 1
+    if e - 1 >= -14:
+        r = math.ldexp(round(m * 2048.0), e - 11)
+    else:
+        r = math.ldexp(round(math.ldexp(v, 24)), -24)
+    if abs(r) > 65504.0:
+        return math.copysign(math.inf, v)
+    return r
+
+
+def test_store_f16_matches_scalar_rounding():
+    x = np.concatenate([RNG.standard_normal(3000) * 37.0, RNG.standard_normal(500) * 3e-5,
+                        RNG.standard_normal(200) * 2e4, [65504.0, 65519.0, 65520.0, -70000.0, 2.0 ** -24,
+                                                        2.0 ** -25, 3 * 2.0 ** -26, 1.0 + 2.0 ** -11]])
+    got = oracle.store_f16(x)
+    want = np.array([_round_to_f16_scalar(float(np.float32(v))) for v in x])
+    np.testing.assert_array_equal(got, want)
+    # bf16 values of magnitude in [2^-14, 65504] are binary16 values: storing is exact
+    b = oracle.store_bf16(RNG.standard_normal(2000) * 0.02)
+    b = b[np.abs(b) >= 2.0 ** -14]
+    np.testing.assert_array_equal(oracle.store_f16(b), b)
+
+
+def test_storage_sites_select_rounding():
+    cfg = tiny_config("gemma")
+    wb = synth.make_weights(cfg, seed=2, sigma=0.3, norm_mode="random")
+    ids = synth.make_ids(cfg, 1, 8, seed=3)
+    ex = oracle.forward(cfg, wb, ids)
+    allb = oracle.forward(cfg, wb, ids, storage={s: "bf16" for s in oracle.STORAGE_SITES})
+    np.testing.assert_array_equal(allb["logits"], oracle.forward(cfg, wb, ids, storage="bf16")["logits"])
+    d16 = np.abs(oracle.forward(cfg, wb, ids, storage="f16")["logits"] - ex["logits"]).max()
+    db = np.abs(allb["logits"] - ex["logits"]).max()
+    assert 0 < d16 < db / 3  # 3 more significant bits
+    # one site at a time moves the result; the head input alone moves only the logits
+    for site in oracle.STORAGE_SITES:
+        one = oracle.forward(cfg, wb, ids, storage={site: "bf16"})
+        assert np.abs(one["logits"] - ex["logits"]).max() > 0, site
+        if site == "head_in":
+            np.testing.assert_array_equal(one["hidden"], ex["hidden"])
+    with pytest.raises(ValueError):
+        oracle.forward(cfg, wb, ids, storage={"nope": "bf16"})

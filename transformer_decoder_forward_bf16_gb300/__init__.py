@@ -27,6 +27,11 @@ STATUS = {0: "FK_OK", 1: "FK_ERR_INVALID_ARG", 2: "FK_ERR_INVALID_CONFIG", 3: "F
           8: "FK_ERR_TIMEOUT", 9: "FK_ERR_WORKSPACE"}
 DEVERR_TOKEN_RANGE = 0x1
 DEVERR_PIPE_TIMEOUT = 0x2
+# activation storage sites stored as IEEE f16 instead of bf16 (fk_config.f16_sites)
+F16_QKV_IN, F16_ATTN, F16_O_IN, F16_FFN_IN, F16_FFN_ACT, F16_HEAD_IN = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
+F16_ALL = 0x3F
+F16_SITE_BITS = {"qkv_in": F16_QKV_IN, "attn": F16_ATTN, "o_in": F16_O_IN, "ffn_in": F16_FFN_IN,
+                 "ffn_act": F16_FFN_ACT, "head_in": F16_HEAD_IN}
 
 
 class FkError(RuntimeError):
@@ -42,7 +47,7 @@ class FkConfig(ctypes.Structure):
                 ("rope_factor", c_float), ("rope_low_freq_factor", c_float), ("rope_high_freq_factor", c_float),
                 ("rope_orig_max_pos", c_int32), ("act", c_int32), ("norm_layout", c_int32), ("qk_norm", c_int32),
                 ("sliding_window", c_int32), ("layer_kinds", c_void_p), ("embed_scale", c_int32),
-                ("final_softcap", c_float), ("tied", c_int32)]
+                ("final_softcap", c_float), ("tied", c_int32), ("f16_sites", c_uint32)]
 
 
 class FkLayerWeights(ctypes.Structure):
@@ -66,12 +71,12 @@ _SIGS = {
     "fk_model_free": (None, [c_void_p]),
     "fk_forward_workspace_bytes": (c_size_t, [c_void_p, c_int32, c_int32]),
     "fk_forward": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p,
-                             c_void_p, c_void_p]),
+                             c_void_p, c_void_p, c_void_p]),
     "fk_session_bytes": (c_size_t, [c_void_p, c_int32, c_int32, c_int32]),
     "fk_session_create": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_size_t, POINTER(c_void_p)]),
     "fk_session_free": (None, [c_void_p]),
-    "fk_session_prefill": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
-    "fk_decode_step": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fk_session_prefill": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fk_decode_step": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "fk_session_reset": (c_int32, [c_void_p]),
     "fk_session_length": (c_int32, [c_void_p]),
     "fk_sync_status": (c_int32, [c_void_p, c_void_p, c_int32, POINTER(c_uint32)]),
@@ -81,12 +86,13 @@ _SIGS = {
                                       c_size_t, c_void_p]),
     "fk_attention_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
                                        c_int32, c_int32, c_int32, c_void_p, c_void_p]),
-    "fk_attention_decode_scratch_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32]),
     "fk_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
-                                      c_int32, c_int32, c_void_p, c_size_t, c_void_p, c_void_p]),
-    "fk_attention_decode_noalloc_limit": (c_size_t, []),
-    "fk_attention_decode_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
-                                              c_int32, c_int32, c_int32, c_void_p, c_void_p]),
+                                      c_int32, c_int32, c_void_p, c_void_p]),
+    "fk_debug_set_op_pipe_fault": (c_int32, [c_int32, c_int32]),
+    "fk_op_rmsnorm": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_float, c_void_p, c_void_p]),
+    "fk_op_rope": (c_int32, [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32,
+                             c_void_p]),
+    "fk_op_head_argmax": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "fk_profile_enable": (None, [c_int32]),
     "fk_profile_reset": (None, []),
     "fk_profile_count": (c_int32, []),
@@ -141,17 +147,24 @@ def fk_gemm_bf16(x_ptr, w_ptr, P, K, N, y_ptr, y_fp32, stream_ptr) -> int:
 
 
 def fk_forward(model_ptr, ids_ptr, ids_on_device, batch, seq, ws_ptr, ws_bytes, hidden_ptr, logits_ptr,
-               argmax_ptr, stream_ptr) -> int:
+               argmax_ptr, margin_ptr, stream_ptr) -> int:
     return load().fk_forward(model_ptr, ids_ptr, ids_on_device, batch, seq, ws_ptr, ws_bytes, hidden_ptr,
-                             logits_ptr, argmax_ptr, stream_ptr)
+                             logits_ptr, argmax_ptr, margin_ptr, stream_ptr)
 
 
-def fk_session_prefill(sess_ptr, ids_ptr, ids_on_device, seq, logits_ptr, next_ptr, stream_ptr) -> int:
-    return load().fk_session_prefill(sess_ptr, ids_ptr, ids_on_device, seq, logits_ptr, next_ptr, stream_ptr)
+def fk_session_prefill(sess_ptr, ids_ptr, ids_on_device, seq, logits_ptr, next_ptr, margin_ptr, stream_ptr) -> int:
+    return load().fk_session_prefill(sess_ptr, ids_ptr, ids_on_device, seq, logits_ptr, next_ptr, margin_ptr,
+                                     stream_ptr)
 
 
-def fk_decode_step(sess_ptr, ids_ptr, logits_ptr, next_ptr, stream_ptr) -> int:
-    return load().fk_decode_step(sess_ptr, ids_ptr, logits_ptr, next_ptr, stream_ptr)
+def fk_decode_step(sess_ptr, ids_ptr, logits_ptr, next_ptr, margin_ptr, stream_ptr) -> int:
+    return load().fk_decode_step(sess_ptr, ids_ptr, logits_ptr, next_ptr, margin_ptr, stream_ptr)
+
+
+def op_sync_status(stream=None, timeout_ms: int = 10000):
+    """Drain `stream`, then read and clear the current device's op-level error
+    word (set by the op-level entry points): returns (status, flags)."""
+    return fk_sync_status(None, _stream_ptr(stream), timeout_ms)
 
 
 def fk_sync_status(model_ptr, stream_ptr, timeout_ms):
@@ -203,21 +216,27 @@ def attention_prefill(q, kcache, vcache, seq: int, pos0: int = 0, window: int = 
     return out
 
 
-def attention_decode(q, kcache, vcache, ctx: int, window: int = 0, out=None, scratch=None, stream=None):
+def attention_decode(q, kcache, vcache, ctx: int, window: int = 0, out=None, stream=None):
     """One decode-attention step: q [B, Hq*hd], kcache [B, Hkv, cap, hd],
     vcache transposed [B, Hkv, hd, cap] (bf16, cap a multiple of 64)."""
     import torch
     B, Hkv, cap, hd = kcache.shape
     Hq = q.shape[1] // hd
-    lib = load()
-    nbytes = lib.fk_attention_decode_scratch_bytes(B, Hq, Hkv, hd, ctx)
-    if scratch is None:
-        scratch = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty_like(q)
-    _check(lib.fk_attention_decode(_ptr(q), _ptr(kcache), _ptr(vcache), B, Hq, Hkv, hd, cap, ctx, window,
-                                   _ptr(scratch), scratch.numel(), _ptr(out), _stream_ptr(stream)),
-           "fk_attention_decode")
+    _check(load().fk_attention_decode(_ptr(q), _ptr(kcache), _ptr(vcache), B, Hq, Hkv, hd, cap, ctx, window,
+                                      _ptr(out), _stream_ptr(stream)), "fk_attention_decode")
+    return out
+
+
+def rmsnorm(x, w, eps: float, out=None, stream=None):
+    """fk_op_rmsnorm: bf16 RMSNorm(x) * w of fp32 rows x [rows, hidden]."""
+    import torch
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=x.device)
+    _check(load().fk_op_rmsnorm(_ptr(x), rows, hidden, _ptr(w), eps, _ptr(out), _stream_ptr(stream)),
+           "fk_op_rmsnorm")
     return out
 
 
@@ -236,7 +255,7 @@ def config_to_c(cfg) -> tuple:
         norm_layout={"pre": 0, "sandwich": 1}[cfg.norm_layout], qk_norm=int(cfg.qk_norm),
         sliding_window=cfg.sliding_window, layer_kinds=ctypes.cast(kbuf, c_void_p) if len(kinds) else None,
         embed_scale={"none": 0, "sqrt_hidden_bf16": 1}[cfg.embed_scale], final_softcap=cfg.final_softcap,
-        tied=int(cfg.tied))
+        tied=int(cfg.tied), f16_sites=int(getattr(cfg, "f16_sites", 0)))
     return c, kbuf
 
 
@@ -281,7 +300,8 @@ class Model:
         except Exception:
             pass
 
-    def forward(self, ids, hidden: bool = True, logits: bool = True, argmax: bool = True, stream=None) -> dict:
+    def forward(self, ids, hidden: bool = True, logits: bool = True, argmax: bool = True, margin: bool = False,
+                stream=None) -> dict:
         """Cacheless forward over ids [B, S] (numpy/CPU int32 = host ids, CUDA
         int32 tensor = device ids). Returns torch tensors on the device."""
         import numpy as np
@@ -301,11 +321,33 @@ class Model:
             "hidden": torch.empty((cfg.n_layers + 2, T, cfg.hidden), dtype=torch.float32, device=dev) if hidden else None,
             "logits": torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev) if logits else None,
             "argmax": torch.empty((T,), dtype=torch.int32, device=dev) if argmax else None,
+            "margin": torch.empty((T,), dtype=torch.float32, device=dev) if argmax and margin else None,
         }
         ids_ptr = _ptr(ids) if on_dev else ids.ctypes.data
         _check(fk_forward(self.handle, ids_ptr, 1 if on_dev else 0, B, S, _ptr(self._ws), self._ws.numel(),
-                          _ptr(out["hidden"]), _ptr(out["logits"]), _ptr(out["argmax"]), _stream_ptr(stream)),
+                          _ptr(out["hidden"]), _ptr(out["logits"]), _ptr(out["argmax"]), _ptr(out["margin"]),
+                          _stream_ptr(stream)),
                "fk_forward")
+        return out
+
+    def rope(self, layer: int, qkv, batch: int, seq: int, pos0: int, kcache, vcache, stream=None):
+        """fk_op_rope: [QK-norm and] RoPE of layer `layer` on qkv rows in
+        place; k and transposed v written into the caches."""
+        cap = kcache.shape[2]
+        _check(load().fk_op_rope(self.handle, layer, _ptr(qkv), batch, seq, pos0, _ptr(kcache), _ptr(vcache), cap,
+                                 _stream_ptr(stream)), "fk_op_rope")
+
+    def head_argmax(self, u, margin: bool = True, stream=None) -> dict:
+        """fk_op_head_argmax: logits (after the softcap), argmax and top-2
+        margin of final-norm rows u [rows, hidden] (bf16)."""
+        import torch
+        rows = u.shape[0]
+        dev = u.device
+        out = {"logits": torch.empty((rows, self.cfg.vocab), dtype=torch.float32, device=dev),
+               "argmax": torch.empty((rows,), dtype=torch.int32, device=dev),
+               "margin": torch.empty((rows,), dtype=torch.float32, device=dev) if margin else None}
+        _check(load().fk_op_head_argmax(self.handle, _ptr(u), rows, _ptr(out["logits"]), _ptr(out["argmax"]),
+                                        _ptr(out["margin"]), _stream_ptr(stream)), "fk_op_head_argmax")
         return out
 
     def session(self, batch: int, max_seq: int, max_chunk: int | None = None) -> "Session":
@@ -343,7 +385,7 @@ class Session:
         except Exception:
             pass
 
-    def prefill(self, ids, logits=None, next_ids=None, stream=None):
+    def prefill(self, ids, logits=None, next_ids=None, margin=None, stream=None):
         import numpy as np
         import torch
         on_dev = isinstance(ids, torch.Tensor) and ids.is_cuda
@@ -352,11 +394,11 @@ class Session:
         S = ids.shape[1]
         ids_ptr = _ptr(ids) if on_dev else ids.ctypes.data
         _check(fk_session_prefill(self.handle, ids_ptr, 1 if on_dev else 0, S, _ptr(logits), _ptr(next_ids),
-                                  _stream_ptr(stream)), "fk_session_prefill")
+                                  _ptr(margin), _stream_ptr(stream)), "fk_session_prefill")
 
-    def decode(self, ids=None, logits=None, next_ids=None, stream=None):
-        _check(fk_decode_step(self.handle, _ptr(ids), _ptr(logits), _ptr(next_ids), _stream_ptr(stream)),
-               "fk_decode_step")
+    def decode(self, ids=None, logits=None, next_ids=None, margin=None, stream=None):
+        _check(fk_decode_step(self.handle, _ptr(ids), _ptr(logits), _ptr(next_ids), _ptr(margin),
+                              _stream_ptr(stream)), "fk_decode_step")
 
     def reset(self):
         _check(load().fk_session_reset(self.handle), "fk_session_reset")

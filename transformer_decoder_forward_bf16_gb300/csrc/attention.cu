@@ -2,14 +2,6 @@
 // Thm 1: causal multi-head/GQA attention; Thm 2 and "pegainfer #878":
 // sliding-window local layers).
 //
-// Prefill (used where the tcgen05 kernel of attention_tc.cu does not apply:
-// row strides or caches without the 16-byte / 64-position alignment its TMA
-// tiles need): flash-style, one CTA per (64 queries, head, sequence), 4 warps
-// x 16 query rows, 64-key blocks double-buffered in shared memory with
-// cp.async, QKᵀ and PV on mma.sync m16n8k16 (bf16, fp32 accumulate), online
-// softmax in fp32 (exp2 domain), P rounded to bf16 for the PV product. Only
-// the key blocks inside the causal (and window) range are visited.
-//
 // Decode: split-KV over a thread-block cluster. The CTAs of one cluster share
 // one (sequence, kv head) and split its key range into equal runs of 64-key
 // tiles streamed by TMA; each scores all query heads of the GQA group against
@@ -19,7 +11,6 @@
 // adding the partials in rank order, so the result does not depend on
 // scheduling and no partial result leaves the chip.
 #include <algorithm>
-#include <mutex>
 
 #include "fk_common.cuh"
 #include "fk_internal.h"
@@ -31,23 +22,8 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-FK_DEVICE void cp_async16(void* smem_dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-FK_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-FK_DEVICE void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 FK_DEVICE void ldsm_x4(uint32_t* r, const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-FK_DEVICE void ldsm_x4_t(uint32_t* r, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_u32(p)));
 }
@@ -58,186 +34,25 @@ FK_DEVICE void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+FK_DEVICE void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// both operands bf16, or both IEEE f16
+FK_DEVICE void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1, int f16) {
+  if (f16)
+    mma_f16_16816(d, a, b0, b1);
+  else
+    mma_bf16_16816(d, a, b0, b1);
+}
 
 // element (r, c) of a [rows][COLS] bf16 tile, 16-byte chunks XOR-swizzled by row
 template <int COLS>
 FK_DEVICE int swz(int r, int c) {
   return r * COLS + ((((c >> 3) ^ (r & 7))) << 3) + (c & 7);
-}
-
-constexpr int BQ = 64, BKV = 64;
-
-template <int HD>
-__global__ void __launch_bounds__(128) attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, int ldq,
-                                                           const __nv_bfloat16* __restrict__ kc,
-                                                           const __nv_bfloat16* __restrict__ vc, int cap, int S,
-                                                           int pos0, int Hq, int Hkv, int window, float scale_log2,
-                                                           __nv_bfloat16* __restrict__ o) {
-  extern __shared__ uint4 smem_u4[];
-  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_u4);
-  __nv_bfloat16* sK = sQ + BQ * HD;
-  __nv_bfloat16* sV = sK + 2 * BKV * HD;
-  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int g = h / (Hq / Hkv);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kv_len = pos0 + S;
-  const int q_lo = qb * BQ;
-  const int q_hi = min(S, q_lo + BQ) - 1;
-  const int qp_lo = pos0 + q_lo, qp_hi = pos0 + q_hi;
-  const int k_lo = window > 0 ? max(0, qp_lo - window + 1) : 0;
-  const int kb_lo = k_lo / BKV, kb_hi = qp_hi / BKV;
-  const size_t head_off = ((size_t)b * Hkv + g) * cap * HD;
-  const __nv_bfloat16* kbase = kc + head_off;
-  const __nv_bfloat16* vbase = vc + head_off;  // V^T: [HD][cap]
-  constexpr int CPR = HD / 8;  // 16-byte chunks per K row
-  constexpr int CPV = BKV / 8;  // 16-byte chunks per V^T row of a tile
-
-  for (int i = tid; i < BQ * CPR; i += 128) {
-    const int r = i / CPR, cc = i % CPR;
-    const int qi = q_lo + r;
-    const __nv_bfloat16* src = q + (size_t)(b * S + min(qi, S - 1)) * ldq + (size_t)h * HD + cc * 8;
-    cp_async16(sQ + swz<HD>(r, cc * 8), src, qi < S ? 16 : 0);
-  }
-  auto load_kv = [&](int kb, int buf) {
-    __nv_bfloat16* dk = sK + buf * BKV * HD;
-    __nv_bfloat16* dv = sV + buf * BKV * HD;
-    for (int i = tid; i < BKV * CPR; i += 128) {
-      const int r = i / CPR, cc = i % CPR;
-      const int kp = kb * BKV + r;
-      const int ok = kp < kv_len ? 16 : 0;
-      cp_async16(dk + swz<HD>(r, cc * 8), kbase + (size_t)min(kp, kv_len - 1) * HD + cc * 8, ok);
-    }
-    // V^T rows: keys [kb*BKV, kb*BKV + BKV) are inside the cache (cap is a
-    // multiple of 64); keys past kv_len hold finite values and get p = 0
-    for (int i = tid; i < HD * CPV; i += 128) {
-      const int d = i / CPV, cc = i % CPV;
-      cp_async16(dv + swz<BKV>(d, cc * 8), vbase + (size_t)d * cap + kb * BKV + cc * 8, 16);
-    }
-  };
-  load_kv(kb_lo, 0);
-  cp_async_commit();
-
-  float oacc[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int qr0 = qp_lo + warp * 16 + (lane >> 2);  // positions of this thread's two rows
-  const int qr1 = qr0 + 8;
-  const int mat = lane >> 3, mr = lane & 7;
-
-  for (int kb = kb_lo; kb <= kb_hi; ++kb) {
-    const int buf = (kb - kb_lo) & 1;
-    if (kb < kb_hi) {
-      load_kv(kb + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const __nv_bfloat16* tK = sK + buf * BKV * HD;
-    const __nv_bfloat16* tV = sV + buf * BKV * HD;
-
-    float s[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int k0 = 0; k0 < HD; k0 += 16) {
-      uint32_t a[4];
-      ldsm_x4(a, sQ + swz<HD>(warp * 16 + mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t bb[4];
-        ldsm_x4(bb, tK + swz<HD>(np * 16 + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
-        mma_bf16_16816(s[2 * np], a, bb[0], bb[1]);
-        mma_bf16_16816(s[2 * np + 1], a, bb[2], bb[3]);
-      }
-    }
-    // mask (causal, window, cache end) and move to the exp2 domain
-    const int key0 = kb * BKV + 2 * (lane & 3);
-    const bool edge = (kb * BKV + BKV - 1 > qp_lo + warp * 16) || (kb * BKV + BKV > kv_len) ||
-                      (window > 0 && qp_hi - kb * BKV >= window);
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = s[nt][e] * scale_log2;
-        if (edge) {
-          const int key = key0 + nt * 8 + (e & 1);
-          const int qp = e < 2 ? qr0 : qr1;
-          const bool ok = key <= qp && key < kv_len && (window == 0 || qp - key < window);
-          v = ok ? v : -INFINITY;
-        }
-        s[nt][e] = v;
-      }
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - base0);
-      s[nt][1] = exp2f(s[nt][1] - base0);
-      s[nt][2] = exp2f(s[nt][2] - base1);
-      s[nt][3] = exp2f(s[nt][3] - base1);
-      rs0 += s[nt][0] + s[nt][1];
-      rs1 += s[nt][2] + s[nt][3];
-    }
-    l0 = l0 * corr0 + rs0;
-    l1 = l1 * corr1 + rs1;
-#pragma unroll
-    for (int i = 0; i < HD / 8; ++i) {
-      oacc[i][0] *= corr0;
-      oacc[i][1] *= corr0;
-      oacc[i][2] *= corr1;
-      oacc[i][3] *= corr1;
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      uint32_t a[4];
-      a[0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
-      a[1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
-      a[2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
-      a[3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < HD / 16; ++dp) {
-        uint32_t bb[4];
-        ldsm_x4(bb, tV + swz<BKV>(dp * 16 + mr + (mat >> 1) * 8, ks * 16 + (mat & 1) * 8));
-        mma_bf16_16816(oacc[2 * dp], a, bb[0], bb[1]);
-        mma_bf16_16816(oacc[2 * dp + 1], a, bb[2], bb[3]);
-      }
-    }
-    __syncthreads();
-  }
-
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  const int qi0 = q_lo + warp * 16 + (lane >> 2), qi1 = qi0 + 8;
-  const size_t ldo = (size_t)Hq * HD;
-#pragma unroll
-  for (int dt = 0; dt < HD / 8; ++dt) {
-    const int col = h * HD + dt * 8 + 2 * (lane & 3);
-    if (qi0 < S)
-      *reinterpret_cast<uint32_t*>(o + (size_t)(b * S + qi0) * ldo + col) =
-          pack_bf16x2(oacc[dt][0] * inv0, oacc[dt][1] * inv0);
-    if (qi1 < S)
-      *reinterpret_cast<uint32_t*>(o + (size_t)(b * S + qi1) * ldo + col) =
-          pack_bf16x2(oacc[dt][2] * inv1, oacc[dt][3] * inv1);
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -286,13 +101,13 @@ FK_DEVICE int kswz(int r, int c) {
 // the new key and value into the caches and attends over them; otherwise q
 // holds the query heads with RoPE applied and the caches are complete.
 struct DecArgs {
-  const __nv_bfloat16* q;
+  const uint16_t* q;  // 16-bit: bf16 or IEEE f16 (io_f16)
   int ldq;
   int cap, ctx_host;
   const int* d_ctx;  // non-null: ctx = *d_ctx + 1
   int Hq, Hkv, window;
   float scale_log2;
-  __nv_bfloat16* o;
+  uint16_t* o;  // bf16 or f16 (out_f16)
   unsigned* dev_err;  // optional device error word (pipeline timeouts)
   // fused RoPE
   const float2* rope;  // [positions][HD/2] (cos, sin) of frequency j
@@ -300,22 +115,24 @@ struct DecArgs {
   const __nv_bfloat16* q_norm;
   const __nv_bfloat16* k_norm;
   float eps;
-  __nv_bfloat16* kc_w;  // the caches, written at position ctx-1
-  __nv_bfloat16* vc_w;
+  uint16_t* kc_w;  // the caches, written at position ctx-1
+  uint16_t* vc_w;
+  int io_f16;   // q, k, v, the caches and the probabilities are IEEE f16 (else bf16)
+  int out_f16;  // the output is stored as f16 (else bf16)
 };
 
 // [QK-norm and] RoPE of one head held by a warp: lane owns elements
 // e0..e0+C-1 of each half (pairs (j, j+HD/2)); cs: this lane's (cos, sin).
 template <int HD>
-FK_DEVICE void rope_head(const __nv_bfloat16* src, const DecArgs& a, const __nv_bfloat16* nw, const float2* cs,
+FK_DEVICE void rope_head(const uint16_t* src, const DecArgs& a, const __nv_bfloat16* nw, const float2* cs,
                          int lane, float* olo, float* ohi) {
   constexpr int C = HD / 64, HALF = HD / 2;
   const int e0 = lane * C;
   float lo[C], hi[C];
 #pragma unroll
   for (int i = 0; i < C; ++i) {
-    lo[i] = __bfloat162float(src[e0 + i]);
-    hi[i] = __bfloat162float(src[HALF + e0 + i]);
+    lo[i] = load_16(src + e0 + i, a.io_f16);
+    hi[i] = load_16(src + HALF + e0 + i, a.io_f16);
   }
   if (a.qk_norm) {
     float ss = 0.f;
@@ -344,12 +161,12 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
   constexpr int NC = HD / 64, HALF = HD / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint16_t* sQ = reinterpret_cast<uint16_t*>(smem);
   uint8_t* ring = smem + C::RING_OFF;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + C::NST;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NST);
-  __shared__ __align__(16) __nv_bfloat16 sNew[2][HD];  // fused RoPE: the new key and value
+  __shared__ __align__(16) uint16_t sNew[2][HD];  // fused RoPE: the new key and value
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int n_splits = gridDim.x;  // = the cluster size: blockIdx.x is the rank
   const int Hq = a.Hq, Hkv = a.Hkv, cap = a.cap, window = a.window;
@@ -429,7 +246,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
 #pragma unroll
       for (int i = 0; i < CC; ++i) cs[i] = a.rope[(size_t)qpos * HALF + lane * CC + i];
       pdl_wait();
-      const __nv_bfloat16* row = a.q + (size_t)b * a.ldq;
+      const uint16_t* row = a.q + (size_t)b * a.ldq;
       for (int r = warp; r < 16; r += kDecConsumers / 32) {
         float olo[NC], ohi[NC];
         if (r < group) {
@@ -440,8 +257,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         }
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
-          sQ[swz<HD>(r, lane * NC + i)] = __float2bfloat16_rn(olo[i]);
-          sQ[swz<HD>(r, HALF + lane * NC + i)] = __float2bfloat16_rn(ohi[i]);
+          sQ[swz<HD>(r, lane * NC + i)] = bits_16(olo[i], a.io_f16);
+          sQ[swz<HD>(r, HALF + lane * NC + i)] = bits_16(ohi[i], a.io_f16);
         }
       }
       if (warp == 0) {
@@ -449,17 +266,17 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         rope_head<HD>(row + (size_t)(Hq + g) * HD, a, a.k_norm, cs, lane, olo, ohi);
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
-          sNew[0][lane * NC + i] = __float2bfloat16_rn(olo[i]);
-          sNew[0][HALF + lane * NC + i] = __float2bfloat16_rn(ohi[i]);
+          sNew[0][lane * NC + i] = bits_16(olo[i], a.io_f16);
+          sNew[0][HALF + lane * NC + i] = bits_16(ohi[i], a.io_f16);
         }
       } else if (warp == 1) {
-        const __nv_bfloat16* vs = row + (size_t)(Hq + Hkv + g) * HD;
+        const uint16_t* vs = row + (size_t)(Hq + Hkv + g) * HD;
         for (int d = lane; d < HD; d += 32) sNew[1][d] = vs[d];
       }
       consumers_sync();
       if (t_new >= 0 && t_new < ntiles) {  // the one CTA whose tiles hold the new token stores it
-        __nv_bfloat16* kw = a.kc_w + ((size_t)head_row * cap + qpos) * HD;
-        __nv_bfloat16* vw = a.vc_w + (size_t)head_row * HD * cap + qpos;
+        uint16_t* kw = a.kc_w + ((size_t)head_row * cap + qpos) * HD;
+        uint16_t* vw = a.vc_w + (size_t)head_row * HD * cap + qpos;
         for (int d = tid; d < HD; d += kDecConsumers) {
           kw[d] = sNew[0][d];
           vw[(size_t)d * cap] = sNew[1][d];
@@ -481,8 +298,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % C::NST;
       if (!mbar_wait(&full[stage], (t / C::NST) & 1, abort_flag, a.dev_err)) break;
-      __nv_bfloat16* tK = reinterpret_cast<__nv_bfloat16*>(ring + stage * C::STAGE_BYTES);
-      __nv_bfloat16* tV = tK + C::TILE_ELEMS;
+      uint16_t* tK = reinterpret_cast<uint16_t*>(ring + stage * C::STAGE_BYTES);
+      uint16_t* tV = tK + C::TILE_ELEMS;
       const bool patch = ROPE && t == t_new && (qpos - (t0 + t * kDecTile)) / 16 == warp;
       if (patch) {  // the cached copy of the new token is stale: this warp's key row
         const int r = qpos - (t0 + t * kDecTile);
@@ -500,8 +317,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         uint32_t qa[4], bb[4];
         ldsm_x4(qa, sQ + swz<HD>(mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
         ldsm_x4(bb, tK + kswz<HD>(kr + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
-        mma_bf16_16816(s[0], qa, bb[0], bb[1]);
-        mma_bf16_16816(s[1], qa, bb[2], bb[3]);
+        mma_16816(s[0], qa, bb[0], bb[1], a.io_f16);
+        mma_16816(s[1], qa, bb[2], bb[3], a.io_f16);
       }
       const int key0 = t0 + t * kDecTile + kr + 2 * (lane & 3);
       float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -539,10 +356,10 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
       l0 = l0 * corr0 + rs0;
       l1 = l1 * corr1 + rs1;
       uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-      pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-      pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-      pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+      pa[0] = pack_16x2(s[0][0], s[0][1], a.io_f16);
+      pa[1] = pack_16x2(s[0][2], s[0][3], a.io_f16);
+      pa[2] = pack_16x2(s[1][0], s[1][1], a.io_f16);
+      pa[3] = pack_16x2(s[1][2], s[1][3], a.io_f16);
 #pragma unroll
       for (int dp = 0; dp < HD / 16; ++dp) {
         oacc[2 * dp][0] *= corr0;
@@ -555,8 +372,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         oacc[2 * dp + 1][3] *= corr1;
         uint32_t bb[4];
         ldsm_x4(bb, tV + swz<kDecTile>(dp * 16 + mr + (mat >> 1) * 8, kr + (mat & 1) * 8));
-        mma_bf16_16816(oacc[2 * dp], pa, bb[0], bb[1]);
-        mma_bf16_16816(oacc[2 * dp + 1], pa, bb[2], bb[3]);
+        mma_16816(oacc[2 * dp], pa, bb[0], bb[1], a.io_f16);
+        mma_16816(oacc[2 * dp + 1], pa, bb[2], bb[3], a.io_f16);
       }
       if (patch) fence_proxy_async_smem();  // generic writes before the slot is refilled by TMA
       __syncwarp();
@@ -650,42 +467,12 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         acc += v[c] * f;
       }
     }
-    a.o[((size_t)b * Hq + g * group + r) * HD + (i - r * HD)] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+    store_16(a.o + ((size_t)b * Hq + g * group + r) * HD + (i - r * HD), L > 0.f ? acc / L : 0.f, a.out_f16);
   }
   cluster_sync();  // no CTA leaves while another may still read its partial
 }
 
-template <int HD>
-cudaError_t prefill_hd(const void* q, int ldq, const void* kc, const void* vc, int cap, int B, int S, int pos0, int Hq,
-                       int Hkv, int window, float scale, void* o, cudaStream_t st) {
-  constexpr int smem = (BQ + 4 * BKV) * HD * 2;
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(attn_prefill_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  });
-  if (err != cudaSuccess) return err;
-  dim3 grid((S + BQ - 1) / BQ, Hq, B);
-  attn_prefill_kernel<HD><<<grid, 128, smem, st>>>(
-      static_cast<const __nv_bfloat16*>(q), ldq, static_cast<const __nv_bfloat16*>(kc),
-      static_cast<const __nv_bfloat16*>(vc), cap, S, pos0, Hq, Hkv, window, scale * kLog2e,
-      static_cast<__nv_bfloat16*>(o));
-  return cudaGetLastError();
-}
-
 }  // namespace
-
-cudaError_t launch_attention_prefill(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
-                                     int S, int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
-                                     cudaStream_t st) {
-  if (B == 0 || S == 0) return cudaSuccess;
-  switch (hd) {
-    case 64: return prefill_hd<64>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, st);
-    case 128: return prefill_hd<128>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, st);
-    case 256: return prefill_hd<256>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, st);
-  }
-  return cudaErrorInvalidValue;
-}
 
 // Largest cluster of decode CTAs the GPU co-schedules for this head_dim
 // (a cluster of 16 is beyond the portable size and is allowed explicitly).
@@ -702,13 +489,14 @@ cudaError_t decode_attrs() {
 template <int HD>
 int decode_max_cluster(cudaError_t* err) {
   using C = DecCfg<HD>;
-  static std::once_flag once;
-  static cudaError_t e0 = cudaSuccess;
-  static int n = 1;
-  std::call_once(once, [] {
-    e0 = decode_attrs<HD, false>();
+  static DeviceOnce once;
+  static int n[kMaxDevices];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  *err = once.run([dev] {
+    cudaError_t e0 = decode_attrs<HD, false>();
     if (e0 == cudaSuccess) e0 = decode_attrs<HD, true>();
-    if (e0 != cudaSuccess) return;
+    if (e0 != cudaSuccess) return e0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kMaxCluster, 1, 1);
     cfg.blockDim = dim3(kDecThreads, 1, 1);
@@ -720,10 +508,10 @@ int decode_max_cluster(cudaError_t* err) {
       cudaGetLastError();
       c = c2 = 8;  // the portable size
     }
-    n = std::min(std::min(c, c2), kMaxCluster);
+    n[dev] = std::min(std::min(c, c2), kMaxCluster);
+    return cudaSuccess;
   });
-  *err = e0;
-  return n;
+  return *err == cudaSuccess ? n[dev] : 1;
 }
 
 template <int HD>
@@ -788,9 +576,11 @@ cudaError_t decode_dispatch(const void* kcache, const void* vcache, const DecArg
 
 cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B,
                                     int ctx, const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
-                                    int n_splits, void* o, cudaStream_t st) {
+                                    int n_splits, void* o, unsigned* dev_err, cudaStream_t st, int io_f16,
+                                    int out_f16) {
   DecArgs a = {};
-  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.dev_err = dev_err;
+  a.q = static_cast<const uint16_t*>(q);
   a.ldq = ldq;
   a.cap = cap;
   a.ctx_host = ctx;
@@ -799,27 +589,32 @@ cudaError_t launch_attention_decode(const void* q, int ldq, const void* kcache, 
   a.Hkv = Hkv;
   a.window = window;
   a.scale_log2 = scale * kLog2e;
-  a.o = static_cast<__nv_bfloat16*>(o);
+  a.o = static_cast<uint16_t*>(o);
+  a.io_f16 = io_f16;
+  a.out_f16 = out_f16;
   return decode_dispatch(kcache, vcache, a, false, hd, B, n_splits, st);
 }
 
 cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcache, void* vcache, int cap, int B,
                                          const int* d_ctx, int Hq, int Hkv, int hd, int window, float scale,
                                          const float2* rope, int qk_norm, const void* q_norm, const void* k_norm,
-                                         float eps, int n_splits, void* o, unsigned* dev_err, cudaStream_t st) {
+                                         float eps, int n_splits, void* o, unsigned* dev_err, cudaStream_t st,
+                                         int io_f16, int out_f16) {
   if (!d_ctx) return cudaErrorInvalidValue;
   DecArgs a = {};
-  a.q = static_cast<const __nv_bfloat16*>(qkv);
+  a.q = static_cast<const uint16_t*>(qkv);
   a.ldq = ldqkv;
-  a.kc_w = static_cast<__nv_bfloat16*>(kcache);
-  a.vc_w = static_cast<__nv_bfloat16*>(vcache);
+  a.kc_w = static_cast<uint16_t*>(kcache);
+  a.vc_w = static_cast<uint16_t*>(vcache);
+  a.io_f16 = io_f16;
+  a.out_f16 = out_f16;
   a.cap = cap;
   a.d_ctx = d_ctx;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.window = window;
   a.scale_log2 = scale * kLog2e;
-  a.o = static_cast<__nv_bfloat16*>(o);
+  a.o = static_cast<uint16_t*>(o);
   a.dev_err = dev_err;
   a.rope = rope;
   a.qk_norm = qk_norm;
@@ -833,64 +628,30 @@ cudaError_t launch_attention_decode_rope(const void* qkv, int ldqkv, void* kcach
 // ---------------------------------------------------------------------------
 // op-level entry point: one decode-attention step over a caller's KV cache
 // ---------------------------------------------------------------------------
-
-namespace {
-// The scratch of fk_attention_decode is kept in the interface (a later kernel
-// may use it) but the cluster kernel writes nothing there.
-constexpr size_t kDecodeScratchBytes = 256;
-
-fk_status check_decode_args(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int hd, int cap,
-                            int ctx, int window, const void* out) {
-  using fk::fail;
-  if (!q || !kc || !vc || !out) return fail(FK_ERR_INVALID_ARG, "attention decode: null pointer");
-  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > 8)
-    return fail(FK_ERR_INVALID_ARG, "attention decode: need batch >= 1 and 1..8 query heads per kv head");
-  if (hd != 64 && hd != 128 && hd != 256) return fail(FK_ERR_INVALID_ARG, "attention decode: head_dim 64/128/256");
-  if (ctx < 1 || ctx > cap || window < 0 || cap % 64)
-    return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap, cap a multiple of 64");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15)
-    return fail(FK_ERR_INVALID_ARG, "attention decode: q and caches must be 16-byte aligned");
-  return FK_OK;
-}
-}  // namespace
-
-namespace fk {
-// shared by the scratch-taking and the allocation-free entry points: the
-// kernel keeps its split partials on chip, so neither needs device memory
-fk_status attention_decode_plan(int B, int Hkv, int hd, int ctx, int* splits) {
-  int sms = 0;
-  fk_status s = check_device(&sms);
-  if (s != FK_OK) return s;
-  *splits = decode_attention_splits(B, Hkv, hd, ctx, sms);
-  return FK_OK;
-}
-fk_status attention_decode_run(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int hd, int cap,
-                               int ctx, int window, int splits, void* out, cudaStream_t st) {
-  cudaError_t e = launch_attention_decode(q, Hq * hd, kc, vc, cap, B, ctx, nullptr, Hq, Hkv, hd, window,
-                                          1.0f / sqrtf((float)hd), splits, out, st);
-  if (e != cudaSuccess) return cuda_fail(e, "attention decode launch");
-  return FK_OK;
-}
-}  // namespace fk
-
-extern "C" size_t fk_attention_decode_scratch_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
-                                                    int32_t head_dim, int32_t ctx) {
-  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || ctx < 1) return 0;
-  return kDecodeScratchBytes;
-}
-
 extern "C" fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
                                          int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap,
-                                         int32_t ctx, int32_t window, void* d_scratch, size_t scratch_bytes,
-                                         void* d_out, void* stream) {
-  fk_status s = check_decode_args(d_q, d_kcache, d_vcache, batch, n_q_heads, n_kv_heads, head_dim, cap, ctx, window,
-                                  d_out);
+                                         int32_t ctx, int32_t window, void* d_out, void* stream) {
+  using fk::fail;
+  if (!d_q || !d_kcache || !d_vcache || !d_out) return fail(FK_ERR_INVALID_ARG, "attention decode: null pointer");
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > 8)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: need batch >= 1 and 1..8 query heads per kv head");
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: head_dim 64/128/256");
+  if (ctx < 1 || ctx > cap || window < 0 || cap % 64)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap, cap a multiple of 64");
+  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_kcache) |
+       reinterpret_cast<uintptr_t>(d_vcache) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+    return fail(FK_ERR_INVALID_ARG, "attention decode: buffers must be 16-byte aligned");
+  int sms = 0;
+  fk_status s = fk::check_device(&sms);
   if (s != FK_OK) return s;
-  if (!d_scratch || scratch_bytes < kDecodeScratchBytes)
-    return fk::fail(FK_ERR_WORKSPACE, "attention decode: scratch too small");
-  int splits = 1;
-  s = fk::attention_decode_plan(batch, n_kv_heads, head_dim, ctx, &splits);
+  unsigned* ctl = nullptr;
+  s = fk::op_control_block(&ctl);
   if (s != FK_OK) return s;
-  return fk::attention_decode_run(d_q, d_kcache, d_vcache, batch, n_q_heads, n_kv_heads, head_dim, cap, ctx, window,
-                                  splits, d_out, static_cast<cudaStream_t>(stream));
+  const int splits = fk::decode_attention_splits(batch, n_kv_heads, head_dim, ctx, sms);
+  cudaError_t e = fk::launch_attention_decode(d_q, n_q_heads * head_dim, d_kcache, d_vcache, cap, batch, ctx, nullptr,
+                                              n_q_heads, n_kv_heads, head_dim, window, 1.0f / sqrtf((float)head_dim),
+                                              splits, d_out, ctl, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fk::cuda_fail(e, "attention decode launch");
+  return FK_OK;
 }

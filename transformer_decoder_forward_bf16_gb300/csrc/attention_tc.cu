@@ -15,16 +15,16 @@
 //                               and Vᵀ_j from shared memory; O in TMEM.
 //   warps 2-5  softmax, one query row per thread (TMEM lane = row): one TMEM
 //              read of S_j, mask (causal, window, sequence end), running max
-//              in the exp2 domain, P = exp2(S - m) packed to bf16 and stored
+//              in the exp2 domain, P = exp2(S - m) packed to 16 bits and stored
 //              back into the same TMEM columns for the PV MMA. The running
 //              max is raised lazily (only when it grows by more than 2^8), and
 //              only then does a warp wait for the previous PV and rescale its
-//              rows of O (tcgen05.ld/st); P <= 2^8 keeps bf16 in range.
+//              rows of O (tcgen05.ld/st); P <= 2^8 keeps bf16 and f16 in range.
+// q, K, Vᵀ and P are bf16, or all IEEE f16 (io_f16); the output bf16 or f16.
 // Every mbarrier wait is bounded (FK_DEVERR_PIPE_TIMEOUT on expiry). Every
 // tcgen05.ld/st is executed by whole warps (they are warp-collective), so
 // per-row decisions that touch TMEM are taken warp-wide.
 #include <algorithm>
-#include <mutex>
 
 #include "fk_common.cuh"
 #include "fk_internal.h"
@@ -51,8 +51,6 @@ struct FaCfg {
   // S/P buffers [0, BKV) and [BKV, 2 BKV); O [2 BKV, 2 BKV + HD)
   static constexpr uint32_t TMEM_COLS = 2 * BKV + HD <= 256 ? 256 : 512;
   static constexpr uint32_t O_COL = 2 * BKV;
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV);
-  static constexpr uint32_t IDESC_O = idesc_bf16_f32(BQ, HD);
 };
 
 FK_DEVICE void tmem_st32(uint32_t taddr, const uint32_t* v) {
@@ -89,7 +87,7 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, int S, int pos0, int Hq, int Hkv, int cap, int window,
-                   float scale_log2, __nv_bfloat16* __restrict__ out, unsigned* dev_err) {
+                   float scale_log2, uint16_t* __restrict__ out, unsigned* dev_err, int io_f16, int out_f16) {
   using C = FaCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // the swizzled tiles need 1024-byte alignment
@@ -195,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
+      const uint32_t idesc_s = idesc_16b_f32(BQ, BKV, io_f16);  // S = Q K^T
+      const uint32_t idesc_o = idesc_16b_f32(BQ, HD, io_f16);   // O += P V
       bool ok = mbar_wait(q_full, 0, abort_flag, dev_err);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t ad = smem_desc_sw128(sQ + (k >> 2) * BQ * 128) + 2 * (k & 3);
           const uint64_t bd = smem_desc_sw128(sK + st * C::K_BYTES + (k >> 2) * BKV * 128) + 2 * (k & 3);
-          umma_bf16(d, ad, bd, C::IDESC_S, k > 0 ? 1u : 0u);
+          umma_bf16(d, ad, bd, idesc_s, k > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[st]);
         umma_commit(&k_empty[st]);
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k) {
           const uint64_t bd = smem_desc_sw128(sV + st * C::V_BYTES) + 2 * k;
-          umma_bf16_ts(tmem + C::O_COL, tmem + (uint32_t)st * BKV + 8 * k, bd, C::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + C::O_COL, tmem + (uint32_t)st * BKV + 8 * k, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&pv_done[st]);
         umma_commit(&v_empty[st]);
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float p1 = live ? fast_exp2(x[e + 1] - m_use) : 0.f;
         l0 += p0;
         l1 += p1;
-        pk[e >> 1] = pack_bf16x2(p0, p1);
+        pk[e >> 1] = pack_16x2(p0, p1, io_f16);
       }
       l += l0 + l1;
       tmem_st32(s_addr, pk);  // P_j over S_j: 32 columns of bf16 pairs
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const int qi = q_lo + r;
-    __nv_bfloat16* orow = out + ((size_t)b * S + qi) * ((size_t)Hq * HD) + (size_t)h * HD;
+    uint16_t* orow = out + ((size_t)b * S + qi) * ((size_t)Hq * HD) + (size_t)h * HD;
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) {
       float v[32];
@@ -333,8 +333,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int e = 0; e < 32; e += 8)
           *reinterpret_cast<uint4*>(orow + c * 32 + e) =
-              make_uint4(pack_bf16x2(v[e] * inv, v[e + 1] * inv), pack_bf16x2(v[e + 2] * inv, v[e + 3] * inv),
-                         pack_bf16x2(v[e + 4] * inv, v[e + 5] * inv), pack_bf16x2(v[e + 6] * inv, v[e + 7] * inv));
+              make_uint4(pack_16x2(v[e] * inv, v[e + 1] * inv, out_f16), pack_16x2(v[e + 2] * inv, v[e + 3] * inv, out_f16),
+                         pack_16x2(v[e + 4] * inv, v[e + 5] * inv, out_f16),
+                         pack_16x2(v[e + 6] * inv, v[e + 7] * inv, out_f16));
       }
     }
   }
@@ -349,13 +350,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int HD>
 fk_status launch_tc(const void* q, int ldq, const void* kc, const void* vc, int cap, int B, int S, int pos0, int Hq,
-                    int Hkv, int window, float scale, void* o, unsigned* dev_err, cudaStream_t st) {
+                    int Hkv, int window, float scale, void* o, unsigned* dev_err, cudaStream_t st, int io_f16,
+                    int out_f16) {
   using C = FaCfg<HD>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  });
+  static DeviceOnce once;
+  const cudaError_t attr = once.run(
+      [] { return cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
   if (attr != cudaSuccess) return cuda_fail(attr, "cudaFuncSetAttribute(attn_tc)");
   CUtensorMap tQ, tK, tV;
   fk_status s = make_tmap_bf16(&tQ, q, (int64_t)B * S, ldq, ldq, BQ);
@@ -364,8 +364,8 @@ fk_status launch_tc(const void* q, int ldq, const void* kc, const void* vc, int 
   if (s != FK_OK) return s;
   const int nqb = (S + BQ - 1) / BQ;
   attn_tc_kernel<HD><<<dim3(Hq * B, nqb), kThreads, C::SMEM, st>>>(tQ, tK, tV, S, pos0, Hq, Hkv, cap, window,
-                                                                   scale * kLog2e, static_cast<__nv_bfloat16*>(o),
-                                                                   dev_err);
+                                                                   scale * kLog2e, static_cast<uint16_t*>(o),
+                                                                   dev_err, io_f16, out_f16);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_tc_kernel launch");
   return FK_OK;
@@ -373,20 +373,20 @@ fk_status launch_tc(const void* q, int ldq, const void* kc, const void* vc, int 
 
 }  // namespace
 
-bool attention_prefill_tc_supported(int hd, int ldq, int cap) {
-  return (hd == 64 || hd == 128 || hd == 256) && ldq % 8 == 0 && cap % 64 == 0;
-}
-
 fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
                                int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
-                               unsigned* dev_err, cudaStream_t st) {
+                               unsigned* dev_err, cudaStream_t st, int io_f16, int out_f16) {
   if (B == 0 || S == 0) return FK_OK;
+  if (ldq % 8 || cap % 64) return fail(FK_ERR_INVALID_ARG, "tensor-core attention: ldq % 8 and cap % 64 must be 0");
   if (hd == 64)
-    return launch_tc<64>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st);
+    return launch_tc<64>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st, io_f16,
+                           out_f16);
   if (hd == 128)
-    return launch_tc<128>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st);
+    return launch_tc<128>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st, io_f16,
+                           out_f16);
   if (hd == 256)
-    return launch_tc<256>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st);
+    return launch_tc<256>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st, io_f16,
+                           out_f16);
   return fail(FK_ERR_INVALID_ARG, "tensor-core attention: head_dim 64, 128 or 256");
 }
 
@@ -408,14 +408,10 @@ extern "C" fk_status fk_attention_prefill(const void* d_q, const void* d_kcache,
     return fail(FK_ERR_INVALID_ARG, "attention prefill: buffers must be 16-byte aligned");
   fk_status s = check_device(nullptr);
   if (s != FK_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* ctl = nullptr;
+  s = op_control_block(&ctl);
+  if (s != FK_OK) return s;
   const int ldq = n_q_heads * head_dim;
-  const float scale = 1.0f / sqrtf((float)head_dim);
-  if (attention_prefill_tc_supported(head_dim, ldq, cap))
-    return attention_prefill_tc(d_q, ldq, d_kcache, d_vcache, cap, batch, seq, pos0, n_q_heads, n_kv_heads, head_dim,
-                                window, scale, d_out, nullptr, st);
-  cudaError_t e = launch_attention_prefill(d_q, ldq, d_kcache, d_vcache, cap, batch, seq, pos0, n_q_heads, n_kv_heads,
-                                           head_dim, window, scale, d_out, st);
-  if (e != cudaSuccess) return cuda_fail(e, "attention prefill launch");
-  return FK_OK;
+  return attention_prefill_tc(d_q, ldq, d_kcache, d_vcache, cap, batch, seq, pos0, n_q_heads, n_kv_heads, head_dim,
+                              window, 1.0f / sqrtf((float)head_dim), d_out, ctl, static_cast<cudaStream_t>(stream));
 }

@@ -1,12 +1,14 @@
 // Bandwidth-bound kernels of the forward pass: embedding gather (+scale) with
 // the first RMSNorm fused, RMSNorm, the sandwich post-norm + residual +
 // next-norm fusion, QK-norm + RoPE + K-cache write, the V-cache transpose of
-// a prefill chunk, and the per-row argmax.
+// a prefill chunk, and the per-row argmax with its top-2 margin.
 //
 // Row kernels read with 16-byte vector loads and reduce with warp shuffles
 // (one warp per row, or one block per row with the row held in registers);
 // the V transpose stages its tile in shared memory so that both sides move
 // 128-byte runs.
+#include <algorithm>
+
 #include "fk_common.cuh"
 #include "fk_ops.h"
 
@@ -26,9 +28,10 @@ FK_DEVICE void load8_bf16(const __nv_bfloat16* p, float* v) {
   v[6] = bf16_lo(u.w);
   v[7] = bf16_hi(u.w);
 }
-FK_DEVICE void store8_bf16(__nv_bfloat16* p, const float* v) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+// 8 values to 16 bytes of bf16 (f16 == 0) or IEEE f16
+FK_DEVICE void store8_16(void* p, const float* v, int f16) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_16x2(v[0], v[1], f16), pack_16x2(v[2], v[3], f16),
+                                            pack_16x2(v[4], v[5], f16), pack_16x2(v[6], v[7], f16));
 }
 
 // ---------------------------------------------------------------------------
@@ -38,7 +41,7 @@ FK_DEVICE void store8_bf16(__nv_bfloat16* p, const float* v) {
 // ---------------------------------------------------------------------------
 __global__ void embed_norm_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ E, int T, int H,
                                   int V, float scale, const __nv_bfloat16* __restrict__ w, float eps,
-                                  float* __restrict__ x, __nv_bfloat16* __restrict__ u, unsigned* dev_err) {
+                                  float* __restrict__ x, uint16_t* __restrict__ u, unsigned* dev_err, int u_f16) {
   pdl_trigger();
   pdl_wait();
   const int warps = blockDim.x >> 5;
@@ -66,14 +69,14 @@ __global__ void embed_norm_kernel(const int32_t* __restrict__ ids, const __nv_bf
   }
   ss = warp_sum(ss);
   const float r = rsqrtf(ss / H + eps);
-  __nv_bfloat16* ur = u + (size_t)t * H;
+  uint16_t* ur = u + (size_t)t * H;
   for (int c = lane * 8; c < H; c += 256) {
     float v[8], wv[8];
     load8_bf16(e + c, v);
     load8_bf16(w + c, wv);
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = v[j] * scale * r * wv[j];
-    store8_bf16(ur + c, v);
+    store8_16(ur + c, v, u_f16);
   }
 }
 
@@ -81,7 +84,7 @@ __global__ void embed_norm_kernel(const int32_t* __restrict__ ids, const __nv_bf
 // u[t] = RMSNorm(x[t]) * w  ("N7", Thm 1: RMSNorm), fp32 in, bf16 out
 // ---------------------------------------------------------------------------
 __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, int T, int H, const __nv_bfloat16* __restrict__ w,
-                               float eps, __nv_bfloat16* __restrict__ u, int ldu) {
+                               float eps, uint16_t* __restrict__ u, int ldu, int u_f16) {
   pdl_trigger();
   pdl_wait();
   const int warps = blockDim.x >> 5;
@@ -96,13 +99,13 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, int T, int 
   }
   ss = warp_sum(ss);
   const float r = rsqrtf(ss / H + eps);
-  __nv_bfloat16* ur = u + (size_t)t * ldu;
+  uint16_t* ur = u + (size_t)t * ldu;
   for (int c = lane * 4; c < H; c += 128) {
     const float4 v = *reinterpret_cast<const float4*>(xr + c);
     const uint2 wp = *reinterpret_cast<const uint2*>(w + c);
     *reinterpret_cast<uint2*>(ur + c) =
-        make_uint2(pack_bf16x2(v.x * r * bf16_lo(wp.x), v.y * r * bf16_hi(wp.x)),
-                   pack_bf16x2(v.z * r * bf16_lo(wp.y), v.w * r * bf16_hi(wp.y)));
+        make_uint2(pack_16x2(v.x * r * bf16_lo(wp.x), v.y * r * bf16_hi(wp.x), u_f16),
+                   pack_16x2(v.z * r * bf16_lo(wp.y), v.w * r * bf16_hi(wp.y), u_f16));
   }
 }
 
@@ -112,7 +115,7 @@ constexpr int kRowsThreads = 256;
 constexpr int kRowsMaxVec = 8;  // float4 per thread: H <= 8192
 __global__ void __launch_bounds__(kRowsThreads) rmsnorm_rows_kernel(const float* __restrict__ x, int ldx, int H,
                                                                     const __nv_bfloat16* __restrict__ w, float eps,
-                                                                    __nv_bfloat16* __restrict__ u, int ldu) {
+                                                                    uint16_t* __restrict__ u, int ldu, int u_f16) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[kRowsThreads / 32];
@@ -133,15 +136,15 @@ __global__ void __launch_bounds__(kRowsThreads) rmsnorm_rows_kernel(const float*
 #pragma unroll
   for (int i = 0; i < kRowsThreads / 32; ++i) tot += red[i];
   const float r = rsqrtf(tot / H + eps);
-  __nv_bfloat16* ur = u + (size_t)t * ldu;
+  uint16_t* ur = u + (size_t)t * ldu;
 #pragma unroll
   for (int i = 0; i < kRowsMaxVec; ++i) {
     const int c = (i * kRowsThreads + threadIdx.x) * 4;
     if (c < H) {
       const uint2 wp = *reinterpret_cast<const uint2*>(w + c);
       *reinterpret_cast<uint2*>(ur + c) =
-          make_uint2(pack_bf16x2(v[i].x * r * bf16_lo(wp.x), v[i].y * r * bf16_hi(wp.x)),
-                     pack_bf16x2(v[i].z * r * bf16_lo(wp.y), v[i].w * r * bf16_hi(wp.y)));
+          make_uint2(pack_16x2(v[i].x * r * bf16_lo(wp.x), v[i].y * r * bf16_hi(wp.x), u_f16),
+                     pack_16x2(v[i].z * r * bf16_lo(wp.y), v[i].w * r * bf16_hi(wp.y), u_f16));
     }
   }
 }
@@ -178,7 +181,7 @@ __global__ void rmsnorm_f32_kernel(const float* __restrict__ x, int T, int H, co
 __global__ void post_norm_residual_kernel(const float* __restrict__ a, const float* x_in, float* x_out, int T, int H,
                                           const __nv_bfloat16* __restrict__ w_post,
                                           const __nv_bfloat16* __restrict__ w_next, float eps,
-                                          __nv_bfloat16* __restrict__ u) {
+                                          uint16_t* __restrict__ u, int u_f16) {
   pdl_trigger();
   pdl_wait();
   const int warps = blockDim.x >> 5;
@@ -211,13 +214,13 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
   ss2 = warp_sum(ss2);
   const float r2 = rsqrtf(ss2 / H + eps);
   __syncwarp();
-  __nv_bfloat16* ur = u + (size_t)t * H;
+  uint16_t* ur = u + (size_t)t * H;
   for (int c = lane * 4; c < H; c += 128) {
     const float4 v = *reinterpret_cast<const float4*>(xo + c);
     const uint2 wp = *reinterpret_cast<const uint2*>(w_next + c);
     *reinterpret_cast<uint2*>(ur + c) =
-        make_uint2(pack_bf16x2(v.x * r2 * bf16_lo(wp.x), v.y * r2 * bf16_hi(wp.x)),
-                   pack_bf16x2(v.z * r2 * bf16_lo(wp.y), v.w * r2 * bf16_hi(wp.y)));
+        make_uint2(pack_16x2(v.x * r2 * bf16_lo(wp.x), v.y * r2 * bf16_hi(wp.x), u_f16),
+                   pack_16x2(v.z * r2 * bf16_lo(wp.y), v.w * r2 * bf16_hi(wp.y), u_f16));
   }
 }
 
@@ -231,10 +234,10 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
 // rope: float2 (cos, sin) table [positions][hd/2].
 // ---------------------------------------------------------------------------
 template <int C>
-__global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int pos0, int Hq,
+__global__ void rope_qkv_kernel(uint16_t* qkv, int ldqkv, int T, int S, int pos0, int Hq,
                                 int Hkv, const float2* __restrict__ rope, int qk_norm,
                                 const __nv_bfloat16* __restrict__ q_norm, const __nv_bfloat16* __restrict__ k_norm,
-                                float eps, __nv_bfloat16* kcache, __nv_bfloat16* vcache, int cap) {
+                                float eps, uint16_t* kcache, int cap, int f16) {
   pdl_trigger();
   pdl_wait();
   constexpr int HD = C * 64;
@@ -248,13 +251,13 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
   const int h = (int)(gw % nh);
   const int b = t / S, s = t % S;
   const int pos = pos0 + s;
-  __nv_bfloat16* row = qkv + (size_t)t * ldqkv + (size_t)h * HD;
+  uint16_t* row = qkv + (size_t)t * ldqkv + (size_t)h * HD;
   float lo[C], hi[C];
   const int e0 = lane * C;  // within each half of size 32*C = HALF
 #pragma unroll
   for (int i = 0; i < C; ++i) {
-    lo[i] = __bfloat162float(row[e0 + i]);
-    hi[i] = __bfloat162float(row[HALF + e0 + i]);
+    lo[i] = load_16(row + e0 + i, f16);
+    hi[i] = load_16(row + HALF + e0 + i, f16);
   }
   const bool is_q = h < Hq;
   if (qk_norm) {
@@ -278,7 +281,7 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
     olo[i] = lo[i] * c.x - hi[i] * c.y;
     ohi[i] = hi[i] * c.x + lo[i] * c.y;
   }
-  __nv_bfloat16* dst;
+  uint16_t* dst;
   if (is_q) {
     dst = row;
   } else {
@@ -287,8 +290,8 @@ __global__ void rope_qkv_kernel(__nv_bfloat16* qkv, int ldqkv, int T, int S, int
   }
 #pragma unroll
   for (int i = 0; i < C; ++i) {
-    dst[e0 + i] = __float2bfloat16_rn(olo[i]);
-    dst[HALF + e0 + i] = __float2bfloat16_rn(ohi[i]);
+    store_16(dst + e0 + i, olo[i], f16);
+    store_16(dst + HALF + e0 + i, ohi[i], f16);
   }
 }
 
@@ -346,126 +349,138 @@ __global__ void __launch_bounds__(256) v_cache_kernel(const __nv_bfloat16* __res
 }
 
 // ---------------------------------------------------------------------------
-// argmax per row over V fp32 values (lowest index wins ties).
-// One block of 256 threads per row.
+// argmax per row over V fp32 values (lowest index wins ties) and the top-2
+// margin: the row maximum minus the largest other value (0 on a tie), the
+// quantity that decides whether rounding noise can flip the argmax ("N7 ·
+// model/forward-parity", Thm 3: near-tie argmax flips).
+// Each thread keeps (best value, its index, runner-up value); two such states
+// merge into the better best, and the runner-up is the larger of the loser's
+// best and the winner's runner-up. One block of 256 threads per row.
 // ---------------------------------------------------------------------------
-FK_DEVICE void better(float& m, int& i, float m2, int i2) {
-  if (m2 > m || (m2 == m && i2 < i)) {
-    m = m2;
-    i = i2;
+struct Top2 {
+  float m;   // best value
+  int i;     // its index (lowest on ties)
+  float m2;  // largest value at any other index
+};
+
+FK_DEVICE bool wins(float m2, int i2, float m, int i) { return m2 > m || (m2 == m && i2 < i); }
+
+FK_DEVICE void top2_push(Top2& t, float v, int c) {
+  if (wins(v, c, t.m, t.i)) {
+    t.m2 = fmaxf(t.m2, t.m);
+    t.m = v;
+    t.i = c;
+  } else {
+    t.m2 = fmaxf(t.m2, v);
   }
 }
 
+FK_DEVICE void top2_merge(Top2& t, const Top2& o) {
+  if (wins(o.m, o.i, t.m, t.i)) {
+    t.m2 = fmaxf(t.m, o.m2);
+    t.m = o.m;
+    t.i = o.i;
+  } else {
+    t.m2 = fmaxf(t.m2, o.m);
+  }
+}
+
+FK_DEVICE Top2 top2_shfl(const Top2& t, int o) {
+  Top2 r;
+  r.m = __shfl_xor_sync(0xffffffffu, t.m, o);
+  r.i = __shfl_xor_sync(0xffffffffu, t.i, o);
+  r.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
+  return r;
+}
+
+// The block's threads reduce their states; thread 0 gets the result.
+FK_DEVICE Top2 top2_block(Top2 t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) top2_merge(t, top2_shfl(t, o));
+  __shared__ float sm[32], sm2[32];
+  __shared__ int si[32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm[w] = t.m;
+    si[w] = t.i;
+    sm2[w] = t.m2;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < (int)(blockDim.x >> 5); ++k) top2_merge(t, Top2{sm[k], si[k], sm2[k]});
+  }
+  return t;
+}
+
+FK_DEVICE void top2_scan(Top2& t, const float* row, int c0, int c1, bool vec) {
+  if (vec) {
+    for (int c = c0 + threadIdx.x * 4; c < c1; c += blockDim.x * 4) {
+      if (c + 4 <= c1) {
+        const float4 v = *reinterpret_cast<const float4*>(row + c);
+        top2_push(t, v.x, c);
+        top2_push(t, v.y, c + 1);
+        top2_push(t, v.z, c + 2);
+        top2_push(t, v.w, c + 3);
+      } else {
+        for (int e = c; e < c1; ++e) top2_push(t, row[e], e);
+      }
+    }
+  } else {
+    for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) top2_push(t, row[c], c);
+  }
+}
+
+FK_DEVICE void top2_store(const Top2& t, int r, int32_t* out, int32_t* out2, float* margin) {
+  const int best = t.i == 0x7fffffff ? 0 : t.i;
+  out[r] = best;
+  if (out2) out2[r] = best;
+  if (margin) margin[r] = t.m - t.m2;
+}
+
 __global__ void argmax_kernel(const float* __restrict__ z, int R, int V, int ldz, int32_t* __restrict__ out,
-                              int32_t* __restrict__ out2) {
+                              int32_t* __restrict__ out2, float* __restrict__ margin) {
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
   if (r >= R) return;
-  const float* row = z + (size_t)r * ldz;
-  float m = -INFINITY;
-  int idx = 0x7fffffff;
-  if ((V & 3) == 0 && (ldz & 3) == 0) {
-    for (int c = threadIdx.x * 4; c < V; c += blockDim.x * 4) {
-      const float4 v = *reinterpret_cast<const float4*>(row + c);
-      better(m, idx, v.x, c);
-      better(m, idx, v.y, c + 1);
-      better(m, idx, v.z, c + 2);
-      better(m, idx, v.w, c + 3);
-    }
-  } else {
-    for (int c = threadIdx.x; c < V; c += blockDim.x) better(m, idx, row[c], c);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-    better(m, idx, m2, i2);
-  }
-  __shared__ float sm[32];
-  __shared__ int si[32];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    sm[w] = m;
-    si[w] = idx;
-  }
-  __syncthreads();
-  if (w == 0) {
-    const int nw = blockDim.x >> 5;
-    m = lane < nw ? sm[lane] : -INFINITY;
-    idx = lane < nw ? si[lane] : 0x7fffffff;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-      better(m, idx, m2, i2);
-    }
-    if (lane == 0) {
-      const int best = idx == 0x7fffffff ? 0 : idx;
-      out[r] = best;
-      if (out2) out2[r] = best;
-    }
-  }
+  Top2 t{-INFINITY, 0x7fffffff, -INFINITY};
+  top2_scan(t, z + (size_t)r * ldz, 0, V, (V & 3) == 0 && (ldz & 3) == 0);
+  t = top2_block(t);
+  if (threadIdx.x == 0) top2_store(t, r, out, out2, margin);
 }
 
-// The same argmax for few rows split across blocks: block (s, r) scans one
-// column chunk of row r and records (max, index); the last block of a row
-// (arrival counter, reset after use) reduces the chunk results in chunk order
-// (lowest index on ties), so the result does not depend on scheduling.
+// The same for few rows split across blocks: block (s, r) scans one column
+// chunk of row r and records its state; the last block of a row (arrival
+// counter, reset after use) merges the chunk states in chunk order, so the
+// result does not depend on scheduling.
 constexpr int kArgmaxSplits = 32;
 __global__ void argmax_split_kernel(const float* __restrict__ z, int V, int ldz, int32_t* __restrict__ out,
-                                    int32_t* __restrict__ out2, float* part_m, int* part_i, unsigned* counters) {
+                                    int32_t* __restrict__ out2, float* __restrict__ margin, float* part_m,
+                                    int* part_i, float* part_m2, unsigned* counters) {
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.y, sp = blockIdx.x;
   const int chunk = ((V + kArgmaxSplits - 1) / kArgmaxSplits + 1023) / 1024 * 1024;
   const int c0 = sp * chunk, c1 = min(V, c0 + chunk);
-  const float* row = z + (size_t)r * ldz;
-  float m = -INFINITY;
-  int idx = 0x7fffffff;
-  for (int c = c0 + threadIdx.x * 4; c < c1; c += blockDim.x * 4) {
-    if (c + 4 <= c1) {
-      const float4 v = *reinterpret_cast<const float4*>(row + c);
-      better(m, idx, v.x, c);
-      better(m, idx, v.y, c + 1);
-      better(m, idx, v.z, c + 2);
-      better(m, idx, v.w, c + 3);
-    } else {
-      for (int e = c; e < c1; ++e) better(m, idx, row[e], e);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-    better(m, idx, m2, i2);
-  }
-  __shared__ float sm[32];
-  __shared__ int si[32];
+  Top2 t{-INFINITY, 0x7fffffff, -INFINITY};
+  top2_scan(t, z + (size_t)r * ldz, c0, c1, true);
+  t = top2_block(t);
   __shared__ int last;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    sm[w] = m;
-    si[w] = idx;
-  }
-  __syncthreads();
   if (threadIdx.x == 0) {
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) better(m, idx, sm[i], si[i]);
-    part_m[r * kArgmaxSplits + sp] = m;
-    part_i[r * kArgmaxSplits + sp] = idx;
+    part_m[r * kArgmaxSplits + sp] = t.m;
+    part_i[r * kArgmaxSplits + sp] = t.i;
+    part_m2[r * kArgmaxSplits + sp] = t.m2;
     __threadfence();
     last = atomicAdd(&counters[r], 1u) == kArgmaxSplits - 1;
   }
   __syncthreads();
   if (!last || threadIdx.x != 0) return;
   __threadfence();
-  float bm = -INFINITY;
-  int bi = 0x7fffffff;
+  Top2 b{-INFINITY, 0x7fffffff, -INFINITY};
   for (int i = 0; i < kArgmaxSplits; ++i)
-    better(bm, bi, __ldcg(part_m + r * kArgmaxSplits + i), __ldcg(part_i + r * kArgmaxSplits + i));
-  const int best = bi == 0x7fffffff ? 0 : bi;
-  out[r] = best;
-  if (out2) out2[r] = best;
+    top2_merge(b, Top2{__ldcg(part_m + r * kArgmaxSplits + i), __ldcg(part_i + r * kArgmaxSplits + i),
+                       __ldcg(part_m2 + r * kArgmaxSplits + i)});
+  top2_store(b, r, out, out2, margin);
   counters[r] = 0;
 }
 
@@ -477,6 +492,16 @@ __global__ void gather_last_rows_kernel(const __nv_bfloat16* src, int ld, int S,
   const __nv_bfloat16* s = src + ((size_t)b * S + S - 1) * ld;
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8)
     *reinterpret_cast<uint4*>(dst + (size_t)b * H + c) = *reinterpret_cast<const uint4*>(s + c);
+}
+
+// bf16 -> IEEE f16 copy (8 elements per 16-byte load), for the f16 copies of
+// the weights of GEMMs whose input activations are stored as f16
+__global__ void bf16_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n8) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 u = src[i];
+    dst[i] = make_uint4(pack_f16x2(bf16_lo(u.x), bf16_hi(u.x)), pack_f16x2(bf16_lo(u.y), bf16_hi(u.y)),
+                        pack_f16x2(bf16_lo(u.z), bf16_hi(u.z)), pack_f16x2(bf16_lo(u.w), bf16_hi(u.w)));
+  }
 }
 
 __global__ void set_int_kernel(int* p, int value) { *p = value; }
@@ -491,21 +516,21 @@ inline int row_blocks(long rows) { return (int)((rows + 7) / 8); }
 }  // namespace
 
 cudaError_t launch_embed_norm(const int32_t* ids, const void* E, int T, int H, int V, float scale, const void* w,
-                              float eps, float* x, void* u, unsigned* dev_err, cudaStream_t st) {
+                              float eps, float* x, void* u, unsigned* dev_err, cudaStream_t st, int u_f16) {
   if (T == 0) return cudaSuccess;
   return fk_launch(embed_norm_kernel, row_blocks(T), kRowThreads, 0, st, ids, static_cast<const __nv_bfloat16*>(E), T, H,
-                   V, scale, static_cast<const __nv_bfloat16*>(w), eps, x, static_cast<__nv_bfloat16*>(u), dev_err);
+                   V, scale, static_cast<const __nv_bfloat16*>(w), eps, x, static_cast<uint16_t*>(u), dev_err, u_f16);
 }
 
 cudaError_t launch_rmsnorm(const float* x, int ldx, int T, int H, const void* w, float eps, void* u, int ldu,
-                           cudaStream_t st) {
+                           cudaStream_t st, int u_f16) {
   if (T == 0) return cudaSuccess;
   if (H <= kRowsThreads * 4 * kRowsMaxVec) {
     return fk_launch(rmsnorm_rows_kernel, T, kRowsThreads, 0, st, x, ldx, H, static_cast<const __nv_bfloat16*>(w), eps,
-                     static_cast<__nv_bfloat16*>(u), ldu);
+                     static_cast<uint16_t*>(u), ldu, u_f16);
   }
   return fk_launch(rmsnorm_kernel, row_blocks(T), kRowThreads, 0, st, x, ldx, T, H, static_cast<const __nv_bfloat16*>(w),
-                   eps, static_cast<__nv_bfloat16*>(u), ldu);
+                   eps, static_cast<uint16_t*>(u), ldu, u_f16);
 }
 
 cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, float eps, float* y, cudaStream_t st) {
@@ -515,16 +540,17 @@ cudaError_t launch_rmsnorm_f32(const float* x, int T, int H, const void* w, floa
 }
 
 cudaError_t launch_post_norm_residual(const float* a, const float* x_in, float* x_out, int T, int H,
-                                      const void* w_post, const void* w_next, float eps, void* u, cudaStream_t st) {
+                                      const void* w_post, const void* w_next, float eps, void* u, cudaStream_t st,
+                                      int u_f16) {
   if (T == 0) return cudaSuccess;
   return fk_launch(post_norm_residual_kernel, row_blocks(T), kRowThreads, 0, st, a, x_in, x_out, T, H,
                    static_cast<const __nv_bfloat16*>(w_post), static_cast<const __nv_bfloat16*>(w_next), eps,
-                   static_cast<__nv_bfloat16*>(u));
+                   static_cast<uint16_t*>(u), u_f16);
 }
 
 cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, int Hq, int Hkv, int hd,
                             const float2* rope, int qk_norm, const void* q_norm, const void* k_norm, float eps,
-                            void* kcache, void* vcache, int cap, cudaStream_t st) {
+                            void* kcache, void* vcache, int cap, cudaStream_t st, int f16) {
   if (T == 0) return cudaSuccess;
   if (ldqkv % 8) return cudaErrorInvalidValue;  // rows 16-byte aligned
   {
@@ -539,21 +565,20 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, int Hq
   }
   const long warps = (long)T * (Hq + Hkv);
   const int blocks = (int)((warps + 7) / 8);
-  auto* q = static_cast<__nv_bfloat16*>(qkv);
+  auto* q = static_cast<uint16_t*>(qkv);
   auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
   auto* kn = static_cast<const __nv_bfloat16*>(k_norm);
-  auto* kc = static_cast<__nv_bfloat16*>(kcache);
-  auto* vc = static_cast<__nv_bfloat16*>(vcache);
+  auto* kc = static_cast<uint16_t*>(kcache);
   switch (hd) {
     case 64:
       return fk_launch(rope_qkv_kernel<1>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, Hq, Hkv, rope, qk_norm, qn,
-                       kn, eps, kc, vc, cap);
+                       kn, eps, kc, cap, f16);
     case 128:
       return fk_launch(rope_qkv_kernel<2>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, Hq, Hkv, rope, qk_norm, qn,
-                       kn, eps, kc, vc, cap);
+                       kn, eps, kc, cap, f16);
     case 256:
       return fk_launch(rope_qkv_kernel<4>, blocks, 256, 0, st, q, ldqkv, T, S, pos0, Hq, Hkv, rope, qk_norm, qn,
-                       kn, eps, kc, vc, cap);
+                       kn, eps, kc, cap, f16);
     default:
       return cudaErrorInvalidValue;
   }
@@ -561,15 +586,27 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, int Hq
 }
 
 cudaError_t launch_argmax(const float* z, int R, int V, int ldz, int32_t* out, cudaStream_t st, int32_t* out2,
-                          void* scratch) {
+                          void* scratch, float* margin) {
   if (R == 0) return cudaSuccess;
   if (scratch && R <= kArgmaxMaxSplitRows && (ldz & 3) == 0) {
+    constexpr int n = kArgmaxMaxSplitRows * kArgmaxSplits;
     float* pm = static_cast<float*>(scratch);
-    int* pi = reinterpret_cast<int*>(pm + kArgmaxMaxSplitRows * kArgmaxSplits);
-    unsigned* cnt = reinterpret_cast<unsigned*>(pi + kArgmaxMaxSplitRows * kArgmaxSplits);
-    return fk_launch(argmax_split_kernel, dim3(kArgmaxSplits, R), 256, 0, st, z, V, ldz, out, out2, pm, pi, cnt);
+    int* pi = reinterpret_cast<int*>(pm + n);
+    float* pm2 = reinterpret_cast<float*>(pi + n);
+    unsigned* cnt = reinterpret_cast<unsigned*>(pm2 + n);
+    return fk_launch(argmax_split_kernel, dim3(kArgmaxSplits, R), 256, 0, st, z, V, ldz, out, out2, margin, pm, pi,
+                     pm2, cnt);
   }
-  return fk_launch(argmax_kernel, R, 256, 0, st, z, R, V, ldz, out, out2);
+  return fk_launch(argmax_kernel, R, 256, 0, st, z, R, V, ldz, out, out2, margin);
+}
+
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  if (n % 8 || (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) return cudaErrorInvalidValue;
+  const size_t n8 = n / 8;
+  const int blocks = (int)std::min<size_t>((n8 + 255) / 256, 4096);
+  bf16_to_f16_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n8);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_set_int(int* p, int value, cudaStream_t st) {

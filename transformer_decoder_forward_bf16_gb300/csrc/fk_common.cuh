@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,17 +54,24 @@ FK_DEVICE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete. Returns false (after
 // setting *abort and the device error word) if the wait exceeds kWaitLimitNs
-// or another role of the CTA has already aborted.
+// or another role of the CTA has already aborted. dev_err points at a device
+// control block (word 0: error bits; word 1: a test override of the limit in
+// microseconds, 0 = kWaitLimitNs) or is null.
 FK_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* dev_err) {
   const uint32_t a = smem_u32(bar);
   for (int i = 0; i < 128; ++i)
     if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  uint64_t limit = kWaitLimitNs;
+  if (dev_err) {
+    const unsigned us = *reinterpret_cast<volatile unsigned*>(dev_err + 1);
+    if (us) limit = (uint64_t)us * 1000ull;
+  }
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 255) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit) {
         *abort_flag = 1;
         if (dev_err) atomicOr(dev_err, FK_DEVERR_PIPE_TIMEOUT);
         return false;
@@ -147,6 +155,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)   // B format: bf16
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with A and B both IEEE f16 (f16 != 0; format code 0) or both
+// bf16 (code 1). One MMA never mixes the two.
+__host__ __device__ constexpr uint32_t idesc_16b_f32(int M, int N, int f16) {
+  return f16 ? ((1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24)) : idesc_bf16_f32(M, N);
+}
 
 // D[tmem] (+)= A[smem] · B[smem]ᵀ, one instruction (M x N x 16).
 FK_DEVICE void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
@@ -220,6 +233,28 @@ FK_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// 16-bit activation storage: bf16 (f16 == 0) or IEEE f16, chosen per storage
+// site at run time (a warp-uniform branch). Conversions round to nearest even.
+FK_DEVICE uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+FK_DEVICE uint32_t pack_16x2(float lo, float hi, int f16) { return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); }
+FK_DEVICE float lo_16(uint32_t packed, int f16) {
+  return f16 ? __half2float(__ushort_as_half((unsigned short)(packed & 0xFFFFu))) : bf16_lo(packed);
+}
+FK_DEVICE float hi_16(uint32_t packed, int f16) {
+  return f16 ? __half2float(__ushort_as_half((unsigned short)(packed >> 16))) : bf16_hi(packed);
+}
+FK_DEVICE float load_16(const void* p, int f16) {
+  const unsigned short b = *static_cast<const unsigned short*>(p);
+  return f16 ? __half2float(__ushort_as_half(b)) : __uint_as_float((uint32_t)b << 16);
+}
+FK_DEVICE unsigned short bits_16(float v, int f16) {
+  return f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+FK_DEVICE void store_16(void* p, float v, int f16) { *static_cast<unsigned short*>(p) = bits_16(v, f16); }
 FK_DEVICE float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

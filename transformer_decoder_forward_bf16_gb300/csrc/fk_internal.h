@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <string>
 
 #include "../../include/fk.h"
@@ -25,6 +26,39 @@ fk_status cuda_fail(cudaError_t e, const char* what);
 
 // Current device is an sm_103 GB300-class GPU (cached per device).
 fk_status check_device(int* sm_count);
+
+// Per-device one-time set-up: kernel attributes (shared-memory size, cluster
+// permissions) belong to a device's context, so they are set once on every
+// device that launches the kernel, with that device current.
+constexpr int kMaxDevices = 64;
+struct DeviceOnce {
+  std::mutex mu;
+  uint64_t done = 0;
+  cudaError_t err[kMaxDevices] = {};
+  template <typename F>
+  cudaError_t run(F&& init) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!((done >> dev) & 1ull)) {
+      err[dev] = init();
+      done |= 1ull << dev;
+    }
+    return err[dev];
+  }
+};
+
+// Device control block: word 0 holds the error bits (FK_DEVERR_*); words 1
+// and 2 are test controls read by the pipelined kernels (word 1: a wait limit
+// in microseconds replacing the default, 0 = default; word 2: nonzero makes
+// the op-level skinny GEMM leave its first pipeline stage unarmed, so its
+// consumers' bounded wait runs out). Models keep theirs in the model arena;
+// op-level calls share one per device, owned by the library.
+constexpr size_t kCtlWords = 4;
+// The op-level control block of the current device (resolved once per device).
+fk_status op_control_block(unsigned** out);
 
 // ---------------------------------------------------------------------------
 // kernel timing: RAII scope recording events around the launches inside it
@@ -63,11 +97,14 @@ struct GemmWeights {
   int seg_start[4] = {0};  // first output row of each stacked matrix; seg_start[nseg] = total rows
   int seg_rows[3] = {0};
   int glu = 0;             // 1: virtual rows interleave gate/up per tile
+  int f16 = 0;             // the matrices (and so the A operand) are IEEE f16, else bf16
   int K = 0;
   int n_out = 0;           // output columns (GLU: rows of one matrix)
 };
 
-fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* rows, int nseg, int K, int glu);
+// f16: the matrices hold IEEE f16 (copies made by the model), else bf16.
+fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* rows, int nseg, int K, int glu,
+                            int f16 = 0);
 
 struct GemmOut {
   int epi = EPI_BF16;
@@ -77,6 +114,7 @@ struct GemmOut {
   int ldr = 0;
   float softcap = 0.f;
   int act = 0;             // GLU activation: 0 SiLU, 1 GELU (tanh form)
+  int out_f16 = 0;         // EPI_BF16 / EPI_GLU_BF16 store IEEE f16 instead of bf16
 };
 
 // A: bf16 [M, K] with row stride lda (elements, multiple of 8). With M <=
@@ -111,11 +149,16 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
                           size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed = true,
                           size_t counter_region = 0);
 
-// tcgen05 flash attention for prefill (head_dim 64 or 128; caches as in the
-// session layout, V transposed, cap a multiple of 64).
-bool attention_prefill_tc_supported(int hd, int ldq, int cap);
+// The op-level few-row GEMM (fk_gemm_bf16_splitk) over a given scratch buffer.
+fk_status gemm_splitk_op(const void* d_x, const void* d_w, int P, int K, int N, void* d_y, int y_fp32,
+                         void* d_scratch, size_t scratch_bytes, cudaStream_t st);
+
+// tcgen05 flash attention for prefill (head_dim 64, 128 or 256; caches as in
+// the session layout, V transposed, cap a multiple of 64, ldq a multiple of 8).
+// io_f16: q, the caches and the probabilities are IEEE f16 (else bf16);
+// out_f16: the output is stored as f16.
 fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
                                int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
-                               unsigned* dev_err, cudaStream_t st);
+                               unsigned* dev_err, cudaStream_t st, int io_f16 = 0, int out_f16 = 0);
 
 }  // namespace fk

@@ -18,8 +18,6 @@
 //   * the weight operand may be up to three matrices stacked along N (Q|K|V
 //     without a repacked copy) or a gate/up pair interleaved per tile.
 #include <algorithm>
-#include <cstdlib>
-#include <mutex>
 
 #include "fk_common.cuh"
 #include "fk_internal.h"
@@ -47,6 +45,8 @@ struct GemmArgs {
   int ldr;
   float softcap;
   unsigned* dev_err;
+  int ab_f16;   // A and B are IEEE f16 (else bf16)
+  int out_f16;  // 16-bit outputs stored as f16 (else bf16)
 };
 
 // MT = 128-row sub-tiles per CTA tile. MT == 2 makes a 256 x BN tile: two
@@ -61,7 +61,6 @@ struct Cfg {
   static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator sets (double buffer when they fit)
   static constexpr uint32_t TMEM_COLS = NACC * MT * BN;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 };
 
 FK_DEVICE void tile_coords(int t, int m_blocks, int n_blocks, int& mb, int& nb) {
@@ -211,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
+      const uint32_t idesc = idesc_16b_f32(BM, BN, args.ab_f16);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int sub = 0; sub < MT; ++sub) {
               const uint64_t ad = smem_desc_sw128(sA + stage * C::A_STAGE + sub * A_BYTES);
-              umma_bf16(d + sub * BN, ad + 2 * k, bd + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+              umma_bf16(d + sub * BN, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
             }
           umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -281,16 +281,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!row_ok) continue;
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = (args.act ? act_gelu_tanh(v[j]) : act_silu(v[j])) * u[j];
-          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + (size_t)row * args.ldo + col0;
+          uint16_t* o = reinterpret_cast<uint16_t*>(args.out) + (size_t)row * args.ldo + col0;  // bf16 or f16
           if (col0 + 32 <= args.n_out) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
-              uint4 pk = make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
-                                    pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
+              const int f = args.out_f16;
+              uint4 pk = make_uint4(pack_16x2(v[j], v[j + 1], f), pack_16x2(v[j + 2], v[j + 3], f),
+                                    pack_16x2(v[j + 4], v[j + 5], f), pack_16x2(v[j + 6], v[j + 7], f));
               *reinterpret_cast<uint4*>(o + j) = pk;
             }
           } else {
-            for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) o[j] = __float2bfloat16_rn(v[j]);
+            for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) store_16(o + j, v[j], args.out_f16);
           }
         }
       } else {
@@ -300,16 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!row_ok || col0 >= args.n_out) continue;
           const bool full_chunk = col0 + 32 <= args.n_out;
           if (args.epi == EPI_BF16) {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + (size_t)row * args.ldo + col0;
+            uint16_t* o = reinterpret_cast<uint16_t*>(args.out) + (size_t)row * args.ldo + col0;  // bf16 or f16
             if (full_chunk) {
 #pragma unroll
               for (int j = 0; j < 32; j += 8) {
-                uint4 pk = make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
-                                      pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
+                const int f = args.out_f16;
+                uint4 pk = make_uint4(pack_16x2(v[j], v[j + 1], f), pack_16x2(v[j + 2], v[j + 3], f),
+                                      pack_16x2(v[j + 4], v[j + 5], f), pack_16x2(v[j + 6], v[j + 7], f));
                 *reinterpret_cast<uint4*>(o + j) = pk;
               }
             } else {
-              for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) o[j] = __float2bfloat16_rn(v[j]);
+              for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) store_16(o + j, v[j], args.out_f16);
             }
           } else {
             float* o = reinterpret_cast<float*>(args.out) + (size_t)row * args.ldo + col0;
@@ -359,11 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int MT>
 fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st) {
   using C = Cfg<BN, MT>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  });
+  static DeviceOnce once;
+  const cudaError_t attr_err = once.run(
+      [] { return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
   const int m_blocks = (a.M + BM * MT - 1) / (BM * MT);
   const int n_blocks = a.glu ? (a.n_out + BN / 2 - 1) / (BN / 2) : (a.n_virtual + BN - 1) / BN;
@@ -378,11 +378,13 @@ fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs&
 
 }  // namespace
 
-fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* rows, int nseg, int K, int glu) {
+fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* rows, int nseg, int K, int glu,
+                            int f16) {
   if (nseg < 1 || nseg > 3 || (glu && nseg != 2) || K <= 0 || K % 8) return fail(FK_ERR_INVALID_ARG, "gemm weights");
   *g = GemmWeights();
   g->nseg = nseg;
   g->glu = glu;
+  g->f16 = f16 ? 1 : 0;
   g->K = K;
   int start = 0;
   for (int s = 0; s < nseg; ++s) {
@@ -437,12 +439,13 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
   a.ldr = o.ldr;
   a.softcap = o.softcap;
   a.dev_err = dev_err;
+  a.ab_f16 = w.f16;
+  a.out_f16 = o.out_f16;
   // 256x256 tiles while they give every SM at least two tiles; then 128x256;
   // else 128-wide.
   const int m_blocks = (M + BM - 1) / BM;
   const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
-  static const bool no_dual = getenv("FK_GEMM_NO_DUAL") != nullptr;
-  if (!no_dual && ((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count) return launch_bn<256, 2>(tA, w, a, sm_count, st);
+  if (((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count) return launch_bn<256, 2>(tA, w, a, sm_count, st);
   if (m_blocks * nb256 >= sm_count) return launch_bn<256, 1>(tA, w, a, sm_count, st);
   return launch_bn<128, 1>(tA, w, a, sm_count, st);
 }
@@ -464,9 +467,12 @@ extern "C" fk_status fk_gemm_bf16(const void* d_x, const void* d_w, int32_t P, i
   int rows[1] = {N};
   s = gemm_weights_init(&w, mats, rows, 1, K, 0);
   if (s != FK_OK) return s;
+  unsigned* ctl = nullptr;
+  s = op_control_block(&ctl);
+  if (s != FK_OK) return s;
   GemmOut o;
   o.epi = y_fp32 ? EPI_F32 : EPI_BF16;
   o.out = d_y;
   o.ldo = N;
-  return gemm_run(d_x, P, K, w, o, nullptr, static_cast<cudaStream_t>(stream));
+  return gemm_run(d_x, P, K, w, o, ctl, static_cast<cudaStream_t>(stream));
 }

@@ -19,7 +19,6 @@
 //   * operands under 8 MB take a single split and apply the epilogue straight
 //     from TMEM.
 #include <algorithm>
-#include <mutex>
 
 #include "fk_common.cuh"
 #include "fk_internal.h"
@@ -43,6 +42,7 @@ struct SkinnyArgs {
   int fused, glu_tiles;  // glu_tiles: feature tiles of one half of a gate|up pair (0 = not GLU)
   int direct;            // one split: the epilogue is applied straight from TMEM
   int epi, act, n_out, ldo, ldr;
+  int ab_f16, out_f16;  // operand type (f16 or bf16); type of 16-bit outputs
   void* out;
   const float* res;
   float softcap;
@@ -58,10 +58,10 @@ FK_DEVICE float act_gelu_tanh(float g) {
 // for GLU), u = the up projection (GLU only).
 FK_DEVICE void store_out(const SkinnyArgs& a, int t, int f, float v, float u) {
   if (a.epi == EPI_GLU_BF16) {
-    static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] =
-        __float2bfloat16_rn((a.act ? act_gelu_tanh(v) : act_silu(v)) * u);
+    store_16(static_cast<uint16_t*>(a.out) + (size_t)t * a.ldo + f, (a.act ? act_gelu_tanh(v) : act_silu(v)) * u,
+             a.out_f16);
   } else if (a.epi == EPI_BF16) {
-    static_cast<__nv_bfloat16*>(a.out)[(size_t)t * a.ldo + f] = __float2bfloat16_rn(v);
+    store_16(static_cast<uint16_t*>(a.out) + (size_t)t * a.ldo + f, v, a.out_f16);
   } else if (a.epi == EPI_ADD_F32) {
     static_cast<float*>(a.out)[(size_t)t * a.ldo + f] = a.res[(size_t)t * a.ldr + f] + v;
   } else {
@@ -101,7 +101,6 @@ struct SCfg {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int SMEM = kStages * STAGE + 1024 + 256;
   static constexpr uint32_t TMEM_COLS = BT < 32 ? 32 : BT;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(128, BT);
 };
 
 template <int BT>
@@ -176,7 +175,11 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     int issued[kStages] = {0, 0, 0, 0};
     bool ok = true;
     const int npre = min(kStages, kb1 - kb0);
+    // test control (word 2 of the control block): leave stage 0 unarmed, so
+    // the MMA issuer's bounded wait on it runs out
+    const bool stall = args.dev_err && *reinterpret_cast<volatile unsigned*>(args.dev_err + 2) != 0;
     for (int it = 0; it < npre; ++it) {  // fresh ring: every stage is free
+      if (stall && it == 0) continue;
       uint8_t* sa = smem + it * C::STAGE;
       mbar_arrive_expect_tx(&full[it], bytes);
       for (int i = 0; i < 2; ++i)
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     pdl_wait();
     pdl_trigger();
     for (int it = 0; it < npre; ++it) {
+      if (stall && it == 0) continue;
       tma_load_2d(&tmX, &full[it], smem + it * C::STAGE + A_BYTES, (kb0 + it) * 64, 0);
       ++issued[it];
     }
@@ -215,6 +219,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
+    const uint32_t idesc = idesc_16b_f32(128, BT, args.ab_f16);
     for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
       const int stage = it % kStages;
       const uint32_t phase = (it / kStages) & 1;
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
       const uint64_t ad = smem_desc_sw128(sa);
       const uint64_t bd = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) umma_bf16(tmem, ad + 2 * k, bd + 2 * k, C::IDESC, (it | k) != 0 ? 1u : 0u);
+      for (int k = 0; k < 4; ++k) umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it | k) != 0 ? 1u : 0u);
       umma_commit(&empty[stage]);
     }
     umma_commit(done);
@@ -274,8 +279,11 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (!args.fused || !have) return;
-  // ---- fused split-K reduction: the last CTA of this feature group finishes it
+  if (!args.fused) return;
+  // ---- fused split-K reduction: the last CTA of this feature group finishes it.
+  // A CTA whose pipeline gave up (the error word is set; its partials are
+  // not valid) still takes part in the arrival, so the counter returns to
+  // zero for the next launch.
   volatile int* last = abort_flag + 1;
   const int group = args.glu_tiles ? (int)blockIdx.x % args.glu_tiles : (int)blockIdx.x;
   const unsigned expect = gridDim.y * (args.glu_tiles ? 2u : 1u);
@@ -298,7 +306,8 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
 
 // Sum the splits in order and apply the epilogue; one thread per (token, 4 features).
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int S, int M, int n_rows, int n_out, int epi,
-                                     int act, void* out, int ldo, const float* res, int ldr, float softcap) {
+                                     int act, void* out, int ldo, const float* res, int ldr, float softcap,
+                                     int out_f16) {
   pdl_trigger();
   pdl_wait();
   const int per_row = (n_out + 3) / 4;
@@ -315,11 +324,11 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int S, int 
         for (int j = 0; j < nf; ++j) u[j] += p[n_out + f + j];
     }
     if (epi == EPI_GLU_BF16) {
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + (size_t)t * ldo + f;
-      for (int j = 0; j < nf; ++j) o[j] = __float2bfloat16_rn((act ? act_gelu_tanh(v[j]) : act_silu(v[j])) * u[j]);
+      uint16_t* o = static_cast<uint16_t*>(out) + (size_t)t * ldo + f;
+      for (int j = 0; j < nf; ++j) store_16(o + j, (act ? act_gelu_tanh(v[j]) : act_silu(v[j])) * u[j], out_f16);
     } else if (epi == EPI_BF16) {
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + (size_t)t * ldo + f;
-      for (int j = 0; j < nf; ++j) o[j] = __float2bfloat16_rn(v[j]);
+      uint16_t* o = static_cast<uint16_t*>(out) + (size_t)t * ldo + f;
+      for (int j = 0; j < nf; ++j) store_16(o + j, v[j], out_f16);
     } else if (epi == EPI_ADD_F32) {
       float* o = static_cast<float*>(out) + (size_t)t * ldo + f;
       const float* r = res + (size_t)t * ldr + f;
@@ -338,15 +347,15 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int S, int 
 
 template <int BT>
 cudaError_t set_smem_attr() {
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfg<BT>::SMEM);
+  static DeviceOnce once;
+  return once.run([] {
+    cudaError_t attr =
+        cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfg<BT>::SMEM);
     if (attr == cudaSuccess)
       attr = cudaFuncSetAttribute(gemv_tc_kernel<BT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   (int)cudaSharedmemCarveoutMaxShared);
+    return attr;
   });
-  return attr;
 }
 
 template <int BT>
@@ -367,17 +376,13 @@ fk_status launch_bt(const CUtensorMap& tX, const GemmWeights& w, const SkinnyArg
 // (the kernels ask for the largest shared-memory carveout, so this is the
 // SM's whole shared memory over each CTA's dynamic + reserved bytes).
 static int resident_per_sm(int M) {
-  static int cached[3] = {0, 0, 0};
   const int i = M <= 16 ? 0 : (M <= 32 ? 1 : 2);
-  if (!cached[i]) {
-    int dev = 0, smem_sm = 0, reserved = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-    const int smem = i == 0 ? SCfg<16>::SMEM : (i == 1 ? SCfg<32>::SMEM : SCfg<64>::SMEM);
-    cached[i] = std::max(1, std::min(2048 / kThreads, smem_sm / (smem + reserved)));
-  }
-  return cached[i];
+  int dev = 0, smem_sm = 0, reserved = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  const int smem = i == 0 ? SCfg<16>::SMEM : (i == 1 ? SCfg<32>::SMEM : SCfg<64>::SMEM);
+  return std::max(1, std::min(2048 / kThreads, smem_sm / (smem + reserved)));
 }
 
 // Small operands (under kDirectBytes of weights, not a gate/up pair) take a
@@ -449,6 +454,8 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   a.counters = static_cast<unsigned*>(scratch);
   a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + creg);
   a.dev_err = dev_err;
+  a.ab_f16 = w.f16;
+  a.out_f16 = o.out_f16;
   // a gate|up pair fuses only when each half is a whole number of 128-row tiles
   // (the last CTA sums M x splits values per feature: worth it only for few tokens)
   a.direct = p.direct;
@@ -473,7 +480,7 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   const long work = (long)M * ((n_out + 3) / 4);
   const int blocks = (int)std::min<long>((work + 255) / 256, 8L * sms);
   cudaError_t e = fk_launch(splitk_reduce_kernel, blocks, 256, 0, st, (const float*)a.part, p.splits, M, n_rows, n_out,
-                            o.epi, o.act, o.out, o.ldo, o.res, o.ldr, o.softcap);
+                            o.epi, o.act, o.out, o.ldo, o.res, o.ldr, o.softcap, o.out_f16);
   if (e != cudaSuccess) return cuda_fail(e, "splitk_reduce_kernel launch");
   return FK_OK;
 }
@@ -487,9 +494,11 @@ extern "C" size_t fk_gemm_bf16_splitk_scratch_bytes(int32_t P, int32_t K, int32_
   return fk::skinny_plan(P, K, N, sms, true).part_bytes;
 }
 
-extern "C" fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
-                                         int32_t y_fp32, void* d_scratch, size_t scratch_bytes, void* stream) {
-  using namespace fk;
+namespace fk {
+// The op-level few-row GEMM over a scratch buffer of scratch_bytes at
+// d_scratch (validation, then the split-K kernel with its counters cleared).
+fk_status gemm_splitk_op(const void* d_x, const void* d_w, int P, int K, int N, void* d_y, int y_fp32,
+                         void* d_scratch, size_t scratch_bytes, cudaStream_t st) {
   if (!d_x || !d_w || !d_y || P < 1 || P > kSkinnyMaxTokens || K <= 0 || N <= 0)
     return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16_splitk: bad argument (1 <= P <= 64)");
   if (K % 8 || N % 8) return fail(FK_ERR_INVALID_ARG, "fk_gemm_bf16_splitk: K and N must be multiples of 8");
@@ -501,10 +510,19 @@ extern "C" fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32
   int rows[1] = {N};
   fk_status s = gemm_weights_init(&w, mats, rows, 1, K, 0);
   if (s != FK_OK) return s;
+  unsigned* ctl = nullptr;
+  s = op_control_block(&ctl);
+  if (s != FK_OK) return s;
   GemmOut o;
   o.epi = y_fp32 ? EPI_F32 : EPI_BF16;
   o.out = d_y;
   o.ldo = N;
-  return gemm_run_skinny(d_x, P, K, w, o, d_scratch, scratch_bytes, nullptr, static_cast<cudaStream_t>(stream),
-                         false);
+  return gemm_run_skinny(d_x, P, K, w, o, d_scratch, scratch_bytes, ctl, st, false);
+}
+}  // namespace fk
+
+extern "C" fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
+                                         int32_t y_fp32, void* d_scratch, size_t scratch_bytes, void* stream) {
+  return fk::gemm_splitk_op(d_x, d_w, P, K, N, d_y, y_fp32, d_scratch, scratch_bytes,
+                            static_cast<cudaStream_t>(stream));
 }

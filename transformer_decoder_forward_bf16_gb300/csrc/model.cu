@@ -66,6 +66,8 @@ struct fk_model {
   float attn_scale = 1.f;
   int sm_count = 0;
   bool has_local = false;
+  // 1 when the activation storage site (an FK_F16_* bit) holds IEEE f16
+  int f16(uint32_t site) const { return (cfg.f16_sites & site) ? 1 : 0; }
 };
 
 struct fk_session {
@@ -88,6 +90,7 @@ struct fk_session {
   cudaGraphExec_t graph = nullptr;
   float* graph_logits = nullptr;
   int32_t* graph_next = nullptr;
+  float* graph_margin = nullptr;
 };
 
 namespace {
@@ -122,6 +125,7 @@ fk_status validate_config(const fk_config* c) {
   // "pegainfer #878": the final-logit softcap is validated positive at parse
   if (!std::isfinite(c->final_softcap) || c->final_softcap < 0.f) return bad("final_softcap must be 0 (off) or > 0");
   if (c->tied != 0 && c->tied != 1) return bad("tied must be 0 or 1");
+  if (c->f16_sites & ~FK_F16_ALL) return bad("f16_sites has bits outside FK_F16_ALL");
   if (c->layer_kinds) {
     for (int l = 0; l < c->n_layers; ++l) {
       if (c->layer_kinds[l] > 1) return bad("layer_kinds entries must be 0 (global) or 1 (local)");
@@ -138,9 +142,25 @@ bool has_local(const fk_config* c) {
   return false;
 }
 
-// Arena: [error word | rope table global | rope table local]
+// Arena: [control block | rope table global | rope table local | f16 weight copies]
 size_t rope_table_bytes(const fk_config* c, int max_pos) {
   return align_up((size_t)max_pos * (c->head_dim / 2) * sizeof(float2));
+}
+
+// Bytes of the f16 copies of the weights whose GEMM input site is f16: per
+// layer Wq, Wk, Wv (FK_F16_QKV_IN), Wo (FK_F16_O_IN), W_gate, W_up
+// (FK_F16_FFN_IN), W_down (FK_F16_FFN_ACT); the head (FK_F16_HEAD_IN).
+size_t f16_copy_bytes(const fk_config* c) {
+  const size_t H = c->hidden, I = c->intermediate, Nq = (size_t)c->n_q_heads * c->head_dim,
+               Nkv = (size_t)c->n_kv_heads * c->head_dim;
+  size_t per_layer = 0;
+  if (c->f16_sites & FK_F16_QKV_IN) per_layer += align_up(Nq * H * 2) + 2 * align_up(Nkv * H * 2);
+  if (c->f16_sites & FK_F16_O_IN) per_layer += align_up(H * Nq * 2);
+  if (c->f16_sites & FK_F16_FFN_IN) per_layer += 2 * align_up(I * H * 2);
+  if (c->f16_sites & FK_F16_FFN_ACT) per_layer += align_up(H * I * 2);
+  size_t b = per_layer * c->n_layers;
+  if (c->f16_sites & FK_F16_HEAD_IN) b += align_up((size_t)c->vocab * H * 2);
+  return b;
 }
 
 // bf16(sqrt(hidden)) by round-to-nearest-even on the float bits ("pegainfer
@@ -257,7 +277,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   const size_t gvb = decode ? sc.gemv_bytes : 0;
   { ProfScope ps(decode ? "embed_norm_dec" : "embed_norm", st);
   FK_LAUNCH(launch_embed_norm(ids ? ids : sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
-                              x_in, sc.u, m->dev_err, st)); }
+                              x_in, sc.u, m->dev_err, st, m->f16(FK_F16_QKV_IN))); }
   for (int l = 0; l < L; ++l) {
     const fk_layer_weights& w = m->layers[l];
     const int kind = m->kinds[l];
@@ -265,11 +285,14 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     float* x_out = slots ? slots + (size_t)(l + 1) * T * H : sc.x0;
     float* x_mid = sc.x1;
     const void* next_norm = l + 1 < L ? m->layers[l + 1].attn_norm : m->final_norm;
+    // the next norm output feeds the next layer's QKV projection, or the LM head
+    const int next_f16 = l + 1 < L ? m->f16(FK_F16_QKV_IN) : m->f16(FK_F16_HEAD_IN);
     __nv_bfloat16* kl = kv.k + kv.layer_stride * l;
     __nv_bfloat16* vl = kv.v + kv.layer_stride * l;
 
     GemmOut o;
     o.epi = EPI_BF16;
+    o.out_f16 = m->f16(FK_F16_ATTN);
     o.out = sc.qkv;
     o.ldo = m->Nqkv;
     { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
@@ -277,19 +300,16 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       ProfScope ps("attn_decode", st);
       FK_LAUNCH(launch_attention_decode_rope(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, d_len, c.n_q_heads, c.n_kv_heads,
                                              hd, window, m->attn_scale, m->rope[kind], c.qk_norm, w.q_norm, w.k_norm,
-                                             c.rms_eps, dsplits, sc.ao, m->dev_err, st));
+                                             c.rms_eps, dsplits, sc.ao, m->dev_err, st, m->f16(FK_F16_ATTN),
+                                             m->f16(FK_F16_O_IN)));
     } else {
       { ProfScope ps("rope_qkv", st);
       FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
-                                m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st)); }
+                                m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st,
+                                m->f16(FK_F16_ATTN))); }
       ProfScope ps("attn_prefill", st);
-      if (attention_prefill_tc_supported(hd, m->Nqkv, kv.cap) && !getenv("FK_ATTN_MMA_SYNC")) {
-        FK_TRY(attention_prefill_tc(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd, window,
-                                    m->attn_scale, sc.ao, m->dev_err, st));
-      } else {
-        FK_LAUNCH(launch_attention_prefill(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
-                                           window, m->attn_scale, sc.ao, st));
-      }
+      FK_TRY(attention_prefill_tc(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd, window,
+                                  m->attn_scale, sc.ao, m->dev_err, st, m->f16(FK_F16_ATTN), m->f16(FK_F16_O_IN)));
     }
     // attention output projection + residual
     if (sandwich) {
@@ -300,7 +320,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_in, x_mid, (int)T, H, w.post_attn_norm, w.ffn_norm, c.rms_eps, sc.u,
-                                          st));
+                                          st, m->f16(FK_F16_FFN_IN)));
     } else {
       o.epi = EPI_ADD_F32;
       o.out = x_mid;
@@ -309,11 +329,12 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.ldr = H;
       { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
-      FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st));
+      FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st, m->f16(FK_F16_FFN_IN)));
     }
     // gated FFN
     GemmOut og;
     og.epi = EPI_GLU_BF16;
+    og.out_f16 = m->f16(FK_F16_FFN_ACT);
     og.out = sc.h;
     og.ldo = c.intermediate;
     og.act = c.act;
@@ -326,7 +347,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
       FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps, sc.u,
-                                          st));
+                                          st, next_f16));
     } else {
       GemmOut od;
       od.epi = EPI_ADD_F32;
@@ -336,7 +357,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       od.ldr = H;
       { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
-      FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st));
+      FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st, next_f16));
     }
     x_in = x_out;
   }
@@ -345,7 +366,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
 }
 
 fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* argmax, const Scratch& sc,
-                   cudaStream_t st, int32_t* argmax2 = nullptr) {
+                   cudaStream_t st, int32_t* argmax2 = nullptr, float* margin = nullptr) {
   GemmOut o;
   o.epi = EPI_F32;
   o.out = logits;
@@ -354,7 +375,7 @@ fk_status run_head(fk_model* m, const void* u, int R, float* logits, int32_t* ar
   { ProfScope ps("gemm_head", st); FK_TRY(gemm_run(u, R, m->cfg.hidden, m->g_head, o, m->dev_err, st, sc.gemv, sc.gemv_bytes,
                                                    sc.gemv_counter_bytes)); }
   ProfScope ps("argmax", st);
-  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st, argmax2, sc.argmax));
+  if (argmax) FK_LAUNCH(launch_argmax(logits, R, m->cfg.vocab, m->cfg.vocab, argmax, st, argmax2, sc.argmax, margin));
   return FK_OK;
 }
 
@@ -380,7 +401,7 @@ extern "C" size_t fk_model_arena_bytes(const fk_config* cfg, int32_t max_positio
     if (max_positions < 1) set_error("max_positions must be >= 1");
     return 0;
   }
-  return kAlign + rope_table_bytes(cfg, max_positions) * (has_local(cfg) ? 2 : 1);
+  return kAlign + rope_table_bytes(cfg, max_positions) * (has_local(cfg) ? 2 : 1) + f16_copy_bytes(cfg);
 }
 
 extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, int32_t max_positions, void* d_arena,
@@ -434,34 +455,6 @@ extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, 
         (!lw.post_attn_norm || !lw.post_ffn_norm || !aligned16(lw.post_attn_norm) || !aligned16(lw.post_ffn_norm)))
       return cleanup(fail(FK_ERR_INVALID_ARG, "sandwich norm weights missing"));
   }
-  // GEMM operands (TMA descriptors of the weights)
-  const int H = cfg->hidden, I = cfg->intermediate;
-  m->g_qkv.resize(cfg->n_layers);
-  m->g_o.resize(cfg->n_layers);
-  m->g_gu.resize(cfg->n_layers);
-  m->g_down.resize(cfg->n_layers);
-  for (int l = 0; l < cfg->n_layers; ++l) {
-    const fk_layer_weights& lw = m->layers[l];
-    const void* qkv[3] = {lw.wq, lw.wk, lw.wv};
-    int rq[3] = {m->Nq, m->Nkv, m->Nkv};
-    fk_status s = gemm_weights_init(&m->g_qkv[l], qkv, rq, 3, H, 0);
-    const void* wo[1] = {lw.wo};
-    int ro[1] = {H};
-    if (s == FK_OK) s = gemm_weights_init(&m->g_o[l], wo, ro, 1, m->Nq, 0);
-    const void* gu[2] = {lw.w_gate, lw.w_up};
-    int rg[2] = {I, I};
-    if (s == FK_OK) s = gemm_weights_init(&m->g_gu[l], gu, rg, 2, H, 1);
-    const void* wd[1] = {lw.w_down};
-    int rd[1] = {H};
-    if (s == FK_OK) s = gemm_weights_init(&m->g_down[l], wd, rd, 1, I, 0);
-    if (s != FK_OK) return cleanup(s);
-  }
-  {
-    const void* hw[1] = {m->head};
-    int rv[1] = {cfg->vocab};
-    fk_status s = gemm_weights_init(&m->g_head, hw, rv, 1, H, 0);
-    if (s != FK_OK) return cleanup(s);
-  }
   // arena: error word + RoPE tables (host double precision -> fp32 cos/sin)
   uint8_t* arena = static_cast<uint8_t*>(d_arena);
   m->dev_err = reinterpret_cast<unsigned*>(arena);
@@ -481,7 +474,62 @@ extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, 
     cudaError_t e = cudaMemcpy(m->rope[kind], table.data(), table.size() * sizeof(float2), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "upload rope table"));
   }
-  cudaError_t e = cudaMemset(m->dev_err, 0, sizeof(unsigned));
+  // f16 copies of the weights of GEMMs whose input activations are f16
+  const int H = cfg->hidden, I = cfg->intermediate;
+  uint8_t* copy_at = arena + kAlign + tb * (m->has_local ? 2 : 1);
+  cudaError_t ce = cudaSuccess;
+  auto f16_copy = [&](const void* src, size_t elems) -> const void* {
+    void* dst = copy_at;
+    copy_at += align_up(elems * 2);
+    if (ce == cudaSuccess) ce = launch_bf16_to_f16(src, dst, elems, nullptr);
+    return dst;
+  };
+  std::vector<fk_layer_weights> gw(m->layers);  // the matrices the GEMMs read
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    fk_layer_weights& lw = gw[l];
+    if (m->f16(FK_F16_QKV_IN)) {
+      lw.wq = f16_copy(lw.wq, (size_t)m->Nq * H);
+      lw.wk = f16_copy(lw.wk, (size_t)m->Nkv * H);
+      lw.wv = f16_copy(lw.wv, (size_t)m->Nkv * H);
+    }
+    if (m->f16(FK_F16_O_IN)) lw.wo = f16_copy(lw.wo, (size_t)H * m->Nq);
+    if (m->f16(FK_F16_FFN_IN)) {
+      lw.w_gate = f16_copy(lw.w_gate, (size_t)I * H);
+      lw.w_up = f16_copy(lw.w_up, (size_t)I * H);
+    }
+    if (m->f16(FK_F16_FFN_ACT)) lw.w_down = f16_copy(lw.w_down, (size_t)H * I);
+  }
+  const void* head_mat = m->f16(FK_F16_HEAD_IN) ? f16_copy(m->head, (size_t)cfg->vocab * H) : m->head;
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(nullptr);
+  if (ce != cudaSuccess) return cleanup(cuda_fail(ce, "f16 weight copies"));
+  // GEMM operands (TMA descriptors of the weights)
+  m->g_qkv.resize(cfg->n_layers);
+  m->g_o.resize(cfg->n_layers);
+  m->g_gu.resize(cfg->n_layers);
+  m->g_down.resize(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const fk_layer_weights& lw = gw[l];
+    const void* qkv[3] = {lw.wq, lw.wk, lw.wv};
+    int rq[3] = {m->Nq, m->Nkv, m->Nkv};
+    fk_status s = gemm_weights_init(&m->g_qkv[l], qkv, rq, 3, H, 0, m->f16(FK_F16_QKV_IN));
+    const void* wo[1] = {lw.wo};
+    int ro[1] = {H};
+    if (s == FK_OK) s = gemm_weights_init(&m->g_o[l], wo, ro, 1, m->Nq, 0, m->f16(FK_F16_O_IN));
+    const void* gu[2] = {lw.w_gate, lw.w_up};
+    int rg[2] = {I, I};
+    if (s == FK_OK) s = gemm_weights_init(&m->g_gu[l], gu, rg, 2, H, 1, m->f16(FK_F16_FFN_IN));
+    const void* wd[1] = {lw.w_down};
+    int rd[1] = {H};
+    if (s == FK_OK) s = gemm_weights_init(&m->g_down[l], wd, rd, 1, I, 0, m->f16(FK_F16_FFN_ACT));
+    if (s != FK_OK) return cleanup(s);
+  }
+  {
+    const void* hw[1] = {head_mat};
+    int rv[1] = {cfg->vocab};
+    fk_status s = gemm_weights_init(&m->g_head, hw, rv, 1, H, 0, m->f16(FK_F16_HEAD_IN));
+    if (s != FK_OK) return cleanup(s);
+  }
+  cudaError_t e = cudaMemset(m->dev_err, 0, kCtlWords * sizeof(unsigned));
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "clear error word"));
   *out = m;
   return FK_OK;
@@ -518,7 +566,7 @@ extern "C" size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, i
 
 extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
                                 void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
-                                void* stream) {
+                                float* d_margin, void* stream) {
   if (!m || !ids || batch < 1 || seq < 1) return fail(FK_ERR_INVALID_ARG, "fk_forward: bad argument");
   if (seq > m->max_pos) return fail(FK_ERR_CONTEXT_FULL, "seq exceeds the model's max_positions");
   const long T = (long)batch * seq;
@@ -528,6 +576,7 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   if (reinterpret_cast<uintptr_t>(d_ws) % kAlign) return fail(FK_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if ((d_hidden && !aligned16(d_hidden)) || (d_logits && !aligned16(d_logits)))
     return fail(FK_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  if (d_margin && !d_argmax) return fail(FK_ERR_INVALID_ARG, "d_margin needs d_argmax");
   FK_TRY(check_device(nullptr));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Scratch sc;
@@ -542,7 +591,8 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   // attention reads V in 64-position blocks: positions past seq must hold finite values
   if (seq % 64) FK_CUDA_TRY(cudaMemsetAsync(kv.v, 0, kv.bytes, st));
   FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, 1, st));
-  if (d_logits || d_argmax) FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st));
+  if (d_logits || d_argmax)
+    FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st, nullptr, d_margin));
   return FK_OK;
 }
 
@@ -653,14 +703,15 @@ extern "C" fk_status fk_session_reset(fk_session* s) {
 
 extern "C" int32_t fk_session_length(const fk_session* s) { return s ? s->len : -1; }
 
-static fk_status session_head(fk_session* s, const void* u_rows, float* d_logits, int32_t* d_next, cudaStream_t st) {
+static fk_status session_head(fk_session* s, const void* u_rows, float* d_logits, int32_t* d_next, float* d_margin,
+                              cudaStream_t st) {
   fk_model* m = s->m;
   float* logits = d_logits ? d_logits : s->logits;
-  return run_head(m, u_rows, s->B, logits, s->next_ids, s->sc, st, d_next);
+  return run_head(m, u_rows, s->B, logits, s->next_ids, s->sc, st, d_next, d_margin);
 }
 
 extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32_t ids_on_device, int32_t seq,
-                                        float* d_last_logits, int32_t* d_next, void* stream) {
+                                        float* d_last_logits, int32_t* d_next, float* d_margin, void* stream) {
   if (!s || !ids || seq < 1) return fail(FK_ERR_INVALID_ARG, "fk_session_prefill: bad argument");
   if (s->len + seq > s->max_seq) return fail(FK_ERR_CONTEXT_FULL, "prefill would exceed the session's max_seq");
   if (d_last_logits && !aligned16(d_last_logits)) return fail(FK_ERR_INVALID_ARG, "logits must be 16-byte aligned");
@@ -681,13 +732,13 @@ extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32
   FK_LAUNCH(launch_gather_last_rows(s->sc.u, m->cfg.hidden, C, m->cfg.hidden, s->B, s->u_last, st));
   FK_LAUNCH(launch_set_int(s->d_len, s->len, st));
   s->d_len_valid = true;
-  return session_head(s, s->u_last, d_last_logits, d_next, st);
+  return session_head(s, s->u_last, d_last_logits, d_next, d_margin, st);
 }
 
 // Enqueue one decode step whose positions come from s->d_len (so the same
 // launches serve every step, captured or not).
 static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next,
-                                cudaStream_t st) {
+                                float* d_margin, cudaStream_t st) {
   fk_model* m = s->m;
   // every launch of the step may overlap its predecessor's tail (each kernel
   // waits for its predecessor before touching data the predecessor writes)
@@ -695,7 +746,7 @@ static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_lo
   KV kv{s->kcache, s->vcache, s->layer_kv, s->cap};
   FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_splits, st,
                    s->d_len, d_ids ? d_ids : s->next_ids));
-  FK_TRY(session_head(s, s->sc.u, d_logits, d_next, st));
+  FK_TRY(session_head(s, s->sc.u, d_logits, d_next, d_margin, st));
   FK_LAUNCH(launch_inc_int(s->d_len, st));
   return FK_OK;
 }
@@ -709,7 +760,7 @@ static bool graphs_disabled() {
 }
 
 extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next,
-                                    void* stream) {
+                                    float* d_margin, void* stream) {
   if (!s) return fail(FK_ERR_INVALID_ARG, "session is NULL");
   if (s->len + 1 > s->max_seq) return fail(FK_ERR_CONTEXT_FULL, "decode would exceed the session's max_seq");
   if (s->len == 0 && !d_ids) return fail(FK_ERR_INVALID_ARG, "no previous greedy ids: prefill first or pass d_ids");
@@ -725,18 +776,18 @@ extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* 
   // buffers change). Steps with caller ids, and steps while kernel timing is
   // on, are launched one by one.
   if (d_ids || profiling_enabled() || graphs_disabled()) {
-    FK_TRY(enqueue_decode(s, d_ids, d_logits, d_next, st));
+    FK_TRY(enqueue_decode(s, d_ids, d_logits, d_next, d_margin, st));
     s->len += 1;
     return FK_OK;
   }
-  if (!s->graph || s->graph_logits != d_logits || s->graph_next != d_next) {
+  if (!s->graph || s->graph_logits != d_logits || s->graph_next != d_next || s->graph_margin != d_margin) {
     if (s->graph) {
       cudaGraphExecDestroy(s->graph);
       s->graph = nullptr;
     }
     if (!s->cap_stream) FK_CUDA_TRY(cudaStreamCreateWithFlags(&s->cap_stream, cudaStreamNonBlocking));
     FK_CUDA_TRY(cudaStreamBeginCapture(s->cap_stream, cudaStreamCaptureModeThreadLocal));
-    fk_status es = enqueue_decode(s, nullptr, d_logits, d_next, s->cap_stream);
+    fk_status es = enqueue_decode(s, nullptr, d_logits, d_next, d_margin, s->cap_stream);
     cudaGraph_t g = nullptr;
     cudaError_t ce = cudaStreamEndCapture(s->cap_stream, &g);
     if (es != FK_OK) {
@@ -752,9 +803,62 @@ extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* 
     }
     s->graph_logits = d_logits;
     s->graph_next = d_next;
+    s->graph_margin = d_margin;
   }
   FK_CUDA_TRY(cudaGraphLaunch(s->graph, st));
   s->len += 1;
+  return FK_OK;
+}
+
+// ===========================================================================
+// op hooks: one step of the path alone, on the same kernels as the forward
+// ===========================================================================
+extern "C" fk_status fk_op_rmsnorm(const float* d_x, int32_t rows, int32_t hidden, const void* d_w, float eps,
+                                   void* d_out, void* stream) {
+  if (!d_x || !d_w || !d_out || rows < 1 || hidden < 8 || hidden % 8)
+    return fail(FK_ERR_INVALID_ARG, "fk_op_rmsnorm: need rows >= 1, hidden a positive multiple of 8, non-null buffers");
+  if (!(eps > 0.f) || !std::isfinite(eps)) return fail(FK_ERR_INVALID_ARG, "fk_op_rmsnorm: eps must be > 0");
+  if (!aligned16(d_x) || !aligned16(d_w) || !aligned16(d_out))
+    return fail(FK_ERR_INVALID_ARG, "fk_op_rmsnorm: buffers must be 16-byte aligned");
+  FK_TRY(check_device(nullptr));
+  FK_LAUNCH(launch_rmsnorm(d_x, hidden, rows, hidden, d_w, eps, d_out, hidden, static_cast<cudaStream_t>(stream), 0));
+  return FK_OK;
+}
+
+extern "C" fk_status fk_op_rope(fk_model* m, int32_t layer, void* d_qkv, int32_t batch, int32_t seq, int32_t pos0,
+                                void* d_kcache, void* d_vcache, int32_t cap, void* stream) {
+  if (!m || !d_qkv || !d_kcache || !d_vcache || batch < 1 || seq < 1 || pos0 < 0)
+    return fail(FK_ERR_INVALID_ARG, "fk_op_rope: bad argument");
+  if (layer < 0 || layer >= m->cfg.n_layers) return fail(FK_ERR_INVALID_ARG, "fk_op_rope: layer out of range");
+  if (pos0 + seq > cap || cap % 64) return fail(FK_ERR_INVALID_ARG, "fk_op_rope: need pos0 + seq <= cap, cap % 64 == 0");
+  if (pos0 + seq > m->max_pos) return fail(FK_ERR_CONTEXT_FULL, "fk_op_rope: positions beyond the model's max_positions");
+  if (!aligned16(d_qkv) || !aligned16(d_kcache) || !aligned16(d_vcache))
+    return fail(FK_ERR_INVALID_ARG, "fk_op_rope: buffers must be 16-byte aligned");
+  FK_TRY(check_device(nullptr));
+  const fk_config& c = m->cfg;
+  const fk_layer_weights& w = m->layers[layer];
+  const int kind = m->kinds[layer];
+  FK_LAUNCH(launch_rope_qkv(d_qkv, m->Nqkv, batch * seq, seq, pos0, c.n_q_heads, c.n_kv_heads, c.head_dim,
+                            m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, d_kcache, d_vcache, cap,
+                            static_cast<cudaStream_t>(stream), m->f16(FK_F16_ATTN)));
+  return FK_OK;
+}
+
+extern "C" fk_status fk_op_head_argmax(fk_model* m, const void* d_u, int32_t rows, float* d_logits,
+                                       int32_t* d_argmax, float* d_margin, void* stream) {
+  if (!m || !d_u || !d_logits || rows < 1) return fail(FK_ERR_INVALID_ARG, "fk_op_head_argmax: bad argument");
+  if (d_margin && !d_argmax) return fail(FK_ERR_INVALID_ARG, "fk_op_head_argmax: d_margin needs d_argmax");
+  if (!aligned16(d_u) || !aligned16(d_logits))
+    return fail(FK_ERR_INVALID_ARG, "fk_op_head_argmax: buffers must be 16-byte aligned");
+  FK_TRY(check_device(nullptr));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmOut o;
+  o.epi = EPI_F32;
+  o.out = d_logits;
+  o.ldo = m->cfg.vocab;
+  o.softcap = m->cfg.final_softcap;
+  FK_TRY(gemm_run(d_u, rows, m->cfg.hidden, m->g_head, o, m->dev_err, st));
+  if (d_argmax) FK_LAUNCH(launch_argmax(d_logits, rows, m->cfg.vocab, m->cfg.vocab, d_argmax, st, nullptr, nullptr, d_margin));
   return FK_OK;
 }
 
@@ -763,7 +867,13 @@ extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* 
 // ===========================================================================
 extern "C" fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_ms, uint32_t* flags) {
   if (flags) *flags = 0;
-  if (!m) return fail(FK_ERR_INVALID_ARG, "model is NULL");
+  unsigned* word = nullptr;
+  if (m) {
+    word = m->dev_err;
+  } else {
+    FK_TRY(check_device(nullptr));
+    FK_TRY(op_control_block(&word));
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaEvent_t ev;
   FK_CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
@@ -788,9 +898,9 @@ extern "C" fk_status fk_sync_status(fk_model* m, void* stream, int32_t timeout_m
   }
   cudaEventDestroy(ev);
   unsigned h = 0;
-  FK_CUDA_TRY(cudaMemcpy(&h, m->dev_err, sizeof h, cudaMemcpyDeviceToHost));
+  FK_CUDA_TRY(cudaMemcpy(&h, word, sizeof h, cudaMemcpyDeviceToHost));
   if (h) {
-    FK_CUDA_TRY(cudaMemset(m->dev_err, 0, sizeof h));
+    FK_CUDA_TRY(cudaMemset(word, 0, sizeof h));
     if (flags) *flags = h;
     char buf[96];
     snprintf(buf, sizeof buf, "device error word 0x%x", h);

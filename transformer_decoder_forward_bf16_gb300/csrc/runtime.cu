@@ -67,6 +67,37 @@ fk_status check_device(int* sm_count) {
   return FK_OK;
 }
 
+// The op-level control block: one per device that loads the library (16
+// bytes). Host code reaches it through its device address, looked up once per
+// device with that device current.
+namespace {
+__device__ __align__(16) unsigned g_op_ctl[kCtlWords];
+std::mutex g_ctl_mu;
+unsigned* g_ctl_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+fk_status op_control_block(unsigned** out) {
+  *out = nullptr;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e == cudaErrorInvalidDevice ? cudaErrorNoDevice : e, "cudaGetDevice");
+  }
+  if (dev < 0 || dev >= kMaxDevices) return fail(FK_ERR_INVALID_ARG, "device index out of range");
+  std::lock_guard<std::mutex> lock(g_ctl_mu);
+  if (!g_ctl_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_op_ctl);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(op control block)");
+    e = cudaMemset(p, 0, kCtlWords * sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e, "clear op control block");
+    g_ctl_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_ctl_ptr[dev];
+  return FK_OK;
+}
+
 fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
@@ -221,5 +252,18 @@ extern "C" const char* fk_status_string(fk_status s) {
 }
 
 extern "C" const char* fk_last_error(void) { return fk::g_last_error.c_str(); }
+
+extern "C" fk_status fk_debug_set_op_pipe_fault(int32_t stall_first_stage, int32_t wait_limit_us) {
+  if (wait_limit_us < 0) return fk::fail(FK_ERR_INVALID_ARG, "wait_limit_us must be >= 0");
+  fk_status s = fk::check_device(nullptr);
+  if (s != FK_OK) return s;
+  unsigned* ctl = nullptr;
+  s = fk::op_control_block(&ctl);
+  if (s != FK_OK) return s;
+  const unsigned w[2] = {(unsigned)wait_limit_us, stall_first_stage ? 1u : 0u};
+  cudaError_t e = cudaMemcpy(ctl + 1, w, sizeof w, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fk::cuda_fail(e, "set op control block");
+  return FK_OK;
+}
 
 extern "C" const char* fk_version(void) { return "fk 0.1 sm_103a"; }
