@@ -341,6 +341,28 @@ fk_status fk_op_rope(fk_model* m, int32_t layer, void* d_qkv, int32_t batch, int
 fk_status fk_op_head_argmax(fk_model* m, const void* d_u, int32_t rows, float* d_logits, int32_t* d_argmax,
                             float* d_margin, void* stream);
 
+/* Allocation-free fk_gemm_bf16_splitk. The pages have no counterpart: this
+ * entry point serves callers that cannot hand the library a scratch buffer --
+ * their device memory belongs to another allocator that must remain its only
+ * owner, or their path must never enter the driver's allocation code. The
+ * split partial sums and arrival counters live in one fixed array of
+ * fk_gemm_bf16_splitk_noalloc_limit() bytes (8 MiB) inside the library's
+ * device image, which every GPU that loads the library holds until the
+ * process exits. Arguments and results are those of fk_gemm_bf16_splitk
+ * without the scratch; a shape whose scratch
+ * (fk_gemm_bf16_splitk_scratch_bytes) exceeds the limit is rejected with
+ * FK_ERR_WORKSPACE before anything is launched. The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ * Every call on a device shares the array and leaves its contents behind;
+ * each call clears the counters it needs on its own stream. Calls whose
+ * kernels overlap on the GPU (other streams, other host threads) race on the
+ * array: serialise them. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make it
+ * before any stream capture begins on that device. */
+size_t fk_gemm_bf16_splitk_noalloc_limit(void);
+fk_status fk_gemm_bf16_splitk_noalloc(const void* d_x, const void* d_w, int32_t P, int32_t K, int32_t N, void* d_y,
+                                      int32_t y_fp32, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Testing hook (failure detection)
  * Sets the test controls of the current device's op-level control block:

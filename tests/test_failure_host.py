@@ -86,6 +86,7 @@ def test_no_device_status_without_gpu():
     st = lib.fk_model_create(ctypes.byref(ccfg), ctypes.byref(w), 64, fake, need, ctypes.byref(h))
     assert st == 5, (st, lib.fk_last_error())  # FK_ERR_NO_DEVICE
     assert lib.fk_gemm_bf16(fake, fake, 16, 64, 64, fake, 1, None) == 5
+    assert lib.fk_gemm_bf16_splitk_noalloc(fake, fake, 1, 64, 64, fake, 1, None) == 5
     assert lib.fk_attention_decode(fake, fake, fake, 1, 4, 1, 64, 64, 10, 0, fake, None) == 5
     assert lib.fk_debug_set_op_pipe_fault(0, 0) == 5
 

@@ -88,6 +88,9 @@ _SIGS = {
                                        c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "fk_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
                                       c_int32, c_int32, c_void_p, c_void_p]),
+    "fk_gemm_bf16_splitk_noalloc_limit": (c_size_t, []),
+    "fk_gemm_bf16_splitk_noalloc": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32,
+                                              c_void_p]),
     "fk_debug_set_op_pipe_fault": (c_int32, [c_int32, c_int32]),
     "fk_op_rmsnorm": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_float, c_void_p, c_void_p]),
     "fk_op_rope": (c_int32, [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32,
