@@ -69,6 +69,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (profiling of a small case only)")
     ap.add_argument("--all-configs", action="store_true", help="time the other workloads (A, B, C, E)")
+    ap.add_argument("--no-f16", action="store_true", help="skip the f16 activation-storage timing")
     return ap.parse_args()
 
 
@@ -380,11 +381,12 @@ def main():
     wbits = host_weights(cfg)
     wdev = upload(wbits, dev)
     setup_gen_s = time.time() - t0
-    max_pos = max(PREFILL_S, DECODE_CTX + G * (args.warmup + args.steps) + 8)
+    k16 = max(2, min(args.steps, 5))  # timed steps of the f16-storage pass (after 2 warm-up steps)
+    max_pos = max(PREFILL_S, DECODE_CTX + G * max(args.warmup + args.steps, 2 + k16) + 8)
     model = fk.Model(cfg, wdev, max_positions=max_pos)
-    sp = model.session(PREFILL_B, PREFILL_S, max_chunk=PREFILL_S)
-    sd = model.session(DECODE_B, max_pos, max_chunk=1024)
-    s1 = model.session(1, max_pos, max_chunk=1024)
+    sp = sp0 = model.session(PREFILL_B, PREFILL_S, max_chunk=PREFILL_S)
+    sd = sd0 = model.session(DECODE_B, max_pos, max_chunk=1024)
+    s1 = s10 = model.session(1, max_pos, max_chunk=1024)
     ids_p = torch.from_numpy(synth.make_ids(cfg, PREFILL_B, PREFILL_S, stream=10 + rank)).to(dev)
     ids_d = torch.from_numpy(synth.make_ids(cfg, DECODE_B, DECODE_CTX, stream=50 + rank)).to(dev)
     z_p = torch.empty((PREFILL_B, cfg.vocab), dtype=torch.float32, device=dev)
@@ -400,7 +402,8 @@ def main():
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
-    def step(events=None, profile_prefill=False):
+    def step(events=None, profile_prefill=False, sessions=None):
+        sp, sd, s1 = sessions or (sp0, sd0, s10)
         sp.reset()
         if events:
             events[0].record(stream)
@@ -532,6 +535,42 @@ def main():
         "clocks": clk,
         "setup_s": round(setup_gen_s, 1),
     }
+
+    # ---- the same step with every activation storage site in IEEE f16
+    # (fk_config.f16_sites): the mode that meets the forward-parity gates on
+    # this shape; same tensor-core rate, weights read from f16 copies
+    if not args.no_f16:
+        m16 = fk.Model(cfg.with_(f16_sites=fk.F16_ALL), wdev, max_positions=max_pos)
+        s16 = (m16.session(PREFILL_B, PREFILL_S, max_chunk=PREFILL_S), m16.session(DECODE_B, max_pos, max_chunk=1024),
+               m16.session(1, max_pos, max_chunk=1024))
+        s16[1].prefill(ids_d)
+        s16[2].prefill(ids_d[:1].contiguous())
+        for _ in range(2):
+            step(sessions=s16)
+        ev16 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(k16)]
+        torch.cuda.synchronize()
+        for k in range(k16):
+            step(ev16[k], sessions=s16)
+        torch.cuda.synchronize()
+        p16 = sum(e[0].elapsed_time(e[1]) for e in ev16)
+        d16 = sum(e[1].elapsed_time(e[2]) for e in ev16)
+        d116 = sum(e[2].elapsed_time(e[3]) for e in ev16)
+        p16, d16, d116 = max_over_ranks([p16, d16, d116], device=dev)
+        st16, fl16 = m16.sync_status()
+        if st16 != 0:
+            raise RuntimeError(f"device error word set (f16 storage): {fl16:#x}")
+        line["f16_storage"] = {
+            "f16_sites": "all", "steps": k16,
+            "prefill_tok_s": job_throughput(PREFILL_B * PREFILL_S * k16, world, p16),
+            "prefill_tc_frac": (2.0 * T * (H * (Nq + 2 * Nkv) + Nq * H + 3 * H * I) * cfg.n_layers
+                                / (p16 / k16 / 1e3) / 1e12 / peak_tf),
+            "decode_tok_s": job_throughput(DECODE_B * G * k16, world, d16),
+            "decode_hbm_frac": step_gbs(DECODE_B, d16 * args.steps / k16) / peaks["hbm"],
+            "decode_b1_tok_s": job_throughput(G * k16, world, d116),
+            "decode_b1_hbm_frac": step_gbs(1, d116 * args.steps / k16) / peaks["hbm"]}
+        gpu_launches += (launches // max(1, args.steps) + 2 * G * per_dec_step) * k16
+        line["gpu_launches"] = gpu_launches
+        del s16, m16
 
     # ---- end to end through the public API: host ids in, host result out
     if not args.no_e2e:

@@ -219,9 +219,14 @@ fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int
 
 /* ---------------------------------------------------------------------------
  * KV-cached session ("N7", Thm 1: NewSession().Prefill and greedy Generate)
- * batch sequences of equal length; bf16 K cache [layer][batch][kv_head][cap][head_dim]
- * and transposed V cache [layer][batch][kv_head][head_dim][cap], cap = max_seq
- * rounded up to 64, both cleared when the session is created.
+ * batch sequences of equal length. Per layer a K cache [batch][kv_head][cap]
+ * [head_dim] and a transposed V cache [batch][kv_head][head_dim][cap] (16-bit,
+ * bf16 or f16 as the config stores attention), both cleared when the session
+ * is created; position p lives in slot p mod cap. Global layers: cap = max_seq
+ * rounded up to 64. Sliding-window layers keep a ring: a query reads at most
+ * the last W positions, and a prefill chunk needs the W - 1 positions before
+ * it plus its own, so cap = W + max_chunk - 1 rounded up to 64 (at most the
+ * global cap); decoding past W reuses the ring.
  * Prefill is processed in chunks of at most max_chunk tokens per sequence.
  * ------------------------------------------------------------------------- */
 size_t fk_session_bytes(const fk_model* m, int32_t batch, int32_t max_seq, int32_t max_chunk);
@@ -282,7 +287,9 @@ fk_status fk_gemm_bf16_splitk(const void* d_x, const void* d_w, int32_t P, int32
  *   d_q:   bf16 [batch*seq][n_q_heads*head_dim] (RoPE applied)
  *   caches as for fk_attention_decode (K [batch][n_kv_heads][cap][head_dim],
  *          V transposed [batch][n_kv_heads][head_dim][cap], cap % 64 == 0,
- *          positions up to the next multiple of 128 finite)
+ *          position p in slot p mod cap, every slot finite); either
+ *          pos0 + seq <= cap, or (a sliding-window ring) window > 0 and
+ *          window + seq - 1 <= cap
  *   d_out: bf16 [batch*seq][n_q_heads*head_dim]
  * head_dim 64, 128 or 256, on the tensor-core (tcgen05) kernel. No scratch. */
 fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch, int32_t seq,
@@ -293,17 +300,18 @@ fk_status fk_attention_prefill(const void* d_q, const void* d_kcache, const void
  * Thm 1: causal GQA attention; "pegainfer #878": sliding-window layers).
  *   d_q:      bf16 [batch][n_q_heads*head_dim], the query at position ctx-1
  *   d_kcache: bf16 [batch][n_kv_heads][cap][head_dim], keys at positions
- *             0..ctx-1 (RoPE already applied)
+ *             0..ctx-1 (RoPE already applied), position p in slot p mod cap
  *   d_vcache: bf16 [batch][n_kv_heads][head_dim][cap], values transposed
- *             (position fastest); cap a multiple of 64, and every position
- *             below the next multiple of 64 above ctx must hold finite values
+ *             (position fastest); cap a multiple of 64, every slot finite;
+ *             ctx <= cap, or (a sliding-window ring) window > 0 and
+ *             window <= cap
  *   window:   0 = attend to all ctx keys; W > 0 = only the last W
  *   d_out:    bf16 [batch][n_q_heads*head_dim]
  * Query head h reads kv head h / (n_q_heads/n_kv_heads); scale 1/sqrt(head_dim).
  * Split-KV: the splits of a (sequence, kv head) run as one thread-block
  * cluster and merge their partials in the cluster's shared memory in a fixed
  * order, so results are bitwise reproducible and no scratch memory is used.
- * head_dim is 64, 128 or 256; 1..8 query heads per kv head; 1 <= ctx <= cap. */
+ * head_dim is 64, 128 or 256; 1..8 query heads per kv head. */
 fk_status fk_attention_decode(const void* d_q, const void* d_kcache, const void* d_vcache, int32_t batch,
                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t cap, int32_t ctx,
                               int32_t window, void* d_out, void* stream);
@@ -328,7 +336,9 @@ fk_status fk_op_rmsnorm(const float* d_x, int32_t rows, int32_t hidden, const vo
  * bf16 [batch][n_kv_heads][cap][head_dim] and v, transposed, to d_vcache bf16
  * [batch][n_kv_heads][head_dim][cap] at positions pos0..pos0+seq-1. Other
  * cache positions are untouched. pos0 + seq <= cap, cap % 64 == 0, and
- * pos0 + seq <= the model's max_positions (FK_ERR_CONTEXT_FULL otherwise). */
+ * pos0 + seq <= the model's max_positions (FK_ERR_CONTEXT_FULL otherwise).
+ * d_qkv and the caches hold IEEE f16 instead of bf16 when the model's
+ * f16_sites has FK_F16_ATTN. */
 fk_status fk_op_rope(fk_model* m, int32_t layer, void* d_qkv, int32_t batch, int32_t seq, int32_t pos0,
                      void* d_kcache, void* d_vcache, int32_t cap, void* stream);
 
@@ -337,9 +347,23 @@ fk_status fk_op_rope(fk_model* m, int32_t layer, void* d_qkv, int32_t batch, int
  * [rows][vocab] = softcap(d_u · headᵀ) with the model's (tied or untied)
  * head, d_u bf16 [rows][hidden] (final-norm output); d_argmax (NULL or int32
  * [rows]) the lowest index of each row maximum; d_margin (NULL or fp32 [rows],
- * needs d_argmax) the row maximum minus the largest other logit. */
+ * needs d_argmax) the row maximum minus the largest other logit. d_u is IEEE
+ * f16 instead of bf16 when the model's f16_sites has FK_F16_HEAD_IN. */
 fk_status fk_op_head_argmax(fk_model* m, const void* d_u, int32_t rows, float* d_logits, int32_t* d_argmax,
                             float* d_margin, void* stream);
+
+/* fk_op_logsoftmax_topk ("pegainfer issue #878", Acceptance Criteria: the
+ * distributional gate reads log-probabilities at each position's top-64
+ * ids): for each of `rows` fp32 logit rows (d_logits, row stride ld >= vocab):
+ *   d_lse (NULL or fp32 [rows]):     lse = max + log(sum(exp(z - max)))
+ *   d_top_ids (int32 [rows][k]):     the k largest logits' ids, by value
+ *                                    descending, ties to the lower id
+ *   d_top_logprobs (fp32 [rows][k]): z[id] - lse at those ids
+ *   d_logprobs (NULL or fp32 [rows][vocab]): the whole log-softmax row
+ * 1 <= k <= min(128, vocab). Logits must be finite. */
+fk_status fk_op_logsoftmax_topk(const float* d_logits, int32_t rows, int32_t vocab, int32_t ld, int32_t k,
+                                float* d_lse, int32_t* d_top_ids, float* d_top_logprobs, float* d_logprobs,
+                                void* stream);
 
 /* Allocation-free fk_gemm_bf16_splitk. The pages have no counterpart: this
  * entry point serves callers that cannot hand the library a scratch buffer --

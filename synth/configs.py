@@ -68,7 +68,20 @@ GEMMA3_TOWER = ModelConfig(
     sliding_window=1024, layer_kinds=_gemma_kinds(48), embed_scale="sqrt_hidden_bf16",
     final_softcap=30.0, tied=True)
 
-CONFIGS = {c.name: c for c in (SMOLLM2_135M, LLAMA3_8B, GEMMA3_TOWER)}
+# Family shapes of the same kernels ("N7 · model/forward-parity", Thm 2 family
+# rungs): Qwen3 puts a per-head RMSNorm on q and k before RoPE in a pre-norm
+# layer; Mistral attends through a sliding window on every layer.
+QWEN3_8B = ModelConfig(
+    name="qwen3-8b", n_layers=36, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+    intermediate=12288, vocab=151936, rms_eps=1e-6, rope_theta_global=1000000.0,
+    rope_theta_local=1000000.0, qk_norm=True, tied=False)
+
+MISTRAL_7B = ModelConfig(
+    name="mistral-7b", n_layers=32, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
+    intermediate=14336, vocab=32000, rms_eps=1e-5, rope_theta_global=10000.0, rope_theta_local=10000.0,
+    sliding_window=4096, layer_kinds=(1,) * 32, tied=False)
+
+CONFIGS = {c.name: c for c in (SMOLLM2_135M, LLAMA3_8B, GEMMA3_TOWER, QWEN3_8B, MISTRAL_7B)}
 
 
 def tiny_config(kind: str = "llama", **kw) -> ModelConfig:
@@ -112,6 +125,14 @@ def small_config(kind: str = "llama", **kw) -> ModelConfig:
                            rope_theta_local=10000.0, act="gelu_tanh", norm_layout="sandwich", qk_norm=True,
                            sliding_window=16, layer_kinds=(1, 1, 0), embed_scale="sqrt_hidden_bf16",
                            final_softcap=30.0, tied=True)
+    elif kind == "qwen3":
+        base = ModelConfig(name="small-qwen3", n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                           intermediate=512, vocab=1024, rms_eps=1e-6, rope_theta_global=1000000.0,
+                           rope_theta_local=1000000.0, qk_norm=True, tied=False)
+    elif kind == "mistral":
+        base = ModelConfig(name="small-mistral", n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64,
+                           intermediate=384, vocab=1000, rms_eps=1e-5, rope_theta_global=10000.0,
+                           rope_theta_local=10000.0, sliding_window=32, layer_kinds=(1, 1), tied=False)
     else:
         raise ValueError(kind)
     return replace(base, **kw)

@@ -51,6 +51,9 @@ SMALL_KINDS = {
     # sliding window on a head_dim-64 model (the tensor-core prefill attention path)
     "llama-window": synth.small_config("llama", sliding_window=24, layer_kinds=(1, 0)),
     "llama3-window": synth.small_config("llama3", sliding_window=40, layer_kinds=(0, 1)),
+    # family rungs: QK-norm in a pre-norm layer (Qwen3), a window on every layer (Mistral)
+    "qwen3": synth.small_config("qwen3"),
+    "mistral": synth.small_config("mistral"),
 }
 
 
@@ -101,3 +104,24 @@ def test_token_range_flagged_on_device(fk):
     assert st == 7 and flags & fk.DEVERR_TOKEN_RANGE
     st, flags = model.sync_status()
     assert st == 0 and flags == 0
+
+
+# f16 activation storage: every site alone (the plumbing of each storage point:
+# a kernel that read or wrote a site in the wrong 16-bit format would fail the
+# cosine gate by far), then all sites together
+F16_SITES = {"qkv_in": 0x1, "attn": 0x2, "o_in": 0x4, "ffn_in": 0x8, "ffn_act": 0x10, "head_in": 0x20, "all": 0x3F}
+
+
+@pytest.mark.parametrize("site", sorted(F16_SITES))
+@pytest.mark.parametrize("kind", ["llama3", "gemma"])
+def test_small_models_f16_storage(fk, kind, site):
+    cfg = SMALL_KINDS[kind].with_(f16_sites=F16_SITES[site])
+    r = check_forward(fk, cfg, 2, 70, norm_mode="random", sigma=0.02)
+    print(kind, site, r)
+
+
+@pytest.mark.parametrize("kind", ["llama", "llama-window", "llama3-window"])
+def test_small_models_f16_storage_all_sites(fk, kind):
+    cfg = SMALL_KINDS[kind].with_(f16_sites=F16_SITES["all"])
+    for B, S in ((1, 9), (2, 130)):
+        check_forward(fk, cfg, B, S, norm_mode="random", sigma=0.02)

@@ -15,12 +15,13 @@ def _setup(fk, cfg, norm_mode="random", sigma=0.02):
     return wb, fk.Model(cfg, weights_to_dev(wb), max_positions=512)
 
 
-@pytest.mark.parametrize("kind,chunk", [("llama", 48), ("llama3", 48), ("gemma", 48), ("llama", 45), ("llama3", 37)])
-def test_cached_prefill_matches_cacheless(fk, kind, chunk):
+@pytest.mark.parametrize("kind,chunk,f16", [("llama", 48, 0), ("llama3", 48, 0), ("gemma", 48, 0), ("llama", 45, 0),
+                                            ("llama3", 37, 0), ("gemma", 45, 0x3F), ("llama3", 48, 0x3F)])
+def test_cached_prefill_matches_cacheless(fk, kind, chunk, f16):
     """Chunks of 48 start at positions that are multiples of 8 (the V cache
     takes 16-byte runs); 45 and 37 exercise the unaligned element path."""
     import torch
-    cfg = synth.small_config(kind)
+    cfg = synth.small_config(kind, f16_sites=f16)
     wb, model = _setup(fk, cfg)
     B, S = 2, 100
     ids = synth.make_ids(cfg, B, S)
@@ -35,10 +36,11 @@ def test_cached_prefill_matches_cacheless(fk, kind, chunk):
     assert sess.length == S
 
 
-@pytest.mark.parametrize("kind", ["llama", "llama3", "gemma"])
-def test_decode_matches_oracle(fk, kind):
+@pytest.mark.parametrize("kind,f16", [("llama", 0), ("llama3", 0), ("gemma", 0), ("llama3", 0x3F), ("gemma", 0x3F),
+                                      ("qwen3", 0), ("qwen3", 0x3F), ("mistral", 0)])
+def test_decode_matches_oracle(fk, kind, f16):
     import torch
-    cfg = synth.small_config(kind)
+    cfg = synth.small_config(kind, f16_sites=f16)
     wb, model = _setup(fk, cfg)
     B, S, steps = 3, 21, 12
     prompt = synth.make_ids(cfg, B, S)
@@ -109,3 +111,64 @@ def test_graph_decode_equals_launched_decode(fk):
         torch.cuda.synchronize()
         assert torch.equal(za, zb) and torch.equal(na, nb)
     assert a.length == b.length == 38
+
+
+@pytest.mark.parametrize("kind,f16", [("gemma", 0), ("gemma", 0x3F), ("llama-window", 0), ("mistral", 0),
+                                      ("mistral", 0x3F)])
+def test_sliding_window_ring_cache_past_the_window(fk, kind, f16):
+    """Sliding-window layers keep a ring of W + max_chunk - 1 positions
+    (rounded up to 64): prefill 100 ids in chunks of 16 and decode 40 greedy
+    steps past it, so a W = 16 (or 24) window is non-vacuous and the 64-slot
+    ring wraps twice; every step against the exact oracle ("N7 ·
+    model/forward-parity", Thm 2: sliding-window layers; "pegainfer issue
+    #878": the window edge)."""
+    import torch
+    if kind == "llama-window":
+        cfg = synth.small_config("llama", sliding_window=24, layer_kinds=(1, 0))
+    else:
+        cfg = synth.small_config(kind, f16_sites=f16)
+    wb, model = _setup(fk, cfg)
+    lib = fk.load()
+    B, S, steps, chunk, max_seq = 2, 100, 40, 16, 160
+    # the session is smaller than one with every layer global by exactly the
+    # ring's savings: 2 caches x B x Hkv x hd x 2 bytes x (global - ring) positions
+    all_global = cfg.with_(layer_kinds=tuple(0 for _ in cfg.kinds()))
+    m_glob = fk.Model(all_global, model.weights, max_positions=512)
+    n_local = sum(1 for k in cfg.kinds() if k == 1)
+    ring = (cfg.sliding_window + chunk - 1 + 63) // 64 * 64
+    glob = (max_seq + 63) // 64 * 64
+    saved = 2 * B * cfg.n_kv_heads * cfg.head_dim * 2 * (glob - ring) * n_local
+    assert lib.fk_session_bytes(m_glob.handle, B, max_seq, chunk) - lib.fk_session_bytes(model.handle, B, max_seq,
+                                                                                         chunk) == saved
+    prompt = synth.make_ids(cfg, B, S, stream=7)
+    ref = oracle.greedy(cfg, wb, prompt, steps)
+    sess = model.session(B, max_seq, max_chunk=chunk)
+    z = torch.empty((B, cfg.vocab), dtype=torch.float32, device="cuda")
+    nxt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    sess.prefill(prompt, logits=z, next_ids=nxt)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(z.cpu().numpy(), ref["first_logits"], atol=0.05)
+    got = [nxt.cpu().numpy().copy()]
+    worst = 0.0
+    for t in range(steps):
+        feed = torch.from_numpy(ref["ids"][t].astype(np.int32)).cuda()  # teacher forcing
+        sess.decode(feed, logits=z, next_ids=nxt)
+        got.append(nxt.cpu().numpy().copy())
+    got = np.stack(got)
+    decided = ref["margins"] > 1e-2
+    np.testing.assert_array_equal(got[decided], ref["ids"][decided])
+    np.testing.assert_allclose(z.cpu().numpy(), ref["last_logits"], atol=0.05)
+    # free-running greedy from the ring (graph replay) matches the oracle's ids
+    sess.reset()
+    sess.prefill(prompt, logits=z, next_ids=nxt)
+    free = [nxt.cpu().numpy().copy()]
+    for t in range(steps):
+        sess.decode(None, logits=z, next_ids=nxt)
+        free.append(nxt.cpu().numpy().copy())
+    free = np.stack(free)
+    for b in range(B):
+        mism = np.nonzero(free[:, b] != ref["ids"][:, b])[0]
+        if len(mism):
+            assert ref["margins"][mism[0], b] <= 1e-2, (b, mism[0], ref["margins"][mism[0], b])
+    st, flags = model.sync_status()
+    assert st == 0, flags

@@ -96,6 +96,8 @@ _SIGS = {
     "fk_op_rope": (c_int32, [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32,
                              c_void_p]),
     "fk_op_head_argmax": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "fk_op_logsoftmax_topk": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p]),
     "fk_profile_enable": (None, [c_int32]),
     "fk_profile_reset": (None, []),
     "fk_profile_count": (c_int32, []),
@@ -240,6 +242,23 @@ def rmsnorm(x, w, eps: float, out=None, stream=None):
         out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=x.device)
     _check(load().fk_op_rmsnorm(_ptr(x), rows, hidden, _ptr(w), eps, _ptr(out), _stream_ptr(stream)),
            "fk_op_rmsnorm")
+    return out
+
+
+def logsoftmax_topk(z, k: int = 64, logprobs: bool = False, stream=None) -> dict:
+    """fk_op_logsoftmax_topk on fp32 logit rows z [rows, vocab]: lse, the top-k
+    ids (value descending, ties to the lower id), their log-probabilities and
+    optionally the whole log-softmax."""
+    import torch
+    rows, V = z.shape
+    dev = z.device
+    out = {"lse": torch.empty((rows,), dtype=torch.float32, device=dev),
+           "ids": torch.empty((rows, k), dtype=torch.int32, device=dev),
+           "top_logprobs": torch.empty((rows, k), dtype=torch.float32, device=dev),
+           "logprobs": torch.empty((rows, V), dtype=torch.float32, device=dev) if logprobs else None}
+    _check(load().fk_op_logsoftmax_topk(_ptr(z), rows, V, z.stride(0), k, _ptr(out["lse"]), _ptr(out["ids"]),
+                                        _ptr(out["top_logprobs"]), _ptr(out["logprobs"]), _stream_ptr(stream)),
+           "fk_op_logsoftmax_topk")
     return out
 
 

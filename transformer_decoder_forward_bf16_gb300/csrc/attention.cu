@@ -117,13 +117,13 @@ struct DecArgs {
   float eps;
   uint16_t* kc_w;  // the caches, written at position ctx-1
   uint16_t* vc_w;
-  int io_f16;   // q, k, v, the caches and the probabilities are IEEE f16 (else bf16)
+  int io_f16;   // q, k, v, the caches and the probabilities are IEEE f16 (else bf16): picks the kernel
   int out_f16;  // the output is stored as f16 (else bf16)
 };
 
 // [QK-norm and] RoPE of one head held by a warp: lane owns elements
 // e0..e0+C-1 of each half (pairs (j, j+HD/2)); cs: this lane's (cos, sin).
-template <int HD>
+template <int HD, bool F16>
 FK_DEVICE void rope_head(const uint16_t* src, const DecArgs& a, const __nv_bfloat16* nw, const float2* cs,
                          int lane, float* olo, float* ohi) {
   constexpr int C = HD / 64, HALF = HD / 2;
@@ -131,8 +131,8 @@ FK_DEVICE void rope_head(const uint16_t* src, const DecArgs& a, const __nv_bfloa
   float lo[C], hi[C];
 #pragma unroll
   for (int i = 0; i < C; ++i) {
-    lo[i] = load_16(src + e0 + i, a.io_f16);
-    hi[i] = load_16(src + HALF + e0 + i, a.io_f16);
+    lo[i] = load_16(src + e0 + i, F16);
+    hi[i] = load_16(src + HALF + e0 + i, F16);
   }
   if (a.qk_norm) {
     float ss = 0.f;
@@ -153,10 +153,11 @@ FK_DEVICE void rope_head(const uint16_t* src, const DecArgs& a, const __nv_bfloa
   }
 }
 
-template <int HD, bool ROPE>
+template <int HD, bool ROPE, bool F16>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const DecArgs a) {
+  constexpr int io_f16 = F16 ? 1 : 0;  // q, k, v, the caches and P are IEEE f16 (else bf16)
   using C = DecCfg<HD>;
   constexpr int NC = HD / 64, HALF = HD / 2;
   extern __shared__ uint8_t smem_raw[];
@@ -224,8 +225,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         const int pos = t0 + t * kDecTile;
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-          tma_load_2d(&tmK, &full[stage], sk + c * kDecTile * 64 * 2, c * 64, head_row * cap + pos);
-        tma_load_2d(&tmV, &full[stage], sv, pos, head_row * HD);
+          tma_load_2d(&tmK, &full[stage], sk + c * kDecTile * 64 * 2, c * 64, head_row * cap + pos % cap);
+        tma_load_2d(&tmV, &full[stage], sv, pos % cap, head_row * HD);
         ++issued[stage];
       }
       // leave only when every requested tile has landed
@@ -250,24 +251,24 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
       for (int r = warp; r < 16; r += kDecConsumers / 32) {
         float olo[NC], ohi[NC];
         if (r < group) {
-          rope_head<HD>(row + (size_t)(g * group + r) * HD, a, a.q_norm, cs, lane, olo, ohi);
+          rope_head<HD, F16>(row + (size_t)(g * group + r) * HD, a, a.q_norm, cs, lane, olo, ohi);
         } else {
 #pragma unroll
           for (int i = 0; i < NC; ++i) olo[i] = ohi[i] = 0.f;
         }
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
-          sQ[swz<HD>(r, lane * NC + i)] = bits_16(olo[i], a.io_f16);
-          sQ[swz<HD>(r, HALF + lane * NC + i)] = bits_16(ohi[i], a.io_f16);
+          sQ[swz<HD>(r, lane * NC + i)] = bits_16(olo[i], io_f16);
+          sQ[swz<HD>(r, HALF + lane * NC + i)] = bits_16(ohi[i], io_f16);
         }
       }
       if (warp == 0) {
         float olo[NC], ohi[NC];
-        rope_head<HD>(row + (size_t)(Hq + g) * HD, a, a.k_norm, cs, lane, olo, ohi);
+        rope_head<HD, F16>(row + (size_t)(Hq + g) * HD, a, a.k_norm, cs, lane, olo, ohi);
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
-          sNew[0][lane * NC + i] = bits_16(olo[i], a.io_f16);
-          sNew[0][HALF + lane * NC + i] = bits_16(ohi[i], a.io_f16);
+          sNew[0][lane * NC + i] = bits_16(olo[i], io_f16);
+          sNew[0][HALF + lane * NC + i] = bits_16(ohi[i], io_f16);
         }
       } else if (warp == 1) {
         const uint16_t* vs = row + (size_t)(Hq + Hkv + g) * HD;
@@ -275,8 +276,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
       }
       consumers_sync();
       if (t_new >= 0 && t_new < ntiles) {  // the one CTA whose tiles hold the new token stores it
-        uint16_t* kw = a.kc_w + ((size_t)head_row * cap + qpos) * HD;
-        uint16_t* vw = a.vc_w + (size_t)head_row * HD * cap + qpos;
+        uint16_t* kw = a.kc_w + ((size_t)head_row * cap + qpos % cap) * HD;
+        uint16_t* vw = a.vc_w + (size_t)head_row * HD * cap + qpos % cap;
         for (int d = tid; d < HD; d += kDecConsumers) {
           kw[d] = sNew[0][d];
           vw[(size_t)d * cap] = sNew[1][d];
@@ -317,8 +318,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         uint32_t qa[4], bb[4];
         ldsm_x4(qa, sQ + swz<HD>(mr + (mat & 1) * 8, k0 + (mat >> 1) * 8));
         ldsm_x4(bb, tK + kswz<HD>(kr + mr + (mat >> 1) * 8, k0 + (mat & 1) * 8));
-        mma_16816(s[0], qa, bb[0], bb[1], a.io_f16);
-        mma_16816(s[1], qa, bb[2], bb[3], a.io_f16);
+        mma_16816(s[0], qa, bb[0], bb[1], io_f16);
+        mma_16816(s[1], qa, bb[2], bb[3], io_f16);
       }
       const int key0 = t0 + t * kDecTile + kr + 2 * (lane & 3);
       float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -356,10 +357,10 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
       l0 = l0 * corr0 + rs0;
       l1 = l1 * corr1 + rs1;
       uint32_t pa[4];
-      pa[0] = pack_16x2(s[0][0], s[0][1], a.io_f16);
-      pa[1] = pack_16x2(s[0][2], s[0][3], a.io_f16);
-      pa[2] = pack_16x2(s[1][0], s[1][1], a.io_f16);
-      pa[3] = pack_16x2(s[1][2], s[1][3], a.io_f16);
+      pa[0] = pack_16x2(s[0][0], s[0][1], io_f16);
+      pa[1] = pack_16x2(s[0][2], s[0][3], io_f16);
+      pa[2] = pack_16x2(s[1][0], s[1][1], io_f16);
+      pa[3] = pack_16x2(s[1][2], s[1][3], io_f16);
 #pragma unroll
       for (int dp = 0; dp < HD / 16; ++dp) {
         oacc[2 * dp][0] *= corr0;
@@ -372,8 +373,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
         oacc[2 * dp + 1][3] *= corr1;
         uint32_t bb[4];
         ldsm_x4(bb, tV + swz<kDecTile>(dp * 16 + mr + (mat >> 1) * 8, kr + (mat & 1) * 8));
-        mma_16816(oacc[2 * dp], pa, bb[0], bb[1], a.io_f16);
-        mma_16816(oacc[2 * dp + 1], pa, bb[2], bb[3], a.io_f16);
+        mma_16816(oacc[2 * dp], pa, bb[0], bb[1], io_f16);
+        mma_16816(oacc[2 * dp + 1], pa, bb[2], bb[3], io_f16);
       }
       if (patch) fence_proxy_async_smem();  // generic writes before the slot is refilled by TMA
       __syncwarp();
@@ -476,13 +477,13 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(const __grid_c
 
 // Largest cluster of decode CTAs the GPU co-schedules for this head_dim
 // (a cluster of 16 is beyond the portable size and is allowed explicitly).
-template <int HD, bool ROPE>
+template <int HD, bool ROPE, bool F16>
 cudaError_t decode_attrs() {
   using C = DecCfg<HD>;
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<HD, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<HD, ROPE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_decode_kernel<HD, ROPE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(attn_decode_kernel<HD, ROPE, F16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
@@ -494,16 +495,18 @@ int decode_max_cluster(cudaError_t* err) {
   int dev = 0;
   cudaGetDevice(&dev);
   *err = once.run([dev] {
-    cudaError_t e0 = decode_attrs<HD, false>();
-    if (e0 == cudaSuccess) e0 = decode_attrs<HD, true>();
+    cudaError_t e0 = decode_attrs<HD, false, false>();
+    if (e0 == cudaSuccess) e0 = decode_attrs<HD, true, false>();
+    if (e0 == cudaSuccess) e0 = decode_attrs<HD, false, true>();
+    if (e0 == cudaSuccess) e0 = decode_attrs<HD, true, true>();
     if (e0 != cudaSuccess) return e0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kMaxCluster, 1, 1);
     cfg.blockDim = dim3(kDecThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     int c = 0, c2 = 0;
-    if (cudaOccupancyMaxPotentialClusterSize(&c, attn_decode_kernel<HD, false>, &cfg) != cudaSuccess ||
-        cudaOccupancyMaxPotentialClusterSize(&c2, attn_decode_kernel<HD, true>, &cfg) != cudaSuccess || c < 1 ||
+    if (cudaOccupancyMaxPotentialClusterSize(&c, attn_decode_kernel<HD, false, false>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxPotentialClusterSize(&c2, attn_decode_kernel<HD, true, false>, &cfg) != cudaSuccess || c < 1 ||
         c2 < 1) {
       cudaGetLastError();
       c = c2 = 8;  // the portable size
@@ -557,9 +560,9 @@ cudaError_t decode_hd(const void* kcache, const void* vcache, const DecArgs& a, 
       make_tmap_bf16(&tV, vcache, (int64_t)B * a.Hkv * HD, a.cap, a.cap, HD) != FK_OK)
     return cudaErrorInvalidValue;
   const dim3 grid(n_splits, a.Hkv, B);
-  if (rope)
-    return fk_launch_cluster(attn_decode_kernel<HD, true>, grid, kDecThreads, C::SMEM, st, n_splits, tK, tV, a);
-  return fk_launch_cluster(attn_decode_kernel<HD, false>, grid, kDecThreads, C::SMEM, st, n_splits, tK, tV, a);
+  auto kernel = rope ? (a.io_f16 ? attn_decode_kernel<HD, true, true> : attn_decode_kernel<HD, true, false>)
+                     : (a.io_f16 ? attn_decode_kernel<HD, false, true> : attn_decode_kernel<HD, false, false>);
+  return fk_launch_cluster(kernel, grid, kDecThreads, C::SMEM, st, n_splits, tK, tV, a);
 }
 
 cudaError_t decode_dispatch(const void* kcache, const void* vcache, const DecArgs& a, bool rope, int hd, int B,
@@ -637,8 +640,8 @@ extern "C" fk_status fk_attention_decode(const void* d_q, const void* d_kcache, 
     return fail(FK_ERR_INVALID_ARG, "attention decode: need batch >= 1 and 1..8 query heads per kv head");
   if (head_dim != 64 && head_dim != 128 && head_dim != 256)
     return fail(FK_ERR_INVALID_ARG, "attention decode: head_dim 64/128/256");
-  if (ctx < 1 || ctx > cap || window < 0 || cap % 64)
-    return fail(FK_ERR_INVALID_ARG, "attention decode: need 1 <= ctx <= cap, cap a multiple of 64");
+  if (ctx < 1 || window < 0 || cap < 64 || cap % 64 || (ctx > cap && (window == 0 || window > cap)))
+    return fail(FK_ERR_INVALID_ARG, "attention decode: need cap % 64 == 0 and 1 <= ctx <= cap (or window <= cap)");
   if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_kcache) |
        reinterpret_cast<uintptr_t>(d_vcache) | reinterpret_cast<uintptr_t>(d_out)) & 15)
     return fail(FK_ERR_INVALID_ARG, "attention decode: buffers must be 16-byte aligned");

@@ -83,11 +83,12 @@ FK_DEVICE float fast_exp2(float x) {
   return y;
 }
 
-template <int HD>
+template <int HD, bool F16>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, int S, int pos0, int Hq, int Hkv, int cap, int window,
-                   float scale_log2, uint16_t* __restrict__ out, unsigned* dev_err, int io_f16, int out_f16) {
+                   float scale_log2, uint16_t* __restrict__ out, unsigned* dev_err, int out_f16) {
+  constexpr int io_f16 = F16 ? 1 : 0;  // q, K, Vᵀ and P are IEEE f16 (else bf16)
   using C = FaCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // the swizzled tiles need 1024-byte alignment
@@ -173,10 +174,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           mbar_arrive_expect_tx(&full[st], C::K_BYTES);
 #pragma unroll
           for (int blk = 0; blk < HD / 64; ++blk)
-            tma_load_2d(&tmK, &full[st], sK + st * C::K_BYTES + blk * BKV * 128, blk * 64, krow + kb * BKV);
+            tma_load_2d(&tmK, &full[st], sK + st * C::K_BYTES + blk * BKV * 128, blk * 64, krow + (kb * BKV) % cap);
         } else {
           mbar_arrive_expect_tx(&full[st], C::V_BYTES);
-          tma_load_2d(&tmV, &full[st], sV + st * C::V_BYTES, kb * BKV, vrow);
+          tma_load_2d(&tmV, &full[st], sV + st * C::V_BYTES, (kb * BKV) % cap, vrow);
         }
         ++issued[st];
       }
@@ -354,8 +355,12 @@ fk_status launch_tc(const void* q, int ldq, const void* kc, const void* vc, int 
                     int out_f16) {
   using C = FaCfg<HD>;
   static DeviceOnce once;
-  const cudaError_t attr = once.run(
-      [] { return cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
+  const cudaError_t attr = once.run([] {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_tc_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    return e;
+  });
   if (attr != cudaSuccess) return cuda_fail(attr, "cudaFuncSetAttribute(attn_tc)");
   CUtensorMap tQ, tK, tV;
   fk_status s = make_tmap_bf16(&tQ, q, (int64_t)B * S, ldq, ldq, BQ);
@@ -363,9 +368,9 @@ fk_status launch_tc(const void* q, int ldq, const void* kc, const void* vc, int 
   if (s == FK_OK) s = make_tmap_bf16(&tV, vc, (int64_t)B * Hkv * HD, cap, cap, HD);
   if (s != FK_OK) return s;
   const int nqb = (S + BQ - 1) / BQ;
-  attn_tc_kernel<HD><<<dim3(Hq * B, nqb), kThreads, C::SMEM, st>>>(tQ, tK, tV, S, pos0, Hq, Hkv, cap, window,
-                                                                   scale * kLog2e, static_cast<uint16_t*>(o),
-                                                                   dev_err, io_f16, out_f16);
+  auto kernel = io_f16 ? attn_tc_kernel<HD, true> : attn_tc_kernel<HD, false>;
+  kernel<<<dim3(Hq * B, nqb), kThreads, C::SMEM, st>>>(tQ, tK, tV, S, pos0, Hq, Hkv, cap, window, scale * kLog2e,
+                                                       static_cast<uint16_t*>(o), dev_err, out_f16);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_tc_kernel launch");
   return FK_OK;
@@ -402,7 +407,11 @@ extern "C" fk_status fk_attention_prefill(const void* d_q, const void* d_kcache,
     return fail(FK_ERR_INVALID_ARG, "attention prefill: n_q_heads must be a multiple of n_kv_heads");
   if (head_dim != 64 && head_dim != 128 && head_dim != 256)
     return fail(FK_ERR_INVALID_ARG, "attention prefill: head_dim 64/128/256");
-  if (pos0 + seq > cap || cap % 64) return fail(FK_ERR_INVALID_ARG, "attention prefill: need pos0 + seq <= cap, cap % 64 == 0");
+  // position p lives in slot p mod cap: every key a query reads must still be
+  // there, so either nothing wrapped or the window plus the chunk fits
+  if (cap < 64 || cap % 64 || (pos0 + seq > cap && (window == 0 || window + seq - 1 > cap)))
+    return fail(FK_ERR_INVALID_ARG,
+                "attention prefill: need cap % 64 == 0 and pos0 + seq <= cap (or window + seq - 1 <= cap)");
   if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_kcache) |
        reinterpret_cast<uintptr_t>(d_vcache) | reinterpret_cast<uintptr_t>(d_out)) & 15)
     return fail(FK_ERR_INVALID_ARG, "attention prefill: buffers must be 16-byte aligned");

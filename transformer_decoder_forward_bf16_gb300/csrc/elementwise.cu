@@ -286,7 +286,7 @@ __global__ void rope_qkv_kernel(uint16_t* qkv, int ldqkv, int T, int S, int pos0
     dst = row;
   } else {
     const int g = h - Hq;
-    dst = kcache + (((size_t)b * Hkv + g) * cap + pos) * HD;
+    dst = kcache + (((size_t)b * Hkv + g) * cap + pos % cap) * HD;  // position p lives in slot p mod cap
   }
 #pragma unroll
   for (int i = 0; i < C; ++i) {
@@ -321,12 +321,16 @@ __global__ void __launch_bounds__(256) v_cache_kernel(const __nv_bfloat16* __res
     t32[3] = v.w;
   }
   __syncthreads();
-  __nv_bfloat16* dst = vcache + ((size_t)b * Hkv + g) * HD * cap + pos0 + s0;
-  if (((pos0 + s0) & 7) == 0) {  // 16-byte aligned runs: 8 positions per store
+  // position P lives in slot P mod cap (cap a multiple of 64: a ring for
+  // sliding-window layers, larger than every position otherwise)
+  __nv_bfloat16* dst = vcache + ((size_t)b * Hkv + g) * HD * cap;
+  const int P0 = pos0 + s0;
+  if ((P0 & 7) == 0) {  // 16-byte aligned runs: 8 positions per store, never across the wrap
     constexpr int CPD = kVTile / 8;
     for (int i = threadIdx.x; i < HD * CPD; i += blockDim.x) {
       const int d = i / CPD, p = (i % CPD) * 8;
       if (p >= n) continue;
+      __nv_bfloat16* row = dst + (size_t)d * cap;
       if (p + 8 <= n) {
         uint32_t w[4];
 #pragma unroll
@@ -335,15 +339,15 @@ __global__ void __launch_bounds__(256) v_cache_kernel(const __nv_bfloat16* __res
           const uint16_t hi = reinterpret_cast<const uint16_t&>(tile[(p + 2 * j + 1) * LD + d]);
           w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
         }
-        *reinterpret_cast<uint4*>(dst + (size_t)d * cap + p) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(row + (P0 + p) % cap) = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
-        for (int j = p; j < n; ++j) dst[(size_t)d * cap + j] = tile[j * LD + d];
+        for (int j = p; j < n; ++j) row[(P0 + j) % cap] = tile[j * LD + d];
       }
     }
   } else {
     for (int i = threadIdx.x; i < HD * kVTile; i += blockDim.x) {
       const int d = i / kVTile, p = i % kVTile;
-      if (p < n) dst[(size_t)d * cap + p] = tile[p * LD + d];
+      if (p < n) dst[(size_t)d * cap + (P0 + p) % cap] = tile[p * LD + d];
     }
   }
 }

@@ -74,10 +74,16 @@ struct fk_session {
   fk_model* m = nullptr;
   int B = 0, max_seq = 0, max_chunk = 0;
   int len = 0;
-  __nv_bfloat16* kcache = nullptr;  // [L][B][Hkv][max_seq][hd]
-  __nv_bfloat16* vcache = nullptr;
-  size_t layer_kv = 0;  // elements per layer
-  int cap = 0;          // cache positions per (sequence, kv head): max_seq rounded up to 64
+  // per layer l: K cache [B][Hkv][cap_l][hd] at kcache + kv_off[l] bytes, V
+  // cache transposed [B][Hkv][hd][cap_l] at vcache + kv_off[l]. Position p
+  // lives in slot p mod cap_l: cap_l is max_seq rounded up to 64 on global
+  // layers and a ring of W + max_chunk - 1 positions (rounded up to 64, at
+  // most the global cap) on sliding-window layers.
+  uint8_t* kcache = nullptr;
+  uint8_t* vcache = nullptr;
+  std::vector<size_t> kv_off;
+  std::vector<int> kv_cap;
+  size_t kv_bytes = 0;  // bytes of all layers' K caches (= of the V caches)
   Scratch sc;
   int32_t* next_ids = nullptr;  // [B]
   float* logits = nullptr;      // [B, V]
@@ -239,11 +245,15 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
 }
 
 struct KV {
-  __nv_bfloat16* k;     // [B][Hkv][cap][hd]
-  __nv_bfloat16* v;     // transposed: [B][Hkv][hd][cap]
-  size_t layer_stride;  // elements between layers (0: one buffer reused by every layer)
-  int cap;              // positions per (sequence, kv head), a multiple of 64
-  size_t bytes = 0;     // bytes of one of k / v (all layers)
+  uint8_t* k = nullptr;           // [B][Hkv][cap][hd] per layer
+  uint8_t* v = nullptr;           // transposed: [B][Hkv][hd][cap] per layer
+  const size_t* off = nullptr;    // per-layer byte offsets (null: one buffer reused by every layer)
+  const int* caps = nullptr;      // per-layer capacities (null: `cap` on every layer)
+  int cap = 0;                    // positions per (sequence, kv head), a multiple of 64
+  size_t bytes = 0;               // bytes of one of k / v (all layers)
+  void* kl(int l) const { return k + (off ? off[l] : 0); }
+  void* vl(int l) const { return v + (off ? off[l] : 0); }
+  int cap_of(int l) const { return caps ? caps[l] : cap; }
 };
 
 #define FK_LAUNCH(expr)                                 \
@@ -287,8 +297,9 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     const void* next_norm = l + 1 < L ? m->layers[l + 1].attn_norm : m->final_norm;
     // the next norm output feeds the next layer's QKV projection, or the LM head
     const int next_f16 = l + 1 < L ? m->f16(FK_F16_QKV_IN) : m->f16(FK_F16_HEAD_IN);
-    __nv_bfloat16* kl = kv.k + kv.layer_stride * l;
-    __nv_bfloat16* vl = kv.v + kv.layer_stride * l;
+    void* kl = kv.kl(l);
+    void* vl = kv.vl(l);
+    const int cap = kv.cap_of(l);
 
     GemmOut o;
     o.epi = EPI_BF16;
@@ -298,17 +309,17 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
     if (decode) {  // RoPE, cache write and attention in one kernel
       ProfScope ps("attn_decode", st);
-      FK_LAUNCH(launch_attention_decode_rope(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, d_len, c.n_q_heads, c.n_kv_heads,
+      FK_LAUNCH(launch_attention_decode_rope(sc.qkv, m->Nqkv, kl, vl, cap, B, d_len, c.n_q_heads, c.n_kv_heads,
                                              hd, window, m->attn_scale, m->rope[kind], c.qk_norm, w.q_norm, w.k_norm,
                                              c.rms_eps, dsplits, sc.ao, m->dev_err, st, m->f16(FK_F16_ATTN),
                                              m->f16(FK_F16_O_IN)));
     } else {
       { ProfScope ps("rope_qkv", st);
       FK_LAUNCH(launch_rope_qkv(sc.qkv, m->Nqkv, (int)T, S, pos0, c.n_q_heads, c.n_kv_heads, hd,
-                                m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, kv.cap, st,
+                                m->rope[kind], c.qk_norm, w.q_norm, w.k_norm, c.rms_eps, kl, vl, cap, st,
                                 m->f16(FK_F16_ATTN))); }
       ProfScope ps("attn_prefill", st);
-      FK_TRY(attention_prefill_tc(sc.qkv, m->Nqkv, kl, vl, kv.cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd, window,
+      FK_TRY(attention_prefill_tc(sc.qkv, m->Nqkv, kl, vl, cap, B, S, pos0, c.n_q_heads, c.n_kv_heads, hd, window,
                                   m->attn_scale, sc.ao, m->dev_err, st, m->f16(FK_F16_ATTN), m->f16(FK_F16_O_IN)));
     }
     // attention output projection + residual
@@ -547,9 +558,8 @@ static size_t forward_layout(const fk_model* m, int B, int S, uint8_t* base, Scr
   const int cap = (S + 63) / 64 * 64;  // attention tiles read whole 64-position blocks
   const size_t kv_elems = (size_t)B * c.n_kv_heads * cap * c.head_dim;
   if (kv) {
-    kv->k = base ? reinterpret_cast<__nv_bfloat16*>(base + off) : nullptr;
-    kv->v = base ? reinterpret_cast<__nv_bfloat16*>(base + off + align_up(kv_elems * 2)) : nullptr;
-    kv->layer_stride = 0;
+    kv->k = base ? base + off : nullptr;
+    kv->v = base ? base + off + align_up(kv_elems * 2) : nullptr;
     kv->cap = cap;
     kv->bytes = kv_elems * 2;
   }
@@ -599,6 +609,19 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
 // ===========================================================================
 // sessions
 // ===========================================================================
+// Cache positions of layer l in a session: max_seq rounded up to 64 on global
+// layers. A sliding-window layer reads at most the last W positions before a
+// query, so it keeps a ring: position p in slot p mod cap. A prefill chunk of
+// C tokens needs the W - 1 positions before it and its own C at once, so the
+// ring holds W + max_chunk - 1 positions (rounded up to 64 for the 64-position
+// attention tiles), never more than the global capacity.
+static int layer_cache_positions(const fk_model* m, int l, int max_seq, int max_chunk) {
+  const int global = (max_seq + 63) / 64 * 64;
+  if (m->kinds[l] != 1) return global;
+  const int ring = (m->cfg.sliding_window + max_chunk - 1 + 63) / 64 * 64;
+  return std::min(global, ring);
+}
+
 static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chunk, uint8_t* base, fk_session* s) {
   const fk_config& c = m->cfg;
   size_t off = 0;
@@ -607,10 +630,16 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
     off += align_up(bytes);
     return p;
   };
-  const int cap = (max_seq + 63) / 64 * 64;
-  const size_t layer_kv = (size_t)B * c.n_kv_heads * cap * c.head_dim;
-  uint8_t* k = take(layer_kv * c.n_layers * 2);
-  uint8_t* v = take(layer_kv * c.n_layers * 2);
+  std::vector<size_t> kv_off(c.n_layers);
+  std::vector<int> kv_cap(c.n_layers);
+  size_t kv_bytes = 0;
+  for (int l = 0; l < c.n_layers; ++l) {
+    kv_cap[l] = layer_cache_positions(m, l, max_seq, max_chunk);
+    kv_off[l] = kv_bytes;
+    kv_bytes += align_up((size_t)B * c.n_kv_heads * kv_cap[l] * c.head_dim * 2);
+  }
+  uint8_t* k = take(kv_bytes);
+  uint8_t* v = take(kv_bytes);
   const long T = (long)B * max_chunk;
   Scratch sc;
   const size_t sb = scratch_bytes(m, T, &sc, base ? base + off : nullptr);
@@ -622,10 +651,11 @@ static size_t session_layout(const fk_model* m, int B, int max_seq, int max_chun
   uint8_t* dl = take(sizeof(int));
   if (s) {
     s->d_len = reinterpret_cast<int*>(dl);
-    s->kcache = reinterpret_cast<__nv_bfloat16*>(k);
-    s->vcache = reinterpret_cast<__nv_bfloat16*>(v);
-    s->layer_kv = layer_kv;
-    s->cap = cap;
+    s->kcache = k;
+    s->vcache = v;
+    s->kv_off = kv_off;
+    s->kv_cap = kv_cap;
+    s->kv_bytes = kv_bytes;
     s->sc = sc;
     s->next_ids = reinterpret_cast<int32_t*>(next);
     s->logits = reinterpret_cast<float*>(logits);
@@ -661,8 +691,8 @@ extern "C" fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_s
   {
     // attention reads whole 64-position blocks of the cache: positions never
     // written must hold finite values
-    cudaError_t e = cudaMemset(s->kcache, 0, s->layer_kv * m->cfg.n_layers * 2);
-    if (e == cudaSuccess) e = cudaMemset(s->vcache, 0, s->layer_kv * m->cfg.n_layers * 2);
+    cudaError_t e = cudaMemset(s->kcache, 0, s->kv_bytes);
+    if (e == cudaSuccess) e = cudaMemset(s->vcache, 0, s->kv_bytes);
     if (e != cudaSuccess) {
       delete s;
       return cuda_fail(e, "clear KV cache");
@@ -719,7 +749,11 @@ extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32
   if (!ids_on_device) FK_TRY(check_ids_host(ids, (long)s->B * seq, m->cfg.vocab));
   FK_TRY(check_device(nullptr));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  KV kv{s->kcache, s->vcache, s->layer_kv, s->cap};
+  KV kv;
+  kv.k = s->kcache;
+  kv.v = s->vcache;
+  kv.off = s->kv_off.data();
+  kv.caps = s->kv_cap.data();
   int C = 0;
   for (int c0 = 0; c0 < seq; c0 += C) {
     C = std::min(s->max_chunk, seq - c0);
@@ -743,7 +777,11 @@ static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_lo
   // every launch of the step may overlap its predecessor's tail (each kernel
   // waits for its predecessor before touching data the predecessor writes)
   PdlScope pdl(true);
-  KV kv{s->kcache, s->vcache, s->layer_kv, s->cap};
+  KV kv;
+  kv.k = s->kcache;
+  kv.v = s->vcache;
+  kv.off = s->kv_off.data();
+  kv.caps = s->kv_cap.data();
   FK_TRY(run_stack(m, s->sc, s->B, 1, s->len, kv, nullptr, true, s->dec_splits, st,
                    s->d_len, d_ids ? d_ids : s->next_ids));
   FK_TRY(session_head(s, s->sc.u, d_logits, d_next, d_margin, st));
