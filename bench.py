@@ -29,7 +29,8 @@ same public API (CUDA events, after warm-up, L2 flushed between repeats):
 
 N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
 path has no cross-sequence exchange, so there is no data-path collective.
-``--impl reference`` times the CPU oracle on the host cores instead.
+``--impl reference`` times the CPU oracle on the host cores instead (a bounded
+sample of the same workload: one sequence of 32 ids through the full model).
 """
 from __future__ import annotations
 
@@ -54,6 +55,7 @@ import synth  # noqa: E402
 METRIC = "prefill tok/s & decode tok/s on 1 GB300; % of bf16 TC / HBM roofline"
 WORKLOAD = "llama3-8b-shaped: session prefill 4x4096 + greedy decode batch 32 at context 2048"
 PREFILL_B, PREFILL_S = 4, 4096
+REF_TOKENS = 32  # the oracle's bounded sample: one sequence of 32 ids through the whole model
 DECODE_B, DECODE_CTX = 32, 2048
 
 
@@ -186,26 +188,42 @@ def upload(wbits: dict, device) -> dict:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_prefill_rate(cfg, wbits, n_tokens: int = 8) -> dict:
-    """Oracle prefill tok/s for the full model, from timing the oracle on the
-    same weights with 1 and 2 decoder layers (embedding + final norm + head
-    included in both) and scaling the per-layer time to cfg.n_layers."""
-    import oracle
-    ids = synth.make_ids(cfg, 1, n_tokens, stream=77)
-    times = {}
-    for nl in (1, 2):
-        c = cfg.with_(n_layers=nl)
-        sub = {k: v for k, v in wbits.items() if not k.startswith("L") or int(k[1:].split(".")[0]) < nl}
+class OracleFullDepth:
+    """The float64 oracle's session prefill through every layer of the full
+    model, on a bounded sample of the workload: 1 sequence of n_tokens ids.
+    The widened weights are cached once (set-up, untimed, like loading a
+    checkpoint) when the host has room for them (float64: 8 bytes per
+    parameter); otherwise each timed pass widens them again."""
+
+    def __init__(self, cfg, wbits, n_tokens: int):
+        import oracle
+        self.oracle = oracle
+        self.cfg = cfg
+        params = sum(int(v.size) for v in wbits.values())
+        ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+        self.cached = params * 8 * 2 < ram
+        self.W = oracle.OracleWeights(wbits, cache_limit_bytes=params * 8 + 1 if self.cached else 2 << 30)
+        self.ids = synth.make_ids(cfg, 1, n_tokens, stream=77)
+        self.n = n_tokens
         t0 = time.perf_counter()
-        oracle.Session(c, sub, 1).prefill(ids)
-        times[nl] = time.perf_counter() - t0
-    per_layer = max(times[2] - times[1], 1e-9)
-    fixed = max(times[1] - per_layer, 0.0)
-    full = fixed + per_layer * cfg.n_layers
-    return {"tok_s": n_tokens / full, "seconds_measured": times[1] + times[2], "full_forward_s": full,
-            "sample": f"oracle session prefill of 1x{n_tokens} tokens on the full-size weights with 1 and 2 "
-                      f"decoder layers (+embedding, final norm, LM head), per-layer time scaled to "
-                      f"{cfg.n_layers} layers"}
+        self.run()  # widens (and caches) the weights
+        self.setup_s = time.perf_counter() - t0
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        self.oracle.Session(self.cfg, self.W, 1).prefill(self.ids)
+        return time.perf_counter() - t0
+
+    def sample(self) -> str:
+        return (f"float64 oracle session prefill of 1x{self.n} ids through all {self.cfg.n_layers} layers of the "
+                f"full-size model (embedding, every layer, final norm, LM head); widened weights "
+                f"{'cached once (untimed)' if self.cached else 'widened per pass'}")
+
+
+def bench_config(world: int, decode_steps: int) -> dict:
+    return {"workload": WORKLOAD, "global_batch": PREFILL_B * world, "seq_len": PREFILL_S,
+            "decode_batch": DECODE_B * world, "decode_context": DECODE_CTX, "decode_steps_per_step": decode_steps,
+            "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (16 GB of weights)"}
 
 
 def run_reference(args):
@@ -213,25 +231,17 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = synth.CONFIGS["llama3-8b"]
-    nl = 2
-    wbits = synth.make_weights(cfg.with_(n_layers=nl))
-    wbits["lm_head"] = synth.make_tensor(cfg, "lm_head")
+    ref = OracleFullDepth(cfg, synth.make_weights(cfg), REF_TOKENS)
     for _ in range(args.warmup):
-        oracle_prefill_rate(cfg, wbits, 32)
-    vals, secs = [], []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        r = oracle_prefill_rate(cfg, wbits, 32)
-        secs.append(time.perf_counter() - t0)
-        vals.append(r["tok_s"])
-    value = statistics.median(vals)
+        ref.run()
+    secs = [ref.run() for _ in range(args.steps)]
+    value = ref.n / statistics.median(secs)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": PREFILL_B, "seq_len": PREFILL_S,
-                       "parallelism": "replicas", "l2": "inputs larger than L2 (16 GB of weights)"},
+            "config": bench_config(args.gpus, args.decode_steps),
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": r["sample"]},
+                             "sample": ref.sample(), "setup_s": round(ref.setup_s, 1)},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -511,9 +521,7 @@ def main():
         "metric": METRIC, "value": prefill_tps, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) bf16 weights, uniform ids)",
-        "config": {"workload": WORKLOAD, "global_batch": PREFILL_B * world, "seq_len": PREFILL_S,
-                   "decode_batch": DECODE_B * world, "decode_context": DECODE_CTX, "decode_steps_per_step": G,
-                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (16 GB of weights)"},
+        "config": bench_config(world, G),
         "decode": {"value": decode_tps, "unit": "tok/s", "batch": DECODE_B, "ms_per_token_step": dec_ms / (G * args.steps),
                    "hbm_gbs": step_gbs(DECODE_B, dec_ms), "hbm_frac": step_gbs(DECODE_B, dec_ms) / peaks["hbm"]},
         "decode_b1": {"value": decode1_tps, "unit": "tok/s", "batch": 1, "ms_per_token_step": dec1_ms / (G * args.steps),
@@ -596,11 +604,11 @@ def main():
 
     # ---- CPU oracle on the host cores (rank 0, N = 1 only)
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        nl = 2
-        sub = {k: v for k, v in wbits.items() if not k.startswith("L") or int(k[1:].split(".")[0]) < nl}
-        r = oracle_prefill_rate(cfg, sub, 256)
-        line["cpu_baseline"] = {"value": r["tok_s"], "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": r["sample"], "seconds": round(r["seconds_measured"], 1)}
+        ref = OracleFullDepth(cfg, wbits, REF_TOKENS)
+        secs = [ref.run() for _ in range(2)]
+        line["cpu_baseline"] = {"value": ref.n / min(secs), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": ref.sample(), "seconds": round(sum(secs), 1),
+                                "setup_s": round(ref.setup_s, 1)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -343,7 +343,8 @@ def test_gemma3_tower_decode_past_the_window(fk):
     P = synth.make_ids(cfg, 1, 1100, stream=4)
     steps = 16
     ram = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
-    W = oracle.OracleWeights(wb, cache_limit_bytes=(120 << 30) if ram > (300 << 30) else (2 << 30))
+    f64_bytes = sum(int(v.size) for v in wb.values()) * 8  # the widened weights, cached if the host has room
+    W = oracle.OracleWeights(wb, cache_limit_bytes=f64_bytes + 1 if ram > f64_bytes + (64 << 30) else (2 << 30))
     osess = oracle.Session(cfg, W, 1)
     zs = [osess.prefill(P)[0]]
     ids = [int(oracle.argmax_first(zs[0]))]

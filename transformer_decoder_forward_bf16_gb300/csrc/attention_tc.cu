@@ -383,6 +383,9 @@ fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const
                                unsigned* dev_err, cudaStream_t st, int io_f16, int out_f16) {
   if (B == 0 || S == 0) return FK_OK;
   if (ldq % 8 || cap % 64) return fail(FK_ERR_INVALID_ARG, "tensor-core attention: ldq % 8 and cap % 64 must be 0");
+  if (hd == 64 || hd == 128)
+    return attention_prefill_pp(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, hd, window, scale, o, dev_err, st,
+                                io_f16, out_f16);
   if (hd == 64)
     return launch_tc<64>(q, ldq, kcache, vcache, cap, B, S, pos0, Hq, Hkv, window, scale, o, dev_err, st, io_f16,
                            out_f16);

@@ -155,6 +155,11 @@ fk_status gemm_splitk_op(const void* d_x, const void* d_w, int P, int K, int N, 
 
 // tcgen05 flash attention for prefill (head_dim 64, 128 or 256; caches as in
 // the session layout, V transposed, cap a multiple of 64, ldq a multiple of 8).
+// The same with two 128-query tiles per CTA taking turns on the tensor core
+// (head_dim 64 or 128); attention_prefill_tc dispatches those head sizes here.
+fk_status attention_prefill_pp(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
+                               int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
+                               unsigned* dev_err, cudaStream_t st, int io_f16, int out_f16);
 // io_f16: q, the caches and the probabilities are IEEE f16 (else bf16);
 // out_f16: the output is stored as f16.
 fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
