@@ -178,6 +178,22 @@ def test_llama3_8b_slice_vs_oracle(fk):
     del model, out
     _free()
 
+    # ---- device ablation of the storage sites: all f16 but one site in bf16
+    # (the prefill of sequence 0 against the exact oracle); every site but
+    # the LM-head input has to be f16 for both gates on this shape
+    sites = {"qkv_in": 0x1, "attn": 0x2, "o_in": 0x4, "ffn_in": 0x8, "ffn_act": 0x10, "head_in": 0x20}
+    print("device ablation, llama3-8b 1x512 prefill vs exact: f16 everywhere but <site> in bf16")
+    for name, bit in sites.items():
+        model = fk.Model(cfg.with_(f16_sites=0x3F & ~bit), wdev, max_positions=600)
+        out = model.forward(prompt[:1], hidden=True, logits=True, argmax=False)
+        torch.cuda.synchronize()
+        h = out["hidden"].view(cfg.n_layers + 2, 512, cfg.hidden).cpu().numpy()
+        zl = out["logits"].view(512, -1)[-1].cpu().numpy().astype(np.float64)
+        print(f"  {name:8s} bf16: worst cosine {_worst_cos(h, ex['hidden'][:, 0], 3):.6f}, "
+              f"last logits max|d| {np.max(np.abs(zl - ex['logits'][0])):.4f}")
+        del model, out
+        _free()
+
     # ---- bf16 activation storage: the noise floor of its storage points
     model = fk.Model(cfg, wdev, max_positions=600)
     forced, first, _ = _greedy_device(fk, model, prompt, steps, forced=ref["ids"][:-1])
