@@ -48,7 +48,7 @@ __all__ = [
     "bf16_to_f64", "round_to_bf16", "embed_scale", "rmsnorm", "rope_inv_freq", "rope_apply",
     "attention", "silu", "gelu_tanh", "softcap", "gemm", "OracleWeights", "forward", "Session",
     "argmax_first", "top2_margin", "log_softmax", "topk_ids", "greedy", "store_bf16", "store_f16",
-    "STORAGE_SITES",
+    "STORAGE_SITES", "moe_route", "moe_ffn",
 ]
 
 
@@ -258,14 +258,88 @@ class OracleWeights:
             out[..., r0:r1] = gemm(x, bf16_to_f64(w[r0:r1]))
         return out
 
+    def expert(self, name: str, e: int) -> np.ndarray:
+        """Float64 view of expert e of a stacked [E, rows, cols] weight."""
+        if self.cache is not None:
+            return self[name][e]
+        return bf16_to_f64(self.bits[name][e])
+
     def head_name(self, cfg) -> str:
         return "embed" if cfg.tied else "lm_head"
 
 
 # ---------------------------------------------------------------------------
+# Mixture-of-experts FFN
+# ---------------------------------------------------------------------------
+def moe_route(cfg, z: np.ndarray):
+    """Routing of a mixture-of-experts FFN ("N7 · model/forward-parity", Thm 2:
+    the qwen3moe rung): p = softmax of the router logits z [..., E] over the
+    experts; the k experts of largest p (ties to the lower index); weights p at
+    those experts, renormalised to sum 1 when cfg.norm_topk.
+
+    Returns (ids [..., k], weights [..., k], margin [...]) where margin is the
+    gap between the k-th and (k+1)-th largest p (how far the choice is from a
+    flip; +inf when k equals the number of experts)."""
+    k, E = cfg.n_experts_per_tok, cfg.n_experts
+    z = np.asarray(z, dtype=np.float64)
+    pz = np.exp(z - np.max(z, axis=-1, keepdims=True))
+    pz = pz / np.sum(pz, axis=-1, keepdims=True)
+    order = np.argsort(-pz, axis=-1, kind="stable")
+    ids = order[..., :k]
+    w = np.take_along_axis(pz, ids, -1)
+    if cfg.norm_topk:
+        w = w / np.sum(w, axis=-1, keepdims=True)
+    if k < E:
+        srt = np.take_along_axis(pz, order[..., k - 1:k + 1], -1)
+        margin = srt[..., 0] - srt[..., 1]
+    else:
+        margin = np.full(z.shape[:-1], np.inf)
+    return ids, w, margin
+
+
+def moe_ffn(cfg, W: "OracleWeights", l: int, u: np.ndarray, R=None, forced_ids=None) -> dict:
+    """The mixture-of-experts FFN of layer l on u [..., H]: router logits
+    z = u·W_routerᵀ, routing by moe_route (or the ids in forced_ids [..., k],
+    weighted by the same softmax), then out = sum over the chosen experts e of
+    w_e · down_e(act(gate_e u) ⊙ up_e u) ("N7", Thm 2: qwen3moe; the expert
+    FFN is the SwiGLU FFN of Thm 1 with the expert's own matrices).
+
+    Returns {"out": [..., H], "ids": [..., k], "margin": [...]}."""
+    if R is None:
+        R = _rounder("exact")
+    p = f"L{l}."
+    z = W.linear(u, p + "router")
+    ids, w, margin = moe_route(cfg, z)
+    if forced_ids is not None:
+        ids = np.asarray(forced_ids).reshape(ids.shape)
+        pz = np.exp(z - np.max(z, axis=-1, keepdims=True))
+        pz = pz / np.sum(pz, axis=-1, keepdims=True)
+        w = np.take_along_axis(pz, ids, -1)
+        if cfg.norm_topk:
+            w = w / np.sum(w, axis=-1, keepdims=True)
+    H = u.shape[-1]
+    U = u.reshape(-1, H)
+    I = ids.reshape(U.shape[0], -1)
+    Wt = w.reshape(U.shape[0], -1)
+    out = np.zeros_like(U)
+    for e in range(cfg.n_experts):
+        rows, slots = np.nonzero(I == e)
+        if rows.size == 0:
+            continue
+        ue = U[rows]
+        g = ue @ W.expert(p + "expert_gate", e).T
+        up = ue @ W.expert(p + "expert_up", e).T
+        act = silu(g) if cfg.act == "silu" else gelu_tanh(g)
+        y = R("ffn_act", act * up) @ W.expert(p + "expert_down", e).T
+        out[rows] += Wt[rows, slots][:, None] * y
+    return {"out": out.reshape(u.shape), "ids": ids, "margin": margin}
+
+
+# ---------------------------------------------------------------------------
 # Decoder layer and forward
 # ---------------------------------------------------------------------------
-def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k, past_v, past_pos, R=None):
+def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k, past_v, past_pos, R=None,
+           moe=None):
     """One decoder layer on x [B, S, H] at positions pos [B, S].
 
     past_k/past_v [B, P, Hkv, hd] (P may be 0) are this layer's cached keys and
@@ -304,10 +378,18 @@ def _layer(cfg, W: OracleWeights, l: int, x: np.ndarray, pos: np.ndarray, past_k
     x = x + a
 
     u = R("ffn_in", rmsnorm(x, W[p + "ffn_norm"], cfg.rms_eps))
-    g = W.linear(u, p + "w_gate")
-    up = W.linear(u, p + "w_up")
-    act = silu(g) if cfg.act == "silu" else gelu_tanh(g)
-    d = W.linear(R("ffn_act", act * up), p + "w_down")
+    if cfg.moe_kinds()[l]:
+        # moe: {"forced": {layer: ids} or None, "trace": {layer: routing}} (optional)
+        forced = (moe or {}).get("forced") or {}
+        r = moe_ffn(cfg, W, l, u, R, forced.get(l))
+        if moe is not None and "trace" in moe:
+            moe["trace"][l] = {"ids": r["ids"], "margin": r["margin"]}
+        d = r["out"]
+    else:
+        g = W.linear(u, p + "w_gate")
+        up = W.linear(u, p + "w_up")
+        act = silu(g) if cfg.act == "silu" else gelu_tanh(g)
+        d = W.linear(R("ffn_act", act * up), p + "w_down")
     if cfg.norm_layout == "sandwich":
         d = rmsnorm(d, W[p + "post_ffn_norm"], cfg.rms_eps)
     x = x + d
@@ -330,13 +412,19 @@ def _head(cfg, W: OracleWeights, y: np.ndarray) -> np.ndarray:
     return z
 
 
-def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "all", storage: str = "exact") -> dict:
+def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "all", storage: str = "exact",
+            moe_forced=None) -> dict:
     """Cacheless forward over ids [B, S] ("N7 · model/forward-parity", Thm 1:
     embedding lookup, decoder stack appending one hidden slot per layer, final
     norm, head matmul to logits).
 
+    moe_forced: optional {layer: expert ids [B, S, k]} replacing the routing
+    choice of those mixture-of-experts layers (their weights still come from
+    this forward's own router softmax).
+
     Returns {"hidden": [L+2, B, S, H] or None, "logits": [B, S, V] ("all") or
-    [B, V] ("last") or None ("none")}.
+    [B, V] ("last") or None ("none"), "moe": {layer: {"ids", "margin"}} of the
+    routing actually used}.
     """
     R = _rounder(storage)
     W = weights if isinstance(weights, OracleWeights) else OracleWeights(weights)
@@ -348,14 +436,15 @@ def forward(cfg, weights, ids: np.ndarray, hidden: bool = True, logits: str = "a
     slots = [x] if hidden else None
     empty_kv = np.zeros((B, 0, Hkv, hd))
     empty_pos = np.zeros((B, 0), dtype=np.int64)
+    moe = {"forced": moe_forced, "trace": {}}
     for l in range(cfg.n_layers):
-        x, _, _ = _layer(cfg, W, l, x, pos, empty_kv, empty_kv, empty_pos, R)
+        x, _, _ = _layer(cfg, W, l, x, pos, empty_kv, empty_kv, empty_pos, R, moe)
         if hidden:
             slots.append(x)
     y = rmsnorm(x, W["final_norm"], cfg.rms_eps)
     if hidden:
         slots.append(y)
-    out = {"hidden": np.stack(slots) if hidden else None}
+    out = {"hidden": np.stack(slots) if hidden else None, "moe": moe["trace"]}
     if logits == "all":
         out["logits"] = _head(cfg, W, R("head_in", y))
     elif logits == "last":
@@ -380,28 +469,30 @@ class Session:
         self.v = [np.zeros((batch, 0, Hkv, hd)) for _ in range(cfg.n_layers)]
         self.length = 0
 
-    def _run(self, ids: np.ndarray) -> np.ndarray:
+    def _run(self, ids: np.ndarray, moe_forced=None) -> np.ndarray:
         cfg, W = self.cfg, self.W
         ids = np.asarray(ids).reshape(self.B, -1)
         S = ids.shape[1]
         pos = np.broadcast_to(np.arange(self.length, self.length + S), (self.B, S))
         past_pos = np.broadcast_to(np.arange(self.length), (self.B, self.length))
         x = _embed(cfg, W, ids)
+        self.moe = {"forced": moe_forced, "trace": {}}
         for l in range(cfg.n_layers):
-            x, k, v = _layer(cfg, W, l, x, pos, self.k[l], self.v[l], past_pos, self.R)
+            x, k, v = _layer(cfg, W, l, x, pos, self.k[l], self.v[l], past_pos, self.R, self.moe)
             self.k[l] = np.concatenate([self.k[l], k], axis=1)
             self.v[l] = np.concatenate([self.v[l], v], axis=1)
         self.length += S
         y = self.R("head_in", rmsnorm(x[:, -1, :], W["final_norm"], cfg.rms_eps))
         return _head(cfg, W, y)
 
-    def prefill(self, ids: np.ndarray) -> np.ndarray:
-        """Append ids [B, S]; return the last-position logits [B, V]."""
-        return self._run(ids)
+    def prefill(self, ids: np.ndarray, moe_forced=None) -> np.ndarray:
+        """Append ids [B, S]; return the last-position logits [B, V]. After the
+        call, self.moe["trace"] holds the routing of each MoE layer."""
+        return self._run(ids, moe_forced)
 
-    def decode(self, ids: np.ndarray) -> np.ndarray:
+    def decode(self, ids: np.ndarray, moe_forced=None) -> np.ndarray:
         """Append one token per sequence (ids [B]); return logits [B, V]."""
-        return self._run(np.asarray(ids).reshape(self.B, 1))
+        return self._run(np.asarray(ids).reshape(self.B, 1), moe_forced)
 
 
 # ---------------------------------------------------------------------------

@@ -116,6 +116,7 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 LAYER_TENSORS = ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "post_attn_norm",
                  "ffn_norm", "w_gate", "w_up", "w_down", "post_ffn_norm")
 NORM_TENSORS = ("attn_norm", "q_norm", "k_norm", "post_attn_norm", "ffn_norm", "post_ffn_norm")
+MOE_TENSORS = ("router", "expert_gate", "expert_up", "expert_down")
 
 
 def tensor_stream(name: str) -> int:
@@ -127,6 +128,8 @@ def tensor_stream(name: str) -> int:
     if name == "final_norm":
         return 3
     layer, t = name.split(".", 1)
+    if t in MOE_TENSORS:
+        return 1_000_000 + 8 * int(layer[1:]) + MOE_TENSORS.index(t)
     return 16 + 16 * int(layer[1:]) + LAYER_TENSORS.index(t)
 
 
@@ -144,9 +147,16 @@ def weight_shapes(cfg: ModelConfig) -> dict:
         shapes[p + "wv"] = (cfg.n_kv_heads * hd, H)
         shapes[p + "wo"] = (H, cfg.n_q_heads * hd)
         shapes[p + "ffn_norm"] = (H,)
-        shapes[p + "w_gate"] = (cfg.intermediate, H)
-        shapes[p + "w_up"] = (cfg.intermediate, H)
-        shapes[p + "w_down"] = (H, cfg.intermediate)
+        if cfg.moe_kinds()[l]:
+            E, Ie = cfg.n_experts, cfg.expert_intermediate
+            shapes[p + "router"] = (E, H)
+            shapes[p + "expert_gate"] = (E, Ie, H)
+            shapes[p + "expert_up"] = (E, Ie, H)
+            shapes[p + "expert_down"] = (E, H, Ie)
+        else:
+            shapes[p + "w_gate"] = (cfg.intermediate, H)
+            shapes[p + "w_up"] = (cfg.intermediate, H)
+            shapes[p + "w_down"] = (H, cfg.intermediate)
         if cfg.qk_norm:
             shapes[p + "q_norm"] = (hd,)
             shapes[p + "k_norm"] = (hd,)

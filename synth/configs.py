@@ -37,9 +37,20 @@ class ModelConfig:
     final_softcap: float = 0.0          # 0 = off
     tied: bool = True
     f16_sites: int = 0                  # activation storage sites kept as IEEE f16 (bit mask; 0 = all bf16)
+    # mixture-of-experts FFN (0 experts = dense FFN on every layer)
+    n_experts: int = 0
+    n_experts_per_tok: int = 0          # k experts per token
+    expert_intermediate: int = 0        # FFN width of one expert
+    norm_topk: bool = True              # renormalise the k routing weights to sum 1
+    moe_layers: tuple = field(default=())  # per layer: 1 = MoE FFN, 0 = dense (empty = all MoE if n_experts)
 
     def kinds(self) -> tuple:
         return self.layer_kinds if self.layer_kinds else (0,) * self.n_layers
+
+    def moe_kinds(self) -> tuple:
+        if not self.n_experts:
+            return (0,) * self.n_layers
+        return self.moe_layers if self.moe_layers else (1,) * self.n_layers
 
     def with_(self, **kw) -> "ModelConfig":
         return replace(self, **kw)
@@ -81,7 +92,15 @@ MISTRAL_7B = ModelConfig(
     intermediate=14336, vocab=32000, rms_eps=1e-5, rope_theta_global=10000.0, rope_theta_local=10000.0,
     sliding_window=4096, layer_kinds=(1,) * 32, tied=False)
 
-CONFIGS = {c.name: c for c in (SMOLLM2_135M, LLAMA3_8B, GEMMA3_TOWER, QWEN3_8B, MISTRAL_7B)}
+# Mixture-of-experts rung ("N7", Thm 2: qwen3moe): the Qwen3-30B-A3B geometry,
+# 128 experts of width 768 per layer, 8 routed per token, softmax routing
+# renormalised over the chosen 8.
+QWEN3_MOE_30B = ModelConfig(
+    name="qwen3-moe-30b-a3b", n_layers=48, hidden=2048, n_q_heads=32, n_kv_heads=4, head_dim=128,
+    intermediate=6144, vocab=151936, rms_eps=1e-6, rope_theta_global=1000000.0, rope_theta_local=1000000.0,
+    qk_norm=True, tied=False, n_experts=128, n_experts_per_tok=8, expert_intermediate=768, norm_topk=True)
+
+CONFIGS = {c.name: c for c in (SMOLLM2_135M, LLAMA3_8B, GEMMA3_TOWER, QWEN3_8B, MISTRAL_7B, QWEN3_MOE_30B)}
 
 
 def tiny_config(kind: str = "llama", **kw) -> ModelConfig:
@@ -102,6 +121,11 @@ def tiny_config(kind: str = "llama", **kw) -> ModelConfig:
                            rope_theta_global=1000000.0, rope_theta_local=10000.0, act="gelu_tanh",
                            norm_layout="sandwich", qk_norm=True, sliding_window=4,
                            layer_kinds=(1, 1, 0), embed_scale="sqrt_hidden_bf16", final_softcap=30.0)
+    elif kind == "moe":
+        base = ModelConfig(name="tiny-moe", n_layers=2, hidden=16, n_q_heads=4, n_kv_heads=2, head_dim=4,
+                           intermediate=24, vocab=32, rms_eps=1e-6, rope_theta_global=10000.0,
+                           rope_theta_local=10000.0, qk_norm=True, tied=False, n_experts=4, n_experts_per_tok=2,
+                           expert_intermediate=8, norm_topk=True, moe_layers=(0, 1))
     else:
         raise ValueError(kind)
     return replace(base, **kw)
@@ -129,6 +153,12 @@ def small_config(kind: str = "llama", **kw) -> ModelConfig:
         base = ModelConfig(name="small-qwen3", n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128,
                            intermediate=512, vocab=1024, rms_eps=1e-6, rope_theta_global=1000000.0,
                            rope_theta_local=1000000.0, qk_norm=True, tied=False)
+    elif kind == "moe":
+        # dense, MoE, MoE layers (a hybrid layer map); 8 experts, 2 per token
+        base = ModelConfig(name="small-moe", n_layers=3, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                           intermediate=384, vocab=1000, rms_eps=1e-6, rope_theta_global=1000000.0,
+                           rope_theta_local=1000000.0, qk_norm=True, tied=False, n_experts=8, n_experts_per_tok=2,
+                           expert_intermediate=128, norm_topk=True, moe_layers=(0, 1, 1))
     elif kind == "mistral":
         base = ModelConfig(name="small-mistral", n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64,
                            intermediate=384, vocab=1000, rms_eps=1e-5, rope_theta_global=10000.0,

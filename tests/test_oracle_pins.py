@@ -380,8 +380,29 @@ def _brute_forward(cfg, wb, ids):
                 a = norm(a, W[p + "post_attn_norm"])
             xt = [xs[t][c] + a[c] for c in range(H)]
             u = norm(xt, W[p + "ffn_norm"])
-            gg, uu = matvec(W[p + "w_gate"], u), matvec(W[p + "w_up"], u)
-            d = matvec(W[p + "w_down"], [gate(gg[i]) * uu[i] for i in range(len(gg))])
+            if cfg.moe_kinds()[l]:
+                # router probabilities, then k times the largest remaining one (lowest expert on ties)
+                r = matvec(W[p + "router"], u)
+                mx = max(r)
+                ex = [math.exp(v - mx) for v in r]
+                pr = [v / sum(ex) for v in ex]
+                chosen = []
+                for _ in range(cfg.n_experts_per_tok):
+                    best = None
+                    for e in range(cfg.n_experts):
+                        if e not in chosen and (best is None or pr[e] > pr[best]):
+                            best = e
+                    chosen.append(best)
+                wsum = sum(pr[e] for e in chosen) if cfg.norm_topk else 1.0
+                d = [0.0] * H
+                for e in chosen:
+                    gg = matvec(W[p + "expert_gate"][e], u)
+                    uu = matvec(W[p + "expert_up"][e], u)
+                    de = matvec(W[p + "expert_down"][e], [gate(gg[i]) * uu[i] for i in range(len(gg))])
+                    d = [d[c] + pr[e] / wsum * de[c] for c in range(H)]
+            else:
+                gg, uu = matvec(W[p + "w_gate"], u), matvec(W[p + "w_up"], u)
+                d = matvec(W[p + "w_down"], [gate(gg[i]) * uu[i] for i in range(len(gg))])
             if cfg.norm_layout == "sandwich":
                 d = norm(d, W[p + "post_ffn_norm"])
             new_xs.append([xt[c] + d[c] for c in range(H)])
@@ -397,9 +418,9 @@ def _brute_forward(cfg, wb, ids):
     return np.array(slots), np.array(logits)
 
 
-@pytest.mark.parametrize("kind", ["llama", "llama3", "gemma"])
+@pytest.mark.parametrize("kind", ["llama", "llama3", "gemma", "moe", "moe-unnormalised"])
 def test_forward_matches_brute_force(kind):
-    cfg = tiny_config(kind)
+    cfg = tiny_config("moe", norm_topk=False) if kind == "moe-unnormalised" else tiny_config(kind)
     wb = synth.make_weights(cfg, seed=11, sigma=0.3, norm_mode="random")
     ids = synth.make_ids(cfg, 1, 7, seed=5)
     out = oracle.forward(cfg, wb, ids)
@@ -539,3 +560,61 @@ def test_storage_sites_select_rounding():
             np.testing.assert_array_equal(one["hidden"], ex["hidden"])
     with pytest.raises(ValueError):
         oracle.forward(cfg, wb, ids, storage={"nope": "bf16"})
+
+
+# ---------------------------------------------------------------------------
+# Mixture-of-experts FFN
+# ---------------------------------------------------------------------------
+def test_moe_route_closed_forms():
+    cfg = tiny_config("moe")  # 4 experts, 2 per token, renormalised
+    z = np.array([[0.0, 1.0, 1.0, -2.0], [3.0, 0.0, 0.0, 0.0]])
+    ids, w, margin = oracle.moe_route(cfg, z)
+    np.testing.assert_array_equal(ids, [[1, 2], [0, 1]])  # equal logits: the lower expert first
+    np.testing.assert_allclose(w[0], [0.5, 0.5], rtol=1e-15)
+    p = np.exp(z[1]) / np.exp(z[1]).sum()
+    np.testing.assert_allclose(w[1], [p[0] / (p[0] + p[1]), p[1] / (p[0] + p[1])], rtol=1e-14)
+    np.testing.assert_allclose(margin, [np.exp(1) / np.exp(z[0]).sum() - 1 / np.exp(z[0]).sum(), 0.0],
+                               rtol=1e-14, atol=1e-16)
+    # without renormalisation the weights are the softmax probabilities; with k = E they are all of them
+    ids2, w2, _ = oracle.moe_route(cfg.with_(norm_topk=False), z)
+    np.testing.assert_allclose(w2[1], p[[0, 1]], rtol=1e-14)
+    ids3, w3, m3 = oracle.moe_route(cfg.with_(n_experts_per_tok=4, norm_topk=False), z)
+    np.testing.assert_allclose(w3.sum(-1), 1.0, rtol=1e-14)
+    assert np.all(np.isinf(m3))
+
+
+def test_moe_single_expert_is_the_dense_ffn():
+    """One expert, routed with weight 1: the MoE layer is the dense FFN with
+    that expert's matrices."""
+    cfg = tiny_config("moe", n_experts=1, n_experts_per_tok=1, expert_intermediate=24, moe_layers=(1, 1))
+    wb = synth.make_weights(cfg, seed=12, sigma=0.3, norm_mode="random")
+    dense_cfg = cfg.with_(n_experts=0, n_experts_per_tok=0, expert_intermediate=0, moe_layers=())
+    db = {k: v for k, v in wb.items() if not k.split(".")[-1] in synth.MOE_TENSORS}
+    for l in range(cfg.n_layers):
+        db[f"L{l}.w_gate"] = wb[f"L{l}.expert_gate"][0]
+        db[f"L{l}.w_up"] = wb[f"L{l}.expert_up"][0]
+        db[f"L{l}.w_down"] = wb[f"L{l}.expert_down"][0]
+    ids = synth.make_ids(cfg, 2, 6, seed=3)
+    a, b = oracle.forward(cfg, wb, ids), oracle.forward(dense_cfg, db, ids)
+    np.testing.assert_allclose(a["logits"], b["logits"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a["hidden"], b["hidden"], rtol=1e-12, atol=1e-12)
+
+
+def test_moe_expert_permutation_and_forced_routing():
+    """Relabelling the experts (router rows and expert matrices together)
+    leaves the output unchanged; forcing the routing the layer would choose
+    anyway changes nothing, and forcing another one does."""
+    cfg = tiny_config("moe")
+    wb = synth.make_weights(cfg, seed=13, sigma=0.3, norm_mode="random")
+    ids = synth.make_ids(cfg, 2, 7, seed=4)
+    base = oracle.forward(cfg, wb, ids)
+    perm = np.array([2, 0, 3, 1])
+    pb = dict(wb)
+    for t in synth.MOE_TENSORS:
+        pb[f"L1.{t}"] = wb[f"L1.{t}"][perm]
+    np.testing.assert_allclose(oracle.forward(cfg, pb, ids)["logits"], base["logits"], rtol=1e-12, atol=1e-12)
+    chosen = base["moe"][1]["ids"]
+    same = oracle.forward(cfg, wb, ids, moe_forced={1: chosen})
+    np.testing.assert_array_equal(same["logits"], base["logits"])
+    other = oracle.forward(cfg, wb, ids, moe_forced={1: (chosen + 1) % cfg.n_experts})
+    assert np.max(np.abs(other["logits"] - base["logits"])) > 1e-3
