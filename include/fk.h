@@ -64,6 +64,7 @@ typedef enum fk_status {
 /* Bits of the device error word. */
 #define FK_DEVERR_TOKEN_RANGE 0x1u   /* a device-resident token id was out of range (clamped) */
 #define FK_DEVERR_PIPE_TIMEOUT 0x2u  /* a kernel pipeline wait gave up */
+#define FK_DEVERR_EXPERT_IDS 0x4u    /* forced expert ids out of range or repeated (that token routed itself) */
 
 typedef enum { FK_ROPE_NONE = 0, FK_ROPE_LLAMA3 = 1 } fk_rope_scaling;
 typedef enum { FK_ACT_SILU = 0, FK_ACT_GELU_TANH = 1 } fk_act;
@@ -110,6 +111,13 @@ typedef enum { FK_EMBED_SCALE_NONE = 0, FK_EMBED_SCALE_SQRT_HIDDEN_BF16 = 1 } fk
  *   qk_norm and tied 0 or 1; sliding_window >= 0; layer_kinds entries 0
  *   (global) or 1 (local), local layers only with sliding_window > 0;
  *   final_softcap == 0 (off) or > 0 and finite; f16_sites within FK_F16_ALL.
+ * Mixture-of-experts layers ("N7 · model/forward-parity", Thm 2: the qwen3moe
+ * rung): n_experts == 0 makes every FFN dense (moe_layers must then be NULL
+ * or all 0). Otherwise n_experts is a multiple of 8 up to 256, 1 <=
+ * n_experts_per_tok <= min(n_experts, 16), expert_intermediate a positive
+ * multiple of 64, norm_topk 0 or 1, moe_layers NULL (every layer MoE) or
+ * entries 0 (dense) / 1 (MoE); intermediate is checked only when some layer
+ * is dense.
  */
 typedef struct fk_config {
   int32_t n_layers;
@@ -136,6 +144,15 @@ typedef struct fk_config {
   float final_softcap;          /* c of z -> c*tanh(z/c); 0 = off */
   int32_t tied;                 /* 1 = LM head is the embedding matrix */
   uint32_t f16_sites;           /* FK_F16_* bits: activation sites stored as f16 (0 = all bf16) */
+  /* Mixture-of-experts FFN: the router picks the n_experts_per_tok experts of
+   * largest softmax probability (ties to the lower expert id) and the FFN
+   * output is the sum of their SwiGLU outputs weighted by those
+   * probabilities, divided by their sum when norm_topk. */
+  int32_t n_experts;            /* 0 = dense FFN on every layer */
+  int32_t n_experts_per_tok;    /* k */
+  int32_t expert_intermediate;  /* FFN width of one expert */
+  int32_t norm_topk;            /* 1 = renormalise the k weights to sum 1 */
+  const uint8_t* moe_layers;    /* host, n_layers entries, 1 = MoE FFN; NULL = every layer (if n_experts) */
 } fk_config;
 
 /* Per-layer device weights, all bf16. Matrices are [out, in] row-major.
@@ -156,6 +173,11 @@ typedef struct fk_layer_weights {
   const void* w_up;            /* [intermediate, hidden] */
   const void* w_down;          /* [hidden, intermediate] */
   const void* post_ffn_norm;   /* [hidden] */
+  /* MoE layers only (w_gate, w_up, w_down are then unused and may be NULL) */
+  const void* router;          /* [n_experts, hidden] */
+  const void* expert_gate;     /* [n_experts][expert_intermediate, hidden] */
+  const void* expert_up;       /* [n_experts][expert_intermediate, hidden] */
+  const void* expert_down;     /* [n_experts][hidden, expert_intermediate] */
 } fk_layer_weights;
 
 typedef struct fk_weights {
@@ -364,6 +386,50 @@ fk_status fk_op_head_argmax(fk_model* m, const void* d_u, int32_t rows, float* d
 fk_status fk_op_logsoftmax_topk(const float* d_logits, int32_t rows, int32_t vocab, int32_t ld, int32_t k,
                                 float* d_lse, int32_t* d_top_ids, float* d_top_logprobs, float* d_logprobs,
                                 void* stream);
+
+/* fk_op_moe_route ("N7 · model/forward-parity", Thm 2: qwen3moe routing):
+ * for each of T rows of fp32 router logits z (d_logits, row stride ld >= E):
+ *   p = softmax(z) over the E experts (fp32);
+ *   d_ids (int32 [T][k]): the k experts of largest z -- the order of p --
+ *       by value descending, ties to the lower id; or, when d_forced (NULL or
+ *       int32 [T][k]) is given, its ids for that row (a row whose forced ids
+ *       are out of [0, E) or repeated routes itself instead and sets
+ *       FK_DEVERR_EXPERT_IDS in the op-level error word);
+ *   d_weights (fp32 [T][k]): p at those ids, divided by their sum when
+ *       norm_topk;
+ *   d_margin (NULL or fp32 [T]): p of the k-th minus p of the (k+1)-th
+ *       largest logit of the row's own ranking (+inf when k == E).
+ * 1 <= E <= 256, 1 <= k <= min(E, 16). */
+fk_status fk_op_moe_route(const float* d_logits, int32_t T, int32_t E, int32_t ld, int32_t k, int32_t norm_topk,
+                          const int32_t* d_forced, int32_t* d_ids, float* d_weights, float* d_margin, void* stream);
+
+/* fk_op_moe_ffn ("N7", Thm 2: the qwen3moe FFN): the mixture-of-experts FFN
+ * of MoE layer `layer` of model m on d_u [T][hidden] (the FFN norm output,
+ * bf16, or f16 when f16_sites has FK_F16_FFN_IN): router logits u·routerᵀ,
+ * routing as fk_op_moe_route (d_forced NULL or int32 [T][k]), then
+ *   d_out[t] (fp32 [T][hidden]) = sum_j w[t][j] * down_e(act(gate_e u) * up_e u)
+ * over the k chosen experts e = ids[t][j], j ascending, the gated activation
+ * stored as bf16 (f16 with FK_F16_FFN_ACT) before the down projection.
+ * d_ids (NULL or int32 [T][k]) and d_margin (NULL or fp32 [T]) receive the
+ * routing. The workspace (256-byte aligned) holds at least
+ * fk_op_moe_ffn_workspace_bytes(m, T) bytes. */
+size_t fk_op_moe_ffn_workspace_bytes(const fk_model* m, int32_t T);
+fk_status fk_op_moe_ffn(fk_model* m, int32_t layer, const void* d_u, int32_t T, const int32_t* d_forced, float* d_out,
+                        int32_t* d_ids, float* d_margin, void* d_ws, size_t ws_bytes, void* stream);
+
+/* Routing hook of the forward, the session prefill and decode. With d_forced
+ * set, the i-th MoE layer (counting MoE layers only, from 0) of each later
+ * call takes its expert ids from d_forced + i*max_tokens*k (int32
+ * [tokens][k], tokens = batch*seq of fk_forward, the chunk of
+ * fk_session_prefill, the batch of fk_decode_step, tokens in [batch][seq]
+ * order); its weights still come from its own router. d_trace_ids (int32,
+ * same layout) and d_trace_margin (fp32 [n_moe_layers][max_tokens]) receive
+ * each MoE layer's routing. While the hook is set, calls with more than
+ * max_tokens tokens, and prefills longer than the session's max_chunk, fail
+ * with FK_ERR_INVALID_ARG, and decode steps run without a CUDA graph. All
+ * NULL clears the hook. For parity tests; not for production use. */
+fk_status fk_model_set_moe_routing(fk_model* m, const int32_t* d_forced, int32_t* d_trace_ids, float* d_trace_margin,
+                                   int32_t max_tokens);
 
 /* Allocation-free fk_gemm_bf16_splitk. The pages have no counterpart: this
  * entry point serves callers that cannot hand the library a scratch buffer --

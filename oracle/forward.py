@@ -304,9 +304,12 @@ def moe_ffn(cfg, W: "OracleWeights", l: int, u: np.ndarray, R=None, forced_ids=N
     w_e · down_e(act(gate_e u) ⊙ up_e u) ("N7", Thm 2: qwen3moe; the expert
     FFN is the SwiGLU FFN of Thm 1 with the expert's own matrices).
 
+    R: the storage rounding of the activation sites (a _Rounder, or a storage
+    name as forward() takes; None = exact).
+
     Returns {"out": [..., H], "ids": [..., k], "margin": [...]}."""
-    if R is None:
-        R = _rounder("exact")
+    if R is None or isinstance(R, str):
+        R = _rounder(R or "exact")
     p = f"L{l}."
     z = W.linear(u, p + "router")
     ids, w, margin = moe_route(cfg, z)

@@ -21,6 +21,7 @@ def _lib():
 
 def _bad_configs():
     base = synth.small_config("gemma")
+    moe = synth.small_config("moe")
     return [
         ("softcap negative", base.with_(final_softcap=-1.0), "final_softcap"),
         ("softcap nan", base.with_(final_softcap=math.nan), "final_softcap"),
@@ -37,6 +38,11 @@ def _bad_configs():
         ("theta <= 1", base.with_(rope_theta_local=1.0), "theta"),
         ("llama3 low >= high", synth.small_config("llama3").with_(rope_low_freq_factor=4.0), "llama3"),
         ("zero layers", base.with_(n_layers=0, layer_kinds=()), "n_layers"),
+        ("experts not multiple of 8", moe.with_(n_experts=12), "n_experts"),
+        ("over 256 experts", moe.with_(n_experts=264), "n_experts"),
+        ("k above experts", moe.with_(n_experts_per_tok=9), "n_experts_per_tok"),
+        ("k above 16", moe.with_(n_experts=32, n_experts_per_tok=17), "n_experts_per_tok"),
+        ("expert width", moe.with_(expert_intermediate=100), "expert_intermediate"),
     ]
 
 
@@ -56,7 +62,8 @@ def test_invalid_config_rejected_before_any_device_work(name, cfg, needle):
 
 def test_valid_config_sizes_its_arena():
     fk, lib = _lib()
-    for cfg in (synth.small_config("gemma"), synth.CONFIGS["llama3-8b"], synth.CONFIGS["gemma3-tower"]):
+    for cfg in (synth.small_config("gemma"), synth.CONFIGS["llama3-8b"], synth.CONFIGS["gemma3-tower"],
+                synth.small_config("moe"), synth.CONFIGS["qwen3-moe-30b-a3b"]):
         ccfg, kinds = fk.config_to_c(cfg)
         assert lib.fk_model_arena_bytes(ctypes.byref(ccfg), 128) > 0, lib.fk_last_error()
 
@@ -103,3 +110,33 @@ def test_bad_arguments_rejected_on_host():
     assert lib.fk_attention_decode(fake, fake, fake, 1, 3, 2, 64, 64, 10, 0, fake, None) == 1   # GQA
     assert lib.fk_attention_prefill(fake, fake, fake, 1, 10, 0, 4, 1, 64, 60, 0, fake, None) == 1  # cap % 64
     assert lib.fk_debug_set_op_pipe_fault(0, -1) == 1
+
+
+def test_moe_arena_counts_expert_f16_copies():
+    """With f16 FFN sites, the arena holds f16 copies of the router and of
+    every expert matrix of each MoE layer (and only the dense FFN of dense
+    layers)."""
+    fk, lib = _lib()
+    cfg = synth.small_config("moe")  # layers: dense, MoE, MoE
+    def arena(c):
+        ccfg, bufs = fk.config_to_c(c)
+        n = lib.fk_model_arena_bytes(ctypes.byref(ccfg), 128)
+        assert n > 0, lib.fk_last_error()
+        return n
+    a0 = arena(cfg.with_(f16_sites=0))
+    a1 = arena(cfg.with_(f16_sites=fk.F16_FFN_IN | fk.F16_FFN_ACT))
+    H, I, E, Ie = cfg.hidden, cfg.intermediate, cfg.n_experts, cfg.expert_intermediate
+    al = lambda b: (b + 255) // 256 * 256
+    dense = 3 * al(I * H * 2)
+    per_moe = al(E * H * 2) + 3 * al(E * Ie * H * 2)
+    assert a1 - a0 == dense + 2 * per_moe
+
+
+def test_moe_layer_map_without_experts_rejected():
+    fk, lib = _lib()
+    cfg = synth.small_config("gemma")
+    ccfg, bufs = fk.config_to_c(cfg)
+    marks = (ctypes.c_uint8 * cfg.n_layers)(*([1] * cfg.n_layers))
+    ccfg.moe_layers = ctypes.cast(marks, ctypes.c_void_p)
+    assert lib.fk_model_arena_bytes(ctypes.byref(ccfg), 64) == 0
+    assert "n_experts is 0" in lib.fk_last_error().decode()

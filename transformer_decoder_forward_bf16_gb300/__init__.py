@@ -27,6 +27,7 @@ STATUS = {0: "FK_OK", 1: "FK_ERR_INVALID_ARG", 2: "FK_ERR_INVALID_CONFIG", 3: "F
           8: "FK_ERR_TIMEOUT", 9: "FK_ERR_WORKSPACE"}
 DEVERR_TOKEN_RANGE = 0x1
 DEVERR_PIPE_TIMEOUT = 0x2
+DEVERR_EXPERT_IDS = 0x4
 # activation storage sites stored as IEEE f16 instead of bf16 (fk_config.f16_sites)
 F16_QKV_IN, F16_ATTN, F16_O_IN, F16_FFN_IN, F16_FFN_ACT, F16_HEAD_IN = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 F16_ALL = 0x3F
@@ -47,12 +48,15 @@ class FkConfig(ctypes.Structure):
                 ("rope_factor", c_float), ("rope_low_freq_factor", c_float), ("rope_high_freq_factor", c_float),
                 ("rope_orig_max_pos", c_int32), ("act", c_int32), ("norm_layout", c_int32), ("qk_norm", c_int32),
                 ("sliding_window", c_int32), ("layer_kinds", c_void_p), ("embed_scale", c_int32),
-                ("final_softcap", c_float), ("tied", c_int32), ("f16_sites", c_uint32)]
+                ("final_softcap", c_float), ("tied", c_int32), ("f16_sites", c_uint32),
+                ("n_experts", c_int32), ("n_experts_per_tok", c_int32), ("expert_intermediate", c_int32),
+                ("norm_topk", c_int32), ("moe_layers", c_void_p)]
 
 
 class FkLayerWeights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "post_attn_norm",
-                                        "ffn_norm", "w_gate", "w_up", "w_down", "post_ffn_norm")]
+                                        "ffn_norm", "w_gate", "w_up", "w_down", "post_ffn_norm",
+                                        "router", "expert_gate", "expert_up", "expert_down")]
 
 
 class FkWeights(ctypes.Structure):
@@ -98,6 +102,12 @@ _SIGS = {
     "fk_op_head_argmax": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "fk_op_logsoftmax_topk": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_void_p]),
+    "fk_op_moe_route": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p]),
+    "fk_op_moe_ffn_workspace_bytes": (c_size_t, [c_void_p, c_int32]),
+    "fk_op_moe_ffn": (c_int32, [c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_size_t, c_void_p]),
+    "fk_model_set_moe_routing": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32]),
     "fk_profile_enable": (None, [c_int32]),
     "fk_profile_reset": (None, []),
     "fk_profile_count": (c_int32, []),
@@ -262,11 +272,28 @@ def logsoftmax_topk(z, k: int = 64, logprobs: bool = False, stream=None) -> dict
     return out
 
 
+def moe_route(z, k: int, norm_topk: bool = True, forced=None, stream=None) -> dict:
+    """fk_op_moe_route on fp32 router logits z [T, E] (CUDA): expert ids and
+    weights [T, k] and the routing margin [T]."""
+    import torch
+    T, E = z.shape
+    dev = z.device
+    out = {"ids": torch.empty((T, k), dtype=torch.int32, device=dev),
+           "weights": torch.empty((T, k), dtype=torch.float32, device=dev),
+           "margin": torch.empty((T,), dtype=torch.float32, device=dev)}
+    _check(load().fk_op_moe_route(_ptr(z), T, E, z.stride(0), k, int(norm_topk), _ptr(forced), _ptr(out["ids"]),
+                                  _ptr(out["weights"]), _ptr(out["margin"]), _stream_ptr(stream)), "fk_op_moe_route")
+    return out
+
+
 def config_to_c(cfg) -> tuple:
     """Fill an FkConfig from any object with the ModelConfig fields; returns
-    (struct, kinds buffer) -- keep the buffer alive while the struct is used."""
+    (struct, buffers) -- keep the buffers alive while the struct is used."""
     kinds = cfg.kinds() if hasattr(cfg, "kinds") else tuple(cfg.layer_kinds)
     kbuf = (ctypes.c_uint8 * max(1, len(kinds)))(*kinds)
+    n_exp = int(getattr(cfg, "n_experts", 0))
+    moe = cfg.moe_kinds() if hasattr(cfg, "moe_kinds") else (0,) * cfg.n_layers
+    mbuf = (ctypes.c_uint8 * max(1, len(moe)))(*moe)
     c = FkConfig(
         n_layers=cfg.n_layers, hidden=cfg.hidden, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
         head_dim=cfg.head_dim, intermediate=cfg.intermediate, vocab=cfg.vocab, rms_eps=cfg.rms_eps,
@@ -277,8 +304,12 @@ def config_to_c(cfg) -> tuple:
         norm_layout={"pre": 0, "sandwich": 1}[cfg.norm_layout], qk_norm=int(cfg.qk_norm),
         sliding_window=cfg.sliding_window, layer_kinds=ctypes.cast(kbuf, c_void_p) if len(kinds) else None,
         embed_scale={"none": 0, "sqrt_hidden_bf16": 1}[cfg.embed_scale], final_softcap=cfg.final_softcap,
-        tied=int(cfg.tied), f16_sites=int(getattr(cfg, "f16_sites", 0)))
-    return c, kbuf
+        tied=int(cfg.tied), f16_sites=int(getattr(cfg, "f16_sites", 0)),
+        n_experts=n_exp, n_experts_per_tok=int(getattr(cfg, "n_experts_per_tok", 0)),
+        expert_intermediate=int(getattr(cfg, "expert_intermediate", 0)),
+        norm_topk=int(getattr(cfg, "norm_topk", True)),
+        moe_layers=ctypes.cast(mbuf, c_void_p) if n_exp and len(moe) else None)
+    return c, (kbuf, mbuf)
 
 
 class Model:
@@ -371,6 +402,33 @@ class Model:
         _check(load().fk_op_head_argmax(self.handle, _ptr(u), rows, _ptr(out["logits"]), _ptr(out["argmax"]),
                                         _ptr(out["margin"]), _stream_ptr(stream)), "fk_op_head_argmax")
         return out
+
+    def moe_ffn(self, layer: int, u, forced=None, stream=None) -> dict:
+        """fk_op_moe_ffn: the MoE FFN of `layer` on u [T, hidden] (16-bit):
+        output fp32 [T, hidden], routing ids [T, k] and margins [T]."""
+        import torch
+        lib = load()
+        T = u.shape[0]
+        dev = u.device
+        k = self.cfg.n_experts_per_tok
+        wsb = lib.fk_op_moe_ffn_workspace_bytes(self.handle, T)
+        if wsb == 0:
+            raise FkError(1, "fk_op_moe_ffn_workspace_bytes", lib.fk_last_error().decode())
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        out = {"out": torch.empty((T, self.cfg.hidden), dtype=torch.float32, device=dev),
+               "ids": torch.empty((T, k), dtype=torch.int32, device=dev),
+               "margin": torch.empty((T,), dtype=torch.float32, device=dev)}
+        _check(lib.fk_op_moe_ffn(self.handle, layer, _ptr(u), T, _ptr(forced), _ptr(out["out"]), _ptr(out["ids"]),
+                                 _ptr(out["margin"]), _ptr(ws), wsb, _stream_ptr(stream)), "fk_op_moe_ffn")
+        return out
+
+    def set_moe_routing(self, forced=None, trace_ids=None, trace_margin=None, max_tokens: int = 0):
+        """fk_model_set_moe_routing: forced expert ids and routing traces,
+        laid out [n_moe_layers][max_tokens][k] (margins [n_moe_layers][max_tokens]);
+        all None clears the hook. The tensors must outlive their use."""
+        self._moe_hook = (forced, trace_ids, trace_margin)
+        _check(load().fk_model_set_moe_routing(self.handle, _ptr(forced), _ptr(trace_ids), _ptr(trace_margin),
+                                               max_tokens), "fk_model_set_moe_routing")
 
     def session(self, batch: int, max_seq: int, max_chunk: int | None = None) -> "Session":
         return Session(self, batch, max_seq, max_chunk or max_seq)

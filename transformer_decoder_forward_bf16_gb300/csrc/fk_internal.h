@@ -100,11 +100,19 @@ struct GemmWeights {
   int f16 = 0;             // the matrices (and so the A operand) are IEEE f16, else bf16
   int K = 0;
   int n_out = 0;           // output columns (GLU: rows of one matrix)
+  int groups = 0;          // grouped (expert) operand: `groups` matrices stacked per map, 0 = plain
+  int group_rows = 0;      // rows of one group's matrix in each map
 };
 
 // f16: the matrices hold IEEE f16 (copies made by the model), else bf16.
 fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* rows, int nseg, int K, int glu,
                             int f16 = 0);
+
+// Grouped operand: each map holds `groups` matrices of rows_per_group x K
+// stacked along the rows (the experts of a MoE layer); nseg 2 with glu 1 is a
+// gate/up pair, nseg 1 a single matrix per group.
+fk_status gemm_weights_init_grouped(GemmWeights* g, const void* const* mats, int nseg, int groups, int rows_per_group,
+                                    int K, int glu, int f16 = 0);
 
 struct GemmOut {
   int epi = EPI_BF16;
@@ -124,6 +132,12 @@ struct GemmOut {
 // arrival counters of every GEMM sharing the scratch (0: this GEMM's own).
 fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
                    cudaStream_t st, void* scratch = nullptr, size_t scratch_bytes = 0, size_t counter_region = 0);
+
+// Grouped GEMM: rows [group_off[g], group_off[g+1]) of A (M rows in all)
+// multiply group g of the grouped operand w; group_off (device, groups + 1
+// entries, nondecreasing, group_off[groups] <= M) is read by the kernel.
+fk_status gemm_run_grouped(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o,
+                           const int* group_off, unsigned* dev_err, cudaStream_t st);
 
 // Skinny (few-token) GEMM: swap-AB tcgen05 split-K + ordered reduction.
 constexpr int kSkinnyMaxTokens = 64;
@@ -165,5 +179,50 @@ fk_status attention_prefill_pp(const void* q, int ldq, const void* kcache, const
 fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const void* vcache, int cap, int B, int S,
                                int pos0, int Hq, int Hkv, int hd, int window, float scale, void* o,
                                unsigned* dev_err, cudaStream_t st, int io_f16 = 0, int out_f16 = 0);
+
+// ---------------------------------------------------------------------------
+// Mixture-of-experts FFN
+// ---------------------------------------------------------------------------
+constexpr int kMoeMaxExperts = 256;
+constexpr int kMoeMaxK = 16;
+struct MoeWeights {
+  GemmWeights router;   // [E, H], fp32 logits
+  GemmWeights gate_up;  // grouped gate/up pair, E groups of [Ie, H]
+  GemmWeights down;     // grouped, E groups of [H, Ie]
+  int E = 0, k = 0, Ie = 0, H = 0;
+  int norm_topk = 1;
+  int act = 0;          // 0 SiLU, 1 GELU (tanh form)
+  int act_f16 = 0;      // the gated activation is stored as f16 (else bf16)
+};
+// Scratch of one MoE FFN call over up to T tokens (layout from moe_scratch).
+struct MoeScratch {
+  float* z = nullptr;        // [T, E] router logits
+  int32_t* ids = nullptr;    // [T, k]
+  float* w = nullptr;        // [T, k]
+  float* margin = nullptr;   // [T]
+  int32_t* counts = nullptr; // [blocks, E] tokens per expert per routing block
+  int32_t* base = nullptr;   // [blocks, E] first sorted row of each block's tokens of each expert
+  int32_t* group_off = nullptr;  // [E + 1] first sorted row of each expert
+  int32_t* pos = nullptr;    // [T, k] sorted row of each (token, slot)
+  int32_t* src = nullptr;    // [T*k] token of each sorted row
+  void* xs = nullptr;        // [T*k, H] 16-bit: gathered FFN inputs, sorted by expert
+  void* hs = nullptr;        // [T*k, Ie] 16-bit: gated activations
+  float* ys = nullptr;       // [T*k, H] expert outputs
+};
+// Bytes of the scratch for T tokens; with base != NULL also fills *s.
+size_t moe_scratch(const MoeWeights& mw, long T, MoeScratch* s, uint8_t* base);
+// The MoE FFN of u [T, H] (16-bit, the type of mw.router): out = res + d when
+// res is given (res may not alias out), else out = d. forced: NULL or int32
+// [T, k] expert ids; trace_ids / trace_margin: NULL or outputs of the routing.
+// gemv/gemv_bytes/gemv_counter: split-K scratch for the router GEMM of few
+// tokens (NULL: tiled GEMM).
+fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScratch& s, const int32_t* forced,
+                      int32_t* trace_ids, float* trace_margin, float* out, const float* res, unsigned* dev_err,
+                      cudaStream_t st, void* gemv = nullptr, size_t gemv_bytes = 0, size_t gemv_counter = 0);
+// The routing step alone (fk_op_moe_route): ids, weights, margins, and per
+// routing block expert counts when counts != NULL.
+fk_status moe_route_launch(const float* z, int T, int E, int ld, int k, int norm_topk, const int32_t* forced,
+                           int32_t* ids, float* w, float* margin, int32_t* counts, unsigned* dev_err,
+                           cudaStream_t st);
 
 }  // namespace fk

@@ -16,7 +16,13 @@
 //     row per thread) then a fused store: bf16, fp32 (+softcap), fp32
 //     residual add, or the gated activation act(gate)*up of the FFN.
 //   * the weight operand may be up to three matrices stacked along N (Q|K|V
-//     without a repacked copy) or a gate/up pair interleaved per tile.
+//     without a repacked copy) or a gate/up pair interleaved per tile;
+//   * grouped mode (the experts of a MoE layer): A holds the rows of every
+//     group back to back, group g at rows [off[g], off[g+1]) (offsets read
+//     from device memory at kernel start), and each group's rows multiply
+//     that group's matrix of a stacked operand. Tiles never span two groups:
+//     each group's rows are cut into 128-row blocks of their own, and rows
+//     past the group's end are computed but not stored.
 #include <algorithm>
 
 #include "fk_common.cuh"
@@ -47,6 +53,9 @@ struct GemmArgs {
   unsigned* dev_err;
   int ab_f16;   // A and B are IEEE f16 (else bf16)
   int out_f16;  // 16-bit outputs stored as f16 (else bf16)
+  const int* group_off;  // grouped mode: groups + 1 row offsets into A
+  int groups;
+  int group_rows;        // B rows of one group in each map
 };
 
 // MT = 128-row sub-tiles per CTA tile. MT == 2 makes a 256 x BN tile: two
@@ -85,9 +94,10 @@ FK_DEVICE float act_gelu_tanh(float g) {
   return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
 }
 
-// Source of the i-th 64-row box of B for output block nb.
+// Source of the i-th 64-row box of B for output block nb (gbase: first row
+// of the tile's group in every map, 0 outside grouped mode).
 template <int BN>
-FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int& map, int& row, bool& valid) {
+FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int gbase, int& map, int& row, bool& valid) {
   if (a.glu) {
     constexpr int half = BN / 128;  // boxes per half tile
     map = (i < half) ? 0 : 1;
@@ -101,9 +111,26 @@ FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int& map, int& row
     row = v - a.seg_start[map];
     valid = v < a.n_virtual;
   }
+  row += gbase;
 }
 
-template <int BN, int MT>
+// A rows of a tile: [row0, row_end) are stored; g is the tile's group.
+struct TileRows {
+  int row0, row_end, g;
+};
+// Grouped mode: m-block mb of the tile order is block mb - mstart[g] of the
+// group g with mstart[g] <= mb < mstart[g+1] (empty groups have no blocks).
+FK_DEVICE TileRows grouped_rows(const int* goff, const int* mstart, int groups, int mb) {
+  int lo = 0, hi = groups;  // mstart[lo] <= mb < mstart[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (mstart[mid] <= mb) lo = mid;
+    else hi = mid;
+  }
+  return TileRows{goff[lo] + (mb - mstart[lo]) * BM, goff[lo + 1], lo};
+}
+
+template <int BN, int MT, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -123,10 +150,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_blocks = (args.M + TM - 1) / TM;
+  int m_blocks = (args.M + TM - 1) / TM;
   const int n_blocks = args.glu ? (args.n_out + BN / 2 - 1) / (BN / 2) : (args.n_virtual + BN - 1) / BN;
-  const int tiles = m_blocks * n_blocks;
   const int nk = (args.K + BK - 1) / BK;
+
+  // grouped mode: the group offsets and the first m-block of every group
+  __shared__ int s_goff[GROUPED ? kMoeMaxExperts + 1 : 1];
+  __shared__ int s_mstart[GROUPED ? kMoeMaxExperts + 1 : 1];
+  if constexpr (GROUPED) {
+    static_assert(MT == 1, "grouped tiles are 128 rows");
+    for (int i = threadIdx.x; i <= args.groups; i += blockDim.x) s_goff[i] = args.group_off[i];
+    __syncthreads();
+    if (warp == 2) {  // exclusive prefix of ceil(rows / 128) over the groups
+      int carry = 0;
+      for (int g0 = 0; g0 < args.groups; g0 += 32) {
+        const int g = g0 + lane;
+        int v = g < args.groups ? (s_goff[g + 1] - s_goff[g] + BM - 1) / BM : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += n;
+        }
+        if (g < args.groups) s_mstart[g + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) s_mstart[0] = 0;
+    }
+  }
+  auto rows_of = [&](int mb) -> TileRows {
+    if constexpr (GROUPED) return grouped_rows(s_goff, s_mstart, args.groups, mb);
+    return TileRows{mb * TM, args.M, 0};
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -152,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (GROUPED) m_blocks = s_mstart[args.groups];
+  const int tiles = m_blocks * n_blocks;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -165,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, m_blocks, n_blocks, mb, nb);
+        const TileRows tr = rows_of(mb);
+        const int gbase = tr.g * args.group_rows;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.dev_err)) {
             ok = false;
@@ -175,18 +233,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN / 64; ++i) {
             int map, row;
             bool valid;
-            b_box_source<BN>(args, nb, i, map, row, valid);
+            b_box_source<BN>(args, nb, i, gbase, map, row, valid);
             if (valid) bytes += 64 * BK * 2;
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
           for (int sub = 0; sub < MT; ++sub)
-            tma_load_2d(&tmA, &full[stage], sA + stage * C::A_STAGE + sub * A_BYTES, kb * BK, mb * TM + sub * BM);
+            tma_load_2d(&tmA, &full[stage], sA + stage * C::A_STAGE + sub * A_BYTES, kb * BK, tr.row0 + sub * BM);
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i) {
             int map, row;
             bool valid;
-            b_box_source<BN>(args, nb, i, map, row, valid);
+            b_box_source<BN>(args, nb, i, gbase, map, row, valid);
             if (valid) tma_load_2d(maps[map], &full[stage], sB + stage * C::B_BYTES + i * 64 * BK * 2, kb * BK, row);
           }
           ++fills[stage];
@@ -247,10 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) umma_commit(&tfull[acc]);
       }
       // every MMA issued by this thread has completed once mma_done fires
-      umma_commit(mma_done);
-      const uint32_t a = smem_u32(mma_done);
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
+      // (a grouped CTA may have had no tile and issued none)
+      if (local > 0) {
+        umma_commit(mma_done);
+        const uint32_t a = smem_u32(mma_done);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
       }
     }
   } else {
@@ -261,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
       int mb, nb;
       tile_coords(t, m_blocks, n_blocks, mb, nb);
+      const TileRows tr = rows_of(mb);
       const int acc = local % C::NACC;
       const uint32_t aphase = (local / C::NACC) & 1;
       // warp-uniform: the tcgen05.ld below are warp-collective
@@ -268,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll 1
       for (int sub = 0; sub < MT; ++sub) {
-      const int row = mb * TM + sub * BM + q * 32 + lane;
-      const bool row_ok = row < args.M;
+      const int row = tr.row0 + sub * BM + q * 32 + lane;
+      const bool row_ok = row < tr.row_end;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (acc * MT + sub) * BN;
       float v[32];
       if (args.epi == EPI_GLU_BF16) {
@@ -358,18 +420,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int MT>
+template <int BN, int MT, bool GROUPED = false>
 fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st) {
   using C = Cfg<BN, MT>;
   static DeviceOnce once;
-  const cudaError_t attr_err = once.run(
-      [] { return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
+  const cudaError_t attr_err = once.run([] {
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
-  const int m_blocks = (a.M + BM * MT - 1) / (BM * MT);
+  // grouped: the m-block count is known on the device only; each group adds
+  // at most one partial block to the M / 128 full ones
+  const int m_blocks = (a.M + BM * MT - 1) / (BM * MT) + (GROUPED ? a.groups : 0);
   const int n_blocks = a.glu ? (a.n_out + BN / 2 - 1) / (BN / 2) : (a.n_virtual + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int grid = std::min(tiles, sm_count);
-  gemm_tc_kernel<BN, MT><<<grid, kThreads, C::SMEM, st>>>(tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0],
+  gemm_tc_kernel<BN, MT, GROUPED><<<grid, kThreads, C::SMEM, st>>>(tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0],
                                                            w.nseg > 2 ? w.map[2] : w.map[0], a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
@@ -407,40 +472,94 @@ fk_status gemm_weights_init(GemmWeights* g, const void* const* mats, const int* 
   return FK_OK;
 }
 
-fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
-                   cudaStream_t st, void* scratch, size_t scratch_bytes, size_t counter_region) {
-  if (M == 0) return FK_OK;
-  if (M <= kSkinnyMaxTokens && scratch)
-    return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st, true, counter_region);
+fk_status gemm_weights_init_grouped(GemmWeights* g, const void* const* mats, int nseg, int groups, int rows_per_group,
+                                    int K, int glu, int f16) {
+  if ((glu ? nseg != 2 : nseg != 1) || groups < 1 || rows_per_group <= 0 || rows_per_group % 64 || K <= 0 || K % 8)
+    return fail(FK_ERR_INVALID_ARG, "grouped gemm weights");
+  *g = GemmWeights();
+  g->nseg = nseg;
+  g->glu = glu;
+  g->f16 = f16 ? 1 : 0;
+  g->K = K;
+  g->groups = groups;
+  g->group_rows = rows_per_group;
+  for (int s = 0; s < nseg; ++s) {
+    if (!mats[s]) return fail(FK_ERR_INVALID_ARG, "grouped gemm weights: null matrix");
+    fk_status st = make_tmap_bf16(&g->map[s], mats[s], (int64_t)groups * rows_per_group, K, K, 64);
+    if (st != FK_OK) return st;
+    g->seg_rows[s] = rows_per_group;
+  }
+  // one group's rows: the whole virtual operand of a tile
+  g->seg_start[0] = 0;
+  g->seg_start[1] = rows_per_group;
+  g->n_out = rows_per_group;
+  return FK_OK;
+}
 
+// Operand checks and kernel arguments shared by the plain and grouped GEMMs.
+static fk_status gemm_args(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
+                           CUtensorMap* tA, GemmArgs* a, int* sm_count) {
   if (!A || !o.out || M < 0 || lda < w.K || lda % 8 || o.ldo % (o.epi == EPI_BF16 || o.epi == EPI_GLU_BF16 ? 8 : 4))
     return fail(FK_ERR_INVALID_ARG, "gemm_run: bad operand");
   if (o.epi == EPI_ADD_F32 && (!o.res || o.ldr % 4)) return fail(FK_ERR_INVALID_ARG, "gemm_run: residual");
-  int sm_count = 0;
-  fk_status s = check_device(&sm_count);
+  fk_status s = check_device(sm_count);
   if (s != FK_OK) return s;
+  s = make_tmap_bf16(tA, A, M, w.K, lda, BM);
+  if (s != FK_OK) return s;
+  *a = GemmArgs{};
+  a->M = M;
+  a->K = w.K;
+  a->n_virtual = w.seg_start[w.nseg];
+  a->nseg = w.nseg;
+  a->glu = w.glu;
+  for (int i = 0; i < 4; ++i) a->seg_start[i] = w.seg_start[i];
+  for (int i = 0; i < 3; ++i) a->seg_rows[i] = w.seg_rows[i];
+  a->n_out = w.n_out;
+  a->epi = o.epi;
+  a->act = o.act;
+  a->out = o.out;
+  a->ldo = o.ldo;
+  a->res = o.res;
+  a->ldr = o.ldr;
+  a->softcap = o.softcap;
+  a->dev_err = dev_err;
+  a->ab_f16 = w.f16;
+  a->out_f16 = o.out_f16;
+  return FK_OK;
+}
+
+fk_status gemm_run_grouped(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o,
+                           const int* group_off, unsigned* dev_err, cudaStream_t st) {
+  if (M == 0) return FK_OK;
+  if (w.groups < 1 || w.groups > kMoeMaxExperts || !group_off)
+    return fail(FK_ERR_INVALID_ARG, "gemm_run_grouped: not a grouped operand");
+  if (w.glu ? w.nseg != 2 : w.nseg != 1) return fail(FK_ERR_INVALID_ARG, "gemm_run_grouped: operand layout");
+  if (o.epi == EPI_ADD_F32) return fail(FK_ERR_INVALID_ARG, "gemm_run_grouped: no residual epilogue");
   CUtensorMap tA;
-  s = make_tmap_bf16(&tA, A, M, w.K, lda, BM);
+  GemmArgs a;
+  int sm_count = 0;
+  fk_status s = gemm_args(A, M, lda, w, o, dev_err, &tA, &a, &sm_count);
   if (s != FK_OK) return s;
-  GemmArgs a{};
-  a.M = M;
-  a.K = w.K;
-  a.n_virtual = w.seg_start[w.nseg];
-  a.nseg = w.nseg;
-  a.glu = w.glu;
-  for (int i = 0; i < 4; ++i) a.seg_start[i] = w.seg_start[i];
-  for (int i = 0; i < 3; ++i) a.seg_rows[i] = w.seg_rows[i];
-  a.n_out = w.n_out;
-  a.epi = o.epi;
-  a.act = o.act;
-  a.out = o.out;
-  a.ldo = o.ldo;
-  a.res = o.res;
-  a.ldr = o.ldr;
-  a.softcap = o.softcap;
-  a.dev_err = dev_err;
-  a.ab_f16 = w.f16;
-  a.out_f16 = o.out_f16;
+  a.group_off = group_off;
+  a.groups = w.groups;
+  a.group_rows = w.group_rows;
+  const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
+  if (((M + BM - 1) / BM) * nb256 >= sm_count) return launch_bn<256, 1, true>(tA, w, a, sm_count, st);
+  return launch_bn<128, 1, true>(tA, w, a, sm_count, st);
+}
+
+fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
+                   cudaStream_t st, void* scratch, size_t scratch_bytes, size_t counter_region) {
+  if (M == 0) return FK_OK;
+  if (w.groups) return fail(FK_ERR_INVALID_ARG, "gemm_run: grouped operand needs gemm_run_grouped");
+  if (M <= kSkinnyMaxTokens && scratch)
+    return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st, true, counter_region);
+
+  CUtensorMap tA;
+  GemmArgs a;
+  int sm_count = 0;
+  fk_status s = gemm_args(A, M, lda, w, o, dev_err, &tA, &a, &sm_count);
+  if (s != FK_OK) return s;
   // 256x256 tiles while they give every SM at least two tiles; then 128x256;
   // else 128-wide.
   const int m_blocks = (M + BM - 1) / BM;

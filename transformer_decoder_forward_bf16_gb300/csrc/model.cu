@@ -12,6 +12,8 @@
 //   u   = RMSNorm(x'')·w_next    (next layer's attn norm, or the final norm)
 // Sandwich layout ("N7", Thm 2, gemma3): the O and down GEMMs write fp32 and a
 // fused kernel adds RMSNorm(a)·w_post to the residual and normalises the sum.
+// Mixture-of-experts layers ("N7", Thm 2, qwen3moe) replace the gated FFN by
+// the routed experts of moe.cu, whose output is added to the residual.
 #include <chrono>
 #include <cstdlib>
 #include <cmath>
@@ -45,6 +47,7 @@ struct Scratch {
   size_t gemv_bytes = 0;
   size_t gemv_counter_bytes = 0;  // leading counters, zero between launches
   void* argmax = nullptr;         // split-row argmax partials + per-row counters (zero between launches)
+  MoeScratch moe;                 // MoE layers' routing and expert buffers (when the model has any)
 };
 
 }  // namespace
@@ -66,6 +69,18 @@ struct fk_model {
   float attn_scale = 1.f;
   int sm_count = 0;
   bool has_local = false;
+  // mixture-of-experts layers: moe_index[l] = the layer's index among the MoE
+  // layers, -1 for a dense layer
+  std::vector<uint8_t> moe_kinds;
+  std::vector<int> moe_index;
+  std::vector<MoeWeights> moe;
+  int n_moe = 0;
+  // routing hook (fk_model_set_moe_routing)
+  const int32_t* moe_forced = nullptr;
+  int32_t* moe_trace_ids = nullptr;
+  float* moe_trace_margin = nullptr;
+  int moe_hook_tokens = 0;
+  bool moe_hook() const { return moe_forced || moe_trace_ids || moe_trace_margin; }
   // 1 when the activation storage site (an FK_F16_* bit) holds IEEE f16
   int f16(uint32_t site) const { return (cfg.f16_sites & site) ? 1 : 0; }
 };
@@ -104,16 +119,45 @@ namespace {
 // ---------------------------------------------------------------------------
 // validation
 // ---------------------------------------------------------------------------
+// 1 for each MoE layer (all layers when moe_layers is NULL and there are experts)
+bool is_moe_layer(const fk_config* c, int l) {
+  if (c->n_experts <= 0) return false;
+  return c->moe_layers ? c->moe_layers[l] == 1 : true;
+}
+
+bool has_dense_layer(const fk_config* c) {
+  for (int l = 0; l < c->n_layers; ++l)
+    if (!is_moe_layer(c, l)) return true;
+  return false;
+}
+
 fk_status validate_config(const fk_config* c) {
   if (!c) return fail(FK_ERR_INVALID_ARG, "config is NULL");
   auto bad = [](const char* m) { return fail(FK_ERR_INVALID_CONFIG, m); };
   if (c->n_layers < 1) return bad("n_layers must be >= 1");
+  if (c->n_experts < 0) return bad("n_experts must be >= 0");
+  if (c->n_experts == 0) {
+    if (c->moe_layers)
+      for (int l = 0; l < c->n_layers; ++l)
+        if (c->moe_layers[l]) return bad("moe_layers marks a MoE layer but n_experts is 0");
+  } else {
+    if (c->n_experts % 8 || c->n_experts > kMoeMaxExperts) return bad("n_experts must be a multiple of 8, at most 256");
+    if (c->n_experts_per_tok < 1 || c->n_experts_per_tok > std::min(c->n_experts, kMoeMaxK))
+      return bad("n_experts_per_tok must be in [1, min(n_experts, 16)]");
+    if (c->expert_intermediate < 64 || c->expert_intermediate % 64)
+      return bad("expert_intermediate must be a positive multiple of 64");
+    if (c->norm_topk != 0 && c->norm_topk != 1) return bad("norm_topk must be 0 or 1");
+    if (c->moe_layers)
+      for (int l = 0; l < c->n_layers; ++l)
+        if (c->moe_layers[l] > 1) return bad("moe_layers entries must be 0 (dense) or 1 (MoE)");
+  }
   if (c->hidden < 64 || c->hidden % 64) return bad("hidden must be a positive multiple of 64");
   if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads)
     return bad("n_q_heads must be a positive multiple of n_kv_heads");
   if (c->n_q_heads / c->n_kv_heads > 8) return bad("more than 8 query heads per kv head");
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return bad("head_dim must be 64, 128 or 256");
-  if (c->intermediate < 64 || c->intermediate % 64) return bad("intermediate must be a positive multiple of 64");
+  if (has_dense_layer(c) && (c->intermediate < 64 || c->intermediate % 64))
+    return bad("intermediate must be a positive multiple of 64");
   if (c->vocab < 8 || c->vocab % 8) return bad("vocab must be a positive multiple of 8");
   if (!(c->rms_eps > 0.f) || !std::isfinite(c->rms_eps)) return bad("rms_eps must be > 0");
   if (!(c->rope_theta_global > 1.0) || !(c->rope_theta_local > 1.0)) return bad("rope thetas must be > 1");
@@ -156,15 +200,24 @@ size_t rope_table_bytes(const fk_config* c, int max_pos) {
 // Bytes of the f16 copies of the weights whose GEMM input site is f16: per
 // layer Wq, Wk, Wv (FK_F16_QKV_IN), Wo (FK_F16_O_IN), W_gate, W_up
 // (FK_F16_FFN_IN), W_down (FK_F16_FFN_ACT); the head (FK_F16_HEAD_IN).
+// MoE layers: the router and the experts' gate/up matrices (FK_F16_FFN_IN),
+// the experts' down matrices (FK_F16_FFN_ACT).
 size_t f16_copy_bytes(const fk_config* c) {
   const size_t H = c->hidden, I = c->intermediate, Nq = (size_t)c->n_q_heads * c->head_dim,
-               Nkv = (size_t)c->n_kv_heads * c->head_dim;
-  size_t per_layer = 0;
-  if (c->f16_sites & FK_F16_QKV_IN) per_layer += align_up(Nq * H * 2) + 2 * align_up(Nkv * H * 2);
-  if (c->f16_sites & FK_F16_O_IN) per_layer += align_up(H * Nq * 2);
-  if (c->f16_sites & FK_F16_FFN_IN) per_layer += 2 * align_up(I * H * 2);
-  if (c->f16_sites & FK_F16_FFN_ACT) per_layer += align_up(H * I * 2);
-  size_t b = per_layer * c->n_layers;
+               Nkv = (size_t)c->n_kv_heads * c->head_dim, E = std::max(c->n_experts, 0),
+               Ie = std::max(c->expert_intermediate, 0);
+  size_t b = 0;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->f16_sites & FK_F16_QKV_IN) b += align_up(Nq * H * 2) + 2 * align_up(Nkv * H * 2);
+    if (c->f16_sites & FK_F16_O_IN) b += align_up(H * Nq * 2);
+    if (is_moe_layer(c, l)) {
+      if (c->f16_sites & FK_F16_FFN_IN) b += align_up(E * H * 2) + 2 * align_up(E * Ie * H * 2);
+      if (c->f16_sites & FK_F16_FFN_ACT) b += align_up(E * H * Ie * 2);
+    } else {
+      if (c->f16_sites & FK_F16_FFN_IN) b += 2 * align_up(I * H * 2);
+      if (c->f16_sites & FK_F16_FFN_ACT) b += align_up(H * I * 2);
+    }
+  }
   if (c->f16_sites & FK_F16_HEAD_IN) b += align_up((size_t)c->vocab * H * 2);
   return b;
 }
@@ -221,14 +274,23 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
   t.u = take((size_t)T * c.hidden * 2);
   t.qkv = take((size_t)T * m->Nqkv * 2);
   t.ao = take((size_t)T * m->Nq * 2);
-  t.h = take((size_t)T * c.intermediate * 2);
+  if (has_dense_layer(&c)) t.h = take((size_t)T * c.intermediate * 2);
   // few-token GEMMs (T <= 64, or decode/short chunks up to that size) need
   // split-K scratch: one counter region sized for the GEMM with the most
   // tiles, then room for the largest GEMM's partial sums
   const int Ms = (int)std::min<long>(T, kSkinnyMaxTokens);
   size_t gb = 0, cb = 0;
   if (!m->g_qkv.empty()) {
-    const GemmWeights* all[5] = {&m->g_qkv[0], &m->g_o[0], &m->g_gu[0], &m->g_down[0], &m->g_head};
+    // every layer's GEMMs have the shapes of layer 0's, or of the first
+    // dense layer's and the MoE router's
+    std::vector<const GemmWeights*> all = {&m->g_qkv[0], &m->g_o[0], &m->g_head};
+    for (int l = 0; l < c.n_layers; ++l)
+      if (m->moe_index[l] < 0) {
+        all.push_back(&m->g_gu[l]);
+        all.push_back(&m->g_down[l]);
+        break;
+      }
+    if (m->n_moe) all.push_back(&m->moe[0].router);
     size_t pb = 0;
     for (const GemmWeights* g : all) {
       cb = std::max(cb, skinny_counter_bytes(*g, Ms, m->sm_count));
@@ -240,6 +302,7 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
   t.gemv_counter_bytes = cb;
   t.gemv = gb ? take(gb) : nullptr;
   t.argmax = take(argmax_scratch_bytes());
+  if (m->n_moe) off += moe_scratch(m->moe[0], T, &t.moe, base ? base + off : nullptr);
   if (s) *s = t;
   return off;
 }
@@ -279,6 +342,8 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   const long T = (long)B * S;
   const bool sandwich = c.norm_layout == FK_NORM_SANDWICH;
   float* x_in = slots ? slots : sc.x0;
+  if (m->moe_hook() && T > m->moe_hook_tokens)
+    return fail(FK_ERR_INVALID_ARG, "more tokens than the MoE routing hook holds");
   // Layer GEMMs of decode steps stream weights through the split-K kernel.
   // Prefill (any chunk size) keeps the tiled kernel, whose per-element
   // summation order does not depend on the row count: chunked cached prefill
@@ -341,6 +406,27 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
       ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
       FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st, m->f16(FK_F16_FFN_IN)));
+    }
+    const int mi = m->moe_index[l];
+    if (mi >= 0) {
+      // mixture-of-experts FFN: out = x_mid + sum of the routed experts (pre-norm) or the sum alone (sandwich)
+      const MoeWeights& mw = m->moe[mi];
+      const size_t hook_rows = (size_t)m->moe_hook_tokens * mw.k;
+      const int32_t* forced = m->moe_forced ? m->moe_forced + (size_t)mi * hook_rows : nullptr;
+      int32_t* t_ids = m->moe_trace_ids ? m->moe_trace_ids + (size_t)mi * hook_rows : nullptr;
+      float* t_margin = m->moe_trace_margin ? m->moe_trace_margin + (size_t)mi * m->moe_hook_tokens : nullptr;
+      FK_TRY(moe_ffn_run(mw, sc.u, (int)T, sc.moe, forced, t_ids, t_margin, sandwich ? sc.a : x_out,
+                         sandwich ? nullptr : x_mid, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes));
+      if (sandwich) {
+        ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
+        FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps,
+                                            sc.u, st, next_f16));
+      } else {
+        ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
+        FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st, next_f16));
+      }
+      x_in = x_out;
+      continue;
     }
     // gated FFN
     GemmOut og;
@@ -445,6 +531,14 @@ extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, 
   m->Nkv = cfg->n_kv_heads * cfg->head_dim;
   m->Nqkv = m->Nq + 2 * m->Nkv;
   m->embed_scale = cfg->embed_scale == FK_EMBED_SCALE_SQRT_HIDDEN_BF16 ? bf16_round(std::sqrt((float)cfg->hidden)) : 1.f;
+  m->moe_kinds.assign(cfg->n_layers, 0);
+  m->moe_index.assign(cfg->n_layers, -1);
+  for (int l = 0; l < cfg->n_layers; ++l)
+    if (is_moe_layer(cfg, l)) {
+      m->moe_kinds[l] = 1;
+      m->moe_index[l] = m->n_moe++;
+    }
+  m->cfg.moe_layers = m->moe_kinds.data();
   m->attn_scale = 1.0f / std::sqrt((float)cfg->head_dim);
 
   auto cleanup = [&](fk_status s) {
@@ -457,9 +551,16 @@ extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, 
     if (!aligned16(p)) return cleanup(fail(FK_ERR_INVALID_ARG, "weights must be 16-byte aligned"));
   for (int l = 0; l < cfg->n_layers; ++l) {
     const fk_layer_weights& lw = m->layers[l];
-    const void* need_ptrs[] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo, lw.ffn_norm, lw.w_gate, lw.w_up, lw.w_down};
+    const void* need_ptrs[] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo, lw.ffn_norm};
     for (const void* p : need_ptrs)
       if (!p || !aligned16(p)) return cleanup(fail(FK_ERR_INVALID_ARG, "layer weight missing or misaligned"));
+    const bool moe = m->moe_index[l] >= 0;
+    const void* ffn_ptrs[4] = {moe ? lw.router : lw.w_gate, moe ? lw.expert_gate : lw.w_up,
+                               moe ? lw.expert_up : lw.w_down, moe ? lw.expert_down : lw.w_down};
+    for (const void* p : ffn_ptrs)
+      if (!p || !aligned16(p))
+        return cleanup(fail(FK_ERR_INVALID_ARG, moe ? "MoE layer weight (router or experts) missing or misaligned"
+                                                    : "layer weight missing or misaligned"));
     if (cfg->qk_norm && (!lw.q_norm || !lw.k_norm || !aligned16(lw.q_norm) || !aligned16(lw.k_norm)))
       return cleanup(fail(FK_ERR_INVALID_ARG, "qk_norm weights missing"));
     if (cfg->norm_layout == FK_NORM_SANDWICH &&
@@ -504,6 +605,16 @@ extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, 
       lw.wv = f16_copy(lw.wv, (size_t)m->Nkv * H);
     }
     if (m->f16(FK_F16_O_IN)) lw.wo = f16_copy(lw.wo, (size_t)H * m->Nq);
+    if (m->moe_index[l] >= 0) {
+      const size_t E = cfg->n_experts, Ie = cfg->expert_intermediate;
+      if (m->f16(FK_F16_FFN_IN)) {
+        lw.router = f16_copy(lw.router, E * H);
+        lw.expert_gate = f16_copy(lw.expert_gate, E * Ie * H);
+        lw.expert_up = f16_copy(lw.expert_up, E * Ie * H);
+      }
+      if (m->f16(FK_F16_FFN_ACT)) lw.expert_down = f16_copy(lw.expert_down, E * H * Ie);
+      continue;
+    }
     if (m->f16(FK_F16_FFN_IN)) {
       lw.w_gate = f16_copy(lw.w_gate, (size_t)I * H);
       lw.w_up = f16_copy(lw.w_up, (size_t)I * H);
@@ -526,9 +637,30 @@ extern "C" fk_status fk_model_create(const fk_config* cfg, const fk_weights* w, 
     const void* wo[1] = {lw.wo};
     int ro[1] = {H};
     if (s == FK_OK) s = gemm_weights_init(&m->g_o[l], wo, ro, 1, m->Nq, 0, m->f16(FK_F16_O_IN));
+    if (s != FK_OK) return cleanup(s);
+    if (m->moe_index[l] >= 0) {
+      MoeWeights mw;
+      mw.E = cfg->n_experts;
+      mw.k = cfg->n_experts_per_tok;
+      mw.Ie = cfg->expert_intermediate;
+      mw.H = H;
+      mw.norm_topk = cfg->norm_topk;
+      mw.act = cfg->act;
+      mw.act_f16 = m->f16(FK_F16_FFN_ACT);
+      const void* rt[1] = {lw.router};
+      int re[1] = {mw.E};
+      s = gemm_weights_init(&mw.router, rt, re, 1, H, 0, m->f16(FK_F16_FFN_IN));
+      const void* egu[2] = {lw.expert_gate, lw.expert_up};
+      if (s == FK_OK) s = gemm_weights_init_grouped(&mw.gate_up, egu, 2, mw.E, mw.Ie, H, 1, m->f16(FK_F16_FFN_IN));
+      const void* ed[1] = {lw.expert_down};
+      if (s == FK_OK) s = gemm_weights_init_grouped(&mw.down, ed, 1, mw.E, H, mw.Ie, 0, m->f16(FK_F16_FFN_ACT));
+      if (s != FK_OK) return cleanup(s);
+      m->moe.push_back(mw);
+      continue;
+    }
     const void* gu[2] = {lw.w_gate, lw.w_up};
     int rg[2] = {I, I};
-    if (s == FK_OK) s = gemm_weights_init(&m->g_gu[l], gu, rg, 2, H, 1, m->f16(FK_F16_FFN_IN));
+    s = gemm_weights_init(&m->g_gu[l], gu, rg, 2, H, 1, m->f16(FK_F16_FFN_IN));
     const void* wd[1] = {lw.w_down};
     int rd[1] = {H};
     if (s == FK_OK) s = gemm_weights_init(&m->g_down[l], wd, rd, 1, I, 0, m->f16(FK_F16_FFN_ACT));
@@ -746,6 +878,8 @@ extern "C" fk_status fk_session_prefill(fk_session* s, const int32_t* ids, int32
   if (s->len + seq > s->max_seq) return fail(FK_ERR_CONTEXT_FULL, "prefill would exceed the session's max_seq");
   if (d_last_logits && !aligned16(d_last_logits)) return fail(FK_ERR_INVALID_ARG, "logits must be 16-byte aligned");
   fk_model* m = s->m;
+  if (m->moe_hook() && seq > s->max_chunk)
+    return fail(FK_ERR_INVALID_ARG, "prefill in more than one chunk while the MoE routing hook is set");
   if (!ids_on_device) FK_TRY(check_ids_host(ids, (long)s->B * seq, m->cfg.vocab));
   FK_TRY(check_device(nullptr));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -813,7 +947,7 @@ extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* 
   // graph captured on the first such call (re-captured if the output
   // buffers change). Steps with caller ids, and steps while kernel timing is
   // on, are launched one by one.
-  if (d_ids || profiling_enabled() || graphs_disabled()) {
+  if (d_ids || profiling_enabled() || graphs_disabled() || s->m->moe_hook()) {
     FK_TRY(enqueue_decode(s, d_ids, d_logits, d_next, d_margin, st));
     s->len += 1;
     return FK_OK;
@@ -898,6 +1032,48 @@ extern "C" fk_status fk_op_head_argmax(fk_model* m, const void* d_u, int32_t row
   FK_TRY(gemm_run(d_u, rows, m->cfg.hidden, m->g_head, o, m->dev_err, st));
   if (d_argmax) FK_LAUNCH(launch_argmax(d_logits, rows, m->cfg.vocab, m->cfg.vocab, d_argmax, st, nullptr, nullptr, d_margin));
   return FK_OK;
+}
+
+extern "C" fk_status fk_model_set_moe_routing(fk_model* m, const int32_t* d_forced, int32_t* d_trace_ids,
+                                              float* d_trace_margin, int32_t max_tokens) {
+  if (!m) return fail(FK_ERR_INVALID_ARG, "fk_model_set_moe_routing: model is NULL");
+  const bool any = d_forced || d_trace_ids || d_trace_margin;
+  if (any && (m->n_moe == 0 || max_tokens < 1))
+    return fail(FK_ERR_INVALID_ARG, "fk_model_set_moe_routing: needs a model with MoE layers and max_tokens >= 1");
+  m->moe_forced = d_forced;
+  m->moe_trace_ids = d_trace_ids;
+  m->moe_trace_margin = d_trace_margin;
+  m->moe_hook_tokens = any ? max_tokens : 0;
+  return FK_OK;
+}
+
+static size_t moe_op_bytes(const fk_model* m, int T, MoeScratch* s, uint8_t* base) {
+  return moe_scratch(m->moe[0], T, s, base);
+}
+
+extern "C" size_t fk_op_moe_ffn_workspace_bytes(const fk_model* m, int32_t T) {
+  if (!m || m->n_moe == 0 || T < 1) {
+    set_error("fk_op_moe_ffn_workspace_bytes: needs a model with MoE layers and T >= 1");
+    return 0;
+  }
+  return moe_op_bytes(m, T, nullptr, nullptr);
+}
+
+extern "C" fk_status fk_op_moe_ffn(fk_model* m, int32_t layer, const void* d_u, int32_t T, const int32_t* d_forced,
+                                   float* d_out, int32_t* d_ids, float* d_margin, void* d_ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!m || !d_u || !d_out || T < 1) return fail(FK_ERR_INVALID_ARG, "fk_op_moe_ffn: bad argument");
+  if (layer < 0 || layer >= m->cfg.n_layers || m->moe_index[layer] < 0)
+    return fail(FK_ERR_INVALID_ARG, "fk_op_moe_ffn: not a MoE layer");
+  if (!aligned16(d_u) || !aligned16(d_out)) return fail(FK_ERR_INVALID_ARG, "fk_op_moe_ffn: buffers must be 16-byte aligned");
+  if (!d_ws || ws_bytes < fk_op_moe_ffn_workspace_bytes(m, T))
+    return fail(FK_ERR_WORKSPACE, "fk_op_moe_ffn: workspace too small");
+  if (reinterpret_cast<uintptr_t>(d_ws) % kAlign) return fail(FK_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  FK_TRY(check_device(nullptr));
+  MoeScratch sc;
+  moe_op_bytes(m, T, &sc, static_cast<uint8_t*>(d_ws));
+  return moe_ffn_run(m->moe[m->moe_index[layer]], d_u, T, sc, d_forced, d_ids, d_margin, d_out, nullptr, m->dev_err,
+                     static_cast<cudaStream_t>(stream));
 }
 
 // ===========================================================================
