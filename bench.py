@@ -25,7 +25,15 @@ same public API (CUDA events, after warm-up, L2 flushed between repeats):
   C  SmolLM2-135M shape with KV cache: 8 x 1024 session prefill (tok/s), then
      64 greedy decode steps (tok/s);
   E  Gemma3-style tower, cacheless forward at 1, 9 and 1024 ids (latency,
-     tok/s).
+     tok/s);
+  M  Qwen3-30B-A3B-shaped mixture-of-experts model at full depth (48 layers,
+     128 experts of width 768, 8 per token): session prefill of 4 x 4096
+     (tok/s, per-kernel time, tensor-core roofline of the grouped expert
+     GEMM), greedy decode at batch 32 and 1 from context 2048 (tok/s, HBM
+     roofline of the step). Its weights are drawn on the device (torch's
+     seeded generator, N(0, 0.02^2) bf16, unit norm weights): 61 GB that the
+     host generator would take minutes to make and copy.
+  python bench.py --all-configs --only M   (a subset of the workloads)
 
 N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
 path has no cross-sequence exchange, so there is no data-path collective.
@@ -70,7 +78,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (profiling of a small case only)")
-    ap.add_argument("--all-configs", action="store_true", help="time the other workloads (A, B, C, E)")
+    ap.add_argument("--all-configs", action="store_true", help="time the other workloads (A, B, C, E, M)")
+    ap.add_argument("--only", default="", help="with --all-configs: comma-separated subset, e.g. M")
     ap.add_argument("--no-f16", action="store_true", help="skip the f16 activation-storage timing")
     return ap.parse_args()
 
@@ -177,6 +186,42 @@ def host_weights(cfg, seed: int = synth.SEED_WEIGHTS) -> dict:
     return synth.make_weights(cfg, seed=seed)
 
 
+def device_weights(cfg, device, seed: int = synth.SEED_WEIGHTS, sigma: float = 0.02) -> dict:
+    """Weights of cfg's shapes drawn on the device: N(0, sigma^2) bf16
+    matrices from torch's generator seeded with `seed`, norm weights 1.0."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = {}
+    for name, shape in synth.weight_shapes(cfg).items():
+        if name == "final_norm" or name.split(".")[-1] in synth.NORM_TENSORS:
+            out[name] = torch.ones(shape, dtype=torch.bfloat16, device=device)
+            continue
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        inner = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+        step = max(1, (1 << 26) // inner)  # bound the fp32 temporary to 256 MB
+        for i in range(0, shape[0], step):
+            j = min(shape[0], i + step)
+            t[i:j] = (torch.randn((j - i,) + tuple(shape[1:]), generator=g, device=device) * sigma).to(torch.bfloat16)
+        out[name] = t
+    return out
+
+
+def read_profile(lib) -> dict:
+    """Kernel-class timings recorded by the library: {name: (launches, ms)};
+    clears them."""
+    import ctypes
+    prof = {}
+    for i in range(lib.fk_profile_count()):
+        name = ctypes.c_char_p()
+        n = ctypes.c_int64()
+        ms = ctypes.c_double()
+        lib.fk_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms))
+        prof[name.value.decode()] = (n.value, ms.value)
+    lib.fk_profile_reset()
+    return prof
+
+
 def upload(wbits: dict, device) -> dict:
     import torch
     out = {}
@@ -266,8 +311,114 @@ def _time_ms(fn, reps: int, flush=None) -> float:
     return statistics.median(times)
 
 
+def run_moe(args, fk, dev, peaks, flush, reps, emit):
+    """Workload M: the Qwen3-30B-A3B-shaped MoE model (module docstring)."""
+    import torch
+    lib = fk.load()
+    cfg = synth.CONFIGS["qwen3-moe-30b-a3b"]
+    if args.layers:
+        cfg = cfg.with_(n_layers=args.layers)
+    G = 8
+    t0 = time.time()
+    wdev = device_weights(cfg, dev)
+    setup_s = time.time() - t0
+    B, S = PREFILL_B, PREFILL_S
+    max_pos = max(S, DECODE_CTX + G * (reps + 6) + 8)
+    model = fk.Model(cfg, wdev, max_positions=max_pos)
+    H, L, E, k, Ie, V = cfg.hidden, cfg.n_layers, cfg.n_experts, cfg.n_experts_per_tok, cfg.expert_intermediate, cfg.vocab
+    Nq, Nkv = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    T = B * S
+
+    # prefill
+    sp = model.session(B, S, max_chunk=S)
+    ids_p = torch.from_numpy(synth.make_ids(cfg, B, S, stream=10)).to(dev)
+    z_p = torch.empty((B, V), dtype=torch.float32, device=dev)
+    n_p = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def prefill():
+        sp.reset()
+        sp.prefill(ids_p, logits=z_p, next_ids=n_p)
+    for _ in range(2):
+        prefill()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    ms_p = _time_ms(prefill, reps, flush)
+    clk = clocks.stop()
+    lib.fk_profile_reset()
+    lib.fk_profile_enable(1)
+    prefill()
+    lib.fk_profile_enable(0)
+    prof = read_profile(lib)
+    del sp
+    torch.cuda.empty_cache()
+    # algorithmic FLOPs of the prefill's GEMMs (expert rows only, no tile padding)
+    fl = {"moe_gate_up": 2.0 * T * k * H * 2 * Ie, "moe_down": 2.0 * T * k * Ie * H, "moe_router": 2.0 * T * H * E,
+          "gemm_qkv": 2.0 * T * H * (Nq + 2 * Nkv), "gemm_o": 2.0 * T * Nq * H}
+    gemm_flops = L * sum(fl.values()) + 2.0 * B * H * V
+    top = max(("moe_gate_up", "moe_down"), key=lambda n: prof.get(n, (0, 0.0))[1])
+    n_top, ms_top = prof.get(top, (0, 0.0))
+    ach = fl[top] * n_top / (ms_top / 1e3) / 1e12 if ms_top > 0 else None
+    tot_prof = sum(m for _, m in prof.values())
+
+    # decode at batch 32 and 1 from context 2048
+    ids_d = torch.from_numpy(synth.make_ids(cfg, DECODE_B, DECODE_CTX, stream=50)).to(dev)
+    dec = {}
+    for Bd in (DECODE_B, 1):
+        sd = model.session(Bd, max_pos, max_chunk=1024)
+        sd.prefill(ids_d[:Bd].contiguous())
+        z_d = torch.empty((Bd, V), dtype=torch.float32, device=dev)
+        n_d = torch.empty((Bd,), dtype=torch.int32, device=dev)
+        for _ in range(2 * G):  # warm-up, graph capture
+            sd.decode(None, logits=z_d, next_ids=n_d)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(G):
+                sd.decode(None, logits=z_d, next_ids=n_d)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / G)
+        ms_tok = statistics.median(times)
+        # the experts a step touches: one traced step (outside the timed region)
+        n_moe = sum(cfg.moe_kinds())
+        tr = torch.empty((n_moe, Bd, k), dtype=torch.int32, device=dev)
+        model.set_moe_routing(None, tr, None, Bd)
+        sd.decode(None, logits=z_d, next_ids=n_d)
+        torch.cuda.synchronize()
+        model.set_moe_routing()
+        uniq = float(np.mean([len(np.unique(tr[i].cpu().numpy())) for i in range(n_moe)]))
+        ctx = DECODE_CTX + 2 * G + G * reps // 2
+        step_bytes = (2.0 * L * (H * (Nq + 2 * Nkv) + Nq * H + E * H + uniq * 3 * H * Ie) + 2.0 * V * H
+                      + 2.0 * 2 * L * Nkv * Bd * ctx)
+        gbs = step_bytes / (ms_tok / 1e3) / 1e9
+        dec[Bd] = {"tok_s": Bd / ms_tok * 1e3, "ms_per_token_step": ms_tok, "experts_touched_per_layer": uniq,
+                   "step_bytes": step_bytes, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"]}
+        del sd
+        torch.cuda.empty_cache()
+    st, flags = model.sync_status()
+    if st != 0:
+        raise RuntimeError(f"device error word set (MoE workload): {flags:#x}")
+    emit({"config": "M", "workload": f"qwen3-30b-a3b-shaped MoE ({L} layers, {E} experts x {Ie}, top-{k}): "
+                                     f"session prefill {B}x{S}, greedy decode batch {DECODE_B} and 1 at context {DECODE_CTX}",
+          "data": "synthetic (device-drawn seeded N(0,0.02) bf16 weights, uniform ids)",
+          "prefill_tok_s": T / ms_p * 1e3, "prefill_ms": ms_p,
+          "prefill_tc_frac": gemm_flops / (ms_p / 1e3) / 1e12 / peaks["bf16_sustained"],
+          "roofline": {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"],
+                       "unit": "TFLOP/s", "frac": (ach / peaks["bf16_sustained"]) if ach else None,
+                       "peak_src": f"{peaks['src']} bf16 sustained",
+                       "flops_per_launch": fl[top], "note": "algorithmic FLOPs of the routed rows, no tile padding"},
+          "decode": {"batch": DECODE_B, **dec[DECODE_B]}, "decode_b1": {"batch": 1, **dec[1]},
+          "kernels_prefill": {n: {"launches": c, "ms": round(m, 3), "share": round(m / tot_prof, 4)}
+                              for n, (c, m) in sorted(prof.items(), key=lambda kv: -kv[1][1])},
+          "clocks": clk, "setup_s": round(setup_s, 1)})
+    del model, wdev
+    torch.cuda.empty_cache()
+
+
 def run_all_configs(args):
-    """One JSON line per workload A, B, C, E (see the module docstring)."""
+    """One JSON line per workload A, B, C, E, M (see the module docstring)."""
     import torch
     import transformer_decoder_forward_bf16_gb300 as fk
     dev = torch.device("cuda", 0)
@@ -277,9 +428,15 @@ def run_all_configs(args):
     hbm, tc = peaks["hbm"], peaks["bf16"]  # launches timed alone: the burst tensor-core figure
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2
     reps = max(5, args.steps)
+    only = set(args.only.split(",")) if args.only else {"A", "B", "C", "E", "M"}
 
     def emit(d):
         print(json.dumps(d), flush=True)
+
+    if "M" in only:
+        run_moe(args, fk, dev, peaks, flush, reps, emit)
+    if not only & {"A", "B", "C", "E"}:
+        return
 
     def weight_bytes(wbits):
         return sum(v.nbytes for v in wbits.values())

@@ -78,6 +78,9 @@ struct ProfScope {
 // of box_rows x 64 columns, 128-byte swizzle, out-of-bounds elements read as 0.
 fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
                          int box_rows);
+// 2-D fp32 row-major output [rows, cols] with row stride ld (elements), boxes
+// of 32 x 32, 128-byte swizzle: the target of TMA stores of staged tiles.
+fk_status make_tmap_f32_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld);
 
 // ---------------------------------------------------------------------------
 // GEMM (tcgen05): out = epilogue(A[M,K] · Bᵀ)

@@ -17,6 +17,10 @@
 //     residual add, or the gated activation act(gate)*up of the FFN.
 //   * the weight operand may be up to three matrices stacked along N (Q|K|V
 //     without a repacked copy) or a gate/up pair interleaved per tile;
+//   * fp32 outputs of the grouped mode are staged per 32 x 32 block in
+//     128-byte-swizzled shared memory and written by TMA bulk tensor stores
+//     (whole 128-byte lines, no per-row scatter from the epilogue threads),
+//     except blocks that cross the end of their group's rows;
 //   * grouped mode (the experts of a MoE layer): A holds the rows of every
 //     group back to back, group g at rows [off[g], off[g+1]) (offsets read
 //     from device memory at kernel start), and each group's rows multiply
@@ -62,12 +66,15 @@ struct GemmArgs {
 // M=128 accumulators share every B tile, a third fewer L2->SM bytes per FLOP
 // than MT == 1, at the price of a single accumulator set (the epilogue of a
 // tile no longer overlaps the next tile's MMAs).
-template <int BN, int MT = 1>
+// SO: fp32 output blocks staged in shared memory (two 4 KiB 32 x 32 blocks
+// per epilogue warp) and stored by TMA; one operand stage fewer to make room.
+template <int BN, int MT = 1, bool SO = false>
 struct Cfg {
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGES = MT == 2 ? 3 : ((BN == 256) ? 4 : 6);
-  static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int STAGES = SO ? ((BN == 256) ? 3 : 4) : (MT == 2 ? 3 : ((BN == 256) ? 4 : 6));
+  static constexpr int OUT_BYTES = SO ? kEpiWarps * 2 * 4096 : 0;
+  static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + OUT_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator sets (double buffer when they fit)
   static constexpr uint32_t TMEM_COLS = NACC * MT * BN;
 };
@@ -130,18 +137,19 @@ FK_DEVICE TileRows grouped_rows(const int* goff, const int* mstart, int groups, 
   return TileRows{goff[lo] + (mb - mstart[lo]) * BM, goff[lo + 1], lo};
 }
 
-template <int BN, int MT, bool GROUPED>
+template <int BN, int MT, bool GROUPED, bool SO>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                   const GemmArgs args) {
-  using C = Cfg<BN, MT>;
+                   const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
+  using C = Cfg<BN, MT, SO>;
   constexpr int TM = BM * MT;  // rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint8_t* sOut = sB + C::STAGES * C::B_BYTES;  // SO: staged output blocks (1024-byte aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + C::OUT_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -318,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue (warps 2..9) ----------------
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // which half of the tile's columns it stores
+    int oslot = 0;                     // SO: which of the warp's two staging blocks is next
     int local = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
       int mb, nb;
@@ -360,6 +369,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
           tmem_ld32(taddr + c * 32, v);
           const int col0 = nb * BN + c * 32;
+          if constexpr (SO) {
+            // a whole 32 x 32 fp32 block inside the output: stage it, store it by TMA
+            const int r0 = tr.row0 + sub * BM + q * 32;
+            if (args.epi == EPI_F32 && r0 + 32 <= tr.row_end && col0 + 32 <= args.n_out) {  // warp-uniform
+              if (args.softcap > 0.f) {
+                const float c_ = args.softcap, inv = 1.0f / args.softcap;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = c_ * tanhf(v[j] * inv);
+              }
+              uint8_t* buf = sOut + ((warp - 2) * 2 + oslot) * 4096;
+              if (lane == 0) bulk_wait_group_read<1>();  // the store issued from this block two blocks ago has read it
+              __syncwarp();
+              // row `lane` of the block: 16-byte chunk j at chunk position j ^ (row % 8) (128-byte swizzle)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmOut, buf, col0, r0);
+                bulk_commit_group();
+              }
+              oslot ^= 1;
+              continue;
+            }
+          }
           if (!row_ok || col0 >= args.n_out) continue;
           const bool full_chunk = col0 + 32 <= args.n_out;
           if (args.epi == EPI_BF16) {
@@ -410,6 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    if constexpr (SO) {
+      // the staged stores must finish before the CTA's shared memory goes away
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
@@ -420,12 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int MT, bool GROUPED = false>
-fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st) {
-  using C = Cfg<BN, MT>;
+template <int BN, int MT, bool GROUPED = false, bool SO = false>
+fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st,
+                    const CUtensorMap* tOut = nullptr) {
+  using C = Cfg<BN, MT, SO>;
   static DeviceOnce once;
   const cudaError_t attr_err = once.run([] {
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT, GROUPED, SO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
   // grouped: the m-block count is known on the device only; each group adds
@@ -434,8 +477,8 @@ fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs&
   const int n_blocks = a.glu ? (a.n_out + BN / 2 - 1) / (BN / 2) : (a.n_virtual + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int grid = std::min(tiles, sm_count);
-  gemm_tc_kernel<BN, MT, GROUPED><<<grid, kThreads, C::SMEM, st>>>(tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0],
-                                                           w.nseg > 2 ? w.map[2] : w.map[0], a);
+  gemm_tc_kernel<BN, MT, GROUPED, SO><<<grid, kThreads, C::SMEM, st>>>(
+      tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0], w.nseg > 2 ? w.map[2] : w.map[0], tOut ? *tOut : w.map[0], a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
   return FK_OK;
@@ -544,7 +587,15 @@ fk_status gemm_run_grouped(const void* A, int M, int lda, const GemmWeights& w, 
   a.groups = w.groups;
   a.group_rows = w.group_rows;
   const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
-  if (((M + BM - 1) / BM) * nb256 >= sm_count) return launch_bn<256, 1, true>(tA, w, a, sm_count, st);
+  const bool wide = ((M + BM - 1) / BM) * nb256 >= sm_count;
+  if (o.epi == EPI_F32) {  // fp32 out: staged blocks, TMA stores
+    CUtensorMap tOut;
+    s = make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo);
+    if (s != FK_OK) return s;
+    if (wide) return launch_bn<256, 1, true, true>(tA, w, a, sm_count, st, &tOut);
+    return launch_bn<128, 1, true, true>(tA, w, a, sm_count, st, &tOut);
+  }
+  if (wide) return launch_bn<256, 1, true>(tA, w, a, sm_count, st);
   return launch_bn<128, 1, true>(tA, w, a, sm_count, st);
 }
 

@@ -98,7 +98,7 @@ fk_status op_control_block(unsigned** out) {
   return FK_OK;
 }
 
-fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -111,6 +111,31 @@ fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64
     else
       cudaGetLastError();
   });
+  return encode;
+}
+
+fk_status make_tmap_f32_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return fail(FK_ERR_NO_DEVICE, "cuTensorMapEncodeTiled is unavailable (no CUDA driver)");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld * 4) % 16 || rows <= 0 || cols <= 0)
+    return fail(FK_ERR_INVALID_ARG, "fp32 tensor map: base must be 16-byte aligned, rows 16-byte multiples");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
+    return fail(FK_ERR_CUDA, buf);
+  }
+  return FK_OK;
+}
+
+fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
   if (!encode) return fail(FK_ERR_NO_DEVICE, "cuTensorMapEncodeTiled is unavailable (no CUDA driver)");
   if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld * 2) % 16 || rows <= 0 || cols <= 0 || box_rows > 256)
     return fail(FK_ERR_INVALID_ARG, "tensor map: base must be 16-byte aligned, rows 16-byte multiples");
