@@ -126,6 +126,24 @@ struct GemmOut {
   float softcap = 0.f;
   int act = 0;             // GLU activation: 0 SiLU, 1 GELU (tanh form)
   int out_f16 = 0;         // EPI_BF16 / EPI_GLU_BF16 store IEEE f16 instead of bf16
+  // few-token EPI_ADD_F32 with the fused split-K reduction (skinny_fused_tail):
+  // per 128-feature group sums of squares of each stored row, [M][ceil(n_out/128)]
+  float* ssq = nullptr;
+};
+
+// RMSNorm of the input fused into the few-token GEMM: the A operand becomes
+// 16-bit(x[t] * rsqrt(mean(x[t]^2) + eps) * w) of fp32 rows x [M, K] (row
+// stride ldx) and bf16 weights w [K]; for M <= kNormFuseMaxTokens.
+constexpr int kNormFuseMaxTokens = 2;
+// ssq (optional): per 128-feature group sums of squares of x's rows, [M][n_ssq],
+// from the GemmOut.ssq of the GEMM that produced x (else the rows are read whole).
+struct NormIn {
+  const float* x = nullptr;
+  int ldx = 0;
+  const void* w = nullptr;
+  float eps = 0.f;
+  const float* ssq = nullptr;
+  int n_ssq = 0;
 };
 
 // A: bf16 [M, K] with row stride lda (elements, multiple of 8). With M <=
@@ -133,8 +151,10 @@ struct GemmOut {
 // the weight-streaming split-K kernel runs instead of the tiled one.
 // counter_region: bytes at the start of the scratch reserved for the split-K
 // arrival counters of every GEMM sharing the scratch (0: this GEMM's own).
+// norm: fused input RMSNorm (few-token path only; A is then not read).
 fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
-                   cudaStream_t st, void* scratch = nullptr, size_t scratch_bytes = 0, size_t counter_region = 0);
+                   cudaStream_t st, void* scratch = nullptr, size_t scratch_bytes = 0, size_t counter_region = 0,
+                   const NormIn* norm = nullptr);
 
 // Grouped GEMM: rows [group_off[g], group_off[g+1]) of A (M rows in all)
 // multiply group g of the grouped operand w; group_off (device, groups + 1
@@ -156,6 +176,9 @@ SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count, bool allow_direct
 // Scratch of one skinny GEMM at up to M tokens: its arrival counters and its
 // fp32 partial sums (the partials of a smaller M never take more).
 size_t skinny_counter_bytes(const GemmWeights& w, int M, int sm_count);
+// The few-token GEMM of M <= kNormFuseMaxTokens rows finishes an epi output in
+// its own last CTAs (and can then write GemmOut.ssq).
+bool skinny_fused_tail(const GemmWeights& w, int M, int sm_count, int epi);
 size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count);
 // The scratch holds [counters: counter_region bytes (0 = this GEMM's own)]
 // [partial sums]. GEMMs that share a scratch share one counter region, sized
@@ -164,7 +187,7 @@ size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count);
 // clears them once; every launch leaves them zero again).
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
                           size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed = true,
-                          size_t counter_region = 0);
+                          size_t counter_region = 0, const NormIn* norm = nullptr);
 
 // The op-level few-row GEMM (fk_gemm_bf16_splitk) over a given scratch buffer.
 fk_status gemm_splitk_op(const void* d_x, const void* d_w, int P, int K, int N, void* d_y, int y_fp32,

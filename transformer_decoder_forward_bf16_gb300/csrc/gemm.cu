@@ -600,11 +600,12 @@ fk_status gemm_run_grouped(const void* A, int M, int lda, const GemmWeights& w, 
 }
 
 fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, unsigned* dev_err,
-                   cudaStream_t st, void* scratch, size_t scratch_bytes, size_t counter_region) {
+                   cudaStream_t st, void* scratch, size_t scratch_bytes, size_t counter_region, const NormIn* norm) {
   if (M == 0) return FK_OK;
   if (w.groups) return fail(FK_ERR_INVALID_ARG, "gemm_run: grouped operand needs gemm_run_grouped");
   if (M <= kSkinnyMaxTokens && scratch)
-    return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st, true, counter_region);
+    return gemm_run_skinny(A, M, lda, w, o, scratch, scratch_bytes, dev_err, st, true, counter_region, norm);
+  if (norm) return fail(FK_ERR_INVALID_ARG, "gemm_run: a fused input norm needs the few-token path");
 
   CUtensorMap tA;
   GemmArgs a;

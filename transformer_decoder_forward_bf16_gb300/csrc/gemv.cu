@@ -17,7 +17,12 @@
 //     fp32 + softcap, fp32 residual add, or the gated FFN activation
 //     act(gate) * up);
 //   * operands under 8 MB take a single split and apply the epilogue straight
-//     from TMEM.
+//     from TMEM;
+//   * an RMSNorm of the input may be fused in front (one or two tokens): the
+//     two otherwise idle warps read the fp32 rows, form the inverse RMS and
+//     write each k-block of the normalised 16-bit tokens into the pipeline
+//     stage themselves, in the layout the TMA copy of a stored input would
+//     have (the norm kernel and its launch boundary drop out of the chain).
 #include <algorithm>
 
 #include "fk_common.cuh"
@@ -46,6 +51,17 @@ struct SkinnyArgs {
   void* out;
   const float* res;
   float softcap;
+  // fused input RMSNorm (xn != NULL): tokens = 16-bit(xn[t] * rsqrt(mean(xn[t]^2) + eps) * nw);
+  // nssq (optional): the upstream GEMM's per-group sums of squares of xn, [M][n_ssq]
+  const float* xn;
+  int ldxn;
+  const __nv_bfloat16* nw;
+  float neps;
+  const float* nssq;
+  int n_ssq;
+  // fused reduction of an EPI_ADD_F32 output: per 128-feature group sums of
+  // squares of each stored row, [M][gridDim.x] (for a fused norm downstream)
+  float* ssq_out;
 };
 
 FK_DEVICE float act_silu(float g) { return g / (1.0f + expf(-g)); }
@@ -118,6 +134,8 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  __shared__ int s_norm_ok;            // fused norm: the stage wait's outcome, for both warps
+  __shared__ float s_ssq[4][kNormFuseMaxTokens];  // per-warp sums of squares of stored rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * 128;
   const int split = blockIdx.y;
@@ -126,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], args.xn ? 2 : 1);  // fused norm: the token tile's writers arrive too
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
@@ -160,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     const CUtensorMap* maps[3] = {&tmW0, &tmW1, &tmW2};
     int map[2], row[2];
     bool valid[2];
-    uint32_t bytes = C::B_BYTES;
+    uint32_t bytes = args.xn ? 0u : (uint32_t)C::B_BYTES;  // fused norm: no token-tile copy
     for (int i = 0; i < 2; ++i) {
       const int v = n0 + i * 64;
       int m = 0;
@@ -190,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
     pdl_trigger();
     for (int it = 0; it < npre; ++it) {
       if (stall && it == 0) continue;
-      tma_load_2d(&tmX, &full[it], smem + it * C::STAGE + A_BYTES, (kb0 + it) * 64, 0);
+      if (!args.xn) tma_load_2d(&tmX, &full[it], smem + it * C::STAGE + A_BYTES, (kb0 + it) * 64, 0);
       ++issued[it];
     }
     for (int kb = kb0 + npre, it = npre; kb < kb1; ++kb, ++it) {
@@ -205,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
       for (int i = 0; i < 2; ++i)
         if (valid[i])
           tma_load_2d_hint(maps[map[i]], &full[stage], sa + i * 64 * 128, kb * 64, row[i], evict_first);
-      tma_load_2d(&tmX, &full[stage], sa + A_BYTES, kb * 64, 0);
+      if (!args.xn) tma_load_2d(&tmX, &full[stage], sa + A_BYTES, kb * 64, 0);
       ++issued[stage];
     }
     if (!ok) {
@@ -233,6 +251,71 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
       umma_commit(&empty[stage]);
     }
     umma_commit(done);
+  } else if (args.xn && warp >= 2) {
+    // ---- fused input RMSNorm: warp 2 writes token 0's row of every stage's
+    // token tile, warp 3 token 1's (at most kNormFuseMaxTokens tokens)
+    const int nt = threadIdx.x - 64;  // 0..63
+    const int M = args.M, K = args.K;
+    const int t = warp - 2, pc = lane * 2;  // this thread's token row and column pair of a k-block
+    const bool act = t < M;
+    // rows M..BT-1 of the token tiles stay zero
+    for (int i = nt; i < kStages * (C::B_BYTES / 16); i += 64) {
+      const int stage = i / (C::B_BYTES / 16), chunk = i % (C::B_BYTES / 16);
+      if (chunk >= M * 8) *reinterpret_cast<uint4*>(smem + stage * C::STAGE + A_BYTES + chunk * 16) = make_uint4(0, 0, 0, 0);
+    }
+    const float* xr = args.xn + (size_t)(act ? t : 0) * args.ldxn;
+    // the first stages' inputs are requested with the row statistics (one round trip)
+    float2 xv[kStages];
+    uint32_t wv[kStages];
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) {
+      const int col = (kb0 + j) * 64 + pc;
+      const bool in = act && kb0 + j < kb1 && col < K;
+      xv[j] = in ? __ldcg(reinterpret_cast<const float2*>(xr + col)) : make_float2(0.f, 0.f);
+      wv[j] = in ? *reinterpret_cast<const uint32_t*>(args.nw + col) : 0u;
+    }
+    float q = 0.f;
+    if (args.nssq) {  // the upstream reduction's group sums, in group order
+      if (act)
+        for (int g = lane; g < args.n_ssq; g += 32) q += __ldcg(args.nssq + (size_t)t * args.n_ssq + g);
+    } else if (act) {  // the whole row
+#pragma unroll 8
+      for (int c = lane * 4; c < K; c += 128) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(xr + c));
+        q += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
+    }
+    const float inv = rsqrtf(warp_sum(q) / K + args.neps);
+    auto write = [&](int stage, float2 x, uint32_t wp) {
+      if (!act) return;
+      uint8_t* xs = smem + stage * C::STAGE + A_BYTES;
+      // 128-byte swizzle: 16-byte chunk j of row t sits at chunk position j ^ (t % 8)
+      *reinterpret_cast<uint32_t*>(xs + t * 128 + ((((pc * 2) >> 4) ^ (t & 7)) << 4) + ((pc * 2) & 15)) =
+          pack_16x2(x.x * inv * bf16_lo(wp), x.y * inv * bf16_hi(wp), args.ab_f16);
+    };
+    auto publish = [&](int stage) {  // the tile's writes, then one arrival for both warps
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      if (nt == 0) mbar_arrive(&full[stage]);
+    };
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) {  // fresh ring: every stage is free
+      if (kb0 + j >= kb1) break;
+      write(j, xv[j], wv[j]);
+      publish(j);
+    }
+    for (int kb = kb0 + kStages, it = kStages; kb < kb1; ++kb, ++it) {
+      const int stage = it % kStages;
+      // the stage's previous k-block has been consumed (one waiter, then both warps)
+      if (nt == 0) s_norm_ok = mbar_wait(&empty[stage], ((it / kStages) - 1) & 1, abort_flag, args.dev_err);
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      if (!s_norm_ok) break;
+      const int col = kb * 64 + pc;
+      const bool in = act && col < K;
+      write(stage, in ? __ldcg(reinterpret_cast<const float2*>(xr + col)) : make_float2(0.f, 0.f),
+            in ? *reinterpret_cast<const uint32_t*>(args.nw + col) : 0u);
+      publish(stage);
+    }
   }
   __syncwarp();
   // ---- epilogue: every warp drains its 32 TMEM lanes (= 32 output features)
@@ -302,6 +385,17 @@ __global__ void __launch_bounds__(kThreads) gemv_tc_kernel(const __grid_constant
   const int f = group * 128 + threadIdx.x;
   if (f < args.n_out) reduce_store(args, gridDim.y, f);
   if (threadIdx.x == 0) args.counters[group] = 0;
+  if (args.ssq_out) {  // this group's sum of squares of every stored row (fixed order)
+    for (int t = 0; t < args.M; ++t) {
+      const float y = f < args.n_out ? static_cast<const float*>(args.out)[(size_t)t * args.ldo + f] : 0.f;
+      const float q = warp_sum(y * y);
+      if (lane == 0) s_ssq[warp][t] = q;
+    }
+    __syncthreads();
+    if (threadIdx.x < args.M)
+      args.ssq_out[(size_t)threadIdx.x * gridDim.x + group] =
+          ((s_ssq[0][threadIdx.x] + s_ssq[1][threadIdx.x]) + s_ssq[2][threadIdx.x]) + s_ssq[3][threadIdx.x];
+  }
 }
 
 // Sum the splits in order and apply the epilogue; one thread per (token, 4 features).
@@ -410,6 +504,11 @@ SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count, bool allow_direct
 }
 
 
+bool skinny_fused_tail(const GemmWeights& w, int M, int sm_count, int epi) {
+  if (epi != EPI_ADD_F32 || w.glu || M < 1 || M > kNormFuseMaxTokens) return false;
+  return !skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count, true).direct;
+}
+
 size_t skinny_counter_bytes(const GemmWeights& w, int M, int sm_count) {
   if (M <= 0 || M > kSkinnyMaxTokens) return 0;
   return skinny_plan(M, w.K, w.seg_start[w.nseg], sm_count, !w.glu).counter_bytes;
@@ -429,10 +528,14 @@ size_t skinny_partial_bytes(const GemmWeights& w, int M, int sm_count) {
 
 fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, const GemmOut& o, void* scratch,
                           size_t scratch_bytes, unsigned* dev_err, cudaStream_t st, bool counters_zeroed,
-                          size_t counter_region) {
+                          size_t counter_region, const NormIn* norm) {
   int sms = 0;
   fk_status s = check_device(&sms);
   if (s != FK_OK) return s;
+  if (norm && (M > kNormFuseMaxTokens || !norm->x || !norm->w || norm->ldx < w.K || norm->ldx % 4 || w.K % 4))
+    return fail(FK_ERR_INVALID_ARG, "skinny GEMM: fused norm needs <= kNormFuseMaxTokens rows and fp32 rows of K");
+  if (o.ssq && !skinny_fused_tail(w, M, sms, o.epi))
+    return fail(FK_ERR_INVALID_ARG, "skinny GEMM: row sums of squares need the fused reduction of a residual output");
   const int n_rows = w.seg_start[w.nseg];
   const SkinnyPlan p = skinny_plan(M, w.K, n_rows, sms, !w.glu);
   const size_t creg = counter_region ? counter_region : p.counter_bytes;
@@ -469,6 +572,15 @@ fk_status gemm_run_skinny(const void* A, int M, int lda, const GemmWeights& w, c
   a.res = o.res;
   a.ldr = o.ldr;
   a.softcap = o.softcap;
+  if (norm) {
+    a.xn = norm->x;
+    a.ldxn = norm->ldx;
+    a.nw = static_cast<const __nv_bfloat16*>(norm->w);
+    a.neps = norm->eps;
+    a.nssq = norm->ssq;
+    a.n_ssq = norm->n_ssq;
+  }
+  a.ssq_out = o.ssq;
   if (a.fused && !counters_zeroed) FK_CUDA_TRY(cudaMemsetAsync(a.counters, 0, p.counter_bytes, st));
   if (BT == 16)
     s = launch_bt<16>(tX, w, a, p.n_tiles, p.splits, st);

@@ -47,6 +47,7 @@ struct Scratch {
   size_t gemv_bytes = 0;
   size_t gemv_counter_bytes = 0;  // leading counters, zero between launches
   void* argmax = nullptr;         // split-row argmax partials + per-row counters (zero between launches)
+  float* ssq = nullptr;           // decode of <= 2 tokens: residual rows' group sums of squares for a fused norm
   MoeScratch moe;                 // MoE layers' routing and expert buffers (when the model has any)
 };
 
@@ -302,6 +303,7 @@ size_t scratch_bytes(const fk_model* m, long T, Scratch* s, uint8_t* base) {
   t.gemv_counter_bytes = cb;
   t.gemv = gb ? take(gb) : nullptr;
   t.argmax = take(argmax_scratch_bytes());
+  t.ssq = reinterpret_cast<float*>(take((size_t)kNormFuseMaxTokens * ((c.hidden + 127) / 128) * 4));
   if (m->n_moe) off += moe_scratch(m->moe[0], T, &t.moe, base ? base + off : nullptr);
   if (s) *s = t;
   return off;
@@ -350,6 +352,13 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
   // then rounds every bf16 activation exactly as the cacheless forward does.
   void* gv = decode ? sc.gemv : nullptr;
   const size_t gvb = decode ? sc.gemv_bytes : 0;
+  // Decode steps of one or two sequences run the RMSNorm in front of a dense
+  // layer's gate/up projection, and in front of the next layer's QKV
+  // projection, inside those GEMMs: the norm kernels and their launch
+  // boundaries drop out of the step's dependency chain.
+  const bool fuse_norm = decode && !sandwich && T <= kNormFuseMaxTokens;
+  NormIn qkv_norm;  // the fused norm of the next QKV projection, when set
+  bool qkv_norm_set = false;
   { ProfScope ps(decode ? "embed_norm_dec" : "embed_norm", st);
   FK_LAUNCH(launch_embed_norm(ids ? ids : sc.ids, m->embed, (int)T, H, c.vocab, m->embed_scale, m->layers[0].attn_norm, c.rms_eps,
                               x_in, sc.u, m->dev_err, st, m->f16(FK_F16_QKV_IN))); }
@@ -371,7 +380,14 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     o.out_f16 = m->f16(FK_F16_ATTN);
     o.out = sc.qkv;
     o.ldo = m->Nqkv;
-    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
+    { ProfScope ps(decode ? "gemm_qkv_dec" : "gemm_qkv", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_qkv[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes, qkv_norm_set ? &qkv_norm : nullptr)); }
+    qkv_norm_set = false;
+    const bool fuse_ffn_norm = fuse_norm && m->moe_index[l] < 0;
+    NormIn ffn_norm;
+    ffn_norm.x = sc.x1;
+    ffn_norm.ldx = H;
+    ffn_norm.w = w.ffn_norm;
+    ffn_norm.eps = c.rms_eps;
     if (decode) {  // RoPE, cache write and attention in one kernel
       ProfScope ps("attn_decode", st);
       FK_LAUNCH(launch_attention_decode_rope(sc.qkv, m->Nqkv, kl, vl, cap, B, d_len, c.n_q_heads, c.n_kv_heads,
@@ -403,9 +419,16 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       o.ldo = H;
       o.res = x_in;
       o.ldr = H;
+      if (fuse_ffn_norm && skinny_fused_tail(m->g_o[l], (int)T, m->sm_count, EPI_ADD_F32)) {
+        o.ssq = sc.ssq;  // the gate/up projection's fused norm reads the row statistics from here
+        ffn_norm.ssq = sc.ssq;
+        ffn_norm.n_ssq = (H + 127) / 128;
+      }
       { ProfScope ps(decode ? "gemm_o_dec" : "gemm_o", st); FK_TRY(gemm_run(sc.ao, (int)T, m->Nq, m->g_o[l], o, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
-      ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
-      FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st, m->f16(FK_F16_FFN_IN)));
+      if (!fuse_ffn_norm) {
+        ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
+        FK_LAUNCH(launch_rmsnorm(x_mid, H, (int)T, H, w.ffn_norm, c.rms_eps, sc.u, H, st, m->f16(FK_F16_FFN_IN)));
+      }
     }
     const int mi = m->moe_index[l];
     if (mi >= 0) {
@@ -435,7 +458,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     og.out = sc.h;
     og.ldo = c.intermediate;
     og.act = c.act;
-    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
+    { ProfScope ps(decode ? "gemm_gate_up_dec" : "gemm_gate_up", st); FK_TRY(gemm_run(sc.u, (int)T, H, m->g_gu[l], og, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes, fuse_ffn_norm ? &ffn_norm : nullptr)); }
     if (sandwich) {
       GemmOut od;
       od.epi = EPI_F32;
@@ -452,9 +475,21 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       od.ldo = H;
       od.res = x_mid;
       od.ldr = H;
+      const bool down_ssq = fuse_norm && l + 1 < L && skinny_fused_tail(m->g_down[l], (int)T, m->sm_count, EPI_ADD_F32);
+      if (down_ssq) od.ssq = sc.ssq;
       { ProfScope ps(decode ? "gemm_down_dec" : "gemm_down", st); FK_TRY(gemm_run(sc.h, (int)T, c.intermediate, m->g_down[l], od, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes)); }
-      ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
-      FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st, next_f16));
+      if (fuse_norm && l + 1 < L) {  // the next QKV projection normalises x_out itself
+        qkv_norm.x = x_out;
+        qkv_norm.ldx = H;
+        qkv_norm.w = next_norm;
+        qkv_norm.eps = c.rms_eps;
+        qkv_norm.ssq = down_ssq ? sc.ssq : nullptr;
+        qkv_norm.n_ssq = (H + 127) / 128;
+        qkv_norm_set = true;
+      } else {
+        ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
+        FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st, next_f16));
+      }
     }
     x_in = x_out;
   }
