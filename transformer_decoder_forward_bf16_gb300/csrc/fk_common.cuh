@@ -83,6 +83,8 @@ FK_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_fla
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
+// Bring the 128-byte line at p into L2 (no register result, no wait).
+FK_DEVICE void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 FK_DEVICE void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

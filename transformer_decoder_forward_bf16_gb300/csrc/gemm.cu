@@ -17,10 +17,11 @@
 //     residual add, or the gated activation act(gate)*up of the FFN.
 //   * the weight operand may be up to three matrices stacked along N (Q|K|V
 //     without a repacked copy) or a gate/up pair interleaved per tile;
-//   * fp32 outputs of the grouped mode are staged per 32 x 32 block in
-//     128-byte-swizzled shared memory and written by TMA bulk tensor stores
-//     (whole 128-byte lines, no per-row scatter from the epilogue threads),
-//     except blocks that cross the end of their group's rows;
+//   * fp32 outputs (plain, softcapped or residual-added) are staged per
+//     32 x 32 block in 128-byte-swizzled shared memory and written by TMA
+//     bulk tensor stores (whole 128-byte lines, no per-row scatter from the
+//     epilogue threads), except blocks that cross the end of the rows (of
+//     their group) or of the columns;
 //   * grouped mode (the experts of a MoE layer): A holds the rows of every
 //     group back to back, group g at rows [off[g], off[g+1]) (offsets read
 //     from device memory at kernel start), and each group's rows multiply
@@ -66,14 +67,16 @@ struct GemmArgs {
 // M=128 accumulators share every B tile, a third fewer L2->SM bytes per FLOP
 // than MT == 1, at the price of a single accumulator set (the epilogue of a
 // tile no longer overlaps the next tile's MMAs).
-// SO: fp32 output blocks staged in shared memory (two 4 KiB 32 x 32 blocks
-// per epilogue warp) and stored by TMA; one operand stage fewer to make room.
+// SO: fp32 output blocks staged in shared memory (OUT_SLOTS 4 KiB 32 x 32
+// blocks per epilogue warp) and stored by TMA; one operand stage fewer to
+// make room (256-row tiles keep their three stages and one slot per warp).
 template <int BN, int MT = 1, bool SO = false>
 struct Cfg {
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGES = SO ? ((BN == 256) ? 3 : 4) : (MT == 2 ? 3 : ((BN == 256) ? 4 : 6));
-  static constexpr int OUT_BYTES = SO ? kEpiWarps * 2 * 4096 : 0;
+  static constexpr int STAGES = MT == 2 ? 3 : (SO ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : 6));
+  static constexpr int OUT_SLOTS = MT == 2 ? 1 : 2;
+  static constexpr int OUT_BYTES = SO ? kEpiWarps * OUT_SLOTS * 4096 : 0;
   static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + OUT_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator sets (double buffer when they fit)
   static constexpr uint32_t TMEM_COLS = NACC * MT * BN;
@@ -367,19 +370,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
-          tmem_ld32(taddr + c * 32, v);
           const int col0 = nb * BN + c * 32;
+          // residual add: the chunk's residual loads go out before the TMEM load's wait
+          float4 rv[8];
+          const bool res_full = args.epi == EPI_ADD_F32 && row_ok && col0 + 32 <= args.n_out;
+          if (res_full) {
+            const float4* r4 = reinterpret_cast<const float4*>(args.res + (size_t)row * args.ldr + col0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) rv[j] = r4[j];
+          }
+          tmem_ld32(taddr + c * 32, v);
           if constexpr (SO) {
             // a whole 32 x 32 fp32 block inside the output: stage it, store it by TMA
             const int r0 = tr.row0 + sub * BM + q * 32;
-            if (args.epi == EPI_F32 && r0 + 32 <= tr.row_end && col0 + 32 <= args.n_out) {  // warp-uniform
-              if (args.softcap > 0.f) {
+            if (r0 + 32 <= tr.row_end && col0 + 32 <= args.n_out) {  // warp-uniform
+              if (args.epi == EPI_ADD_F32) {  // res_full holds for every row of the block
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  v[4 * j] += rv[j].x;
+                  v[4 * j + 1] += rv[j].y;
+                  v[4 * j + 2] += rv[j].z;
+                  v[4 * j + 3] += rv[j].w;
+                }
+              } else if (args.softcap > 0.f) {
                 const float c_ = args.softcap, inv = 1.0f / args.softcap;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = c_ * tanhf(v[j] * inv);
               }
-              uint8_t* buf = sOut + ((warp - 2) * 2 + oslot) * 4096;
-              if (lane == 0) bulk_wait_group_read<1>();  // the store issued from this block two blocks ago has read it
+              uint8_t* buf = sOut + ((warp - 2) * C::OUT_SLOTS + oslot) * 4096;
+              // the store issued from this slot OUT_SLOTS blocks ago has read it
+              if (lane == 0) bulk_wait_group_read<C::OUT_SLOTS - 1>();
               __syncwarp();
               // row `lane` of the block: 16-byte chunk j at chunk position j ^ (row % 8) (128-byte swizzle)
 #pragma unroll
@@ -392,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_store_2d(&tmOut, buf, col0, r0);
                 bulk_commit_group();
               }
-              oslot ^= 1;
+              oslot = (oslot + 1) % C::OUT_SLOTS;
               continue;
             }
           }
@@ -415,14 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* o = reinterpret_cast<float*>(args.out) + (size_t)row * args.ldo + col0;
             if (args.epi == EPI_ADD_F32) {
               const float* r = args.res + (size_t)row * args.ldr + col0;
-              if (full_chunk) {
+              if (res_full) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                  float4 rv = *reinterpret_cast<const float4*>(r + j);
-                  v[j] += rv.x;
-                  v[j + 1] += rv.y;
-                  v[j + 2] += rv.z;
-                  v[j + 3] += rv.w;
+                for (int j = 0; j < 8; ++j) {
+                  v[4 * j] += rv[j].x;
+                  v[4 * j + 1] += rv[j].y;
+                  v[4 * j + 2] += rv[j].z;
+                  v[4 * j + 3] += rv[j].w;
                 }
               } else {
                 for (int j = 0; j < 32 && col0 + j < args.n_out; ++j) v[j] += r[j];
@@ -613,11 +632,20 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
   fk_status s = gemm_args(A, M, lda, w, o, dev_err, &tA, &a, &sm_count);
   if (s != FK_OK) return s;
   // 256x256 tiles while they give every SM at least two tiles; then 128x256;
-  // else 128-wide.
+  // else 128-wide. fp32 outputs: staged blocks, TMA stores.
   const int m_blocks = (M + BM - 1) / BM;
   const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
-  if (((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count) return launch_bn<256, 2>(tA, w, a, sm_count, st);
-  if (m_blocks * nb256 >= sm_count) return launch_bn<256, 1>(tA, w, a, sm_count, st);
+  const bool big = ((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count, wide = m_blocks * nb256 >= sm_count;
+  if (o.epi == EPI_F32 || o.epi == EPI_ADD_F32) {
+    CUtensorMap tOut;
+    s = make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo);
+    if (s != FK_OK) return s;
+    if (big) return launch_bn<256, 2, false, true>(tA, w, a, sm_count, st, &tOut);
+    if (wide) return launch_bn<256, 1, false, true>(tA, w, a, sm_count, st, &tOut);
+    return launch_bn<128, 1, false, true>(tA, w, a, sm_count, st, &tOut);
+  }
+  if (big) return launch_bn<256, 2>(tA, w, a, sm_count, st);
+  if (wide) return launch_bn<256, 1>(tA, w, a, sm_count, st);
   return launch_bn<128, 1>(tA, w, a, sm_count, st);
 }
 
