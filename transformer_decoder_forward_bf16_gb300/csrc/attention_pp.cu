@@ -18,18 +18,24 @@
 //              and the completion of S_i(j+1) implies PV_i(j) is done.
 //   warps 2-9  softmax of tile 0, warps 10-17 of tile 1: two warps per TMEM
 //              lane quarter (32 query rows, TMEM lane = row), one per 64-key
-//              half of the block. Mask (causal, window, sequence end), row
-//              maximum exchanged with the partner warp through shared memory,
-//              running max in the exp2 domain raised lazily (only when it
-//              grows by more than 2^8; then each warp rescales its half of the
-//              rows' O, which the S completion already guarantees idle),
-//              P = exp2(S - m) packed to 16 bits into the first 32 of the
-//              half's own 64 score columns, then the output O / l.
+//              half of the block. The running max m (exp2 domain) is raised
+//              lazily, only when a row's maximum grows by more than 2^8, so
+//              each warp first forms P = exp2(S - m) against the current m in
+//              one pipelined pass over its 64 score columns (mask: causal,
+//              window, sequence end), keeping P packed to 16 bits in
+//              registers, and only then exchanges its row maxima with the
+//              partner warp through shared memory. If some row's maximum
+//              outgrew m (and on a row's first visible block) both warps
+//              recompute P from the scores, still intact in TMEM, against
+//              the new m and rescale their half of the rows' O (idle: the S
+//              completion implies the previous PV). P goes to the first 32 of
+//              the half's own 64 score columns; at the end the output O / l.
 // q, K, Vᵀ and P are bf16, or all IEEE f16 (F16); the output bf16 or f16.
 // Every mbarrier wait is bounded (FK_DEVERR_PIPE_TIMEOUT on expiry); every
 // tcgen05.ld/st is executed by whole warps (decisions that touch TMEM are
 // taken warp-wide).
 #include <algorithm>
+#include <type_traits>
 
 #include "fk_common.cuh"
 #include "fk_internal.h"
@@ -60,28 +66,24 @@ struct PPCfg {
   static constexpr uint32_t O_COL = 2 * BKV;
 };
 
-// 64 consecutive fp32 columns of this thread's TMEM lane in one warp-wide
-// load (32x32b shape, .x64), then one wait
-FK_DEVICE void tmem_ld64(uint32_t taddr, float* v) {
-  uint32_t r[64];
+// 16 consecutive fp32 columns of this thread's TMEM lane, without the wait:
+// the registers may be read only after tmem_wait_ld16 on the same array
+FK_DEVICE void tmem_ld16_async(uint32_t taddr, uint32_t* r) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+// wait for the outstanding TMEM loads; r is passed through so that no use of
+// the loaded registers can be scheduled before the wait
+FK_DEVICE void tmem_wait_ld16(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (32x32b shape, .x16), then a wait
@@ -101,10 +103,6 @@ FK_DEVICE void tmem_st16(uint32_t taddr, const uint32_t* v) {
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
-}
-FK_DEVICE void tmem_st32_pp(uint32_t taddr, const uint32_t* v) {
-  tmem_st16(taddr, v);
-  tmem_st16(taddr + 16, v + 16);
 }
 FK_DEVICE void tmem_st_wait_pp() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -371,80 +369,85 @@ __global__ void __launch_bounds__(kPPThreads, 1)
       const bool edge = (j * BKV + BKV - 1 > tr.qp_lo) || (j * BKV + BKV > kv_len) ||
                         (window > 0 && tr.qp_hi - j * BKV >= window);
       auto visible = [&](int k) { return k <= qp && k < kv_len && (window == 0 || qp - k < window); };
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      {
-      float x[64];
-      tmem_ld64(lane_base + s_col, x);
-      if (edge) {
+      // P against the current m (0 where masked), 16-bit pairs in registers;
+      // the row maximum of the visible raw scores on the way. Four 16-column
+      // TMEM loads, each issued while the previous one is turned into P.
+      // (With no m yet the values are discarded below.)
+      uint32_t pk[32];
+      float mx = -INFINITY, l0 = 0.f, l1 = 0.f;
+      // the masked and unmasked versions are separate loops (edge is warp-uniform)
+      auto p_pass_as = [&](auto edge_c, auto want_max_c, float neg_m) {
+        constexpr bool kEdge = decltype(edge_c)::value, kMax = decltype(want_max_c)::value;
+        uint32_t sa[16], sb[16];
+        tmem_ld16_async(lane_base + s_col, sa);
+        tmem_wait_ld16(sa);
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          if (visible(key0 + e)) mx0 = fmaxf(mx0, x[e]);
-          if (visible(key0 + e + 1)) mx1 = fmaxf(mx1, x[e + 1]);
-        }
-      } else {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t* cur = (c & 1) ? sb : sa;
+          uint32_t* nxt = (c & 1) ? sa : sb;
+          if (c + 1 < 4) tmem_ld16_async(lane_base + s_col + (c + 1) * 16, nxt);
 #pragma unroll
-        for (int e = 0; e < 64; e += 4) {
-          mx0 = max3(mx0, x[e], x[e + 1]);
-          mx1 = max3(mx1, x[e + 2], x[e + 3]);
+          for (int e = 0; e < 16; e += 2) {
+            const float x0 = __uint_as_float(cur[e]), x1 = __uint_as_float(cur[e + 1]);
+            float p0 = ex2(fmaf(x0, scale_log2, neg_m));
+            float p1 = ex2(fmaf(x1, scale_log2, neg_m));
+            if constexpr (kEdge) {
+              const bool v0 = visible(key0 + c * 16 + e), v1 = visible(key0 + c * 16 + e + 1);
+              if constexpr (kMax) {
+                if (v0) mx = fmaxf(mx, x0);
+                if (v1) mx = fmaxf(mx, x1);
+              }
+              if (!v0) p0 = 0.f;
+              if (!v1) p1 = 0.f;
+            } else if constexpr (kMax) {
+              mx = max3(mx, x0, x1);
+            }
+            l0 += p0;
+            l1 += p1;
+            pk[(c * 16 + e) >> 1] = pack_16x2(p0, p1, io_f16);
+          }
+          if (c + 1 < 4) tmem_wait_ld16(nxt);
         }
-      }
-      }
-      my_max[r] = fmaxf(mx0, mx1);
+      };
+      using kT = std::true_type;
+      using kF = std::false_type;
+      auto p_pass = [&](float neg_m, auto want_max_c) {
+        if (edge) p_pass_as(kT{}, want_max_c, neg_m);
+        else p_pass_as(kF{}, want_max_c, neg_m);
+      };
+      p_pass(m == -INFINITY ? 0.f : -m, kT{});
+      my_max[r] = mx;
       // both warps of the row have published their maxima
       pair_sync();
       // scale_log2 > 0: the maximum of the scaled scores is the scaled maximum
-      const float m_new = fmaxf(m, fmaxf(my_max[r], other_max[r]) * scale_log2);
-      float m_use = m;
-      bool rescale = false;
-      if (m == -INFINITY) {
-        m_use = m_new;  // nothing accumulated in this row yet (O and l are 0)
-      } else if (m_new > m + kLazyRescale) {
-        m_use = m_new;
-        rescale = true;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // PV of the previous block is complete: S of this block was issued after it
-        const float corr = rescale ? ex2(m - m_use) : 1.f;
-        l *= corr;
+      const float m_new = fmaxf(m, fmaxf(mx, other_max[r]) * scale_log2);
+      const bool first = m == -INFINITY;  // nothing accumulated in this row yet (O and l are 0)
+      const bool raise = first || m_new > m + kLazyRescale;
+      // the two warps of these rows see the same maxima: they take the same path
+      if (__any_sync(0xffffffffu, raise)) {
+        const float m_use = raise ? m_new : m;
+        if (__any_sync(0xffffffffu, raise && !first)) {
+          const float corr = raise && !first ? ex2(m - m_use) : 1.f;
+          l *= corr;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {  // 16 columns at a time: the scores stay in registers meanwhile
-          uint32_t o[16];
-          tmem_ld16(lane_base + o_col + c * 16, o);
+          for (int c = 0; c < HD / 32; ++c) {  // this warp's half of the row's O, 16 columns at a time
+            uint32_t o[16];
+            tmem_ld16(lane_base + o_col + c * 16, o);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tmem_st16(lane_base + o_col + c * 16, o);
-        }
-        tmem_st_wait_pp();
-      }
-      m = m_use;
-      // m_use is -inf only if no key of this or an earlier block is visible
-      // to the row: then every P is masked to 0 below (an edge block)
-      const float neg_m = -m_use;
-      float l0 = 0.f, l1 = 0.f;
-      // P = exp2(S * scale - m) (0 where masked), packed to 16 bits into the
-      // first 32 of this warp's 64 score columns (read again here: the scores
-      // are not kept in registers across the barrier; only this warp writes
-      // these columns, after reading them)
-      float x[64];
-      tmem_ld64(lane_base + s_col, x);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {  // two stores of 16 columns (32 keys) keep fewer registers live
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(x[c * 32 + e], scale_log2, neg_m));
-          float p1 = ex2(fmaf(x[c * 32 + e + 1], scale_log2, neg_m));
-          if (edge) {
-            if (!visible(key0 + c * 32 + e)) p0 = 0.f;
-            if (!visible(key0 + c * 32 + e + 1)) p1 = 0.f;
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st16(lane_base + o_col + c * 16, o);
           }
-          l0 += p0;
-          l1 += p1;
-          pk[e >> 1] = pack_16x2(p0, p1, io_f16);
+          tmem_st_wait_pp();
         }
-        tmem_st16(lane_base + p_col + c * 16, pk);
+        // m_use is -inf only if no key of this or an earlier block is visible
+        // to the row: then every P is masked to 0 (an edge block)
+        m = m_use;
+        l0 = l1 = 0.f;
+        p_pass(-m_use, kF{});
       }
       l += l0 + l1;
+      tmem_st16(lane_base + p_col, pk);
+      tmem_st16(lane_base + p_col + 16, pk + 16);
       tmem_st_wait_pp();
       tc_fence_before();
       mbar_arrive(&p_full[i]);
