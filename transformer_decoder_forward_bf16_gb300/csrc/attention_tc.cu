@@ -258,18 +258,27 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld32(s_addr, x);
       tmem_ld32(s_addr + 32, x + 32);
       float mx0 = -INFINITY, mx1 = -INFINITY;
+      // masked and unmasked blocks take separate loops (edge is warp-uniform)
+      if (edge) {
 #pragma unroll
-      for (int e = 0; e < BKV; e += 2) {
-        float a0 = x[e] * scale_log2, a1 = x[e + 1] * scale_log2;
-        if (edge) {
+        for (int e = 0; e < BKV; e += 2) {
+          float a0 = x[e] * scale_log2, a1 = x[e + 1] * scale_log2;
           const int k0 = key0 + e, k1 = k0 + 1;
           if (!(k0 <= qp && k0 < kv_len && (window == 0 || qp - k0 < window))) a0 = -INFINITY;
           if (!(k1 <= qp && k1 < kv_len && (window == 0 || qp - k1 < window))) a1 = -INFINITY;
+          x[e] = a0;
+          x[e + 1] = a1;
+          mx0 = fmaxf(mx0, a0);
+          mx1 = fmaxf(mx1, a1);
         }
-        x[e] = a0;
-        x[e + 1] = a1;
-        mx0 = fmaxf(mx0, a0);
-        mx1 = fmaxf(mx1, a1);
+      } else {
+#pragma unroll
+        for (int e = 0; e < BKV; e += 2) {
+          x[e] *= scale_log2;
+          x[e + 1] *= scale_log2;
+          mx0 = fmaxf(mx0, x[e]);
+          mx1 = fmaxf(mx1, x[e + 1]);
+        }
       }
       const float m_new = fmaxf(m, fmaxf(mx0, mx1));
       float m_use = m;
