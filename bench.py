@@ -389,12 +389,21 @@ def run_moe(args, fk, dev, peaks, flush, reps, emit):
         torch.cuda.synchronize()
         model.set_moe_routing()
         uniq = float(np.mean([len(np.unique(tr[i].cpu().numpy())) for i in range(n_moe)]))
+        # per-kernel times of two steps launched one by one (outside the timed region)
+        lib.fk_profile_reset()
+        lib.fk_profile_enable(1)
+        for _ in range(2):
+            sd.decode(None, logits=z_d, next_ids=n_d)
+        lib.fk_profile_enable(0)
+        prof_d = read_profile(lib)
         ctx = DECODE_CTX + 2 * G + G * reps // 2
         step_bytes = (2.0 * L * (H * (Nq + 2 * Nkv) + Nq * H + E * H + uniq * 3 * H * Ie) + 2.0 * V * H
                       + 2.0 * 2 * L * Nkv * Bd * ctx)
         gbs = step_bytes / (ms_tok / 1e3) / 1e9
         dec[Bd] = {"tok_s": Bd / ms_tok * 1e3, "ms_per_token_step": ms_tok, "experts_touched_per_layer": uniq,
-                   "step_bytes": step_bytes, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"]}
+                   "step_bytes": step_bytes, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
+                   "kernels_per_2_steps": {n: {"launches": c, "ms": round(m, 3)}
+                                           for n, (c, m) in sorted(prof_d.items(), key=lambda kv: -kv[1][1])}}
         del sd
         torch.cuda.empty_cache()
     st, flags = model.sync_status()

@@ -211,6 +211,7 @@ fk_status attention_prefill_tc(const void* q, int ldq, const void* kcache, const
 // ---------------------------------------------------------------------------
 constexpr int kMoeMaxExperts = 256;
 constexpr int kMoeMaxK = 16;
+constexpr int kMoeFewMaxTokens = 64;  // calls of up to this many tokens may take the split-K expert GEMM
 struct MoeWeights {
   GemmWeights router;   // [E, H], fp32 logits
   GemmWeights gate_up;  // grouped gate/up pair, E groups of [Ie, H]
@@ -229,6 +230,10 @@ struct MoeScratch {
   int32_t* counts = nullptr; // [blocks, E] tokens per expert per routing block
   int32_t* base = nullptr;   // [blocks, E] first sorted row of each block's tokens of each expert
   int32_t* group_off = nullptr;  // [E + 1] first sorted row of each expert
+  int32_t* active = nullptr;     // [kMoeMaxExperts + 1] experts with rows in id order, then their number
+  unsigned* exp_counters = nullptr;  // few-token expert GEMMs: arrival counters, zero between launches
+  size_t exp_counters_bytes = 0;
+  float* exp_part = nullptr;         // few-token expert GEMMs: split partial sums
   int32_t* pos = nullptr;    // [T, k] sorted row of each (token, slot)
   int32_t* src = nullptr;    // [T*k] token of each sorted row
   void* xs = nullptr;        // [T*k, H] 16-bit: gathered FFN inputs, sorted by expert
@@ -240,11 +245,14 @@ size_t moe_scratch(const MoeWeights& mw, long T, MoeScratch* s, uint8_t* base);
 // The MoE FFN of u [T, H] (16-bit, the type of mw.router): out = res + d when
 // res is given (res may not alias out), else out = d. forced: NULL or int32
 // [T, k] expert ids; trace_ids / trace_margin: NULL or outputs of the routing.
-// gemv/gemv_bytes/gemv_counter: split-K scratch for the router GEMM of few
-// tokens (NULL: tiled GEMM).
+// few: up to kMoeFewMaxTokens tokens run the expert GEMMs as a split-K weight
+// stream (its arrival counters, s.exp_counters, must be zero between calls;
+// each call leaves them zero). gemv/gemv_bytes/gemv_counter: split-K scratch
+// for the router GEMM of few tokens (NULL: tiled GEMM).
 fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScratch& s, const int32_t* forced,
                       int32_t* trace_ids, float* trace_margin, float* out, const float* res, unsigned* dev_err,
-                      cudaStream_t st, void* gemv = nullptr, size_t gemv_bytes = 0, size_t gemv_counter = 0);
+                      cudaStream_t st, bool few = false, void* gemv = nullptr, size_t gemv_bytes = 0,
+                      size_t gemv_counter = 0);
 // The routing step alone (fk_op_moe_route): ids, weights, margins, and per
 // routing block expert counts when counts != NULL.
 fk_status moe_route_launch(const float* z, int T, int E, int ld, int k, int norm_topk, const int32_t* forced,

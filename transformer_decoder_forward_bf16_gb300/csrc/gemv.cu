@@ -16,7 +16,7 @@
 //     one reduction kernel, which applies the fused epilogue (bf16 store,
 //     fp32 + softcap, fp32 residual add, or the gated FFN activation
 //     act(gate) * up);
-//   * operands under 8 MB take a single split and apply the epilogue straight
+//   * operands under 8 MB with K <= 1024 take a single split and apply the epilogue straight
 //     from TMEM;
 //   * an RMSNorm of the input may be fused in front (one or two tokens): the
 //     two otherwise idle warps read the fp32 rows, form the inverse RMS and
@@ -479,11 +479,12 @@ static int resident_per_sm(int M) {
   return std::max(1, std::min(2048 / kThreads, smem_sm / (smem + reserved)));
 }
 
-// Small operands (under kDirectBytes of weights, not a gate/up pair) take a
-// single split: the CTAs write the epilogue straight from TMEM, with no
+// Small operands (under kDirectBytes of weights and kDirectMaxKBlocks k-blocks,
+// not a gate/up pair) take a single split: the CTAs write the epilogue straight from TMEM, with no
 // partial sums, arrival counters or ordered reduction on the critical path,
 // which for so few bytes cost more than the split's extra bandwidth gains.
 constexpr size_t kDirectBytes = 8u << 20;
+constexpr int kDirectMaxKBlocks = 16;
 
 // Split K so that the whole grid is one wave of resident CTAs, every SM
 // holding the same number: each CTA starts at once and streams an equal
@@ -493,7 +494,9 @@ SkinnyPlan skinny_plan(int M, int K, int n_rows, int sm_count, bool allow_direct
   const int nk = (K + 63) / 64;
   const int n_tiles = (n_rows + 127) / 128;
   const int wave = resident_per_sm(M) * sm_count;
-  p.direct = allow_direct && (size_t)n_rows * K * 2 < kDirectBytes;
+  // a single split streams 128 rows x K per CTA: only for short K (a router
+  // of 128 experts x 2048 would leave one CTA streaming 512 KB)
+  p.direct = allow_direct && (size_t)n_rows * K * 2 < kDirectBytes && nk <= kDirectMaxKBlocks;
   p.splits = p.direct ? 1 : std::max(1, std::min(nk, wave / n_tiles));
   p.kb_per_split = (nk + p.splits - 1) / p.splits;  // the longest split
   p.n_tiles = n_tiles;

@@ -439,7 +439,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       int32_t* t_ids = m->moe_trace_ids ? m->moe_trace_ids + (size_t)mi * hook_rows : nullptr;
       float* t_margin = m->moe_trace_margin ? m->moe_trace_margin + (size_t)mi * m->moe_hook_tokens : nullptr;
       FK_TRY(moe_ffn_run(mw, sc.u, (int)T, sc.moe, forced, t_ids, t_margin, sandwich ? sc.a : x_out,
-                         sandwich ? nullptr : x_mid, m->dev_err, st, gv, gvb, sc.gemv_counter_bytes));
+                         sandwich ? nullptr : x_mid, m->dev_err, st, decode, gv, gvb, sc.gemv_counter_bytes));
       if (sandwich) {
         ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
         FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps,
@@ -880,6 +880,13 @@ extern "C" fk_status fk_session_create(fk_model* m, int32_t batch, int32_t max_s
       return cuda_fail(e, "clear split-K counters");
     }
   }
+  if (m->n_moe) {  // the decode steps' expert GEMMs leave their counters zero after every launch
+    cudaError_t e = cudaMemset(s->sc.moe.exp_counters, 0, s->sc.moe.exp_counters_bytes);
+    if (e != cudaSuccess) {
+      delete s;
+      return cuda_fail(e, "clear expert split-K counters");
+    }
+  }
   *out = s;
   return FK_OK;
 }
@@ -1107,8 +1114,12 @@ extern "C" fk_status fk_op_moe_ffn(fk_model* m, int32_t layer, const void* d_u, 
   FK_TRY(check_device(nullptr));
   MoeScratch sc;
   moe_op_bytes(m, T, &sc, static_cast<uint8_t*>(d_ws));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // up to kMoeFewMaxTokens tokens: the split-K expert GEMMs (their counters start at zero)
+  const bool few = T <= kMoeFewMaxTokens;
+  if (few) FK_CUDA_TRY(cudaMemsetAsync(sc.exp_counters, 0, sc.exp_counters_bytes, st));
   return moe_ffn_run(m->moe[m->moe_index[layer]], d_u, T, sc, d_forced, d_ids, d_margin, d_out, nullptr, m->dev_err,
-                     static_cast<cudaStream_t>(stream));
+                     st, few);
 }
 
 // ===========================================================================
