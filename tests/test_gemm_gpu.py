@@ -65,22 +65,26 @@ def test_gemm_exact_integers(fk):
     np.testing.assert_array_equal(y.cpu().numpy(), oracle.gemm(xi, wi))  # partial sums < 2^24: exact
 
 
+@pytest.mark.slow
 @pytest.mark.parametrize("P,K,N", [(4096, 4096, 14336), (4096, 4096, 128256)])
-def test_gemm_large_sampled(fk, P, K, N):
+def test_gemm_large_full(fk, P, K, N):
+    """The two large op-level shapes, every element against the float64
+    oracle ("N9 · metalgemm", Thm 1: err/scale over the whole output), the
+    reference computed in blocks of rows."""
     import torch
     x, w = _inputs(P, K, N, s=1)
     y = fk.gemm(to_dev_bf16(x), to_dev_bf16(w), out_fp32=True)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(P, 64, replace=False))
-    cols = np.sort(rng.choice(N, 256, replace=False))
     xf = oracle.bf16_to_f64(x)
-    ref_rows = oracle.gemm(xf[rows], oracle.bf16_to_f64(w))
-    got_rows = y[torch.from_numpy(rows).cuda()].cpu().numpy()
-    assert err_scale(got_rows, ref_rows) < 2e-5
-    ref_cols = oracle.gemm(xf, oracle.bf16_to_f64(w[cols]))
-    got_cols = y[:, torch.from_numpy(cols).cuda()].cpu().numpy()
-    assert err_scale(got_cols, ref_cols) < 2e-5
+    wf = oracle.bf16_to_f64(w)
+    max_err, max_ref = 0.0, 0.0
+    for r0 in range(0, P, 512):
+        ref = oracle.gemm(xf[r0:r0 + 512], wf)
+        got = y[r0:r0 + 512].cpu().numpy().astype(np.float64)
+        max_err = max(max_err, float(np.max(np.abs(got - ref))))
+        max_ref = max(max_ref, float(np.max(np.abs(ref))))
+    print(f"gemm {P}x{K}x{N}: err/scale over all {P * N} elements {max_err / max_ref:.2e}")
+    assert max_err / max_ref < 2e-5
 
 
 def test_gemm_rejects_bad_args(fk):
