@@ -81,6 +81,9 @@ fk_status make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64
 // 2-D fp32 row-major output [rows, cols] with row stride ld (elements), boxes
 // of 32 x 32, 128-byte swizzle: the target of TMA stores of staged tiles.
 fk_status make_tmap_f32_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld);
+// The same for a 16-bit (bf16 or f16: TMA moves the bits) output, boxes of
+// 32 rows x 64 columns.
+fk_status make_tmap_16_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld);
 
 // ---------------------------------------------------------------------------
 // GEMM (tcgen05): out = epilogue(A[M,K] · Bᵀ)

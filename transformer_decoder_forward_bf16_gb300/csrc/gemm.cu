@@ -346,6 +346,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = row < tr.row_end;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (acc * MT + sub) * BN;
       float v[32];
+      if constexpr (SO && BN == 256) {
+        // 16-bit outputs: this warp's 32 rows x 64-column boxes (two for a
+        // plain output, one for the gated one), staged and stored by TMA
+        if (args.epi == EPI_BF16 || args.epi == EPI_GLU_BF16) {
+          const bool glu = args.epi == EPI_GLU_BF16;
+          const int r0 = tr.row0 + sub * BM + q * 32;
+          const int f = args.out_f16;
+#pragma unroll 1
+          for (int bx = 0; bx < (glu ? 1 : 2); ++bx) {
+            const int ocol0 = glu ? nb * (BN / 2) + half * 64 : nb * BN + half * (BN / 2) + bx * 64;
+            uint32_t pk[32];
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {  // two 32-column TMEM loads per box
+              float x[32];
+              if (glu) {
+                float g[32];
+                tmem_ld32(taddr + (half * 2 + hc) * 32, g);
+                tmem_ld32(taddr + BN / 2 + (half * 2 + hc) * 32, x);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = (args.act ? act_gelu_tanh(g[j]) : act_silu(g[j])) * x[j];
+              } else {
+                tmem_ld32(taddr + half * (BN / 2) + bx * 64 + hc * 32, x);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) pk[hc * 16 + j] = pack_16x2(x[2 * j], x[2 * j + 1], f);
+            }
+            if (r0 + 32 <= tr.row_end && ocol0 + 64 <= args.n_out) {  // warp-uniform: a whole box
+              uint8_t* buf = sOut + ((warp - 2) * C::OUT_SLOTS + oslot) * 4096;
+              if (lane == 0) bulk_wait_group_read<C::OUT_SLOTS - 1>();
+              __syncwarp();
+              // row `lane`: 16-byte chunk j at chunk position j ^ (row % 8) (128-byte swizzle)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmOut, buf, ocol0, r0);
+                bulk_commit_group();
+              }
+              oslot = (oslot + 1) % C::OUT_SLOTS;
+            } else if (row_ok) {
+              uint16_t* o = reinterpret_cast<uint16_t*>(args.out) + (size_t)row * args.ldo + ocol0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (ocol0 + 2 * j < args.n_out) o[2 * j] = (uint16_t)(pk[j] & 0xFFFFu);
+                if (ocol0 + 2 * j + 1 < args.n_out) o[2 * j + 1] = (uint16_t)(pk[j] >> 16);
+              }
+            }
+          }
+          continue;  // next sub-tile
+        }
+      }
       if (args.epi == EPI_GLU_BF16) {
         for (int c = half * (BN / 128); c < (half + 1) * (BN / 128); ++c) {
           float u[32];
@@ -643,6 +697,13 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
     if (big) return launch_bn<256, 2, false, true>(tA, w, a, sm_count, st, &tOut);
     if (wide) return launch_bn<256, 1, false, true>(tA, w, a, sm_count, st, &tOut);
     return launch_bn<128, 1, false, true>(tA, w, a, sm_count, st, &tOut);
+  }
+  if (big || wide) {  // 16-bit outputs of 256-wide tiles: staged boxes, TMA stores
+    CUtensorMap tOut;
+    s = make_tmap_16_out(&tOut, o.out, M, w.n_out, o.ldo);
+    if (s != FK_OK) return s;
+    if (big) return launch_bn<256, 2, false, true>(tA, w, a, sm_count, st, &tOut);
+    return launch_bn<256, 1, false, true>(tA, w, a, sm_count, st, &tOut);
   }
   if (big) return launch_bn<256, 2>(tA, w, a, sm_count, st);
   if (wide) return launch_bn<256, 1>(tA, w, a, sm_count, st);

@@ -114,6 +114,26 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return encode;
 }
 
+fk_status make_tmap_16_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return fail(FK_ERR_NO_DEVICE, "cuTensorMapEncodeTiled is unavailable (no CUDA driver)");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld * 2) % 16 || rows <= 0 || cols <= 0)
+    return fail(FK_ERR_INVALID_ARG, "16-bit tensor map: base must be 16-byte aligned, rows 16-byte multiples");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (16-bit out) failed (%d)", (int)r);
+    return fail(FK_ERR_CUDA, buf);
+  }
+  return FK_OK;
+}
+
 fk_status make_tmap_f32_out(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
   if (!encode) return fail(FK_ERR_NO_DEVICE, "cuTensorMapEncodeTiled is unavailable (no CUDA driver)");
