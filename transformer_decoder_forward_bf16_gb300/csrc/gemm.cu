@@ -668,7 +668,12 @@ fk_status gemm_run_grouped(const void* A, int M, int lda, const GemmWeights& w, 
     if (wide) return launch_bn<256, 1, true, true>(tA, w, a, sm_count, st, &tOut);
     return launch_bn<128, 1, true, true>(tA, w, a, sm_count, st, &tOut);
   }
-  if (wide) return launch_bn<256, 1, true>(tA, w, a, sm_count, st);
+  if (wide) {  // 16-bit outputs of 256-wide tiles: staged boxes, TMA stores (blocks crossing a group's end: direct)
+    CUtensorMap tOut;
+    s = make_tmap_16_out(&tOut, o.out, M, w.n_out, o.ldo);
+    if (s != FK_OK) return s;
+    return launch_bn<256, 1, true, true>(tA, w, a, sm_count, st, &tOut);
+  }
   return launch_bn<128, 1, true>(tA, w, a, sm_count, st);
 }
 
