@@ -128,16 +128,17 @@ FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int gbase, int& ma
 struct TileRows {
   int row0, row_end, g;
 };
-// Grouped mode: m-block mb of the tile order is block mb - mstart[g] of the
-// group g with mstart[g] <= mb < mstart[g+1] (empty groups have no blocks).
-FK_DEVICE TileRows grouped_rows(const int* goff, const int* mstart, int groups, int mb) {
+// Grouped mode: m-block mb (of TM rows) of the tile order is block
+// mb - mstart[g] of the group g with mstart[g] <= mb < mstart[g+1] (empty
+// groups have no blocks). mstart is 16-bit: at most 65535 m-blocks.
+FK_DEVICE TileRows grouped_rows(const int* goff, const unsigned short* mstart, int groups, int mb, int TM) {
   int lo = 0, hi = groups;  // mstart[lo] <= mb < mstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (mstart[mid] <= mb) lo = mid;
+    if ((int)mstart[mid] <= mb) lo = mid;
     else hi = mid;
   }
-  return TileRows{goff[lo] + (mb - mstart[lo]) * BM, goff[lo + 1], lo};
+  return TileRows{goff[lo] + (mb - (int)mstart[lo]) * TM, goff[lo + 1], lo};
 }
 
 template <int BN, int MT, bool GROUPED, bool SO>
@@ -167,29 +168,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // grouped mode: the group offsets and the first m-block of every group
   __shared__ int s_goff[GROUPED ? kMoeMaxExperts + 1 : 1];
-  __shared__ int s_mstart[GROUPED ? kMoeMaxExperts + 1 : 1];
+  __shared__ unsigned short s_mstart[GROUPED ? kMoeMaxExperts + 1 : 1];
   if constexpr (GROUPED) {
-    static_assert(MT == 1, "grouped tiles are 128 rows");
     for (int i = threadIdx.x; i <= args.groups; i += blockDim.x) s_goff[i] = args.group_off[i];
     __syncthreads();
-    if (warp == 2) {  // exclusive prefix of ceil(rows / 128) over the groups
+    if (warp == 2) {  // exclusive prefix of ceil(rows / TM) over the groups
       int carry = 0;
       for (int g0 = 0; g0 < args.groups; g0 += 32) {
         const int g = g0 + lane;
-        int v = g < args.groups ? (s_goff[g + 1] - s_goff[g] + BM - 1) / BM : 0;
+        int v = g < args.groups ? (s_goff[g + 1] - s_goff[g] + TM - 1) / TM : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int n = __shfl_up_sync(0xffffffffu, v, o);
           if (lane >= o) v += n;
         }
-        if (g < args.groups) s_mstart[g + 1] = carry + v;
+        if (g < args.groups) s_mstart[g + 1] = (unsigned short)(carry + v);
         carry += __shfl_sync(0xffffffffu, v, 31);
       }
       if (lane == 0) s_mstart[0] = 0;
     }
   }
   auto rows_of = [&](int mb) -> TileRows {
-    if constexpr (GROUPED) return grouped_rows(s_goff, s_mstart, args.groups, mb);
+    if constexpr (GROUPED) return grouped_rows(s_goff, s_mstart, args.groups, mb, TM);
     return TileRows{mb * TM, args.M, 0};
   };
 
@@ -659,20 +659,22 @@ fk_status gemm_run_grouped(const void* A, int M, int lda, const GemmWeights& w, 
   a.group_off = group_off;
   a.groups = w.groups;
   a.group_rows = w.group_rows;
+  if ((M + BM - 1) / BM + w.groups > 65535) return fail(FK_ERR_INVALID_ARG, "gemm_run_grouped: too many rows");
+  // 256-row tiles (two M=128 accumulators sharing each B tile: a third less
+  // operand traffic per FLOP) once they give every SM two tiles; then
+  // 128 x 256; else 128-wide. Outputs of 256-wide tiles are staged and stored
+  // by TMA (blocks crossing a group's last row are stored directly).
   const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
+  const bool big = ((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count;
   const bool wide = ((M + BM - 1) / BM) * nb256 >= sm_count;
-  if (o.epi == EPI_F32) {  // fp32 out: staged blocks, TMA stores
+  if (big || wide || o.epi == EPI_F32) {
     CUtensorMap tOut;
-    s = make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo);
+    s = o.epi == EPI_F32 ? make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo)
+                         : make_tmap_16_out(&tOut, o.out, M, w.n_out, o.ldo);
     if (s != FK_OK) return s;
+    if (big) return launch_bn<256, 2, true, true>(tA, w, a, sm_count, st, &tOut);
     if (wide) return launch_bn<256, 1, true, true>(tA, w, a, sm_count, st, &tOut);
     return launch_bn<128, 1, true, true>(tA, w, a, sm_count, st, &tOut);
-  }
-  if (wide) {  // 16-bit outputs of 256-wide tiles: staged boxes, TMA stores (blocks crossing a group's end: direct)
-    CUtensorMap tOut;
-    s = make_tmap_16_out(&tOut, o.out, M, w.n_out, o.ldo);
-    if (s != FK_OK) return s;
-    return launch_bn<256, 1, true, true>(tA, w, a, sm_count, st, &tOut);
   }
   return launch_bn<128, 1, true>(tA, w, a, sm_count, st);
 }
