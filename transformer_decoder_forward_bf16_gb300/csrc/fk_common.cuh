@@ -83,8 +83,6 @@ FK_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_fla
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
-// Bring the 128-byte line at p into L2 (no register result, no wait).
-FK_DEVICE void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 FK_DEVICE void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -110,6 +108,15 @@ FK_DEVICE void tma_load_2d_hint(const CUtensorMap* map, uint64_t* bar, void* sme
 // at non-negative coordinates.
 FK_DEVICE void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+// 2-D tiled reduction of one staged box into global memory: each element of
+// the box is added to the one in place (fp32 add, round to nearest), the
+// read-modify-write done by the memory system, not by this SM.
+FK_DEVICE void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                : "memory");

@@ -21,7 +21,9 @@
 //     32 x 32 block in 128-byte-swizzled shared memory and written by TMA
 //     bulk tensor stores (whole 128-byte lines, no per-row scatter from the
 //     epilogue threads), except blocks that cross the end of the rows (of
-//     their group) or of the columns;
+//     their group) or of the columns; a residual add in place (res == out)
+//     stores each whole block by a TMA reduce-add, so the residual is never
+//     loaded into the SM and the epilogue does not wait on its latency;
 //   * grouped mode (the experts of a MoE layer): A holds the rows of every
 //     group back to back, group g at rows [off[g], off[g+1]) (offsets read
 //     from device memory at kernel start), and each group's rows multiply
@@ -58,6 +60,7 @@ struct GemmArgs {
   unsigned* dev_err;
   int ab_f16;   // A and B are IEEE f16 (else bf16)
   int out_f16;  // 16-bit outputs stored as f16 (else bf16)
+  int res_inplace;  // EPI_ADD_F32 with res == out: whole staged blocks are added by TMA reductions
   const int* group_off;  // grouped mode: groups + 1 row offsets into A
   int groups;
   int group_rows;        // B rows of one group in each map
@@ -425,9 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
           const int col0 = nb * BN + c * 32;
+          // in-place residual add of a whole staged block: the TMA reduction
+          // adds it to the output, so the residual is never loaded here
+          const bool red_blk = SO && args.res_inplace && tr.row0 + sub * BM + q * 32 + 32 <= tr.row_end &&
+                               col0 + 32 <= args.n_out;  // warp-uniform
           // residual add: the chunk's residual loads go out before the TMEM load's wait
           float4 rv[8];
-          const bool res_full = args.epi == EPI_ADD_F32 && row_ok && col0 + 32 <= args.n_out;
+          const bool res_full = args.epi == EPI_ADD_F32 && !red_blk && row_ok && col0 + 32 <= args.n_out;
           if (res_full) {
             const float4* r4 = reinterpret_cast<const float4*>(args.res + (size_t)row * args.ldr + col0);
 #pragma unroll
@@ -438,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // a whole 32 x 32 fp32 block inside the output: stage it, store it by TMA
             const int r0 = tr.row0 + sub * BM + q * 32;
             if (r0 + 32 <= tr.row_end && col0 + 32 <= args.n_out) {  // warp-uniform
-              if (args.epi == EPI_ADD_F32) {  // res_full holds for every row of the block
+              if (args.epi == EPI_ADD_F32 && !red_blk) {  // res_full holds for every row of the block
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                   v[4 * j] += rv[j].x;
@@ -463,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmOut, buf, col0, r0);
+                if (red_blk)
+                  tma_reduce_add_2d(&tmOut, buf, col0, r0);
+                else
+                  tma_store_2d(&tmOut, buf, col0, r0);
                 bulk_commit_group();
               }
               oslot = (oslot + 1) % C::OUT_SLOTS;
@@ -641,6 +651,7 @@ static fk_status gemm_args(const void* A, int M, int lda, const GemmWeights& w, 
   a->dev_err = dev_err;
   a->ab_f16 = w.f16;
   a->out_f16 = o.out_f16;
+  a->res_inplace = o.epi == EPI_ADD_F32 && o.res == o.out && o.ldr == o.ldo;
   return FK_OK;
 }
 
@@ -712,8 +723,6 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
     if (big) return launch_bn<256, 2, false, true>(tA, w, a, sm_count, st, &tOut);
     return launch_bn<256, 1, false, true>(tA, w, a, sm_count, st, &tOut);
   }
-  if (big) return launch_bn<256, 2>(tA, w, a, sm_count, st);
-  if (wide) return launch_bn<256, 1>(tA, w, a, sm_count, st);
   return launch_bn<128, 1>(tA, w, a, sm_count, st);
 }
 

@@ -367,7 +367,12 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     const int kind = m->kinds[l];
     const int window = kind == 1 ? c.sliding_window : 0;
     float* x_out = slots ? slots + (size_t)(l + 1) * T * H : sc.x0;
-    float* x_mid = sc.x1;
+    // A dense pre-norm layer keeps the residual stream in one buffer: the
+    // down projection adds into x_out in place (as does the attention output
+    // projection when x_out is x_in), which the tiled GEMM turns into TMA
+    // reduce-adds instead of residual loads.
+    const bool in_place = !sandwich && m->moe_index[l] < 0;
+    float* x_mid = in_place ? x_out : sc.x1;
     const void* next_norm = l + 1 < L ? m->layers[l + 1].attn_norm : m->final_norm;
     // the next norm output feeds the next layer's QKV projection, or the LM head
     const int next_f16 = l + 1 < L ? m->f16(FK_F16_QKV_IN) : m->f16(FK_F16_HEAD_IN);
@@ -384,7 +389,7 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
     qkv_norm_set = false;
     const bool fuse_ffn_norm = fuse_norm && m->moe_index[l] < 0;
     NormIn ffn_norm;
-    ffn_norm.x = sc.x1;
+    ffn_norm.x = x_mid;
     ffn_norm.ldx = H;
     ffn_norm.w = w.ffn_norm;
     ffn_norm.eps = c.rms_eps;
