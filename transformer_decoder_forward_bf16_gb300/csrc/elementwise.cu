@@ -226,8 +226,10 @@ __global__ void post_norm_residual_kernel(const float* __restrict__ a, const flo
 
 // ---------------------------------------------------------------------------
 // QK-norm + RoPE + KV-cache write ("N7", Thm 1: RoPE on q and k; Thm 2: qwen3
-// / gemma3 QK-norm). One warp per (token, head). Head element j pairs with
-// j + hd/2; lane owns C = hd/64 consecutive elements of each half.
+// / gemma3 QK-norm). Head element j pairs with j + hd/2. Each lane owns 8
+// consecutive elements of each half of a head (16-byte loads and stores), so
+// a head takes hd/16 lanes and a warp covers 512/hd heads of one token (4 at
+// hd = 128): enough bytes in flight per warp to stream at the memory's rate.
 //   q: rotated in place inside the qkv rows;
 //   k: rotated and written to kcache[b][g][pos][:]
 // (v goes to the transposed value cache through v_cache_kernel below).
@@ -242,44 +244,62 @@ __global__ void rope_qkv_kernel(uint16_t* qkv, int ldqkv, int T, int S, int pos0
   pdl_wait();
   constexpr int HD = C * 64;
   constexpr int HALF = HD / 2;
+  constexpr int LPH = HALF / 8;    // lanes per head
+  constexpr int HPW = 32 / LPH;    // heads per warp
   const int warps = blockDim.x >> 5;
   const long gw = (long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int nh = Hq + Hkv;  // q and k heads; v is moved by v_cache_kernel
-  if (gw >= (long)T * nh) return;
-  const int t = (int)(gw / nh);
-  const int h = (int)(gw % nh);
+  const int groups = (nh + HPW - 1) / HPW;
+  if (gw >= (long)T * groups) return;  // warp-uniform
+  const int t = (int)(gw / groups);
+  const int h = (int)(gw % groups) * HPW + lane / LPH;
+  const bool live = h < nh;
   const int b = t / S, s = t % S;
   const int pos = pos0 + s;
+  const int e0 = (lane % LPH) * 8;  // within each half
   uint16_t* row = qkv + (size_t)t * ldqkv + (size_t)h * HD;
-  float lo[C], hi[C];
-  const int e0 = lane * C;  // within each half of size 32*C = HALF
+  float lo[8], hi[8];
+  if (live) {
+    const uint4 a = *reinterpret_cast<const uint4*>(row + e0);
+    const uint4 c = *reinterpret_cast<const uint4*>(row + HALF + e0);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int i = 0; i < C; ++i) {
-    lo[i] = load_16(row + e0 + i, f16);
-    hi[i] = load_16(row + HALF + e0 + i, f16);
+    for (int i = 0; i < 4; ++i) {
+      lo[2 * i] = lo_16(aw[i], f16);
+      lo[2 * i + 1] = hi_16(aw[i], f16);
+      hi[2 * i] = lo_16(cw[i], f16);
+      hi[2 * i + 1] = hi_16(cw[i], f16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo[i] = hi[i] = 0.f;
   }
   const bool is_q = h < Hq;
-  if (qk_norm) {
+  if (qk_norm) {  // every lane takes part in the shuffles
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < C; ++i) ss += lo[i] * lo[i] + hi[i] * hi[i];
-    ss = warp_sum(ss);
+    for (int i = 0; i < 8; ++i) ss += lo[i] * lo[i] + hi[i] * hi[i];
+#pragma unroll
+    for (int o = LPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = rsqrtf(ss / HD + eps);
     const __nv_bfloat16* nw = is_q ? q_norm : k_norm;
+    if (live) {
 #pragma unroll
-    for (int i = 0; i < C; ++i) {
-      lo[i] = lo[i] * r * __bfloat162float(nw[e0 + i]);
-      hi[i] = hi[i] * r * __bfloat162float(nw[HALF + e0 + i]);
+      for (int i = 0; i < 8; ++i) {
+        lo[i] = lo[i] * r * __bfloat162float(nw[e0 + i]);
+        hi[i] = hi[i] * r * __bfloat162float(nw[HALF + e0 + i]);
+      }
     }
   }
-  const float2* cs = rope + (size_t)pos * HALF + e0;
-  float olo[C], ohi[C];
+  if (!live) return;
+  const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)pos * HALF + e0);
+  uint32_t olo[4], ohi[4];
 #pragma unroll
-  for (int i = 0; i < C; ++i) {
-    const float2 c = cs[i];
-    olo[i] = lo[i] * c.x - hi[i] * c.y;
-    ohi[i] = hi[i] * c.x + lo[i] * c.y;
+  for (int i = 0; i < 4; ++i) {
+    const float4 c = cs[i];  // (cos, sin) of elements 2i and 2i + 1
+    olo[i] = pack_16x2(lo[2 * i] * c.x - hi[2 * i] * c.y, lo[2 * i + 1] * c.z - hi[2 * i + 1] * c.w, f16);
+    ohi[i] = pack_16x2(hi[2 * i] * c.x + lo[2 * i] * c.y, hi[2 * i + 1] * c.z + lo[2 * i + 1] * c.w, f16);
   }
   uint16_t* dst;
   if (is_q) {
@@ -288,11 +308,8 @@ __global__ void rope_qkv_kernel(uint16_t* qkv, int ldqkv, int T, int S, int pos0
     const int g = h - Hq;
     dst = kcache + (((size_t)b * Hkv + g) * cap + pos % cap) * HD;  // position p lives in slot p mod cap
   }
-#pragma unroll
-  for (int i = 0; i < C; ++i) {
-    store_16(dst + e0 + i, olo[i], f16);
-    store_16(dst + HALF + e0 + i, ohi[i], f16);
-  }
+  *reinterpret_cast<uint4*>(dst + e0) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+  *reinterpret_cast<uint4*>(dst + HALF + e0) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
 }
 
 // V rows of a prefill chunk into the transposed cache vcache[b][g][d][pos]:
@@ -567,7 +584,8 @@ cudaError_t launch_rope_qkv(void* qkv, int ldqkv, int T, int S, int pos0, int Hq
     if (hd == 256) e = fk_launch(v_cache_kernel<256>, grid, 256, 0, st, src, ldqkv, S, pos0, Hq, Hkv, vdst, cap);
     if (e != cudaSuccess) return e;
   }
-  const long warps = (long)T * (Hq + Hkv);
+  const int hpw = 512 / hd;  // heads per warp
+  const long warps = (long)T * ((Hq + Hkv + hpw - 1) / hpw);
   const int blocks = (int)((warps + 7) / 8);
   auto* q = static_cast<uint16_t*>(qkv);
   auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
