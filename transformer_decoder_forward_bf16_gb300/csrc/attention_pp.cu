@@ -415,7 +415,32 @@ __global__ void __launch_bounds__(kPPThreads, 1)
         if (edge) p_pass_as(kT{}, want_max_c, neg_m);
         else p_pass_as(kF{}, want_max_c, neg_m);
       };
-      p_pass(m == -INFINITY ? 0.f : -m, kT{});
+      if (ns == 0) {
+        // the tile's first block: no row has an m yet, so P is formed only
+        // after the exchange below; this pass takes the row maxima alone
+        auto max_pass = [&](auto edge_c) {
+          constexpr bool kEdge = decltype(edge_c)::value;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sv[16];
+            tmem_ld16(lane_base + s_col + c * 16, sv);
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float x0 = __uint_as_float(sv[e]), x1 = __uint_as_float(sv[e + 1]);
+              if constexpr (kEdge) {
+                if (visible(key0 + c * 16 + e)) mx = fmaxf(mx, x0);
+                if (visible(key0 + c * 16 + e + 1)) mx = fmaxf(mx, x1);
+              } else {
+                mx = max3(mx, x0, x1);
+              }
+            }
+          }
+        };
+        if (edge) max_pass(kT{});
+        else max_pass(kF{});
+      } else {
+        p_pass(m == -INFINITY ? 0.f : -m, kT{});
+      }
       my_max[r] = mx;
       // both warps of the row have published their maxima
       pair_sync();

@@ -56,22 +56,24 @@ FK_DEVICE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // setting *abort and the device error word) if the wait exceeds kWaitLimitNs
 // or another role of the CTA has already aborted. dev_err points at a device
 // control block (word 0: error bits; word 1: a test override of the limit in
-// microseconds, 0 = kWaitLimitNs) or is null.
+// microseconds, 0 = kWaitLimitNs) or is null. The barrier is polled from the
+// first iteration on; the clock, the abort flag and the limit override (a
+// device-memory load) are read only every 256 polls, and the loaded limit is
+// first used 256 polls later, so no load latency sits between the phase's
+// completion and the waiter's return.
 FK_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* dev_err) {
   const uint32_t a = smem_u32(bar);
-  for (int i = 0; i < 128; ++i)
-    if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint64_t limit = kWaitLimitNs;
-  if (dev_err) {
-    const unsigned us = *reinterpret_cast<volatile unsigned*>(dev_err + 1);
-    if (us) limit = (uint64_t)us * 1000ull;
-  }
-  for (uint32_t i = 0;; ++i) {
+  uint64_t t0 = 0;
+  unsigned us = 0;
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 255) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+        if (dev_err) us = *reinterpret_cast<volatile unsigned*>(dev_err + 1);
+      } else if (now - t0 > (us ? (uint64_t)us * 1000ull : kWaitLimitNs)) {
         *abort_flag = 1;
         if (dev_err) atomicOr(dev_err, FK_DEVERR_PIPE_TIMEOUT);
         return false;
