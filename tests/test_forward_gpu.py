@@ -65,6 +65,17 @@ def test_small_models(fk, kind, B, S):
     print(kind, B, S, r)
 
 
+def test_wide_model_k_split_tail(fk):
+    """A narrow residual stream with wide projections (Q|K|V 10240 and gate/up
+    2 x 20480 outputs over K = 256) at 2 x 1000 tokens: the Q|K|V and gate/up
+    GEMMs run 256 x 256 tiles several waves deep with a ragged last row block,
+    and attention has 64 query heads over 8 KV heads; every hidden slot
+    against the oracle."""
+    cfg = synth.small_config("llama3", hidden=256, n_q_heads=64, n_kv_heads=8, head_dim=128, intermediate=20480)
+    r = check_forward(fk, cfg, 2, 1000, norm_mode="random", sigma=0.02)
+    print(r)
+
+
 def test_smollm2_shape_9_tokens(fk):
     """The SmolLM2-135M-shaped llama, one sequence of 9 ids, norm weights 1.0."""
     r = check_forward(fk, synth.CONFIGS["smollm2-135m"], 1, 9)
