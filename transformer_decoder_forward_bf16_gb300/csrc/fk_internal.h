@@ -252,10 +252,18 @@ size_t moe_scratch(const MoeWeights& mw, long T, MoeScratch* s, uint8_t* base);
 // stream (its arrival counters, s.exp_counters, must be zero between calls;
 // each call leaves them zero). gemv/gemv_bytes/gemv_counter: split-K scratch
 // for the router GEMM of few tokens (NULL: tiled GEMM).
+// next_norm: NULL, or the RMSNorm of out for the next consumer (the next
+// layer's Q|K|V projection or the LM head), made by the combine step.
+struct NormOut {
+  const void* w = nullptr;  // bf16 [H]
+  float eps = 0.f;
+  void* u = nullptr;        // 16-bit [T, H]
+  int f16 = 0;              // u holds IEEE f16 (else bf16)
+};
 fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScratch& s, const int32_t* forced,
                       int32_t* trace_ids, float* trace_margin, float* out, const float* res, unsigned* dev_err,
                       cudaStream_t st, bool few = false, void* gemv = nullptr, size_t gemv_bytes = 0,
-                      size_t gemv_counter = 0);
+                      size_t gemv_counter = 0, const NormOut* next_norm = nullptr);
 // The routing step alone (fk_op_moe_route): ids, weights, margins, and per
 // routing block expert counts when counts != NULL.
 fk_status moe_route_launch(const float* z, int T, int E, int ld, int k, int norm_topk, const int32_t* forced,

@@ -443,15 +443,19 @@ fk_status run_stack(fk_model* m, const Scratch& sc, int B, int S, int pos0, cons
       const int32_t* forced = m->moe_forced ? m->moe_forced + (size_t)mi * hook_rows : nullptr;
       int32_t* t_ids = m->moe_trace_ids ? m->moe_trace_ids + (size_t)mi * hook_rows : nullptr;
       float* t_margin = m->moe_trace_margin ? m->moe_trace_margin + (size_t)mi * m->moe_hook_tokens : nullptr;
+      // pre-norm: the combine step also makes the next consumer's normalised rows
+      NormOut nn;
+      nn.w = next_norm;
+      nn.eps = c.rms_eps;
+      nn.u = sc.u;
+      nn.f16 = next_f16;
       FK_TRY(moe_ffn_run(mw, sc.u, (int)T, sc.moe, forced, t_ids, t_margin, sandwich ? sc.a : x_out,
-                         sandwich ? nullptr : x_mid, m->dev_err, st, decode, gv, gvb, sc.gemv_counter_bytes));
+                         sandwich ? nullptr : x_mid, m->dev_err, st, decode, gv, gvb, sc.gemv_counter_bytes,
+                         sandwich ? nullptr : &nn));
       if (sandwich) {
         ProfScope ps(decode ? "post_norm_dec" : "post_norm", st);
         FK_LAUNCH(launch_post_norm_residual(sc.a, x_mid, x_out, (int)T, H, w.post_ffn_norm, next_norm, c.rms_eps,
                                             sc.u, st, next_f16));
-      } else {
-        ProfScope ps(decode ? "rmsnorm_dec" : "rmsnorm", st);
-        FK_LAUNCH(launch_rmsnorm(x_out, H, (int)T, H, next_norm, c.rms_eps, sc.u, H, st, next_f16));
       }
       x_in = x_out;
       continue;

@@ -29,6 +29,7 @@
 
 #include "fk_common.cuh"
 #include "fk_internal.h"
+#include "fk_ops.h"
 #include "fk_launch.h"
 
 namespace fk {
@@ -37,6 +38,7 @@ namespace {
 
 constexpr int kRouteTokens = 64;  // tokens per routing block (one 64-bit mask per expert)
 constexpr int kRouteThreads = 256;
+constexpr int kFusedGatherRows = 16;  // routed rows up to which the routing CTA gathers them itself
 constexpr int kEPL = kMoeMaxExperts / 32;  // experts per lane
 
 constexpr size_t kAlign = 256;
@@ -262,9 +264,11 @@ __global__ void __launch_bounds__(kRouteThreads)
     moe_route_small_kernel(const float* __restrict__ z, int ld, int T, int E, int k, int norm_topk,
                            const int32_t* __restrict__ forced, int32_t* __restrict__ ids, float* __restrict__ wts,
                            float* __restrict__ margin, int32_t* __restrict__ group_off, int32_t* __restrict__ active,
-                           int32_t* __restrict__ pos, int32_t* __restrict__ src, unsigned* dev_err) {
+                           int32_t* __restrict__ pos, int32_t* __restrict__ src, unsigned* dev_err,
+                           const uint16_t* __restrict__ u, int H, uint16_t* __restrict__ xs) {
   pdl_wait();  // inside a decode step: the predecessor's outputs, then release the successor
   pdl_trigger();
+  __shared__ int ssrc[kRouteTokens * kMoeMaxK];
   __shared__ int hist[kMoeMaxExperts];
   __shared__ int off[kMoeMaxExperts + 1];
   __shared__ int has[kMoeMaxExperts];
@@ -293,6 +297,15 @@ __global__ void __launch_bounds__(kRouteThreads)
     const int p = off[e] + __popcll(mask[e] & ((1ull << t) - 1ull));
     pos[i] = p;
     src[p] = t;
+    ssrc[p] = t;
+  }
+  if (xs) {  // the gather of the expert-sorted rows (few rows): xs[r] = u[src[r]], a warp per row
+    __syncthreads();
+    for (int r = threadIdx.x >> 5; r < n; r += blockDim.x >> 5) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(u + (size_t)ssrc[r] * H);
+      uint4* d4 = reinterpret_cast<uint4*>(xs + (size_t)r * H);
+      for (int c = threadIdx.x & 31; c < H / 8; c += 32) d4[c] = s4[c];
+    }
   }
 }
 
@@ -309,21 +322,35 @@ __global__ void __launch_bounds__(256)
   for (int c = threadIdx.x & 31; c < H / 8; c += 32) d[c] = s[c];
 }
 
-// out[t] = [res[t] +] sum_j w[t,j] ys[pos[t,j]] (j ascending, fp32)
+// out[t] = [res[t] +] sum_j w[t,j] ys[pos[t,j]] (j ascending, fp32). With
+// NORM, also the RMSNorm of the row for the next consumer, u[t] =
+// 16-bit(out * rsqrt(mean(out^2) + eps) * nw), with the row held in registers:
+// thread i holds elements 4 (m blockDim + i) .. + 3 (m = 0, 1, ...) and the
+// sums of squares are reduced in the order of the standalone row norm, so u
+// equals what that kernel would make of out.
+constexpr int kCombineMaxVec = 8;  // float4 per thread with NORM: H <= 8192
+template <bool NORM>
 __global__ void __launch_bounds__(256)
     moe_combine_kernel(const float* __restrict__ ys, int H, const int32_t* __restrict__ pos,
-                       const float* __restrict__ w, int k, const float* __restrict__ res, float* __restrict__ out) {
+                       const float* __restrict__ w, int k, const float* __restrict__ res, float* __restrict__ out,
+                       const __nv_bfloat16* __restrict__ nw, float eps, uint16_t* __restrict__ u, int u_f16) {
   pdl_wait();  // inside a decode step: the predecessor's outputs, then release the successor
   pdl_trigger();
   __shared__ int sp[kMoeMaxK];
   __shared__ float sw[kMoeMaxK];
+  __shared__ float red[8];
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     sp[threadIdx.x] = pos[(size_t)t * k + threadIdx.x];
     sw[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
   }
   __syncthreads();
-  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+  float4 v[NORM ? kCombineMaxVec : 1];
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < (NORM ? kCombineMaxVec : 1 << 20); ++m) {
+    const int c = (m * blockDim.x + threadIdx.x) * 4;
+    if (c >= H) break;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const float4 y = *reinterpret_cast<const float4*>(ys + (size_t)sp[j] * H + c);
@@ -341,6 +368,28 @@ __global__ void __launch_bounds__(256)
       acc.w = x.w + acc.w;
     }
     *reinterpret_cast<float4*>(out + (size_t)t * H + c) = acc;
+    if constexpr (NORM) {
+      v[m] = acc;
+      ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
+    }
+  }
+  if constexpr (NORM) {
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+    const float r = rsqrtf(tot / H + eps);
+    uint16_t* ur = u + (size_t)t * H;
+#pragma unroll
+    for (int m = 0; m < kCombineMaxVec; ++m) {
+      const int c = (m * blockDim.x + threadIdx.x) * 4;
+      if (c >= H) break;
+      const uint2 wp = *reinterpret_cast<const uint2*>(nw + c);
+      *reinterpret_cast<uint2*>(ur + c) =
+          make_uint2(pack_16x2(v[m].x * r * bf16_lo(wp.x), v[m].y * r * bf16_hi(wp.x), u_f16),
+                     pack_16x2(v[m].z * r * bf16_lo(wp.y), v[m].w * r * bf16_hi(wp.y), u_f16));
+    }
   }
 }
 
@@ -653,7 +702,8 @@ fk_status moe_route_launch(const float* z, int T, int E, int ld, int k, int norm
 
 fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScratch& s, const int32_t* forced,
                       int32_t* trace_ids, float* trace_margin, float* out, const float* res, unsigned* dev_err,
-                      cudaStream_t st, bool few, void* gemv, size_t gemv_bytes, size_t gemv_counter) {
+                      cudaStream_t st, bool few, void* gemv, size_t gemv_bytes, size_t gemv_counter,
+                      const NormOut* next_norm) {
   if (T == 0) return FK_OK;
   const int E = mw.E, k = mw.k, H = mw.H;
   const int Tk = T * k;
@@ -666,11 +716,14 @@ fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScrat
     oz.ldo = E;
     FK_TRY_STATUS(gemm_run(u, T, H, mw.router, oz, dev_err, st, gemv, gemv_bytes, gemv_counter));
   }
+  // few routed rows: the routing CTA copies them into expert order itself
+  const bool fused_gather = T <= kRouteTokens && Tk <= kFusedGatherRows;
   if (T <= kRouteTokens) {  // one routing block: routing, offsets and placement in one CTA
     ProfScope ps("moe_route", st);
     cudaError_t e = fk_launch(moe_route_small_kernel, dim3(1), dim3(kRouteThreads), 0, st, (const float*)s.z, E, T, E,
                               k, mw.norm_topk, forced, s.ids, s.w, s.margin, s.group_off, s.active, s.pos, s.src,
-                              dev_err);
+                              dev_err, static_cast<const uint16_t*>(u), H,
+                              fused_gather ? static_cast<uint16_t*>(s.xs) : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "moe_route_small_kernel launch");
   } else {
     ProfScope ps("moe_route", st);
@@ -680,7 +733,7 @@ fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScrat
     moe_place_kernel<<<nblk, 256, 0, st>>>(s.ids, T, E, k, s.base, s.pos, s.src);
     FK_TRY_LAUNCH("moe_place_kernel launch");
   }
-  {
+  if (!fused_gather) {
     ProfScope ps("moe_gather", st);
     cudaError_t e = fk_launch(moe_gather_kernel, dim3((Tk + 7) / 8), dim3(256), 0, st, static_cast<const uint16_t*>(u),
                               H, (const int32_t*)s.src, Tk, static_cast<uint16_t*>(s.xs));
@@ -713,9 +766,18 @@ fk_status moe_ffn_run(const MoeWeights& mw, const void* u, int T, const MoeScrat
   }
   {
     ProfScope ps("moe_combine", st);
-    cudaError_t e = fk_launch(moe_combine_kernel, dim3(T), dim3(std::min(256, H / 4)), 0, st, (const float*)s.ys, H,
-                              (const int32_t*)s.pos, (const float*)s.w, k, res, out);
+    const bool norm = next_norm && H % 128 == 0 && H <= 256 * 4 * kCombineMaxVec;  // whole warps
+    cudaError_t e =
+        norm ? fk_launch(moe_combine_kernel<true>, dim3(T), dim3(std::min(256, H / 4)), 0, st, (const float*)s.ys, H,
+                         (const int32_t*)s.pos, (const float*)s.w, k, res, out,
+                         static_cast<const __nv_bfloat16*>(next_norm->w), next_norm->eps,
+                         static_cast<uint16_t*>(next_norm->u), next_norm->f16)
+             : fk_launch(moe_combine_kernel<false>, dim3(T), dim3(std::min(256, H / 4)), 0, st, (const float*)s.ys, H,
+                         (const int32_t*)s.pos, (const float*)s.w, k, res, out, (const __nv_bfloat16*)nullptr, 0.f,
+                         (uint16_t*)nullptr, 0);
     if (e != cudaSuccess) return cuda_fail(e, "moe_combine_kernel launch");
+    if (next_norm && !norm)
+      FK_CUDA_TRY(launch_rmsnorm(out, H, T, H, next_norm->w, next_norm->eps, next_norm->u, H, st, next_norm->f16));
   }
   if (trace_ids) FK_CUDA_TRY(cudaMemcpyAsync(trace_ids, s.ids, (size_t)Tk * 4, cudaMemcpyDeviceToDevice, st));
   if (trace_margin) FK_CUDA_TRY(cudaMemcpyAsync(trace_margin, s.margin, (size_t)T * 4, cudaMemcpyDeviceToDevice, st));
