@@ -18,6 +18,7 @@
 #include <cstdlib>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -84,6 +85,26 @@ struct fk_model {
   bool moe_hook() const { return moe_forced || moe_trace_ids || moe_trace_margin; }
   // 1 when the activation storage site (an FK_F16_* bit) holds IEEE f16
   int f16(uint32_t site) const { return (cfg.f16_sites & site) ? 1 : 0; }
+  // cacheless forwards of few tokens: the second call with the same shape,
+  // workspace and outputs captures the launches after the ids copy into a
+  // CUDA graph, which later such calls replay (fk_forward)
+  struct FwdKey {
+    int B = 0, S = 0;
+    const void* ws = nullptr;
+    const void* out[4] = {nullptr, nullptr, nullptr, nullptr};
+    bool operator==(const FwdKey& o) const {
+      return B == o.B && S == o.S && ws == o.ws && out[0] == o.out[0] && out[1] == o.out[1] &&
+             out[2] == o.out[2] && out[3] == o.out[3];
+    }
+  };
+  std::mutex fwd_mu;
+  cudaStream_t fwd_cap_stream = nullptr;
+  cudaGraphExec_t fwd_graph = nullptr;
+  FwdKey fwd_key, fwd_seen;
+  ~fk_model() {
+    if (fwd_graph) cudaGraphExecDestroy(fwd_graph);
+    if (fwd_cap_stream) cudaStreamDestroy(fwd_cap_stream);
+  }
 };
 
 struct fk_session {
@@ -750,6 +771,14 @@ extern "C" size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, i
   return forward_layout(m, batch, seq, nullptr, nullptr, nullptr, nullptr);
 }
 
+static bool graphs_disabled() {
+  static const bool off = [] {
+    const char* e = getenv("FK_NO_GRAPH");
+    return e && *e && *e != '0';
+  }();
+  return off;
+}
+
 extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
                                 void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
                                 float* d_margin, void* stream) {
@@ -771,14 +800,63 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   forward_layout(m, batch, seq, static_cast<uint8_t*>(d_ws), &sc, &kv, &ws_logits);
   FK_CUDA_TRY(cudaMemcpyAsync(sc.ids, ids, T * sizeof(int32_t),
                               ids_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
-  if (sc.gemv_counter_bytes) FK_CUDA_TRY(cudaMemsetAsync(sc.gemv, 0, sc.gemv_counter_bytes, st));
-  FK_CUDA_TRY(cudaMemsetAsync(static_cast<uint8_t*>(sc.argmax) + argmax_counter_offset(), 0,
-                              argmax_scratch_bytes() - argmax_counter_offset(), st));
-  // attention reads V in 64-position blocks: positions past seq must hold finite values
-  if (seq % 64) FK_CUDA_TRY(cudaMemsetAsync(kv.v, 0, kv.bytes, st));
-  FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, 1, st));
-  if (d_logits || d_argmax)
-    FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, st, nullptr, d_margin));
+  auto enqueue = [&](cudaStream_t s2) -> fk_status {
+    if (sc.gemv_counter_bytes) FK_CUDA_TRY(cudaMemsetAsync(sc.gemv, 0, sc.gemv_counter_bytes, s2));
+    FK_CUDA_TRY(cudaMemsetAsync(static_cast<uint8_t*>(sc.argmax) + argmax_counter_offset(), 0,
+                                argmax_scratch_bytes() - argmax_counter_offset(), s2));
+    // attention reads V in 64-position blocks: positions past seq must hold finite values
+    if (seq % 64) FK_CUDA_TRY(cudaMemsetAsync(kv.v, 0, kv.bytes, s2));
+    FK_TRY(run_stack(m, sc, batch, seq, 0, kv, d_hidden, false, 1, s2));
+    if (d_logits || d_argmax)
+      FK_TRY(run_head(m, sc.u, (int)T, d_logits ? d_logits : ws_logits, d_argmax, sc, s2, nullptr, d_margin));
+    return FK_OK;
+  };
+  // A forward of few tokens is mostly launch latency: replay it from a graph
+  // once the same call has been seen before (the first call runs eagerly, so
+  // every lazy set-up is done before a capture). Larger forwards, timed or
+  // hooked runs and calls on a capturing stream launch one by one.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  FK_CUDA_TRY(cudaStreamIsCapturing(st, &cs));
+  if (T > kSkinnyMaxTokens || cs != cudaStreamCaptureStatusNone || profiling_enabled() || graphs_disabled() ||
+      m->moe_hook())
+    return enqueue(st);
+  fk_model::FwdKey key;
+  key.B = batch;
+  key.S = seq;
+  key.ws = d_ws;
+  key.out[0] = d_hidden;
+  key.out[1] = d_logits;
+  key.out[2] = d_argmax;
+  key.out[3] = d_margin;
+  std::lock_guard<std::mutex> lock(m->fwd_mu);
+  if (!(m->fwd_graph && m->fwd_key == key)) {
+    if (!(m->fwd_seen == key)) {
+      m->fwd_seen = key;
+      return enqueue(st);
+    }
+    if (m->fwd_graph) {
+      cudaGraphExecDestroy(m->fwd_graph);
+      m->fwd_graph = nullptr;
+    }
+    if (!m->fwd_cap_stream) FK_CUDA_TRY(cudaStreamCreateWithFlags(&m->fwd_cap_stream, cudaStreamNonBlocking));
+    FK_CUDA_TRY(cudaStreamBeginCapture(m->fwd_cap_stream, cudaStreamCaptureModeThreadLocal));
+    const fk_status es = enqueue(m->fwd_cap_stream);
+    cudaGraph_t g = nullptr;
+    cudaError_t ce = cudaStreamEndCapture(m->fwd_cap_stream, &g);
+    if (es != FK_OK) {
+      if (g) cudaGraphDestroy(g);
+      return es;
+    }
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamEndCapture(forward)");
+    ce = cudaGraphInstantiate(&m->fwd_graph, g, 0);
+    cudaGraphDestroy(g);
+    if (ce != cudaSuccess) {
+      m->fwd_graph = nullptr;
+      return cuda_fail(ce, "cudaGraphInstantiate(forward)");
+    }
+    m->fwd_key = key;
+  }
+  FK_CUDA_TRY(cudaGraphLaunch(m->fwd_graph, st));
   return FK_OK;
 }
 
@@ -974,13 +1052,6 @@ static fk_status enqueue_decode(fk_session* s, const int32_t* d_ids, float* d_lo
   return FK_OK;
 }
 
-static bool graphs_disabled() {
-  static const bool off = [] {
-    const char* e = getenv("FK_NO_GRAPH");
-    return e && *e && *e != '0';
-  }();
-  return off;
-}
 
 extern "C" fk_status fk_decode_step(fk_session* s, const int32_t* d_ids, float* d_logits, int32_t* d_next,
                                     float* d_margin, void* stream) {
