@@ -234,7 +234,14 @@ size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, int32_t seq)
  *   d_margin: NULL, or fp32 [batch*seq]: the row maximum minus the largest
  *        other logit (0 on a tie) -- how far the argmax is from a flip ("N7 ·
  *        model/forward-parity", Thm 3: near-tie argmax flips). Needs d_argmax.
- * A host `ids` buffer is copied synchronously before the call returns. */
+ * A host `ids` buffer is copied synchronously before the call returns.
+ * Forwards of at most 64 tokens (batch*seq) are launch-bound: the model
+ * keeps one CUDA graph of the launches that follow the ids copy, captured on
+ * the second consecutive call with the same batch, seq, workspace and output
+ * pointers and replayed by later such calls (another key replaces it; calls
+ * on a capturing stream, with kernel timing on, or with FK_NO_GRAPH set in
+ * the environment launch one by one). Results are the same either way.
+ * Calls on one model from several host threads must be serialised. */
 fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
                      void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
                      float* d_margin, void* stream);
