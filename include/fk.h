@@ -241,7 +241,8 @@ size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, int32_t seq)
  * pointers and replayed by later such calls (another key replaces it; calls
  * on a capturing stream, with kernel timing on, or with FK_NO_GRAPH set in
  * the environment launch one by one). Results are the same either way.
- * Calls on one model from several host threads must be serialised. */
+ * Such calls on one model from several host threads are serialised by the
+ * model (its graph cache is guarded). */
 fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_device, int32_t batch, int32_t seq,
                      void* d_ws, size_t ws_bytes, float* d_hidden, float* d_logits, int32_t* d_argmax,
                      float* d_margin, void* stream);
