@@ -236,9 +236,9 @@ size_t fk_forward_workspace_bytes(const fk_model* m, int32_t batch, int32_t seq)
  *        model/forward-parity", Thm 3: near-tie argmax flips). Needs d_argmax.
  * A host `ids` buffer is copied synchronously before the call returns.
  * Forwards of at most 64 tokens (batch*seq) are launch-bound: the model
- * keeps one CUDA graph of the launches that follow the ids copy, captured on
- * the second consecutive call with the same batch, seq, workspace and output
- * pointers and replayed by later such calls (another key replaces it; calls
+ * keeps CUDA graphs of the launches that follow the ids copy, one per batch,
+ * seq, workspace and output pointers (the 4 most recent keys), captured on
+ * the second call with that key and replayed by later ones (calls
  * on a capturing stream, with kernel timing on, or with FK_NO_GRAPH set in
  * the environment launch one by one). Results are the same either way.
  * Such calls on one model from several host threads are serialised by the

@@ -41,6 +41,23 @@ def test_gemm_full(fk, P, K, N, fp32):
     assert e < (2e-5 if fp32 else 6e-3), e
 
 
+@pytest.mark.parametrize("fp32", [True, False])
+def test_gemm_rows_independent_of_call_size(fk, fp32):
+    """Each output row is a function of its own input row alone, bit for bit:
+    the first rows of an 8192-row call (256 x 256 tiles), of a 4096-row call
+    (128 x 256), of a 1000-row call (128 x 128) and of a 60-row call (128 x
+    64) are the same bits. A chunked cached prefill then rounds every
+    activation exactly as the cacheless forward does."""
+    import torch
+    x, w = _inputs(8192, 1024, 3840, s=5)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    full = fk.gemm(xd, wd, out_fp32=fp32)
+    for rows in (4096, 1000, 60):
+        part = fk.gemm(xd[:rows].contiguous(), wd, out_fp32=fp32)
+        torch.cuda.synchronize()
+        assert torch.equal(part, full[:rows]), rows
+
+
 @pytest.mark.parametrize("P,K,N", [(4160, 1024, 8192), (3000, 512, 9000), (1000, 512, 8200)])
 @pytest.mark.parametrize("fp32", [True, False])
 def test_gemm_dual_tile_ragged(fk, P, K, N, fp32):

@@ -5,7 +5,9 @@
 //
 // Design (sm_103a):
 //   * persistent kernel, one CTA per SM, 128 x BN output tiles walked in
-//     groups of 16 M-blocks so that a wave of CTAs shares A and B tiles in L2;
+//     groups of 16 M-blocks so that a wave of CTAs shares A and B tiles in L2
+//     (BN = 256, with 256-row tiles once there are two per SM; 128; or 64
+//     for few rows, so that more CTAs stream the weights);
 //   * warp 0: TMA producer (128-byte swizzled 128x64 A boxes and 64x64 B
 //     boxes into a STAGES-deep ring, completion on mbarriers);
 //   * warp 1: TMEM allocator and single-thread tcgen05.mma issuer
@@ -77,7 +79,8 @@ template <int BN, int MT = 1, bool SO = false>
 struct Cfg {
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGES = MT == 2 ? 3 : (SO ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : 6));
+  static constexpr int STAGES =
+      MT == 2 ? 3 : (BN == 64 ? (SO ? 6 : 8) : (SO ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : 6)));
   static constexpr int OUT_SLOTS = MT == 2 ? 1 : 2;
   static constexpr int OUT_BYTES = SO ? kEpiWarps * OUT_SLOTS * 4096 : 0;
   static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + OUT_BYTES + 1024 /*align*/ + 256 /*barriers*/;
@@ -112,7 +115,7 @@ FK_DEVICE float act_gelu_tanh(float g) {
 template <int BN>
 FK_DEVICE void b_box_source(const GemmArgs& a, int nb, int i, int gbase, int& map, int& row, bool& valid) {
   if (a.glu) {
-    constexpr int half = BN / 128;  // boxes per half tile
+    constexpr int half = BN >= 128 ? BN / 128 : 1;  // boxes per half tile (gated tiles have BN >= 128)
     map = (i < half) ? 0 : 1;
     row = nb * (BN / 2) + (i % half) * 64;
     valid = row < a.seg_rows[map];
@@ -708,12 +711,17 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
   const int m_blocks = (M + BM - 1) / BM;
   const int nb256 = w.glu ? (w.n_out + 127) / 128 : (a.n_virtual + 255) / 256;
   const bool big = ((M + 2 * BM - 1) / (2 * BM)) * nb256 >= 2 * sm_count, wide = m_blocks * nb256 >= sm_count;
+  // few rows (a short forward or prefill chunk): 128 x 64 tiles while 128-wide
+  // ones would leave SMs without a tile, so that more CTAs stream the weights
+  // (not for the gated operand, whose halves are 64-row boxes each)
+  const bool narrow = !w.glu && m_blocks * ((a.n_virtual + 127) / 128) < sm_count;
   if (o.epi == EPI_F32 || o.epi == EPI_ADD_F32) {
     CUtensorMap tOut;
     s = make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo);
     if (s != FK_OK) return s;
     if (big) return launch_bn<256, 2, false, true>(tA, w, a, sm_count, st, &tOut);
     if (wide) return launch_bn<256, 1, false, true>(tA, w, a, sm_count, st, &tOut);
+    if (narrow) return launch_bn<64, 1, false, true>(tA, w, a, sm_count, st, &tOut);
     return launch_bn<128, 1, false, true>(tA, w, a, sm_count, st, &tOut);
   }
   if (big || wide) {  // 16-bit outputs of 256-wide tiles: staged boxes, TMA stores
@@ -723,6 +731,7 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
     if (big) return launch_bn<256, 2, false, true>(tA, w, a, sm_count, st, &tOut);
     return launch_bn<256, 1, false, true>(tA, w, a, sm_count, st, &tOut);
   }
+  if (narrow) return launch_bn<64, 1>(tA, w, a, sm_count, st);
   return launch_bn<128, 1>(tA, w, a, sm_count, st);
 }
 

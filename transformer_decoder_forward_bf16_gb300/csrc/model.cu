@@ -87,7 +87,8 @@ struct fk_model {
   int f16(uint32_t site) const { return (cfg.f16_sites & site) ? 1 : 0; }
   // cacheless forwards of few tokens: the second call with the same shape,
   // workspace and outputs captures the launches after the ids copy into a
-  // CUDA graph, which later such calls replay (fk_forward)
+  // CUDA graph, which later such calls replay (fk_forward); kFwdGraphs keys
+  // are kept
   struct FwdKey {
     int B = 0, S = 0;
     const void* ws = nullptr;
@@ -97,12 +98,22 @@ struct fk_model {
              out[2] == o.out[2] && out[3] == o.out[3];
     }
   };
+  // a few most recent keys: a caller alternating between output buffers
+  // still finds its graphs (least recently used entry replaced)
+  static constexpr int kFwdGraphs = 4;
+  struct FwdEntry {
+    FwdKey key;
+    cudaGraphExec_t exec = nullptr;  // null: seen once, not captured yet
+    bool used = false;
+    unsigned long long last = 0;
+  };
   std::mutex fwd_mu;
   cudaStream_t fwd_cap_stream = nullptr;
-  cudaGraphExec_t fwd_graph = nullptr;
-  FwdKey fwd_key, fwd_seen;
+  FwdEntry fwd[kFwdGraphs];
+  unsigned long long fwd_clock = 0;
   ~fk_model() {
-    if (fwd_graph) cudaGraphExecDestroy(fwd_graph);
+    for (FwdEntry& e : fwd)
+      if (e.exec) cudaGraphExecDestroy(e.exec);
     if (fwd_cap_stream) cudaStreamDestroy(fwd_cap_stream);
   }
 };
@@ -829,15 +840,22 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
   key.out[2] = d_argmax;
   key.out[3] = d_margin;
   std::lock_guard<std::mutex> lock(m->fwd_mu);
-  if (!(m->fwd_graph && m->fwd_key == key)) {
-    if (!(m->fwd_seen == key)) {
-      m->fwd_seen = key;
-      return enqueue(st);
-    }
-    if (m->fwd_graph) {
-      cudaGraphExecDestroy(m->fwd_graph);
-      m->fwd_graph = nullptr;
-    }
+  fk_model::FwdEntry* hit = nullptr;
+  fk_model::FwdEntry* lru = &m->fwd[0];
+  for (fk_model::FwdEntry& e : m->fwd) {
+    if (e.used && e.key == key) hit = &e;
+    if (!e.used || (lru->used && e.last < lru->last)) lru = &e;
+  }
+  if (!hit) {  // first call with this key: launched one by one, remembered
+    if (lru->exec) cudaGraphExecDestroy(lru->exec);
+    *lru = fk_model::FwdEntry();
+    lru->key = key;
+    lru->used = true;
+    lru->last = ++m->fwd_clock;
+    return enqueue(st);
+  }
+  hit->last = ++m->fwd_clock;
+  if (!hit->exec) {  // second call: capture
     if (!m->fwd_cap_stream) FK_CUDA_TRY(cudaStreamCreateWithFlags(&m->fwd_cap_stream, cudaStreamNonBlocking));
     FK_CUDA_TRY(cudaStreamBeginCapture(m->fwd_cap_stream, cudaStreamCaptureModeThreadLocal));
     const fk_status es = enqueue(m->fwd_cap_stream);
@@ -848,15 +866,14 @@ extern "C" fk_status fk_forward(fk_model* m, const int32_t* ids, int32_t ids_on_
       return es;
     }
     if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamEndCapture(forward)");
-    ce = cudaGraphInstantiate(&m->fwd_graph, g, 0);
+    ce = cudaGraphInstantiate(&hit->exec, g, 0);
     cudaGraphDestroy(g);
     if (ce != cudaSuccess) {
-      m->fwd_graph = nullptr;
+      hit->exec = nullptr;
       return cuda_fail(ce, "cudaGraphInstantiate(forward)");
     }
-    m->fwd_key = key;
   }
-  FK_CUDA_TRY(cudaGraphLaunch(m->fwd_graph, st));
+  FK_CUDA_TRY(cudaGraphLaunch(hit->exec, st));
   return FK_OK;
 }
 
