@@ -116,6 +116,40 @@ def test_forward_graph_replay(fk):
     assert st == 0, flags
 
 
+def test_forward_graph_cache_many_keys(fk):
+    """Five forward shapes called in turn, more than the graphs the model
+    keeps: keys are remembered, captured, replayed and replaced in least
+    recently used order, and every call equals its eager result bit for bit."""
+    import torch
+    cfg = synth.small_config("llama")
+    wb = synth.make_weights(cfg, norm_mode="random", sigma=0.02)
+    model = fk.Model(cfg, weights_to_dev(wb), max_positions=64)
+    lib = fk.load()
+    shapes = [(1, 5), (2, 9), (1, 17), (3, 4), (2, 21)]
+    bufs = {}
+    refs = {}
+    for B, S in shapes:
+        T = B * S
+        wsb = lib.fk_forward_workspace_bytes(model.handle, B, S)
+        bufs[(B, S)] = (torch.empty(wsb, dtype=torch.uint8, device="cuda"),
+                        torch.empty((T, cfg.vocab), dtype=torch.float32, device="cuda"),
+                        torch.empty((T,), dtype=torch.int32, device="cuda"))
+        ids = synth.make_ids(cfg, B, S, seed=B * 100 + S)
+        refs[(B, S)] = (ids, model.forward(ids, hidden=False))
+    torch.cuda.synchronize()
+    for rnd in range(4):
+        for B, S in (shapes if rnd % 2 == 0 else shapes[::-1]):
+            ws, z, am = bufs[(B, S)]
+            ids, ref = refs[(B, S)]
+            ids = np.ascontiguousarray(ids, dtype=np.int32)
+            st = fk.fk_forward(model.handle, ids.ctypes.data, 0, B, S, ws.data_ptr(), ws.numel(), 0, z.data_ptr(),
+                               am.data_ptr(), 0, 0)
+            assert st == 0, lib.fk_last_error()
+            torch.cuda.synchronize()
+            assert torch.equal(z, ref["logits"]), (rnd, B, S)
+            assert torch.equal(am, ref["argmax"]), (rnd, B, S)
+
+
 def test_smollm2_shape_9_tokens(fk):
     """The SmolLM2-135M-shaped llama, one sequence of 9 ids, norm weights 1.0."""
     r = check_forward(fk, synth.CONFIGS["smollm2-135m"], 1, 9)
