@@ -12,7 +12,9 @@ random token ids):
   * decode at batch 1 from the same context length (the per-sequence
     latency case), G greedy steps per timed step.
 One step = one prefill of the 4 x 4096 batch + G decode steps at batch 32 + G
-at batch 1; decode steps replay the session's captured CUDA graph.
+at batch 1; decode steps replay the session's captured CUDA graph. The timed
+steps run inside the NVTX range "timed_steps", so a profiler can keep exactly
+their launches (ncu --nvtx --nvtx-include "timed_steps/").
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fk|reference]
   python bench.py --all-configs     (one JSON line per other workload, below)
