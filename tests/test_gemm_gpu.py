@@ -45,14 +45,15 @@ def test_gemm_full(fk, P, K, N, fp32):
 def test_gemm_rows_independent_of_call_size(fk, fp32):
     """Each output row is a function of its own input row alone, bit for bit:
     the first rows of an 8192-row call (256 x 256 tiles), of a 4096-row call
-    (128 x 256), of a 1000-row call (128 x 128) and of a 60-row call (128 x
-    64) are the same bits. A chunked cached prefill then rounds every
-    activation exactly as the cacheless forward does."""
+    (128 x 256), of a 1000-row call (128 x 128), of a 60-row call (128 x 64,
+    few-row mode with 64-row A boxes) and of a 10-row call (16-row A boxes)
+    are the same bits. A chunked cached prefill then rounds every activation
+    exactly as the cacheless forward does."""
     import torch
     x, w = _inputs(8192, 1024, 3840, s=5)
     xd, wd = to_dev_bf16(x), to_dev_bf16(w)
     full = fk.gemm(xd, wd, out_fp32=fp32)
-    for rows in (4096, 1000, 60):
+    for rows in (4096, 1000, 60, 10):
         part = fk.gemm(xd[:rows].contiguous(), wd, out_fp32=fp32)
         torch.cuda.synchronize()
         assert torch.equal(part, full[:rows]), rows

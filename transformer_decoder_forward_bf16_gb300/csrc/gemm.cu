@@ -75,15 +75,32 @@ struct GemmArgs {
 // SO: fp32 output blocks staged in shared memory (OUT_SLOTS 4 KiB 32 x 32
 // blocks per epilogue warp) and stored by TMA; one operand stage fewer to
 // make room (256-row tiles keep their three stages and one slot per warp).
-template <int BN, int MT = 1, bool SO = false>
+// AR: few-row mode (a call of at most AR rows, MT == 1). The TMA writes only
+// the AR valid rows of each A stage, and a stage's A slot is only that big:
+// the MMA still reads 128 rows from the slot's start, the rows past AR being
+// whatever the next slots hold. Those rows' outputs are never stored, and each
+// output row depends on its own A row alone, so the stored rows are the same
+// bits as with whole A tiles. The shared memory saved deepens the weight ring.
+constexpr int kSmemBudget = 232448;  // dynamic shared memory of one CTA (227 KiB)
+template <int BN, int MT = 1, bool SO = false, int AR = 0>
 struct Cfg {
-  static constexpr int A_STAGE = MT * A_BYTES;
+  static_assert(AR == 0 || MT == 1, "few-row mode takes 128-row tiles");
+  static constexpr int A_STAGE = AR ? (AR * BK * 2 + 1023) / 1024 * 1024 : MT * A_BYTES;  // slot stride
+  static constexpr int A_TX = AR ? AR * BK * 2 : MT * A_BYTES;                          // bytes loaded
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGES =
-      MT == 2 ? 3 : (BN == 64 ? (SO ? 6 : 8) : (SO ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : 6)));
   static constexpr int OUT_SLOTS = MT == 2 ? 1 : 2;
   static constexpr int OUT_BYTES = SO ? kEpiWarps * OUT_SLOTS * 4096 : 0;
-  static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + OUT_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // mbarriers (two per stage and five), TMEM address, abort flag: the deep
+  // rings of few-row mode need more than 256 bytes
+  static constexpr int BAR_BYTES = AR ? 512 : 256;
+  static constexpr int AR_STAGES = (kSmemBudget - OUT_BYTES - 1024 - BAR_BYTES) / (A_STAGE + B_BYTES);
+  static constexpr int STAGES =
+      AR ? (AR_STAGES < 24 ? AR_STAGES : 24)
+         : (MT == 2 ? 3 : (BN == 64 ? (SO ? 6 : 8) : (SO ? ((BN == 256) ? 3 : 4) : ((BN == 256) ? 4 : 6))));
+  static constexpr int SMEM = STAGES * (A_STAGE + B_BYTES) + OUT_BYTES + 1024 /*align*/ + BAR_BYTES;
+  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert(SMEM <= kSmemBudget, "shared memory");
+  static_assert(AR == 0 || STAGES * B_BYTES >= A_BYTES, "a slot's 128-row read stays inside the operand ring");
   static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator sets (double buffer when they fit)
   static constexpr uint32_t TMEM_COLS = NACC * MT * BN;
 };
@@ -147,12 +164,12 @@ FK_DEVICE TileRows grouped_rows(const int* goff, const unsigned short* mstart, i
   return TileRows{goff[lo] + (mb - (int)mstart[lo]) * TM, goff[lo + 1], lo};
 }
 
-template <int BN, int MT, bool GROUPED, bool SO>
+template <int BN, int MT, bool GROUPED, bool SO, int AR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
-  using C = Cfg<BN, MT, SO>;
+  using C = Cfg<BN, MT, SO, AR>;
   constexpr int TM = BM * MT;  // rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint32_t bytes = C::A_STAGE;
+          uint32_t bytes = C::A_TX;
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i) {
             int map, row;
@@ -257,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int sub = 0; sub < MT; ++sub)
             tma_load_2d(&tmA, &full[stage], sA + stage * C::A_STAGE + sub * A_BYTES, kb * BK, tr.row0 + sub * BM);
+          // (few-row mode: the map's box is AR rows high, so this writes A_TX bytes)
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i) {
             int map, row;
@@ -547,13 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int MT, bool GROUPED = false, bool SO = false>
+template <int BN, int MT, bool GROUPED = false, bool SO = false, int AR = 0>
 fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs& a, int sm_count, cudaStream_t st,
                     const CUtensorMap* tOut = nullptr) {
-  using C = Cfg<BN, MT, SO>;
+  using C = Cfg<BN, MT, SO, AR>;
   static DeviceOnce once;
   const cudaError_t attr_err = once.run([] {
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT, GROUPED, SO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, MT, GROUPED, SO, AR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::SMEM);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
@@ -563,7 +581,7 @@ fk_status launch_bn(const CUtensorMap& tA, const GemmWeights& w, const GemmArgs&
   const int n_blocks = a.glu ? (a.n_out + BN / 2 - 1) / (BN / 2) : (a.n_virtual + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int grid = std::min(tiles, sm_count);
-  gemm_tc_kernel<BN, MT, GROUPED, SO><<<grid, kThreads, C::SMEM, st>>>(
+  gemm_tc_kernel<BN, MT, GROUPED, SO, AR><<<grid, kThreads, C::SMEM, st>>>(
       tA, w.map[0], w.nseg > 1 ? w.map[1] : w.map[0], w.nseg > 2 ? w.map[2] : w.map[0], tOut ? *tOut : w.map[0], a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
@@ -715,6 +733,28 @@ fk_status gemm_run(const void* A, int M, int lda, const GemmWeights& w, const Ge
   // ones would leave SMs without a tile, so that more CTAs stream the weights
   // (not for the gated operand, whose halves are 64-row boxes each)
   const bool narrow = !w.glu && m_blocks * ((a.n_virtual + 127) / 128) < sm_count;
+  if (M <= 64 && !big && !wide) {
+    // few rows: the A map's box holds only the valid rows (16 or 64), and the
+    // shared memory of the rest deepens the weight ring (Cfg, AR)
+    const int ar = M <= 16 ? 16 : 64;
+    s = make_tmap_bf16(&tA, A, M, w.K, lda, ar);
+    if (s != FK_OK) return s;
+    if (o.epi == EPI_F32 || o.epi == EPI_ADD_F32) {
+      CUtensorMap tOut;
+      s = make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo);
+      if (s != FK_OK) return s;
+      if (narrow)
+        return ar == 16 ? launch_bn<64, 1, false, true, 16>(tA, w, a, sm_count, st, &tOut)
+                        : launch_bn<64, 1, false, true, 64>(tA, w, a, sm_count, st, &tOut);
+      return ar == 16 ? launch_bn<128, 1, false, true, 16>(tA, w, a, sm_count, st, &tOut)
+                      : launch_bn<128, 1, false, true, 64>(tA, w, a, sm_count, st, &tOut);
+    }
+    if (narrow)
+      return ar == 16 ? launch_bn<64, 1, false, false, 16>(tA, w, a, sm_count, st)
+                      : launch_bn<64, 1, false, false, 64>(tA, w, a, sm_count, st);
+    return ar == 16 ? launch_bn<128, 1, false, false, 16>(tA, w, a, sm_count, st)
+                    : launch_bn<128, 1, false, false, 64>(tA, w, a, sm_count, st);
+  }
   if (o.epi == EPI_F32 || o.epi == EPI_ADD_F32) {
     CUtensorMap tOut;
     s = make_tmap_f32_out(&tOut, o.out, M, w.n_out, o.ldo);
