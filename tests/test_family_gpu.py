@@ -3,7 +3,7 @@ forward over the family axes): the Qwen3-8B shape (per-head QK-norm in a
 pre-norm layer, RoPE base 1e6, untied 151936-word head) and the Mistral-7B
 shape (a sliding window on every layer), each as a two-layer slice of the
 full-width model against the exact oracle. Both run with f16 activation
-storage and meet the spec gates: hidden cosine >= 0.9999 at every slot
+storage and meet the forward-parity gates: hidden cosine >= 0.9999 at every slot
 and position, logits within 0.05, argmax exact where the oracle's top-1/top-2
 margin exceeds 1e-2. The Mistral slice shrinks the window to 256 so that a
 600-token prefill in chunks of 128 makes it non-vacuous and wraps the

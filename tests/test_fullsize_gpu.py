@@ -27,7 +27,7 @@ those roundings (storage="bf16") lands 3-6% (hidden state) from the exact
 result, and any other bf16 realisation, the device included, lands as far from
 it as from the exact one. Storing the same activations as IEEE f16 (3 more
 significant bits, fk_config.f16_sites) brings both shapes inside the gates at
-the same tensor-core rate, so there the gates are the spec ones, checked
+the same tensor-core rate, so there the gates are the forward-parity ones, checked
 against the exact oracle. The bf16 storage mode keeps gates derived from its
 own noise floor: the device's distance from the exact oracle may be at most
 1.25x the bf16-storage oracle's, and the argmax must match wherever the exact
@@ -144,7 +144,7 @@ def _strict_gates(h, h_ref, z_last, z_last_ref, what):
 def test_llama3_8b_slice_vs_oracle(fk):
     """2 x 512 prefill + 16 decode steps of the full Llama-3-8B shape against
     the exact oracle, in both activation storage formats. f16 storage must
-    meet the spec gates; bf16 storage is held to its own noise floor
+    meet the forward-parity gates; bf16 storage is held to its own noise floor
     (the oracle evaluated with exactly the bf16 storage points)."""
     import torch
     cfg = synth.CONFIGS["llama3-8b"]
@@ -159,7 +159,7 @@ def test_llama3_8b_slice_vs_oracle(fk):
     del W
     gc.collect()
 
-    # ---- f16 activation storage: the spec gates
+    # ---- f16 activation storage: the forward-parity gates
     model = fk.Model(cfg.with_(f16_sites=0x3F), wdev, max_positions=600)
     forced, first, _ = _greedy_device(fk, model, prompt, steps, forced=ref["ids"][:-1])
     free, _, _ = _greedy_device(fk, model, prompt, steps)
@@ -299,7 +299,7 @@ def test_gemma3_tower_1_9_1024(fk):
         assert top1.sum() >= 802 and min(quarters) >= 179 and dlp <= 16.4
         return z
 
-    # ---- f16 activation storage: the spec gates at 1 and 9 tokens
+    # ---- f16 activation storage: the forward-parity gates at 1 and 9 tokens
     model = fk.Model(cfg.with_(f16_sites=0x3F), wdev, max_positions=1024)
     for S in (1, 9):
         out = model.forward(P[:, :S])
@@ -349,7 +349,7 @@ def test_gemma3_tower_decode_past_the_window(fk):
     positions and wraps), then 16 teacher-forced decode steps, every call's
     logits against the exact oracle session ("N7 · model/forward-parity",
     Thm 2: sliding-window non-vacuity; "pegainfer issue #878": beyond the
-    window edge). f16 storage: the spec logit and argmax gates on all
+    window edge). f16 storage: the forward-parity logit and argmax gates on all
     17 calls; bf16 storage: the distributional gate."""
     import os
     import torch
